@@ -1,0 +1,520 @@
+/*
+ * dspark_oracle.c — plain, slow, fp64 CPU oracle of the DSpark per-round hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or calls this
+ * file: only the tests, the smoke check and the benchmark's CPU-baseline leg do.  It
+ * shares no code, header or table with the CUDA library; the two meet only through
+ * the seeded synthetic inputs.
+ *
+ * Every function follows the method's definition step by step, in double precision,
+ * from inputs converted exactly (fp32 -> fp64, bf16 -> fp64).  No blocking, fusion
+ * or reordering beyond what the definition states.  OpenMP runs independent requests
+ * in parallel; each request's arithmetic is sequential and in a fixed order.
+ *
+ * Sources (web pages about the DSpark paper, arXiv 2607.05147):
+ *   [EXPL]  numb3r33 blog, "DSpark: confidence-scheduled speculative decoding"
+ *   [VLLM]  vllmbangkok blog, "DSpark: Confidence-Scheduled Speculative Decoding with
+ *           Semi-Autoregressive Generation"
+ *   [KB]    edgeai1 knowledge base, "DSpark 精读"
+ *   [FR]    mkdocs.reaper.mx, "3 · DSpark"
+ *   [PHILOX] Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3",
+ *           SC'11 — the Philox4x32-10 counter-based generator.
+ *
+ * Parity pins: every function here is pinned by the not-gpu tests (worked examples
+ * printed on the pages, closed forms, brute-force law at V=8, chi-square over 10^6
+ * seeded trials, brute-force scheduler optimum).  No function is "parity unpinned".
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_F32 0
+#define ORC_BF16 1
+
+#define ORC_EARLY_STOP 0
+#define ORC_FULL_SEARCH 1
+#define ORC_CAPACITY_K 2
+#define ORC_FIXED 3
+
+#define ORC_STREAM_DRAFT 0u
+#define ORC_STREAM_ACCEPT 1u
+#define ORC_STREAM_CORRECT 2u
+
+/* ------------------------------------------------------------------------- */
+/* Philox4x32-10 [PHILOX]: S-box free bijection built from two 32x32->64
+ * multiplications per round, 10 rounds, key bumped by the Weyl constants
+ * (golden ratio and sqrt(3)-1 fractions) between rounds.                    */
+/* ------------------------------------------------------------------------- */
+void orc_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4]) {
+    const uint64_t MUL_A = 0xD2511F53u, MUL_B = 0xCD9E8D57u;
+    const uint32_t WEYL_A = 0x9E3779B9u, WEYL_B = 0xBB67AE85u;
+    uint32_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
+    uint32_t k0 = key_in[0], k1 = key_in[1];
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) {
+            k0 += WEYL_A;
+            k1 += WEYL_B;
+        }
+        uint64_t pa = MUL_A * (uint64_t)c0;
+        uint64_t pb = MUL_B * (uint64_t)c2;
+        uint32_t hi_a = (uint32_t)(pa >> 32), lo_a = (uint32_t)pa;
+        uint32_t hi_b = (uint32_t)(pb >> 32), lo_b = (uint32_t)pb;
+        uint32_t n0 = hi_b ^ c1 ^ k0;
+        uint32_t n1 = lo_b;
+        uint32_t n2 = hi_a ^ c3 ^ k1;
+        uint32_t n3 = lo_a;
+        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* The counter layout of the method's random draws ("counter-based RNG keyed by
+ * (seed, request, position)"): counter = (lo32 req_id, lo32 round,
+ * stream<<24 | position, chunk), key = (lo32 seed, hi32 seed).  Element v of a
+ * vocabulary row takes word v%4 of chunk v/4.  Returns the raw 32-bit word.  */
+uint32_t orc_draw_bits(uint64_t seed, uint64_t req_id, uint64_t round, uint32_t stream,
+                       uint32_t position, uint32_t chunk, uint32_t lane) {
+    uint32_t ctr[4] = {(uint32_t)req_id, (uint32_t)round, (stream << 24) | position, chunk};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t out[4];
+    orc_philox4x32_10(ctr, key, out);
+    return out[lane & 3u];
+}
+
+/* Uniform in (0,1): the top 24 bits, centred in their cell: ((b>>8)+1/2) / 2^24. */
+double orc_uniform(uint32_t bits) { return ((double)(bits >> 8) + 0.5) * (1.0 / 16777216.0); }
+
+/* Standard Gumbel from a uniform: g = -ln(-ln u).  ln u is taken as log1p(u-1),
+ * u-1 being exact in binary64, so the tail u -> 1 keeps full relative accuracy. */
+double orc_gumbel(double u) { return -log(-log1p(u - 1.0)); }
+
+static double orc_load(const void* base, int dtype, size_t idx) {
+    if (dtype == ORC_F32) return (double)((const float*)base)[idx];
+    uint16_t b = ((const uint16_t*)base)[idx];
+    uint32_t f = ((uint32_t)b) << 16;
+    float x;
+    memcpy(&x, &f, sizeof x);
+    return (double)x;
+}
+
+static int orc_threads(int want) {
+#ifdef _OPENMP
+    if (want > 0) return want;
+    return omp_get_max_threads();
+#else
+    (void)want;
+    return 1;
+#endif
+}
+
+/* z = (U_k + W1[x_prev,:] W2) / T over the whole vocabulary ([EXPL] "Markov sequential
+ * head": p_k(v|x_{k-1}) = softmax(U_k(v) + B(x_{k-1},v)), B(x,:) = W1[x,:] W2; [KB] §2
+ * writes the same law with the anchor x_0 conditioning position 1).  The temperature
+ * divides the whole logit row. */
+static void orc_draft_logits(int V, int rank, int dtype_u, int dtype_w, const void* U, size_t u_row,
+                             const void* W1, const void* W2, int x_prev, double temperature,
+                             double* z) {
+    for (int v = 0; v < V; ++v) z[v] = 0.0;
+    for (int i = 0; i < rank; ++i) {
+        double w1 = orc_load(W1, dtype_w, (size_t)x_prev * rank + i);
+        for (int v = 0; v < V; ++v) z[v] += w1 * orc_load(W2, dtype_w, (size_t)i * V + v);
+    }
+    for (int v = 0; v < V; ++v) z[v] = (orc_load(U, dtype_u, u_row + v) + z[v]) / temperature;
+}
+
+static double orc_logsumexp(const double* z, int V) {
+    double m = -INFINITY;
+    for (int v = 0; v < V; ++v)
+        if (z[v] > m) m = z[v];
+    double s = 0.0;
+    for (int v = 0; v < V; ++v) s += exp(z[v] - m);
+    return m + log(s);
+}
+
+/* argmax_v (score_v + g_v), g_v standard Gumbel from the given stream/position,
+ * restricted to v with valid[v] != 0 (valid == NULL: all).  Lowest v wins ties.
+ * Also reports the runner-up and the key margin between the two. */
+static int orc_gumbel_argmax(const double* score, const unsigned char* valid, int V, uint64_t seed,
+                             uint64_t req_id, uint64_t round, uint32_t stream, uint32_t position,
+                             int* runner_up, double* margin) {
+    int best = -1, second = -1;
+    double kbest = -INFINITY, ksecond = -INFINITY;
+    for (int v = 0; v < V; ++v) {
+        if (valid && !valid[v]) continue;
+        double g = orc_gumbel(orc_uniform(orc_draw_bits(seed, req_id, round, stream, position,
+                                                        (uint32_t)v >> 2, (uint32_t)v & 3u)));
+        double key = score[v] + g;
+        if (best < 0 || key > kbest) {
+            second = best; ksecond = kbest;
+            best = v; kbest = key;
+        } else if (second < 0 || key > ksecond) {
+            second = v; ksecond = key;
+        }
+    }
+    if (runner_up) *runner_up = second;
+    if (margin) *margin = (second < 0) ? INFINITY : kbest - ksecond;
+    return best;
+}
+
+static double orc_sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+/* ------------------------------------------------------------------------- */
+/* Stage 1 — Markov-head draft loop with the confidence head.                 */
+/* ------------------------------------------------------------------------- */
+/* For each request r and k = 1..gamma (x_0 = anchor):
+ *   z      = (U[r,k-1,:] + W1[x_{k-1},:] W2) / T                     [EXPL] Markov head
+ *   lse_k  = log sum_v exp z_v ;  x_k = argmax_v z_v + g_v (Gumbel-max draw of
+ *            softmax(z), stream 0 at position k)                      [VLLM] §4.1
+ *   logq_k = z_{x_k} - lse_k
+ *   c_k    = sigmoid(kappa * (w_h . h[r,k-1,:] + w_e . W1[x_{k-1},:] + b) / T_k)
+ *            (linear + sigmoid on [h_k ; W1[x_{k-1}]], [KB] §4; per-position
+ *            temperature of sequential temperature scaling, [EXPL] "Sequential
+ *            temperature scaling"; kappa scales the raw logit).
+ * Diagnostics: runner_up / margin of the Gumbel draw (boundary-case rule). */
+int orc_markov_draft(int R, int gamma, int V, int rank, int d, int dtype_u, int dtype_w, int dtype_h,
+                     const void* U, const void* W1, const void* W2, const void* h,
+                     const float* conf_w, double conf_b, double conf_logit_scale,
+                     const float* conf_temp, double temperature, const int32_t* x0,
+                     const int64_t* req_id, uint64_t seed, uint64_t round, int32_t* x_out,
+                     double* logq_out, double* lse_out, double* conf_out, int32_t* runner_up_out,
+                     double* margin_out, int nthreads) {
+    if (R < 0 || gamma < 1 || V < 1 || rank < 1 || d < 0 || temperature <= 0.0) return 1;
+    int nt = orc_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
+    for (int r = 0; r < R; ++r) {
+        double* z = (double*)malloc(sizeof(double) * (size_t)V);
+        int x_prev = x0[r];
+        for (int k = 1; k <= gamma; ++k) {
+            size_t row = ((size_t)r * gamma + (k - 1));
+            orc_draft_logits(V, rank, dtype_u, dtype_w, U, row * (size_t)V, W1, W2, x_prev,
+                             temperature, z);
+            double lse = orc_logsumexp(z, V);
+            int ru = -1;
+            double mg = 0.0;
+            int xk = orc_gumbel_argmax(z, NULL, V, seed, (uint64_t)req_id[r], round,
+                                       ORC_STREAM_DRAFT, (uint32_t)k, &ru, &mg);
+            double s_h = 0.0;
+            for (int i = 0; i < d; ++i) s_h += (double)conf_w[i] * orc_load(h, dtype_h, row * (size_t)d + i);
+            double s_e = 0.0;
+            for (int i = 0; i < rank; ++i)
+                s_e += (double)conf_w[d + i] * orc_load(W1, dtype_w, (size_t)x_prev * rank + i);
+            double logit = conf_logit_scale * (s_h + s_e + conf_b);
+            double c = orc_sigmoid(logit / (double)conf_temp[k - 1]);
+            x_out[row] = xk;
+            logq_out[row] = z[xk] - lse;
+            lse_out[row] = lse;
+            conf_out[row] = c;
+            if (runner_up_out) runner_up_out[row] = ru;
+            if (margin_out) margin_out[row] = mg;
+            x_prev = xk;
+        }
+        free(z);
+    }
+    return 0;
+}
+
+/* Full draft distribution q_k(. | x_prev) for one request/position (test helper). */
+int orc_draft_distribution(int V, int rank, int dtype_u, int dtype_w, const void* U_row,
+                           const void* W1, const void* W2, int x_prev, double temperature,
+                           double* q_out) {
+    orc_draft_logits(V, rank, dtype_u, dtype_w, U_row, 0, W1, W2, x_prev, temperature, q_out);
+    double lse = orc_logsumexp(q_out, V);
+    for (int v = 0; v < V; ++v) q_out[v] = exp(q_out[v] - lse);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Stage 2 — confidence scheduler.                                            */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+    double a;
+    int depth; /* j, 1-based */
+    int req;   /* r */
+} orc_cand;
+
+/* (a desc, depth asc, request asc): a is non-increasing along each request's chain,
+ * so with depth ascending on ties a request's prefix is always admitted in order
+ * ([EXPL] "Greedy prefix allocation"). */
+static int orc_cand_cmp(const void* pa, const void* pb) {
+    const orc_cand* a = (const orc_cand*)pa;
+    const orc_cand* b = (const orc_cand*)pb;
+    if (a->a > b->a) return -1;
+    if (a->a < b->a) return 1;
+    if (a->depth != b->depth) return a->depth < b->depth ? -1 : 1;
+    if (a->req != b->req) return a->req < b->req ? -1 : 1;
+    return 0;
+}
+
+/* a_{r,j} = prod_{i<=j} c_{r,i}, multiplied left to right in binary64 ([KB] §4,
+ * [FR] §3.3), then sorted globally. */
+static void orc_sorted_candidates(int R, int gamma, const float* conf, orc_cand* out) {
+    for (int r = 0; r < R; ++r) {
+        double a = 1.0;
+        for (int j = 1; j <= gamma; ++j) {
+            a = a * (double)conf[(size_t)r * gamma + (j - 1)];
+            orc_cand c = {a, j, r};
+            out[(size_t)r * gamma + (j - 1)] = c;
+        }
+    }
+    qsort(out, (size_t)R * gamma, sizeof(orc_cand), orc_cand_cmp);
+}
+
+/* Theta(n) = tau(n) * SPS(R + n) along the admission path, tau(n) = R + sum of the
+ * first n sorted a's ([KB] §4: B = sum_r (1 + l_r), tau = sum_r (1 + sum_{j<=l_r} a),
+ * maximise tau * SPS(B); [EXPL] "Scheduler objective"). */
+static void orc_theta_path(int R, int N, const orc_cand* sorted, const double* sps, double* tau,
+                           double* theta) {
+    tau[0] = (double)R;
+    theta[0] = tau[0] * sps[R];
+    for (int n = 1; n <= N; ++n) {
+        tau[n] = tau[n - 1] + sorted[n - 1].a;
+        theta[n] = tau[n] * sps[R + n];
+    }
+}
+
+static int orc_full_search(int N, const double* theta) {
+    int best = 0;
+    for (int n = 1; n <= N; ++n)
+        if (theta[n] > theta[best]) best = n;
+    return best;
+}
+
+/* Modes:
+ *  EARLY_STOP  — admit in sorted order, stop at the first n with Theta(n+1) <= Theta(n)
+ *                (non-anticipating ideal scheduler, [EXPL] "Losslessness and
+ *                non-anticipation", [KB] §4 "首次不增").
+ *  FULL_SEARCH — n* = argmax_n Theta(n), smallest n on ties ([VLLM] §4.2.2, jagged SPS).
+ *  CAPACITY_K  — K = FULL_SEARCH count on the stale confidences conf_hist; admit the
+ *                top-K by the current order ([EXPL] "Async scheduler in practice").
+ *  FIXED       — l_r = min(fixed_len, gamma) for every request (scheduler off).
+ * Diagnostics (boundary-case rule): diag[0] = smallest relative Theta gap met by a
+ * decision on the path, diag[1] = relative gap between the a's either side of the cut. */
+int orc_schedule(int R, int gamma, const float* conf, const double* sps, int sps_len, int mode,
+                 const float* conf_hist, int fixed_len, int32_t* ell_out, int32_t* B_out,
+                 double* tau_out, double* diag) {
+    int N = R * gamma;
+    if (R < 0 || gamma < 1 || sps_len < R * (gamma + 1) + 1) return 1;
+    if (mode == ORC_CAPACITY_K && conf_hist == NULL) return 1;
+    orc_cand* cand = (orc_cand*)malloc(sizeof(orc_cand) * (size_t)(N > 0 ? N : 1));
+    double* tau = (double*)malloc(sizeof(double) * (size_t)(N + 1));
+    double* theta = (double*)malloc(sizeof(double) * (size_t)(N + 1));
+    orc_sorted_candidates(R, gamma, conf, cand);
+    orc_theta_path(R, N, cand, sps, tau, theta);
+    for (int r = 0; r < R; ++r) ell_out[r] = 0;
+    double gap = INFINITY, tie = INFINITY;
+    int nstar = 0;
+    if (mode == ORC_FIXED) {
+        int L = fixed_len < 0 ? 0 : (fixed_len > gamma ? gamma : fixed_len);
+        double t = (double)R;
+        for (int r = 0; r < R; ++r) {
+            double a = 1.0;
+            for (int j = 1; j <= L; ++j) {
+                a = a * (double)conf[(size_t)r * gamma + (j - 1)];
+                t += a;
+            }
+            ell_out[r] = L;
+        }
+        *B_out = R + R * L;
+        *tau_out = t;
+        if (diag) { diag[0] = INFINITY; diag[1] = INFINITY; }
+        free(cand); free(tau); free(theta);
+        return 0;
+    }
+    if (mode == ORC_EARLY_STOP) {
+        nstar = N;
+        for (int n = 0; n < N; ++n) {
+            double g = fabs(theta[n + 1] - theta[n]) / theta[n];
+            if (g < gap) gap = g;
+            if (theta[n + 1] <= theta[n]) { nstar = n; break; }
+        }
+    } else if (mode == ORC_FULL_SEARCH) {
+        nstar = orc_full_search(N, theta);
+        for (int n = 0; n <= N; ++n) {
+            if (n == nstar) continue;
+            double g = fabs(theta[nstar] - theta[n]) / theta[nstar];
+            if (g < gap) gap = g;
+        }
+    } else if (mode == ORC_CAPACITY_K) {
+        orc_cand* hc = (orc_cand*)malloc(sizeof(orc_cand) * (size_t)(N > 0 ? N : 1));
+        double* ht = (double*)malloc(sizeof(double) * (size_t)(N + 1));
+        double* hth = (double*)malloc(sizeof(double) * (size_t)(N + 1));
+        orc_sorted_candidates(R, gamma, conf_hist, hc);
+        orc_theta_path(R, N, hc, sps, ht, hth);
+        int K = orc_full_search(N, hth);
+        for (int n = 0; n <= N; ++n) {
+            if (n == K) continue;
+            double g = fabs(hth[K] - hth[n]) / hth[K];
+            if (g < gap) gap = g;
+        }
+        nstar = K < N ? K : N;
+        free(hc); free(ht); free(hth);
+    } else {
+        free(cand); free(tau); free(theta);
+        return 1;
+    }
+    if (nstar > 0 && nstar < N) {
+        double hi = cand[nstar - 1].a, lo = cand[nstar].a;
+        tie = (hi - lo) / hi;
+    }
+    for (int n = 0; n < nstar; ++n) ell_out[cand[n].req] += 1;
+    *B_out = R + nstar;
+    *tau_out = tau[nstar];
+    if (diag) { diag[0] = gap; diag[1] = tie; }
+    free(cand); free(tau); free(theta);
+    return 0;
+}
+
+/* Theta path along the sorted order, for tests: writes a_(n) (n=1..N) and Theta(n). */
+int orc_schedule_path(int R, int gamma, const float* conf, const double* sps, double* a_sorted,
+                      int32_t* req_sorted, int32_t* depth_sorted, double* theta_out) {
+    int N = R * gamma;
+    orc_cand* cand = (orc_cand*)malloc(sizeof(orc_cand) * (size_t)(N > 0 ? N : 1));
+    double* tau = (double*)malloc(sizeof(double) * (size_t)(N + 1));
+    orc_sorted_candidates(R, gamma, conf, cand);
+    orc_theta_path(R, N, cand, sps, tau, theta_out);
+    for (int n = 0; n < N; ++n) {
+        a_sorted[n] = cand[n].a;
+        req_sorted[n] = cand[n].req;
+        depth_sorted[n] = cand[n].depth;
+    }
+    free(cand); free(tau);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Stage 3 — exact speculative-sampling verification.                         */
+/* ------------------------------------------------------------------------- */
+/* For request r with verify length l = ell[r]:
+ *   for j = 1..l: p_t = softmax(target[r,j-1,:] / T); accept x_j iff
+ *       u_j < p_t(x_j) / q_j(x_j), u_j uniform from stream 1 at position j
+ *       (min(1, p/q) acceptance, [EXPL] "One-token exactness"); stop at the first
+ *       rejection ([EXPL] "Why only the longest accepted prefix survives").
+ *   n_acc = accepted count.
+ *   if n_acc < l: j* = n_acc+1, q = softmax(z) with z the draft logits of position j*
+ *       (recomputed from U, W1[x_{j*-1}], W2 and normalised by the draft's lse),
+ *       p = softmax(target[r,j*-1]/T), rho = (p - q)_+, y drawn from rho/sum(rho) as
+ *       argmax_{rho_v>0} ln rho_v + g_v (stream 2 at position j*) — residual
+ *       correction ([EXPL] "One-token exactness").  If no rho_v > 0 (rounding only),
+ *       y is drawn from p with the same Gumbels.
+ *   else (every verified draft accepted, including l = 0): bonus token
+ *       y = argmax_v target[r,l,v]/T + g_v (stream 2 at position l+1) ([EXPL] "Prefix
+ *       survival and accepted length"; [KB] §6 counts it in tau).
+ *   tokens = x_1..x_{n_acc}, y;  n_out = n_acc + 1.
+ * Diagnostics per request: acc_margin[r*gamma + j-1] = u_j - ratio_j for tested j;
+ * corr_margin[r] = Gumbel key margin of the correction draw; corr_rho[r*2 + 0/1] =
+ * rho/max(p,q) of winner/runner-up for a residual draw (1 for a bonus draw). */
+int orc_verify(int R, int gamma, int V, int rank, int dtype_t, int dtype_u, int dtype_w,
+               const void* target, const void* U, const void* W1, const void* W2,
+               const int32_t* x0, const int32_t* x, const double* logq, const double* lse_q,
+               const int32_t* ell, double temperature, const int64_t* req_id, uint64_t seed,
+               uint64_t round, int32_t* n_acc_out, int32_t* tokens_out, int32_t* n_out,
+               double* acc_margin, double* corr_margin, double* corr_rho, int32_t* corr_kind,
+               int nthreads) {
+    if (R < 0 || gamma < 1 || V < 1 || temperature <= 0.0) return 1;
+    for (int r = 0; r < R; ++r)
+        if (ell[r] < 0 || ell[r] > gamma) return 1;
+    int nt = orc_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
+    for (int r = 0; r < R; ++r) {
+        double* t = (double*)malloc(sizeof(double) * (size_t)V);
+        double* z = (double*)malloc(sizeof(double) * (size_t)V);
+        unsigned char* pos = (unsigned char*)malloc((size_t)V);
+        const int l = ell[r];
+        const uint64_t rid = (uint64_t)req_id[r];
+        for (int j = 0; j < gamma; ++j)
+            if (acc_margin) acc_margin[(size_t)r * gamma + j] = NAN;
+        int n_acc = 0;
+        for (int j = 1; j <= l; ++j) {
+            size_t trow = ((size_t)r * (gamma + 1) + (j - 1)) * (size_t)V;
+            for (int v = 0; v < V; ++v) t[v] = orc_load(target, dtype_t, trow + v) / temperature;
+            double lse_t = orc_logsumexp(t, V);
+            int xj = x[(size_t)r * gamma + (j - 1)];
+            double lp = t[xj] - lse_t;
+            double ratio = exp(lp - logq[(size_t)r * gamma + (j - 1)]);
+            double u = orc_uniform(orc_draw_bits(seed, rid, round, ORC_STREAM_ACCEPT, (uint32_t)j, 0u, 0u));
+            if (acc_margin) acc_margin[(size_t)r * gamma + (j - 1)] = u - ratio;
+            if (u < ratio) n_acc += 1;
+            else break;
+        }
+        int y, ru = -1;
+        double mg = INFINITY;
+        int kind;
+        if (n_acc < l) {
+            int js = n_acc + 1;
+            int xprev = (js == 1) ? x0[r] : x[(size_t)r * gamma + (js - 2)];
+            size_t urow = ((size_t)r * gamma + (js - 1)) * (size_t)V;
+            orc_draft_logits(V, rank, dtype_u, dtype_w, U, urow, W1, W2, xprev, temperature, z);
+            double lq = lse_q[(size_t)r * gamma + (js - 1)];
+            size_t trow = ((size_t)r * (gamma + 1) + (js - 1)) * (size_t)V;
+            for (int v = 0; v < V; ++v) t[v] = orc_load(target, dtype_t, trow + v) / temperature;
+            double lse_t = orc_logsumexp(t, V);
+            int any = 0;
+            double* score = z; /* reuse: score_v = ln rho_v */
+            double* rho_rel = (double*)malloc(sizeof(double) * (size_t)V);
+            for (int v = 0; v < V; ++v) {
+                double p = exp(t[v] - lse_t);
+                double q = exp(z[v] - lq);
+                double rho = p - q;
+                double mx = p > q ? p : q;
+                rho_rel[v] = mx > 0.0 ? rho / mx : 0.0;
+                pos[v] = rho > 0.0;
+                any |= pos[v];
+                score[v] = rho > 0.0 ? log(rho) : -INFINITY;
+            }
+            if (any) {
+                y = orc_gumbel_argmax(score, pos, V, seed, rid, round, ORC_STREAM_CORRECT,
+                                      (uint32_t)js, &ru, &mg);
+                kind = 1;
+                if (corr_rho) {
+                    corr_rho[(size_t)r * 2 + 0] = rho_rel[y];
+                    corr_rho[(size_t)r * 2 + 1] = ru >= 0 ? rho_rel[ru] : 1.0;
+                }
+            } else {
+                y = orc_gumbel_argmax(t, NULL, V, seed, rid, round, ORC_STREAM_CORRECT,
+                                      (uint32_t)js, &ru, &mg);
+                kind = 2;
+                if (corr_rho) { corr_rho[(size_t)r * 2 + 0] = 0.0; corr_rho[(size_t)r * 2 + 1] = 0.0; }
+            }
+            free(rho_rel);
+        } else {
+            size_t trow = ((size_t)r * (gamma + 1) + l) * (size_t)V;
+            for (int v = 0; v < V; ++v) t[v] = orc_load(target, dtype_t, trow + v) / temperature;
+            y = orc_gumbel_argmax(t, NULL, V, seed, rid, round, ORC_STREAM_CORRECT,
+                                  (uint32_t)(l + 1), &ru, &mg);
+            kind = 0;
+            if (corr_rho) { corr_rho[(size_t)r * 2 + 0] = 1.0; corr_rho[(size_t)r * 2 + 1] = 1.0; }
+        }
+        for (int j = 0; j <= gamma; ++j) tokens_out[(size_t)r * (gamma + 1) + j] = -1;
+        for (int j = 0; j < n_acc; ++j) tokens_out[(size_t)r * (gamma + 1) + j] = x[(size_t)r * gamma + j];
+        tokens_out[(size_t)r * (gamma + 1) + n_acc] = y;
+        n_acc_out[r] = n_acc;
+        n_out[r] = n_acc + 1;
+        if (corr_margin) corr_margin[r] = mg;
+        if (corr_kind) corr_kind[r] = kind;
+        free(t); free(z); free(pos);
+    }
+    return 0;
+}
+
+/* Many independent scheduler problems of the same shape, one after another (used by
+ * the law tests, which run 10^6 small batches). */
+int orc_schedule_many(int nbatch, int R, int gamma, const float* conf, const double* sps,
+                      int sps_len, int mode, const float* conf_hist, int fixed_len,
+                      int32_t* ell_out) {
+    for (int b = 0; b < nbatch; ++b) {
+        int32_t B;
+        double tau;
+        const size_t off = (size_t)b * R * gamma;
+        int rc = orc_schedule(R, gamma, conf + off, sps, sps_len, mode,
+                              conf_hist ? conf_hist + off : NULL, fixed_len,
+                              ell_out + (size_t)b * R, &B, &tau, NULL);
+        if (rc) return rc;
+    }
+    return 0;
+}
+
+int orc_max_threads(void) { return orc_threads(0); }
