@@ -1,0 +1,200 @@
+/*
+ * dspark.h — C ABI of the DSpark per-round speculative-decoding hot path on GB300
+ * (sm_103a): Markov-head draft -> confidence scheduler -> exact verification.
+ *
+ * The method is the one described on the pages about DSpark (Cheng, Yu, Shao et al.,
+ * "DSpark: Confidence-Scheduled Speculative Decoding with Semi-Autoregressive
+ * Generation", arXiv 2607.05147):
+ *   - numb3r33 blog "DSpark: confidence-scheduled speculative decoding" (sections
+ *     "One-token exactness", "Prefix survival and accepted length", "Markov sequential
+ *     head", "Confidence head", "Sequential temperature scaling", "Scheduler
+ *     objective", "Greedy prefix allocation", "Async scheduler in practice");
+ *   - vllmbangkok blog "DSpark: Confidence-Scheduled Speculative Decoding with
+ *     Semi-Autoregressive Generation" (§4.1, §4.2.1, §4.2.2);
+ *   - edgeai1 knowledge base "DSpark 精读" (§2 proposal law, §4 confidence head and
+ *     batch scheduler);
+ *   - mkdocs.reaper.mx "3 · DSpark" (§3.1-§3.3).
+ *
+ * Conventions for every entry point
+ *   - All array pointers are DEVICE pointers owned by the caller, C-contiguous,
+ *     row-major.  "U[R,gamma,V]" means element U[(r*gamma + k-1)*V + v] for request r,
+ *     draft position k (1-based) and vocabulary id v.
+ *   - The library never allocates device memory: scratch comes from the caller's
+ *     `workspace` (at least the size the matching *_workspace_size() returns, 256-byte
+ *     aligned).  A workspace may be reused by later calls on the same stream; calls that
+ *     run concurrently need separate workspaces.
+ *   - Work is enqueued on `stream` and returns without synchronising the host.  No call
+ *     reads device data on the host, so a whole round can be captured in a CUDA graph.
+ *   - Arguments are validated on the host before anything is enqueued.  On a non-OK
+ *     status nothing was launched; dspark_last_error_message() (thread-local) says why.
+ *   - Kernels never trap.  A bounded wait that gives up records DSPARK_TIMEOUT in the
+ *     workspace's device status word; read it with dspark_workspace_status().
+ *   - There is no CPU fallback: every step runs in this library's CUDA kernels.
+ *
+ * Random numbers: Philox4x32-10 (Salmon et al., SC'11) with key (lo32 seed, hi32 seed)
+ * and counter (lo32 req_id[r], lo32 round, stream<<24 | position, v/4); vocabulary
+ * element v takes output word v%4; uniform u = ((word>>8) + 0.5) * 2^-24 in (0,1).
+ * Streams: 0 draft Gumbel at position k, 1 acceptance uniform at position j (word 0
+ * of chunk 0), 2 correction Gumbel (residual or bonus) at position n_acc+1.  The same
+ * (seed, req_id, round) always reproduces the same round, whatever the batch layout.
+ */
+#ifndef DSPARK_H
+#define DSPARK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DSPARK_API __attribute__((visibility("default")))
+#else
+#define DSPARK_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int dspark_status;
+
+#define DSPARK_OK 0
+#define DSPARK_INVALID_ARG 1          /* null pointer, negative size, bad enum, T <= 0 */
+#define DSPARK_UNSUPPORTED_SHAPE 2    /* size outside the limits stated per call */
+#define DSPARK_WORKSPACE_TOO_SMALL 3  /* ws_bytes below *_workspace_size() */
+#define DSPARK_CUDA_ERROR 4           /* a CUDA runtime call or launch failed */
+#define DSPARK_TIMEOUT 5              /* a device wait gave up (reported via the status word) */
+
+#define DSPARK_F32 0
+#define DSPARK_BF16 1
+
+#define DSPARK_EARLY_STOP 0
+#define DSPARK_FULL_SEARCH 1
+#define DSPARK_CAPACITY_K 2
+#define DSPARK_FIXED 3
+
+/* Human-readable name of a status code (static storage). */
+DSPARK_API const char* dspark_status_string(int status);
+
+/* Detail of the last non-OK status returned on the calling host thread. */
+DSPARK_API const char* dspark_last_error_message(void);
+
+/* Copies the device status word kept at the start of `workspace` (written by kernels
+ * whose bounded waits gave up) into *status, synchronising `stream`.  0 = OK,
+ * DSPARK_TIMEOUT otherwise.  Resets the word to 0 when reset != 0. */
+DSPARK_API dspark_status dspark_workspace_status(void* workspace, int reset, int* status, void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * Stage 1: Markov-head draft loop with the confidence head.
+ *
+ * Defines (numb3r33 blog "Markov sequential head"; DSpark 精读 §2; vllmbangkok §4.1):
+ *   for k = 1..gamma, with x_0 = x0[r]:
+ *     z_v     = (U[r,k,v] + sum_i W1[x_{k-1},i] * W2[i,v]) / temperature
+ *     x_k     = argmax_v z_v + g_v, g_v = -ln(-ln u_v) from stream 0 at position k
+ *               (a Gumbel-max draw of p_k = softmax(z))
+ *     lse_k   = ln sum_v exp z_v ;  logq_k = z_{x_k} - lse_k
+ *   and the confidence head (DSpark 精读 §4: linear + sigmoid on [h_k ; W1[x_{k-1}]];
+ *   numb3r33 blog "Sequential temperature scaling": one temperature per position):
+ *     c_k = sigmoid(conf_logit_scale * (w_h . h[r,k,:] + w_e . W1[x_{k-1},:] + conf_b)
+ *                   / conf_temp[k-1])
+ *
+ * Arguments
+ *   R, gamma, V, rank, d  sizes: requests, draft length, vocabulary, low-rank factor
+ *                         rank, backbone hidden size.
+ *   dtype_u   DSPARK_F32 or DSPARK_BF16 for U.
+ *   dtype_w   dtype of W1 and W2.  DSPARK_BF16 runs the bias contraction on the
+ *             tcgen05 tensor cores (bf16 x bf16 -> fp32); DSPARK_F32 on CUDA cores (fp32).
+ *   dtype_h   dtype of h.
+ *   U         [R,gamma,V] backbone base logits.
+ *   W1        [V,rank] first low-rank factor (row x is the token's embedding).
+ *   W2        [rank,V] second low-rank factor.
+ *   h         [R,gamma,d] backbone hidden states.
+ *   conf_w    [d+rank] fp32 confidence weights: w_h (d entries) then w_e (rank entries).
+ *   conf_b, conf_logit_scale   scalar bias and raw-logit scale of the confidence head.
+ *   conf_temp [gamma] fp32 per-position temperatures (> 0).
+ *   temperature  sampling temperature T > 0.
+ *   x0        [R] int32 anchor tokens in [0,V).
+ *   req_id    [R] int64 request keys of the random stream.
+ *   seed, round  random-stream key and round index.
+ * Outputs ([R,gamma] each): x_out int32 tokens; logq_out, lse_out, conf_out fp32.
+ * Limits: 1 <= R, 1 <= gamma <= 64, 1 <= V, rank >= 1, d >= 0.  The bf16 tensor-core
+ *   path needs rank % 64 == 0 and rank <= 256 and V % 8 == 0; other bf16 shapes run
+ *   on CUDA cores.
+ * ---------------------------------------------------------------------------------- */
+DSPARK_API size_t dspark_markov_draft_workspace_size(int R, int gamma, int V, int rank, int d, int dtype_w);
+
+DSPARK_API dspark_status dspark_markov_draft(
+    int R, int gamma, int V, int rank, int d, int dtype_u, int dtype_w, int dtype_h,
+    const void* U, const void* W1, const void* W2, const void* h, const float* conf_w,
+    float conf_b, float conf_logit_scale, const float* conf_temp, float temperature,
+    const int32_t* x0, const int64_t* req_id, uint64_t seed, uint64_t round,
+    int32_t* x_out, float* logq_out, float* lse_out, float* conf_out,
+    void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * Stage 2: confidence scheduler.
+ *
+ * Defines (DSpark 精读 §4; mkdocs.reaper.mx §3.3; numb3r33 blog "Scheduler objective",
+ * "Greedy prefix allocation", "Async scheduler in practice"; vllmbangkok §4.2.2):
+ *   a[r,j] = prod_{i<=j} conf[r,i]   (binary64, multiplied left to right)
+ *   candidates (r,j) sorted by a desc, then j asc, then r asc; admitting the first n
+ *   gives B(n) = R + n verify tokens and tau(n) = R + sum of the first n a's;
+ *   Theta(n) = tau(n) * sps[B(n)].
+ *   mode DSPARK_EARLY_STOP  n* = first n with Theta(n+1) <= Theta(n) (else R*gamma)
+ *        DSPARK_FULL_SEARCH n* = argmax_n Theta(n), smallest n on ties
+ *        DSPARK_CAPACITY_K  K = the full-search n* computed on conf_hist (the stale
+ *                           confidences); n* = min(K, R*gamma) on the current order
+ *        DSPARK_FIXED       ell_r = min(fixed_len, gamma) for every r
+ *   ell_out[r] = number of admitted candidates of request r (always a prefix 1..ell_r),
+ *   B_out = R + n*, tau_out = tau(n*).
+ * Arguments
+ *   conf      [R,gamma] fp32 conditional confidences (stage 1's conf_out).
+ *   sps       [sps_len] fp64 profiled target steps/s indexed by B; sps_len >= R*(gamma+1)+1.
+ *   conf_hist [R,gamma] fp32, required for DSPARK_CAPACITY_K, ignored otherwise.
+ *   fixed_len used by DSPARK_FIXED only (clamped to [0,gamma]).
+ * Outputs: ell_out [R] int32, B_out [1] int32, tau_out [1] fp64.
+ * Limits: 1 <= R, 1 <= gamma <= 64, R*gamma <= 8192.
+ * ---------------------------------------------------------------------------------- */
+DSPARK_API size_t dspark_schedule_workspace_size(int R, int gamma);
+
+DSPARK_API dspark_status dspark_schedule(
+    int R, int gamma, const float* conf, const double* sps, int sps_len, int mode,
+    const float* conf_hist, int fixed_len, int32_t* ell_out, int32_t* B_out, double* tau_out,
+    void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * Stage 3: exact speculative-sampling verification.
+ *
+ * Defines (numb3r33 blog "One-token exactness", "Why only the longest accepted prefix
+ * survives", "Prefix survival and accepted length"):
+ *   for j = 1..ell[r]: p = softmax(target[r,j,:]/T) (row j-1 of target, 0-based);
+ *     accept x_j iff u_j < p(x_j) / q_j(x_j), q_j(x_j) = exp(logq[r,j]), u_j from
+ *     stream 1 at position j; stop at the first rejection.  n_acc = accepted count.
+ *   if n_acc < ell[r]: j* = n_acc + 1; q = exp(z - lse_q[r,j*]) with z the draft logits
+ *     of position j* recomputed from U, W1[x_{j*-1}], W2 (x_0 = x0[r]);
+ *     p = softmax(target row j*-1 / T); y = argmax over {v : p_v > q_v} of
+ *     ln(p_v - q_v) + g_v (stream 2, position j*): a draw from (p - q)+ normalised.
+ *     If no p_v > q_v (possible only through rounding), y = argmax_v ln p_v + g_v.
+ *   else: bonus y = argmax_v target[r,ell,v]/T + g_v (stream 2, position ell+1).
+ *   tokens_out[r,:] = x_1..x_{n_acc}, y, then -1 padding; n_out[r] = n_acc + 1.
+ * Arguments
+ *   target    [R,gamma+1,V] target logits (dtype_t).
+ *   U, W1, W2 as in stage 1 (for the residual recomputation).
+ *   x0 [R], x [R,gamma] int32; logq, lse_q [R,gamma] fp32 (stage 1 outputs);
+ *   ell [R] int32 in [0,gamma] (stage 2 output).
+ * Outputs: n_acc_out [R] int32, tokens_out [R,gamma+1] int32, n_out [R] int32.
+ * Limits: as stage 1, plus target rows of V elements.
+ * ---------------------------------------------------------------------------------- */
+DSPARK_API size_t dspark_verify_workspace_size(int R, int gamma, int V, int rank, int dtype_w);
+
+DSPARK_API dspark_status dspark_verify(
+    int R, int gamma, int V, int rank, int dtype_t, int dtype_u, int dtype_w,
+    const void* target, const void* U, const void* W1, const void* W2,
+    const int32_t* x0, const int32_t* x, const float* logq, const float* lse_q,
+    const int32_t* ell, float temperature, const int64_t* req_id, uint64_t seed, uint64_t round,
+    int32_t* n_acc_out, int32_t* tokens_out, int32_t* n_out,
+    void* workspace, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_H */

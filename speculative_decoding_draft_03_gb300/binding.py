@@ -1,0 +1,237 @@
+"""Thin ctypes binding of ``libdspark.so`` (argument marshalling only).
+
+Every step of the path runs in the library's CUDA kernels; this module checks tensor
+placement/dtypes, passes ``data_ptr()``s and the current CUDA stream, and owns the
+caller-side buffers (outputs and workspaces) through PyTorch.  If the library is
+missing this module raises at import: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+F32, BF16 = 0, 1
+EARLY_STOP, FULL_SEARCH, CAPACITY_K, FIXED = 0, 1, 2, 3
+_DT = {torch.float32: F32, torch.bfloat16: BF16}
+
+
+class DSparkError(RuntimeError):
+    pass
+
+
+def _load_library():
+    path = _build.LIB
+    if not os.path.exists(path):
+        raise DSparkError(f"libdspark.so is not built ({path}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    P, i32, u64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_float, ctypes.c_size_t
+    lib.dspark_status_string.restype = ctypes.c_char_p
+    lib.dspark_status_string.argtypes = [i32]
+    lib.dspark_last_error_message.restype = ctypes.c_char_p
+    lib.dspark_workspace_status.argtypes = [P, i32, P, P]
+    lib.dspark_markov_draft_workspace_size.restype = sz
+    lib.dspark_markov_draft_workspace_size.argtypes = [i32] * 5 + [i32]
+    lib.dspark_markov_draft.argtypes = ([i32] * 8 + [P] * 4 + [P, f32, f32, P, f32, P, P, u64, u64]
+                                        + [P] * 4 + [P, sz, P])
+    lib.dspark_schedule_workspace_size.restype = sz
+    lib.dspark_schedule_workspace_size.argtypes = [i32, i32]
+    lib.dspark_schedule.argtypes = [i32, i32, P, P, i32, i32, P, i32, P, P, P, P, sz, P]
+    lib.dspark_verify_workspace_size.restype = sz
+    lib.dspark_verify_workspace_size.argtypes = [i32] * 5
+    lib.dspark_verify.argtypes = ([i32] * 7 + [P] * 4 + [P] * 5 + [f32, P, u64, u64] + [P] * 3 + [P, sz, P])
+    for fn in ("dspark_markov_draft", "dspark_schedule", "dspark_verify", "dspark_workspace_status"):
+        getattr(lib, fn).restype = i32
+    return lib
+
+
+lib = _load_library()
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        name = lib.dspark_status_string(status).decode()
+        msg = lib.dspark_last_error_message().decode()
+        raise DSparkError(f"{what}: {name}: {msg}")
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _cuda(t, name, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise DSparkError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise DSparkError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise DSparkError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def _dt(t, name):
+    if t.dtype not in _DT:
+        raise DSparkError(f"{name} must be float32 or bfloat16, got {t.dtype}")
+    return _DT[t.dtype]
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def workspace(nbytes: int, device) -> torch.Tensor:
+    """A caller-owned, 256-byte aligned device workspace whose status word starts at 0."""
+    ws = torch.zeros(max(256, int(nbytes)) + 256, dtype=torch.uint8, device=device)
+    off = (-ws.data_ptr()) % 256
+    return ws[off:off + max(256, int(nbytes))]
+
+
+def draft_workspace_size(R, gamma, V, rank, d, w_dtype) -> int:
+    return int(lib.dspark_markov_draft_workspace_size(R, gamma, V, rank, d, _DT[w_dtype]))
+
+
+def schedule_workspace_size(R, gamma) -> int:
+    return int(lib.dspark_schedule_workspace_size(R, gamma))
+
+
+def verify_workspace_size(R, gamma, V, rank, w_dtype) -> int:
+    return int(lib.dspark_verify_workspace_size(R, gamma, V, rank, _DT[w_dtype]))
+
+
+def markov_draft(U, W1, W2, h, conf_w, conf_b, conf_logit_scale, conf_temp, temperature, x0, req_id,
+                 seed, rnd, out=None, ws=None, stream=None):
+    """Stage 1 (dspark_markov_draft).  Returns dict x, logq, lse, conf (device tensors)."""
+    R, gamma, V = U.shape
+    rank = W1.shape[1]
+    d = h.shape[2] if h is not None else 0
+    dev = U.device
+    for t, n in ((U, "U"), (W1, "W1"), (W2, "W2")):
+        _cuda(t, n)
+    if h is not None:
+        _cuda(h, "h")
+    _cuda(conf_w, "conf_w", torch.float32)
+    _cuda(conf_temp, "conf_temp", torch.float32)
+    _cuda(x0, "x0", torch.int32)
+    _cuda(req_id, "req_id", torch.int64)
+    if W1.dtype != W2.dtype:
+        raise DSparkError("W1 and W2 must share a dtype")
+    if out is None:
+        out = dict(x=torch.empty((R, gamma), dtype=torch.int32, device=dev),
+                   logq=torch.empty((R, gamma), dtype=torch.float32, device=dev),
+                   lse=torch.empty((R, gamma), dtype=torch.float32, device=dev),
+                   conf=torch.empty((R, gamma), dtype=torch.float32, device=dev))
+    if ws is None:
+        ws = workspace(draft_workspace_size(R, gamma, V, rank, d, W1.dtype), dev)
+    st = lib.dspark_markov_draft(R, gamma, V, rank, d, _dt(U, "U"), _dt(W1, "W1"),
+                                 _dt(h, "h") if h is not None else F32,
+                                 _p(U), _p(W1), _p(W2), _p(h), _p(conf_w), float(conf_b),
+                                 float(conf_logit_scale), _p(conf_temp), float(temperature), _p(x0),
+                                 _p(req_id), int(seed), int(rnd), _p(out["x"]), _p(out["logq"]),
+                                 _p(out["lse"]), _p(out["conf"]), _p(ws), ws.numel(), _stream(stream))
+    _check(st, "dspark_markov_draft")
+    return out
+
+
+def schedule(conf, sps, mode, conf_hist=None, fixed_len=0, out=None, ws=None, stream=None):
+    """Stage 2 (dspark_schedule).  Returns dict ell [R] int32, B [1] int32, tau [1] float64."""
+    _cuda(conf, "conf", torch.float32)
+    R, gamma = conf.shape
+    dev = conf.device
+    if sps is not None:
+        _cuda(sps, "sps", torch.float64)
+    if conf_hist is not None:
+        _cuda(conf_hist, "conf_hist", torch.float32)
+    if out is None:
+        out = dict(ell=torch.empty(R, dtype=torch.int32, device=dev),
+                   B=torch.empty(1, dtype=torch.int32, device=dev),
+                   tau=torch.empty(1, dtype=torch.float64, device=dev))
+    if ws is None:
+        ws = workspace(schedule_workspace_size(R, gamma), dev)
+    st = lib.dspark_schedule(R, gamma, _p(conf), _p(sps), 0 if sps is None else sps.numel(), int(mode),
+                             _p(conf_hist), int(fixed_len), _p(out["ell"]), _p(out["B"]), _p(out["tau"]),
+                             _p(ws), ws.numel(), _stream(stream))
+    _check(st, "dspark_schedule")
+    return out
+
+
+def verify(target, U, W1, W2, x0, x, logq, lse_q, ell, temperature, req_id, seed, rnd, out=None,
+           ws=None, stream=None):
+    """Stage 3 (dspark_verify).  Returns dict n_acc [R], tokens [R,gamma+1], n_out [R]."""
+    R, g1, V = target.shape
+    gamma = g1 - 1
+    rank = W1.shape[1]
+    dev = target.device
+    for t, n in ((target, "target"), (U, "U"), (W1, "W1"), (W2, "W2")):
+        _cuda(t, n)
+    _cuda(x0, "x0", torch.int32)
+    _cuda(x, "x", torch.int32)
+    _cuda(logq, "logq", torch.float32)
+    _cuda(lse_q, "lse_q", torch.float32)
+    _cuda(ell, "ell", torch.int32)
+    _cuda(req_id, "req_id", torch.int64)
+    if out is None:
+        out = dict(n_acc=torch.empty(R, dtype=torch.int32, device=dev),
+                   tokens=torch.empty((R, gamma + 1), dtype=torch.int32, device=dev),
+                   n_out=torch.empty(R, dtype=torch.int32, device=dev))
+    if ws is None:
+        ws = workspace(verify_workspace_size(R, gamma, V, rank, W1.dtype), dev)
+    st = lib.dspark_verify(R, gamma, V, rank, _dt(target, "target"), _dt(U, "U"), _dt(W1, "W1"),
+                           _p(target), _p(U), _p(W1), _p(W2), _p(x0), _p(x), _p(logq), _p(lse_q), _p(ell),
+                           float(temperature), _p(req_id), int(seed), int(rnd), _p(out["n_acc"]),
+                           _p(out["tokens"]), _p(out["n_out"]), _p(ws), ws.numel(), _stream(stream))
+    _check(st, "dspark_verify")
+    return out
+
+
+def device_status(ws, reset=False, stream=None) -> int:
+    """The workspace's device status word (0 OK, 5 a bounded wait gave up, 1 bad device data)."""
+    val = ctypes.c_int(0)
+    _check(lib.dspark_workspace_status(_p(ws), int(reset), ctypes.byref(val), _stream(stream)),
+           "dspark_workspace_status")
+    return int(val.value)
+
+
+class Round:
+    """One DSpark round (draft -> schedule -> verify) over a fixed workload shape, with
+    every output and workspace allocated once, so that repeated rounds (and CUDA-graph
+    capture) launch kernels only."""
+
+    def __init__(self, w: dict):
+        self.w = w
+        R, gamma, V, rank, d = w["R"], w["gamma"], w["V"], w["rank"], w["d"]
+        dev = w["U"].device
+        self.draft_out = dict(x=torch.empty((R, gamma), dtype=torch.int32, device=dev),
+                              logq=torch.empty((R, gamma), dtype=torch.float32, device=dev),
+                              lse=torch.empty((R, gamma), dtype=torch.float32, device=dev),
+                              conf=torch.empty((R, gamma), dtype=torch.float32, device=dev))
+        self.sched_out = dict(ell=torch.empty(R, dtype=torch.int32, device=dev),
+                              B=torch.empty(1, dtype=torch.int32, device=dev),
+                              tau=torch.empty(1, dtype=torch.float64, device=dev))
+        self.verify_out = dict(n_acc=torch.empty(R, dtype=torch.int32, device=dev),
+                               tokens=torch.empty((R, gamma + 1), dtype=torch.int32, device=dev),
+                               n_out=torch.empty(R, dtype=torch.int32, device=dev))
+        self.ws_draft = workspace(draft_workspace_size(R, gamma, V, rank, d, w["W1"].dtype), dev)
+        self.ws_sched = workspace(schedule_workspace_size(R, gamma), dev)
+        self.ws_verify = workspace(verify_workspace_size(R, gamma, V, rank, w["W1"].dtype), dev)
+        self.x0 = w["x0"].clone()
+
+    def run(self, rnd=0, x0=None, stream=None):
+        w = self.w
+        x0 = self.x0 if x0 is None else x0
+        d = markov_draft(w["U"], w["W1"], w["W2"], w["h"], w["conf_w"], w["conf_b"], w["conf_logit_scale"],
+                         w["conf_temp"], w["temperature"], x0, w["req_id"], w["seed"], rnd,
+                         out=self.draft_out, ws=self.ws_draft, stream=stream)
+        s = schedule(d["conf"], w["sps"], w["mode"], w.get("conf_hist"), w.get("fixed_len", 0),
+                     out=self.sched_out, ws=self.ws_sched, stream=stream)
+        v = verify(w["target"], w["U"], w["W1"], w["W2"], x0, d["x"], d["logq"], d["lse"], s["ell"],
+                   w["temperature"], w["req_id"], w["seed"], rnd, out=self.verify_out, ws=self.ws_verify,
+                   stream=stream)
+        return d, s, v
+
+    def status(self) -> int:
+        codes = [device_status(ws) for ws in (self.ws_draft, self.ws_sched, self.ws_verify)]
+        return max(codes)

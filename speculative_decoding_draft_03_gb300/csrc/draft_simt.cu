@@ -1,0 +1,249 @@
+// draft_simt.cu — Markov-head draft stage: the parts that run on CUDA cores.
+//
+//   conf_hdot      s_h[r,k] = w_h . h[r,k,:]        (confidence head, hidden-state part)
+//   draft_prepare  for position k: x_{k-1} -> gathered factor row W1[x_{k-1},:] (the
+//                  A operand of the bias contraction) and the confidence
+//                  c_k = sigmoid(kappa (s_h + w_e . W1[x_{k-1}] + b) / T_k)
+//   draft_step_simt  fp32 (or small bf16) path of one draft position: bias row
+//                  W1[x_{k-1}] W2 on CUDA cores, z = (U_k + bias)/T, online softmax
+//                  statistics and Gumbel-max draw, one partial record per
+//                  (vocabulary chunk, request)
+//   draft_combine  merges the partials of a position into x_k, lse_k, logq_k and
+//                  prepares position k+1.
+//
+// Method: numb3r33 blog "DSpark: confidence-scheduled speculative decoding", sections
+// "Markov sequential head" (p_k(v|x_{k-1}) = softmax(U_k(v) + W1[x_{k-1}] W2)) and
+// "Confidence head"; DSpark 精读 §2 and §4 (confidence on [h_k ; W1[x_{k-1}]]).
+#include "dspark_common.cuh"
+#include "dspark_internal.h"
+
+namespace dspark {
+
+// One warp per (r,k) row of h.
+__global__ void conf_hdot_kernel(int rows, int d, int dtype_h, const void* __restrict__ h,
+                                 const float* __restrict__ w_h, float* __restrict__ s_h) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= rows) return;
+  float acc = 0.f;
+  const size_t base = (size_t)warp * d;
+  if (dtype_h == DSPARK_BF16 && (d % 8) == 0) {
+    const uint4* hp = reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned short*>(h) + base);
+    for (int c = lane; c < d / 8; c += 32) {
+      const uint4 q = __ldg(hp + c);
+      const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc = fmaf(__ldg(w_h + c * 8 + 2 * e), bf16_bits_to_float(wd[e] & 0xFFFFu), acc);
+        acc = fmaf(__ldg(w_h + c * 8 + 2 * e + 1), bf16_bits_to_float(wd[e] >> 16), acc);
+      }
+    }
+  } else {
+    for (int i = lane; i < d; i += 32) acc = fmaf(__ldg(w_h + i), load_elem(h, dtype_h, base + i), acc);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) s_h[warp] = acc;
+}
+
+// Gather W1[x_prev] into W1g[r] and write c_k; executed by one full warp.
+__device__ __forceinline__ void prepare_position(const DraftArgs& a, int r, int k, int x_prev, int lane) {
+  const size_t src = (size_t)x_prev * a.rank;
+  const size_t dst = (size_t)r * a.rank;
+  float acc = 0.f;
+  const float* w_e = a.conf_w + a.d;
+  if (a.dtype_w == DSPARK_BF16) {
+    const unsigned short* w1 = reinterpret_cast<const unsigned short*>(a.W1);
+    unsigned short* g = reinterpret_cast<unsigned short*>(a.W1g);
+    for (int i = lane; i < a.rank; i += 32) {
+      const unsigned short b = __ldg(w1 + src + i);
+      g[dst + i] = b;
+      acc = fmaf(__ldg(w_e + i), bf16_bits_to_float(b), acc);
+    }
+  } else {
+    const float* w1 = reinterpret_cast<const float*>(a.W1);
+    float* g = reinterpret_cast<float*>(a.W1g);
+    for (int i = lane; i < a.rank; i += 32) {
+      const float b = __ldg(w1 + src + i);
+      g[dst + i] = b;
+      acc = fmaf(__ldg(w_e + i), b, acc);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) {
+    const size_t row = (size_t)r * a.gamma + (k - 1);
+    const float logit = a.conf_scale * (a.s_h[row] + acc + a.conf_b);
+    a.conf_out[row] = sigmoidf_dev(logit / __ldg(a.conf_temp + (k - 1)));
+  }
+}
+
+__global__ void draft_prepare_kernel(DraftArgs a, int k) {
+  const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (r >= a.R) return;
+  const int raw = (k == 1) ? __ldg(a.x0 + r) : a.x_out[(size_t)r * a.gamma + (k - 2)];
+  const int x_prev = checked_token(raw, a.V, a.status, 1);
+  prepare_position(a, r, k, x_prev, lane);
+}
+
+// ---------------------------------------------------------------------------------
+// CUDA-core draft step.  blockIdx.x: vocabulary chunk of kSimtGroups*4*blockDim.x ids;
+// blockIdx.y: block of RB requests.  Each thread owns groups of 4 consecutive ids so
+// that one Philox block serves its 4 elements of a request row.
+// ---------------------------------------------------------------------------------
+template <int RB>
+__global__ void __launch_bounds__(kSimtThreads) draft_step_simt_kernel(DraftArgs a, int k) {
+  extern __shared__ float w1s[];  // [RB][rank]
+  const int r0 = blockIdx.y * RB;
+  for (int i = threadIdx.x; i < RB * a.rank; i += blockDim.x) {
+    const int rr = i / a.rank, c = i % a.rank;
+    const int r = r0 + rr;
+    w1s[i] = (r < a.R) ? load_elem(a.W1g, a.dtype_w, (size_t)r * a.rank + c) : 0.f;
+  }
+  __syncthreads();
+
+  Stats st[RB];
+  RngRow rng[RB];
+#pragma unroll
+  for (int rr = 0; rr < RB; ++rr) {
+    st[rr] = stats_empty();
+    const int r = min(r0 + rr, a.R - 1);
+    rng[rr] = rng_row(a.seed, __ldg(a.req_id + r), a.round, kStreamDraft, (uint32_t)k);
+  }
+  const int groups_total = (a.V + 3) / 4;
+  const int g0 = blockIdx.x * kSimtGroups * blockDim.x;
+  for (int t = 0; t < kSimtGroups; ++t) {
+    const int g = g0 + t * blockDim.x + threadIdx.x;
+    if (g >= groups_total) break;
+    float acc[RB][4];
+#pragma unroll
+    for (int rr = 0; rr < RB; ++rr)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[rr][e] = 0.f;
+    for (int i = 0; i < a.rank; ++i) {
+      float w2[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int v = 4 * g + e;
+        w2[e] = (v < a.V) ? load_elem(a.W2, a.dtype_w, (size_t)i * a.V + v) : 0.f;
+      }
+#pragma unroll
+      for (int rr = 0; rr < RB; ++rr) {
+        const float w1 = w1s[rr * a.rank + i];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[rr][e] = fmaf(w1, w2[e], acc[rr][e]);
+      }
+    }
+#pragma unroll
+    for (int rr = 0; rr < RB; ++rr) {
+      const int r = r0 + rr;
+      if (r >= a.R) break;
+      const Philox4 bits = rng_chunk(rng[rr], (uint32_t)g);
+      const uint32_t wd[4] = {bits.x, bits.y, bits.z, bits.w};
+      const size_t urow = ((size_t)r * a.gamma + (k - 1)) * a.V;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int v = 4 * g + e;
+        if (v >= a.V) break;
+        const float z = (load_elem(a.U, a.dtype_u, urow + v) + acc[rr][e]) * a.inv_temp;
+        // online softmax statistics
+        if (z > st[rr].m) {
+          st[rr].s = st[rr].s * __expf(st[rr].m - z) + 1.f;
+          st[rr].m = z;
+        } else {
+          st[rr].s += __expf(z - st[rr].m);
+        }
+        // Gumbel-max: skip the draw when even the largest Gumbel cannot win
+        if (z + kGumbelMax >= st[rr].key || st[rr].idx < 0) {
+          const float key = z + gumbel_from_bits(wd[e]);
+          if (key > st[rr].key || st[rr].idx < 0) {
+            st[rr].key = key;
+            st[rr].idx = v;
+            st[rr].zsel = z;
+          }
+        }
+      }
+    }
+  }
+  // block reduction per request: warp shuffle, then across warps through shared memory
+  __shared__ Partial red[kSimtThreads / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int rr = 0; rr < RB; ++rr) {
+    const int r = r0 + rr;
+    Stats w = warp_reduce_stats(st[rr]);
+    if (lane == 0) red[warp] = to_partial(w);
+    __syncthreads();
+    if (warp == 0) {
+      Stats b = (lane < (int)(blockDim.x >> 5)) ? from_partial(red[lane]) : stats_empty();
+      b = warp_reduce_stats(b);
+      if (lane == 0 && r < a.R) a.partials[(size_t)blockIdx.x * a.R + r] = to_partial(b);
+    }
+    __syncthreads();
+  }
+}
+
+// One warp per request: merge npart partials of position k; then prepare position k+1.
+__global__ void draft_combine_kernel(DraftArgs a, int k, int npart) {
+  const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (r >= a.R) return;
+  Stats st = stats_empty();
+  for (int p = lane; p < npart; p += 32) stats_merge(st, from_partial(a.partials[(size_t)p * a.R + r]));
+  st = warp_reduce_stats(st);
+  const int xk = st.idx;
+  if (lane == 0) {
+    const size_t row = (size_t)r * a.gamma + (k - 1);
+    const float lse = st.m + logf(st.s);
+    a.x_out[row] = xk;
+    a.lse_out[row] = lse;
+    a.logq_out[row] = st.zsel - lse;
+  }
+  if (k < a.gamma) prepare_position(a, r, k + 1, checked_token(xk, a.V, a.status, 2), lane);
+}
+
+// ---------------------------------------------------------------------------------
+// Host-side launchers
+// ---------------------------------------------------------------------------------
+cudaError_t launch_conf_hdot(const DraftArgs& a, cudaStream_t s) {
+  const int rows = a.R * a.gamma;
+  const int threads = 256;
+  const int blocks = (rows * 32 + threads - 1) / threads;
+  conf_hdot_kernel<<<blocks, threads, 0, s>>>(rows, a.d, a.dtype_h, a.h, a.conf_w, a.s_h);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_draft_prepare(const DraftArgs& a, int k, cudaStream_t s) {
+  const int threads = 256;
+  const int blocks = (a.R * 32 + threads - 1) / threads;
+  draft_prepare_kernel<<<blocks, threads, 0, s>>>(a, k);
+  return cudaGetLastError();
+}
+
+int simt_num_chunks(int V) {
+  const int groups = (V + 3) / 4;
+  const int per = kSimtGroups * kSimtThreads;
+  return (groups + per - 1) / per;
+}
+
+cudaError_t launch_draft_step_simt(const DraftArgs& a, int k, cudaStream_t s) {
+  dim3 grid(simt_num_chunks(a.V), (a.R + kSimtRB - 1) / kSimtRB);
+  const size_t smem = sizeof(float) * kSimtRB * a.rank;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(draft_step_simt_kernel<kSimtRB>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  draft_step_simt_kernel<kSimtRB><<<grid, kSimtThreads, smem, s>>>(a, k);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_draft_combine(const DraftArgs& a, int k, int npart, cudaStream_t s) {
+  const int threads = 256;
+  const int blocks = (a.R * 32 + threads - 1) / threads;
+  draft_combine_kernel<<<blocks, threads, 0, s>>>(a, k, npart);
+  return cudaGetLastError();
+}
+
+}  // namespace dspark

@@ -1,0 +1,327 @@
+// dspark_api.cu — the C ABI: argument validation, workspace layout, stream-ordered
+// launches.  No device memory is allocated here; no call synchronises the host except
+// dspark_workspace_status().
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "dspark_common.cuh"
+#include "dspark_internal.h"
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+dspark_status fail(dspark_status code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+dspark_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(DSPARK_CUDA_ERROR, "%s: %s", what, cudaGetErrorString(e));
+}
+
+size_t elem_size(int dtype) { return dtype == DSPARK_BF16 ? 2 : 4; }
+bool valid_dtype(int d) { return d == DSPARK_F32 || d == DSPARK_BF16; }
+
+constexpr int kMaxGamma = 64;
+constexpr int kVerifyChunk = 8192;
+
+struct DraftLayout {
+  size_t s_h, W1g, partials, total;
+  int npart;
+};
+
+DraftLayout draft_layout(int R, int gamma, int V, int rank, int dtype_w) {
+  using namespace dspark;
+  DraftLayout L;
+  size_t off = 256;  // status block
+  L.s_h = off;
+  off += align256(sizeof(float) * (size_t)R * gamma);
+  L.W1g = off;
+  off += align256(elem_size(dtype_w) * (size_t)round_up_rows(R) * rank);
+  L.npart = draft_num_partials(V, rank, dtype_w);
+  L.partials = off;
+  off += align256((size_t)32 * L.npart * R);
+  L.total = off;
+  return L;
+}
+
+struct VerifyLayout {
+  size_t counters, row_req, row_t, row_base, row_part, lse_t, jstar, res_list, W1g, res_part, res_part2, total;
+  int nchunk, npart;
+};
+
+VerifyLayout verify_layout(int R, int gamma, int V, int rank, int dtype_w) {
+  using namespace dspark;
+  VerifyLayout L;
+  const size_t rows = (size_t)R * (gamma + 1);
+  L.nchunk = (V + kVerifyChunk - 1) / kVerifyChunk;
+  L.npart = simt_num_chunks(V);
+  size_t off = 256;
+  L.counters = off;
+  off += 256;
+  L.row_req = off;
+  off += align256(4 * rows);
+  L.row_t = off;
+  off += align256(4 * rows);
+  L.row_base = off;
+  off += align256(4 * (size_t)R);
+  L.row_part = off;
+  off += align256(32 * rows * L.nchunk);
+  L.lse_t = off;
+  off += align256(4 * (size_t)R);
+  L.jstar = off;
+  off += align256(4 * (size_t)R);
+  L.res_list = off;
+  off += align256(4 * (size_t)R);
+  L.W1g = off;
+  off += align256(elem_size(dtype_w) * (size_t)round_up_rows(R) * rank);
+  L.res_part = off;
+  off += align256((size_t)32 * L.npart * R);
+  L.res_part2 = off;
+  off += align256((size_t)32 * L.npart * R);
+  L.total = off;
+  return L;
+}
+
+#define CHECK_PTR(p)                                                              \
+  do {                                                                            \
+    if ((p) == nullptr) return fail(DSPARK_INVALID_ARG, "null pointer: %s", #p); \
+  } while (0)
+
+bool aligned256(const void* p) { return ((uintptr_t)p & 255u) == 0; }
+
+}  // namespace
+
+namespace dspark {
+
+int round_up_rows(int R) { return ((R + 127) / 128) * 128; }
+
+int draft_num_partials(int V, int rank, int dtype_w) {
+  const int simt = simt_num_chunks(V);
+  if (tc_supported(V, rank, dtype_w)) {
+    const int tc = tc_grid_size();
+    return simt > tc ? simt : tc;
+  }
+  return simt;
+}
+
+}  // namespace dspark
+
+extern "C" {
+
+const char* dspark_status_string(int status) {
+  switch (status) {
+    case DSPARK_OK: return "DSPARK_OK";
+    case DSPARK_INVALID_ARG: return "DSPARK_INVALID_ARG";
+    case DSPARK_UNSUPPORTED_SHAPE: return "DSPARK_UNSUPPORTED_SHAPE";
+    case DSPARK_WORKSPACE_TOO_SMALL: return "DSPARK_WORKSPACE_TOO_SMALL";
+    case DSPARK_CUDA_ERROR: return "DSPARK_CUDA_ERROR";
+    case DSPARK_TIMEOUT: return "DSPARK_TIMEOUT";
+    default: return "DSPARK_UNKNOWN_STATUS";
+  }
+}
+
+const char* dspark_last_error_message(void) { return g_msg; }
+
+dspark_status dspark_workspace_status(void* workspace, int reset, int* status, void* stream) {
+  CHECK_PTR(workspace);
+  CHECK_PTR(status);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  dspark::DeviceStatus host;
+  cudaError_t e = cudaMemcpyAsync(&host, workspace, sizeof host, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+  *status = host.code;
+  if (reset) {
+    e = cudaMemsetAsync(workspace, 0, sizeof host, s);
+    if (e != cudaSuccess) return cuda_fail(e, "resetting the device status word");
+  }
+  return DSPARK_OK;
+}
+
+size_t dspark_markov_draft_workspace_size(int R, int gamma, int V, int rank, int d, int dtype_w) {
+  (void)d;
+  if (R < 1 || gamma < 1 || V < 1 || rank < 1) return 0;
+  return draft_layout(R, gamma, V, rank, dtype_w).total;
+}
+
+dspark_status dspark_markov_draft(int R, int gamma, int V, int rank, int d, int dtype_u, int dtype_w, int dtype_h,
+                                  const void* U, const void* W1, const void* W2, const void* h,
+                                  const float* conf_w, float conf_b, float conf_logit_scale,
+                                  const float* conf_temp, float temperature, const int32_t* x0,
+                                  const int64_t* req_id, uint64_t seed, uint64_t round, int32_t* x_out,
+                                  float* logq_out, float* lse_out, float* conf_out, void* workspace,
+                                  size_t ws_bytes, void* stream) {
+  if (R < 1 || gamma < 1 || V < 1 || rank < 1 || d < 0)
+    return fail(DSPARK_INVALID_ARG, "sizes must be positive (R=%d gamma=%d V=%d rank=%d d=%d)", R, gamma, V, rank, d);
+  if (gamma > kMaxGamma) return fail(DSPARK_UNSUPPORTED_SHAPE, "gamma=%d exceeds %d", gamma, kMaxGamma);
+  if ((long long)V > (1ll << 30)) return fail(DSPARK_UNSUPPORTED_SHAPE, "V=%d too large", V);
+  if (!valid_dtype(dtype_u) || !valid_dtype(dtype_w) || !valid_dtype(dtype_h))
+    return fail(DSPARK_INVALID_ARG, "dtype codes must be DSPARK_F32 or DSPARK_BF16");
+  if (!(temperature > 0.f) || !isfinite(temperature))
+    return fail(DSPARK_INVALID_ARG, "temperature must be finite and > 0");
+  CHECK_PTR(U);
+  CHECK_PTR(W1);
+  CHECK_PTR(W2);
+  if (d > 0) CHECK_PTR(h);
+  CHECK_PTR(conf_w);
+  CHECK_PTR(conf_temp);
+  CHECK_PTR(x0);
+  CHECK_PTR(req_id);
+  CHECK_PTR(x_out);
+  CHECK_PTR(logq_out);
+  CHECK_PTR(lse_out);
+  CHECK_PTR(conf_out);
+  CHECK_PTR(workspace);
+  if (!aligned256(workspace)) return fail(DSPARK_INVALID_ARG, "workspace must be 256-byte aligned");
+  const DraftLayout L = draft_layout(R, gamma, V, rank, dtype_w);
+  if (ws_bytes < L.total)
+    return fail(DSPARK_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, L.total);
+
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  dspark::DraftArgs a;
+  a.R = R; a.gamma = gamma; a.V = V; a.rank = rank; a.d = d;
+  a.dtype_u = dtype_u; a.dtype_w = dtype_w; a.dtype_h = dtype_h;
+  a.U = U; a.W1 = W1; a.W2 = W2; a.h = h;
+  a.conf_w = conf_w; a.conf_b = conf_b; a.conf_scale = conf_logit_scale; a.conf_temp = conf_temp;
+  a.inv_temp = 1.0f / temperature;
+  a.x0 = x0; a.req_id = req_id; a.seed = seed; a.round = round;
+  a.x_out = x_out; a.logq_out = logq_out; a.lse_out = lse_out; a.conf_out = conf_out;
+  a.status = reinterpret_cast<dspark::DeviceStatus*>(ws);
+  a.s_h = reinterpret_cast<float*>(ws + L.s_h);
+  a.W1g = ws + L.W1g;
+  a.partials = reinterpret_cast<dspark::Partial*>(ws + L.partials);
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (d > 0) {
+    if ((e = dspark::launch_conf_hdot(a, s)) != cudaSuccess) return cuda_fail(e, "conf_hdot");
+  } else {
+    if ((e = cudaMemsetAsync(a.s_h, 0, sizeof(float) * (size_t)R * gamma, s)) != cudaSuccess)
+      return cuda_fail(e, "s_h clear");
+  }
+  if ((e = dspark::launch_draft_prepare(a, 1, s)) != cudaSuccess) return cuda_fail(e, "draft_prepare");
+  const bool tc = dspark::tc_supported(V, rank, dtype_w) != 0;
+  for (int k = 1; k <= gamma; ++k) {
+    int npart;
+    if (tc) {
+      if ((e = dspark::launch_draft_step_tc(a, k, s)) != cudaSuccess) return cuda_fail(e, "draft_step_tc");
+      npart = dspark::tc_grid_size();
+    } else {
+      if ((e = dspark::launch_draft_step_simt(a, k, s)) != cudaSuccess) return cuda_fail(e, "draft_step_simt");
+      npart = dspark::simt_num_chunks(V);
+    }
+    if ((e = dspark::launch_draft_combine(a, k, npart, s)) != cudaSuccess) return cuda_fail(e, "draft_combine");
+  }
+  return DSPARK_OK;
+}
+
+size_t dspark_schedule_workspace_size(int R, int gamma) {
+  (void)R;
+  (void)gamma;
+  return 256;
+}
+
+dspark_status dspark_schedule(int R, int gamma, const float* conf, const double* sps, int sps_len, int mode,
+                              const float* conf_hist, int fixed_len, int32_t* ell_out, int32_t* B_out,
+                              double* tau_out, void* workspace, size_t ws_bytes, void* stream) {
+  if (R < 1 || gamma < 1) return fail(DSPARK_INVALID_ARG, "sizes must be positive (R=%d gamma=%d)", R, gamma);
+  if (gamma > kMaxGamma) return fail(DSPARK_UNSUPPORTED_SHAPE, "gamma=%d exceeds %d", gamma, kMaxGamma);
+  if ((long long)R * gamma > 8192)
+    return fail(DSPARK_UNSUPPORTED_SHAPE, "R*gamma=%lld exceeds 8192 candidates", (long long)R * gamma);
+  if (mode < DSPARK_EARLY_STOP || mode > DSPARK_FIXED) return fail(DSPARK_INVALID_ARG, "unknown mode %d", mode);
+  CHECK_PTR(conf);
+  CHECK_PTR(ell_out);
+  CHECK_PTR(B_out);
+  CHECK_PTR(tau_out);
+  CHECK_PTR(workspace);
+  if (mode != DSPARK_FIXED) CHECK_PTR(sps);
+  if (mode == DSPARK_CAPACITY_K) CHECK_PTR(conf_hist);
+  if (mode != DSPARK_FIXED && (long long)sps_len < (long long)R * (gamma + 1) + 1)
+    return fail(DSPARK_INVALID_ARG, "sps_len=%d below R*(gamma+1)+1=%d", sps_len, R * (gamma + 1) + 1);
+  if (!aligned256(workspace)) return fail(DSPARK_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (ws_bytes < dspark_schedule_workspace_size(R, gamma))
+    return fail(DSPARK_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes,
+                dspark_schedule_workspace_size(R, gamma));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = dspark::launch_schedule(R, gamma, conf, sps, mode, conf_hist, fixed_len, ell_out, B_out, tau_out,
+                                          reinterpret_cast<dspark::DeviceStatus*>(workspace), s);
+  if (e != cudaSuccess) return cuda_fail(e, "schedule");
+  return DSPARK_OK;
+}
+
+size_t dspark_verify_workspace_size(int R, int gamma, int V, int rank, int dtype_w) {
+  if (R < 1 || gamma < 1 || V < 1 || rank < 1) return 0;
+  return verify_layout(R, gamma, V, rank, dtype_w).total;
+}
+
+dspark_status dspark_verify(int R, int gamma, int V, int rank, int dtype_t, int dtype_u, int dtype_w,
+                            const void* target, const void* U, const void* W1, const void* W2, const int32_t* x0,
+                            const int32_t* x, const float* logq, const float* lse_q, const int32_t* ell,
+                            float temperature, const int64_t* req_id, uint64_t seed, uint64_t round,
+                            int32_t* n_acc_out, int32_t* tokens_out, int32_t* n_out, void* workspace,
+                            size_t ws_bytes, void* stream) {
+  if (R < 1 || gamma < 1 || V < 1 || rank < 1)
+    return fail(DSPARK_INVALID_ARG, "sizes must be positive (R=%d gamma=%d V=%d rank=%d)", R, gamma, V, rank);
+  if (gamma > kMaxGamma) return fail(DSPARK_UNSUPPORTED_SHAPE, "gamma=%d exceeds %d", gamma, kMaxGamma);
+  if ((long long)V > (1ll << 30)) return fail(DSPARK_UNSUPPORTED_SHAPE, "V=%d too large", V);
+  if ((long long)R * (gamma + 1) > (1ll << 24)) return fail(DSPARK_UNSUPPORTED_SHAPE, "R*(gamma+1) too large");
+  if (!valid_dtype(dtype_t) || !valid_dtype(dtype_u) || !valid_dtype(dtype_w))
+    return fail(DSPARK_INVALID_ARG, "dtype codes must be DSPARK_F32 or DSPARK_BF16");
+  if (!(temperature > 0.f) || !isfinite(temperature))
+    return fail(DSPARK_INVALID_ARG, "temperature must be finite and > 0");
+  CHECK_PTR(target);
+  CHECK_PTR(U);
+  CHECK_PTR(W1);
+  CHECK_PTR(W2);
+  CHECK_PTR(x0);
+  CHECK_PTR(x);
+  CHECK_PTR(logq);
+  CHECK_PTR(lse_q);
+  CHECK_PTR(ell);
+  CHECK_PTR(req_id);
+  CHECK_PTR(n_acc_out);
+  CHECK_PTR(tokens_out);
+  CHECK_PTR(n_out);
+  CHECK_PTR(workspace);
+  if (!aligned256(workspace)) return fail(DSPARK_INVALID_ARG, "workspace must be 256-byte aligned");
+  const VerifyLayout L = verify_layout(R, gamma, V, rank, dtype_w);
+  if (ws_bytes < L.total) return fail(DSPARK_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, L.total);
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  dspark::VerifyArgs a;
+  a.R = R; a.gamma = gamma; a.V = V; a.rank = rank;
+  a.dtype_t = dtype_t; a.dtype_u = dtype_u; a.dtype_w = dtype_w;
+  a.target = target; a.U = U; a.W1 = W1; a.W2 = W2;
+  a.x0 = x0; a.x = x; a.logq = logq; a.lse_q = lse_q; a.ell = ell;
+  a.inv_temp = 1.0f / temperature;
+  a.req_id = req_id; a.seed = seed; a.round = round;
+  a.n_acc_out = n_acc_out; a.tokens_out = tokens_out; a.n_out = n_out;
+  a.status = reinterpret_cast<dspark::DeviceStatus*>(ws);
+  int* counters = reinterpret_cast<int*>(ws + L.counters);
+  a.n_rows = counters;
+  a.n_res = counters + 1;
+  a.row_req = reinterpret_cast<int*>(ws + L.row_req);
+  a.row_t = reinterpret_cast<int*>(ws + L.row_t);
+  a.row_base = reinterpret_cast<int*>(ws + L.row_base);
+  a.row_part = reinterpret_cast<dspark::Partial*>(ws + L.row_part);
+  a.nchunk = L.nchunk;
+  a.chunk = kVerifyChunk;
+  a.lse_t = reinterpret_cast<float*>(ws + L.lse_t);
+  a.jstar = reinterpret_cast<int*>(ws + L.jstar);
+  a.res_list = reinterpret_cast<int*>(ws + L.res_list);
+  a.W1g = ws + L.W1g;
+  a.res_part = reinterpret_cast<dspark::Partial*>(ws + L.res_part);
+  a.res_part2 = reinterpret_cast<dspark::Partial*>(ws + L.res_part2);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = dspark::launch_verify(a, s);
+  if (e != cudaSuccess) return cuda_fail(e, "verify");
+  return DSPARK_OK;
+}
+
+}  // extern "C"

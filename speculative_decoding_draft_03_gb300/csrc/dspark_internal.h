@@ -1,0 +1,102 @@
+// dspark_internal.h — argument blocks, workspace layouts and launcher declarations
+// shared by the library's translation units (host and device).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace dspark {
+
+struct Partial;
+struct DeviceStatus;
+
+constexpr int kSimtThreads = 256;
+constexpr int kSimtGroups = 4;   // groups of 4 vocabulary ids per thread per chunk
+constexpr int kSimtRB = 4;       // requests per CTA in the CUDA-core draft step
+
+// Everything one draft position needs (passed by value to kernels).
+struct DraftArgs {
+  int R, gamma, V, rank, d;
+  int dtype_u, dtype_w, dtype_h;
+  const void* U;
+  const void* W1;
+  const void* W2;
+  const void* h;
+  const float* conf_w;
+  float conf_b, conf_scale;
+  const float* conf_temp;
+  float inv_temp;
+  const int32_t* x0;
+  const int64_t* req_id;
+  uint64_t seed, round;
+  int32_t* x_out;
+  float* logq_out;
+  float* lse_out;
+  float* conf_out;
+  // workspace pieces
+  DeviceStatus* status;
+  float* s_h;        // [R*gamma]
+  void* W1g;         // [Rpad, rank] gathered factor rows (dtype_w)
+  Partial* partials; // [npart, R]
+};
+
+struct VerifyArgs {
+  int R, gamma, V, rank;
+  int dtype_t, dtype_u, dtype_w;
+  const void* target;
+  const void* U;
+  const void* W1;
+  const void* W2;
+  const int32_t* x0;
+  const int32_t* x;
+  const float* logq;
+  const float* lse_q;
+  const int32_t* ell;
+  float inv_temp;
+  const int64_t* req_id;
+  uint64_t seed, round;
+  int32_t* n_acc_out;
+  int32_t* tokens_out;
+  int32_t* n_out;
+  // workspace pieces
+  DeviceStatus* status;
+  int* n_rows;        // [1] number of verify rows
+  int* row_req;       // [R*(gamma+1)] request of compact row
+  int* row_t;         // [R*(gamma+1)] target row index (0-based) of compact row
+  int* row_base;      // [R] first compact row of request r
+  Partial* row_part;  // [R*(gamma+1), nchunk]
+  int nchunk;         // vocabulary chunks per row
+  int chunk;          // ids per chunk
+  float* lse_t;       // [R] target log-normaliser of the residual row
+  int* jstar;         // [R] residual position (0 = none)
+  int* res_list;      // [R] requests that need a residual draw
+  int* n_res;         // [1]
+  void* W1g;          // [Rpad, rank] gathered factor rows of the residual positions
+  Partial* res_part;  // [npart, R] residual partials: key = ln rho + g
+  Partial* res_part2; // [npart, R] fallback partials: key = ln p + g
+};
+
+// Workspace layout: a 256-byte status block, then 256-byte aligned pieces.
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+int simt_num_chunks(int V);
+int tc_supported(int V, int rank, int dtype_w);
+int tc_grid_size();
+int draft_num_partials(int V, int rank, int dtype_w);
+int round_up_rows(int R);
+
+cudaError_t launch_conf_hdot(const DraftArgs& a, cudaStream_t s);
+cudaError_t launch_draft_prepare(const DraftArgs& a, int k, cudaStream_t s);
+cudaError_t launch_draft_step_simt(const DraftArgs& a, int k, cudaStream_t s);
+cudaError_t launch_draft_combine(const DraftArgs& a, int k, int npart, cudaStream_t s);
+cudaError_t launch_draft_step_tc(const DraftArgs& a, int k, cudaStream_t s);
+
+cudaError_t launch_schedule(int R, int gamma, const float* conf, const double* sps, int mode,
+                            const float* conf_hist, int fixed_len, int32_t* ell_out, int32_t* B_out,
+                            double* tau_out, DeviceStatus* status, cudaStream_t s);
+size_t schedule_smem_bytes(int R, int gamma);
+
+cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s);
+
+}  // namespace dspark

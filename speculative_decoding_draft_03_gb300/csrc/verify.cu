@@ -1,0 +1,376 @@
+// verify.cu — exact speculative-sampling verification.
+//
+// Method (numb3r33 blog "DSpark: confidence-scheduled speculative decoding", sections
+// "One-token exactness", "Why only the longest accepted prefix survives", "Prefix
+// survival and accepted length"):
+//   accept x_j with probability min(1, p(x_j)/q(x_j)), stop at the first rejection,
+//   resample that position from (p - q)+ normalised, or emit a bonus token from the
+//   next target row when every verified draft survives.
+//
+// Kernels (one round, stream-ordered, no host synchronisation):
+//   verify_plan      ell -> compact list of the target rows that must be read:
+//                    rows 0..ell_r of request r (sum_r (ell_r + 1) rows)
+//   verify_rows      streams those rows once, coalesced and vectorised: per
+//                    (row, vocabulary chunk) the online (max, sum exp) of t/T and, on
+//                    row ell_r, the bonus Gumbel-max draw
+//   verify_accept    per request: row log-normalisers, the acceptance scan, the
+//                    bonus token, and the residual position j* when a draft is rejected
+//   residual_step    per rejected request: recompute the draft logits of position j*
+//                    (U + W1[x_{j*-1}] W2), q = exp(z - lse_q), p = exp(t/T - lse_t),
+//                    Gumbel-max of ln(p - q)+ (and of ln p, the rounding fallback)
+//   residual_combine merges the residual partials into the correction token.
+#include "dspark_common.cuh"
+#include "dspark_internal.h"
+
+namespace dspark {
+
+constexpr int kPlanThreads = 1024;
+constexpr int kRowThreads = 256;
+
+// verify length of request r, clamped to [0,gamma] (out-of-range values are reported)
+__device__ __forceinline__ int clamp_ell(const VerifyArgs& a, int r) {
+  const int l = __ldg(a.ell + r);
+  if (l < 0 || l > a.gamma) {
+    report_bad_input(a.status, 10);
+    return l < 0 ? 0 : a.gamma;
+  }
+  return l;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) verify_plan_kernel(VerifyArgs a) {
+  __shared__ int wsum[32];
+  const int per = (a.R + blockDim.x - 1) / blockDim.x;
+  const int lo = threadIdx.x * per, hi = min(lo + per, a.R);
+  int run = 0;
+  for (int r = lo; r < hi; ++r) run += clamp_ell(a, r) + 1;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = (lane < (int)(blockDim.x >> 5)) ? wsum[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += t;
+    }
+    wsum[lane] = w;
+  }
+  __syncthreads();
+  int base = (incl - run) + (warp > 0 ? wsum[warp - 1] : 0);
+  for (int r = lo; r < hi; ++r) {
+    const int n = clamp_ell(a, r) + 1;
+    a.row_base[r] = base;
+    for (int t = 0; t < n; ++t) {
+      a.row_req[base + t] = r;
+      a.row_t[base + t] = t;
+    }
+    a.jstar[r] = 0;
+    base += n;
+  }
+  if (threadIdx.x == blockDim.x - 1) *a.n_rows = base;
+  if (threadIdx.x == 0) *a.n_res = 0;
+}
+
+// Per (row, chunk): online (max, sum exp) of t/T; on the bonus row also the
+// Gumbel-max record of t/T + g (stream 2, position ell+1).
+__global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyArgs a) {
+  const int n_items = (*a.n_rows) * a.nchunk;
+  __shared__ Partial red[kRowThreads / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const int row = item / a.nchunk, c = item % a.nchunk;
+    const int r = a.row_req[row], t = a.row_t[row];
+    const bool bonus = (t == clamp_ell(a, r));
+    const size_t rbase = ((size_t)r * (a.gamma + 1) + t) * a.V;
+    const int v0 = c * a.chunk, v1 = min(v0 + a.chunk, a.V);
+    Stats st = stats_empty();
+    RngRow rng;
+    if (bonus) rng = rng_row(a.seed, __ldg(a.req_id + r), a.round, kStreamCorrect, (uint32_t)(t + 1));
+    // groups of 4 consecutive ids (chunk starts are multiples of 4)
+    for (int g = v0 / 4 + threadIdx.x; 4 * g < v1; g += blockDim.x) {
+      float x[4];
+      const int vb = 4 * g;
+      if (a.dtype_t == DSPARK_F32 && (a.V % 4) == 0) {
+        const float4 q = __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.target) + rbase) + g);
+        x[0] = q.x; x[1] = q.y; x[2] = q.z; x[3] = q.w;
+      } else if (a.dtype_t == DSPARK_BF16 && (a.V % 4) == 0) {
+        const uint2 q = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const unsigned short*>(a.target) + rbase) + g);
+        x[0] = bf16_bits_to_float(q.x & 0xFFFFu); x[1] = bf16_bits_to_float(q.x >> 16);
+        x[2] = bf16_bits_to_float(q.y & 0xFFFFu); x[3] = bf16_bits_to_float(q.y >> 16);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[e] = (vb + e < v1) ? load_elem(a.target, a.dtype_t, rbase + vb + e) : 0.f;
+      }
+      Philox4 bits;
+      if (bonus) bits = rng_chunk(rng, (uint32_t)g);
+      const uint32_t wd[4] = {bits.x, bits.y, bits.z, bits.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (vb + e >= v1) break;
+        const float z = x[e] * a.inv_temp;
+        if (z > st.m) {
+          st.s = st.s * __expf(st.m - z) + 1.f;
+          st.m = z;
+        } else {
+          st.s += __expf(z - st.m);
+        }
+        if (bonus && (z + kGumbelMax >= st.key || st.idx < 0)) {
+          const float key = z + gumbel_from_bits(wd[e]);
+          if (key > st.key || st.idx < 0) {
+            st.key = key;
+            st.idx = vb + e;
+            st.zsel = z;
+          }
+        }
+      }
+    }
+    Stats w = warp_reduce_stats(st);
+    if (lane == 0) red[warp] = to_partial(w);
+    __syncthreads();
+    if (warp == 0) {
+      Stats b = (lane < (int)(blockDim.x >> 5)) ? from_partial(red[lane]) : stats_empty();
+      b = warp_reduce_stats(b);
+      if (lane == 0) a.row_part[(size_t)row * a.nchunk + c] = to_partial(b);
+    }
+    __syncthreads();
+  }
+}
+
+// One warp per request.
+__global__ void verify_accept_kernel(VerifyArgs a) {
+  const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (r >= a.R) return;
+  const int ell = clamp_ell(a, r);
+  const int base = a.row_base[r];
+  const RngRow acc_rng = rng_row(a.seed, __ldg(a.req_id + r), a.round, kStreamAccept, 0u);
+  int n_acc = 0;
+  float lse_stop = 0.f;
+  for (int t = 0; t <= ell; ++t) {
+    Stats st = stats_empty();
+    for (int c = lane; c < a.nchunk; c += 32) stats_merge(st, from_partial(a.row_part[(size_t)(base + t) * a.nchunk + c]));
+    st = warp_reduce_stats(st);
+    const float lse = st.m + logf(st.s);
+    if (t == ell) {  // every verified draft accepted: bonus token from row ell
+      if (lane == 0) a.tokens_out[(size_t)r * (a.gamma + 1) + ell] = st.idx;
+      n_acc = ell;
+      break;
+    }
+    // acceptance test of draft j = t+1 against target row t
+    const int xj = checked_token(__ldg(a.x + (size_t)r * a.gamma + t), a.V, a.status, 11);
+    const float tx = load_elem(a.target, a.dtype_t, ((size_t)r * (a.gamma + 1) + t) * a.V + xj) * a.inv_temp;
+    const double lp = (double)tx - (double)lse;
+    const double ratio = exp(lp - (double)__ldg(a.logq + (size_t)r * a.gamma + t));
+    RngRow rr = acc_rng;
+    rr.c2 = (kStreamAccept << 24) | (uint32_t)(t + 1);
+    const double u = uniform_from_bits_f64(rng_chunk(rr, 0u).x);
+    if (u < ratio) {
+      n_acc = t + 1;
+      continue;
+    }
+    n_acc = t;
+    lse_stop = lse;
+    break;
+  }
+  const size_t orow = (size_t)r * (a.gamma + 1);
+  for (int j = lane; j <= a.gamma; j += 32) {
+    if (j < n_acc) a.tokens_out[orow + j] = __ldg(a.x + (size_t)r * a.gamma + j);
+    else if (j > n_acc) a.tokens_out[orow + j] = -1;
+  }
+  if (lane == 0) {
+    a.n_acc_out[r] = n_acc;
+    a.n_out[r] = n_acc + 1;
+  }
+  if (n_acc < ell) {
+    const int js = n_acc + 1;
+    if (lane == 0) {
+      a.jstar[r] = js;
+      a.lse_t[r] = lse_stop;
+      const int slot = atomicAdd(a.n_res, 1);
+      a.res_list[slot] = r;
+    }
+    // gather W1[x_{j*-1}] for the bias recomputation
+    const int xprev = checked_token((js == 1) ? __ldg(a.x0 + r) : __ldg(a.x + (size_t)r * a.gamma + (js - 2)),
+                                    a.V, a.status, 12);
+    const size_t src = (size_t)xprev * a.rank, dst = (size_t)r * a.rank;
+    if (a.dtype_w == DSPARK_BF16) {
+      const unsigned short* w1 = reinterpret_cast<const unsigned short*>(a.W1);
+      unsigned short* g = reinterpret_cast<unsigned short*>(a.W1g);
+      for (int i = lane; i < a.rank; i += 32) g[dst + i] = __ldg(w1 + src + i);
+    } else {
+      const float* w1 = reinterpret_cast<const float*>(a.W1);
+      float* g = reinterpret_cast<float*>(a.W1g);
+      for (int i = lane; i < a.rank; i += 32) g[dst + i] = __ldg(w1 + src + i);
+    }
+  }
+}
+
+// CUDA-core residual pass.  blockIdx.x: vocabulary chunk; blockIdx.y: request block.
+template <int RB>
+__global__ void __launch_bounds__(kSimtThreads) residual_step_simt_kernel(VerifyArgs a) {
+  extern __shared__ float w1s[];  // [RB][rank]
+  const int r0 = blockIdx.y * RB;
+  int js[RB];
+  bool any = false;
+#pragma unroll
+  for (int rr = 0; rr < RB; ++rr) {
+    const int r = r0 + rr;
+    js[rr] = (r < a.R) ? a.jstar[r] : 0;
+    any |= js[rr] > 0;
+  }
+  if (!any) {
+    if (threadIdx.x < RB) {
+      const int r = r0 + threadIdx.x;
+      if (r < a.R) {
+        a.res_part[(size_t)blockIdx.x * a.R + r] = to_partial(stats_empty());
+        a.res_part2[(size_t)blockIdx.x * a.R + r] = to_partial(stats_empty());
+      }
+    }
+    return;
+  }
+  for (int i = threadIdx.x; i < RB * a.rank; i += blockDim.x) {
+    const int rr = i / a.rank, c = i % a.rank;
+    const int r = r0 + rr;
+    w1s[i] = (r < a.R && js[rr] > 0) ? load_elem(a.W1g, a.dtype_w, (size_t)r * a.rank + c) : 0.f;
+  }
+  __syncthreads();
+  Stats st[RB], fb[RB];
+  RngRow rng[RB];
+  float lq[RB], lt[RB];
+#pragma unroll
+  for (int rr = 0; rr < RB; ++rr) {
+    st[rr] = stats_empty();
+    fb[rr] = stats_empty();
+    const int r = min(r0 + rr, a.R - 1);
+    const int j = max(js[rr], 1);
+    rng[rr] = rng_row(a.seed, __ldg(a.req_id + r), a.round, kStreamCorrect, (uint32_t)j);
+    lq[rr] = __ldg(a.lse_q + (size_t)r * a.gamma + (j - 1));
+    lt[rr] = a.lse_t[r];
+  }
+  const int groups_total = (a.V + 3) / 4;
+  const int g0 = blockIdx.x * kSimtGroups * blockDim.x;
+  for (int t = 0; t < kSimtGroups; ++t) {
+    const int g = g0 + t * blockDim.x + threadIdx.x;
+    if (g >= groups_total) break;
+    float acc[RB][4];
+#pragma unroll
+    for (int rr = 0; rr < RB; ++rr)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[rr][e] = 0.f;
+    for (int i = 0; i < a.rank; ++i) {
+      float w2[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int v = 4 * g + e;
+        w2[e] = (v < a.V) ? load_elem(a.W2, a.dtype_w, (size_t)i * a.V + v) : 0.f;
+      }
+#pragma unroll
+      for (int rr = 0; rr < RB; ++rr) {
+        const float w1 = w1s[rr * a.rank + i];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[rr][e] = fmaf(w1, w2[e], acc[rr][e]);
+      }
+    }
+#pragma unroll
+    for (int rr = 0; rr < RB; ++rr) {
+      const int r = r0 + rr;
+      if (r >= a.R || js[rr] == 0) continue;
+      const Philox4 bits = rng_chunk(rng[rr], (uint32_t)g);
+      const uint32_t wd[4] = {bits.x, bits.y, bits.z, bits.w};
+      const size_t urow = ((size_t)r * a.gamma + (js[rr] - 1)) * a.V;
+      const size_t trow = ((size_t)r * (a.gamma + 1) + (js[rr] - 1)) * a.V;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int v = 4 * g + e;
+        if (v >= a.V) break;
+        const float z = (load_elem(a.U, a.dtype_u, urow + v) + acc[rr][e]) * a.inv_temp;
+        const float lp = load_elem(a.target, a.dtype_t, trow + v) * a.inv_temp - lt[rr];
+        const float p = __expf(lp);
+        const float q = __expf(z - lq[rr]);
+        const float rho = p - q;
+        const float g_ = gumbel_from_bits(wd[e]);
+        if (rho > 0.f) {
+          const float key = __logf(rho) + g_;
+          if (key > st[rr].key || st[rr].idx < 0) {
+            st[rr].key = key;
+            st[rr].idx = v;
+          }
+        }
+        const float k2 = lp + g_;
+        if (k2 > fb[rr].key || fb[rr].idx < 0) {
+          fb[rr].key = k2;
+          fb[rr].idx = v;
+        }
+      }
+    }
+  }
+  __shared__ Partial red[kSimtThreads / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int rr = 0; rr < RB; ++rr) {
+    const int r = r0 + rr;
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+      Stats w = warp_reduce_stats(which ? fb[rr] : st[rr]);
+      if (lane == 0) red[warp] = to_partial(w);
+      __syncthreads();
+      if (warp == 0) {
+        Stats b = (lane < (int)(blockDim.x >> 5)) ? from_partial(red[lane]) : stats_empty();
+        b = warp_reduce_stats(b);
+        if (lane == 0 && r < a.R) (which ? a.res_part2 : a.res_part)[(size_t)blockIdx.x * a.R + r] = to_partial(b);
+      }
+      __syncthreads();
+    }
+  }
+}
+
+__global__ void residual_combine_kernel(VerifyArgs a, int npart) {
+  const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (r >= a.R) return;
+  const int js = a.jstar[r];
+  if (js == 0) return;
+  Stats st = stats_empty(), fb = stats_empty();
+  for (int p = lane; p < npart; p += 32) {
+    stats_merge(st, from_partial(a.res_part[(size_t)p * a.R + r]));
+    stats_merge(fb, from_partial(a.res_part2[(size_t)p * a.R + r]));
+  }
+  st = warp_reduce_stats(st);
+  fb = warp_reduce_stats(fb);
+  if (lane == 0) a.tokens_out[(size_t)r * (a.gamma + 1) + (js - 1)] = (st.idx >= 0) ? st.idx : fb.idx;
+}
+
+cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s) {
+  verify_plan_kernel<<<1, kPlanThreads, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int max_items = a.R * (a.gamma + 1) * a.nchunk;
+  const int grid = min(max_items, sms * 8);
+  verify_rows_kernel<<<grid, kRowThreads, 0, s>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int wblocks = (a.R * 32 + 255) / 256;
+  verify_accept_kernel<<<wblocks, 256, 0, s>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  dim3 rgrid(simt_num_chunks(a.V), (a.R + kSimtRB - 1) / kSimtRB);
+  const size_t smem = sizeof(float) * kSimtRB * a.rank;
+  if (smem > 48 * 1024) {
+    e = cudaFuncSetAttribute(residual_step_simt_kernel<kSimtRB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  residual_step_simt_kernel<kSimtRB><<<rgrid, kSimtThreads, smem, s>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  residual_combine_kernel<<<wblocks, 256, 0, s>>>(a, (int)rgrid.x);
+  return cudaGetLastError();
+}
+
+}  // namespace dspark

@@ -1,0 +1,115 @@
+"""The C-ABI library: it loads, exports exactly the symbols include/dspark.h declares,
+and its host-side validation rejects bad arguments before anything is launched (these
+calls never reach the GPU, so they run on CPU-only machines)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dspark.h")
+
+
+def _declared():
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"DSPARK_API\s+[\w\s\*]*?\b(dspark_\w+)\s*\(", txt)))
+
+
+@pytest.fixture(scope="module")
+def b():
+    from speculative_decoding_draft_03_gb300 import build
+    build.build()
+    from speculative_decoding_draft_03_gb300 import binding
+    return binding
+
+
+def test_exports_match_header(b):
+    declared = _declared()
+    assert len(declared) >= 9
+    out = subprocess.run(["nm", "-D", "--defined-only", b._build.LIB], capture_output=True, text=True).stdout
+    exported = sorted(set(m for m in re.findall(r"\bT\s+(\w+)", out)))
+    assert exported == declared
+    for name in declared:
+        assert hasattr(b.lib, name)
+
+
+def test_status_strings(b):
+    for code, name in enumerate(["DSPARK_OK", "DSPARK_INVALID_ARG", "DSPARK_UNSUPPORTED_SHAPE",
+                                 "DSPARK_WORKSPACE_TOO_SMALL", "DSPARK_CUDA_ERROR", "DSPARK_TIMEOUT"]):
+        assert b.lib.dspark_status_string(code).decode() == name
+
+
+def _fake(n=1):
+    # distinct non-null, 256-aligned host-side stand-ins: validation never dereferences them
+    return [ctypes.c_void_p(0x10000 + 0x1000 * i) for i in range(n)]
+
+
+def _draft_call(b, **kw):
+    args = dict(R=4, gamma=4, V=1024, rank=32, d=64, du=0, dw=0, dh=0, T=1.0, ws_bytes=1 << 30)
+    args.update(kw)
+    P = _fake(13)
+    for k in kw.get("null", []):
+        P[k] = None
+    return b.lib.dspark_markov_draft(args["R"], args["gamma"], args["V"], args["rank"], args["d"], args["du"],
+                                     args["dw"], args["dh"], P[0], P[1], P[2], P[3], P[4], 0.0, 1.0, P[5],
+                                     args["T"], P[6], P[7], 0, 0, P[8], P[9], P[10], P[11], P[12],
+                                     args["ws_bytes"], None)
+
+
+def test_draft_validation(b):
+    assert _draft_call(b, R=0) == 1
+    assert _draft_call(b, gamma=0) == 1
+    assert _draft_call(b, rank=-1) == 1
+    assert _draft_call(b, gamma=65) == 2
+    assert _draft_call(b, du=7) == 1
+    assert _draft_call(b, T=0.0) == 1
+    assert _draft_call(b, T=float("nan")) == 1
+    for k in (0, 1, 2, 4, 5, 6, 7, 8, 9, 10, 11, 12):
+        assert _draft_call(b, null=[k]) == 1, k
+    assert _draft_call(b, ws_bytes=16) == 3
+    assert "workspace" in b.lib.dspark_last_error_message().decode()
+
+
+def test_schedule_validation(b):
+    P = _fake(6)
+    L = b.lib.dspark_schedule
+    assert L(0, 4, P[0], P[1], 100, 0, None, 0, P[2], P[3], P[4], P[5], 256, None) == 1
+    assert L(4, 4, P[0], P[1], 100, 9, None, 0, P[2], P[3], P[4], P[5], 256, None) == 1
+    assert L(4, 4, P[0], P[1], 10, 0, None, 0, P[2], P[3], P[4], P[5], 256, None) == 1  # sps too short
+    assert L(4, 4, P[0], P[1], 100, 2, None, 0, P[2], P[3], P[4], P[5], 256, None) == 1  # capacity needs hist
+    assert L(1024, 16, P[0], P[1], 1 << 20, 0, None, 0, P[2], P[3], P[4], P[5], 256, None) == 2
+    assert L(4, 4, P[0], P[1], 100, 0, None, 0, P[2], P[3], P[4], P[5], 8, None) == 3
+    assert L(4, 4, None, P[1], 100, 0, None, 0, P[2], P[3], P[4], P[5], 256, None) == 1
+
+
+def test_verify_validation(b):
+    P = _fake(17)
+    L = b.lib.dspark_verify
+
+    def call(**kw):
+        a = dict(R=4, g=4, V=1024, rank=32, dt=0, T=1.0, ws=1 << 30)
+        a.update(kw)
+        p = list(P)
+        for k in kw.get("null", []):
+            p[k] = None
+        return L(a["R"], a["g"], a["V"], a["rank"], a["dt"], 0, 0, p[0], p[1], p[2], p[3], p[4], p[5], p[6],
+                 p[7], p[8], a["T"], p[9], 0, 0, p[10], p[11], p[12], p[13], a["ws"], None)
+
+    assert call(R=0) == 1
+    assert call(g=100) == 2
+    assert call(dt=3) == 1
+    assert call(T=-1.0) == 1
+    for k in range(14):
+        assert call(null=[k]) == 1, k
+    assert call(ws=100) == 3
+
+
+def test_workspace_sizes_grow_with_shape(b):
+    import torch
+    s1 = b.draft_workspace_size(4, 4, 1024, 32, 64, torch.float32)
+    s2 = b.draft_workspace_size(32, 7, 151936, 256, 4096, torch.bfloat16)
+    assert 256 < s1 < s2
+    assert b.verify_workspace_size(4, 4, 1024, 32, torch.float32) > 256
+    assert b.schedule_workspace_size(512, 15) >= 256

@@ -47,7 +47,13 @@ def test_uniform_mapping_exact_and_open_interval():
     for b in (0, 0xFF, 0x100, 0x7FFFFFFF, 0x80000000, 0xFFFFFF00, 0xFFFFFFFF):
         u = oracle.uniform(b)
         assert u == ((b >> 8) + 0.5) / 2**24
-        assert np.float32(u) == u  # representable in binary32: both sides see the same u
+        # binary32 holds u exactly below 1/2 and 1-u exactly above: a single-precision
+        # Gumbel can therefore take -ln u from u (lower half) or log1p(-(1-u)) (upper half)
+        # without rounding the draw
+        if u < 0.5:
+            assert float(np.float32(u)) == u
+        else:
+            assert float(np.float32(1.0 - u)) == 1.0 - u
         assert 0.0 < u < 1.0
     assert oracle.uniform(0) == 2.0**-25
     assert oracle.uniform(0xFFFFFFFF) == 1.0 - 2.0**-25
