@@ -69,7 +69,7 @@ def compare_draft(gpu, ref, tol, tally: Tally, rows=None):
     return compared
 
 
-def compare_schedule(gpu, ref, tally: Tally):
+def compare_schedule(gpu, ref, tally: Tally, tau_tol=1e-9):
     tally.draws += 1
     same = (np.array_equal(gpu["ell"], ref["ell"]) and int(gpu["B"]) == ref["B"])
     if not same:
@@ -78,7 +78,9 @@ def compare_schedule(gpu, ref, tally: Tally):
         tally.boundary += 1
         tally.notes.append(("schedule",))
         return False
-    assert abs(float(gpu["tau"]) - ref["tau"]) <= 1e-9 * max(1.0, abs(ref["tau"])), (float(gpu["tau"]), ref["tau"])
+    # identical confidences give tau equal up to summation order (binary64); confidences
+    # that went through the two draft stages differ within the probability tolerance
+    assert abs(float(gpu["tau"]) - ref["tau"]) <= tau_tol * max(1.0, abs(ref["tau"])), (float(gpu["tau"]), ref["tau"])
     return True
 
 

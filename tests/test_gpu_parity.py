@@ -131,7 +131,8 @@ def test_round_matches_oracle(name):
     compare_draft(_np(d), ref["draft"], _tol(wg), tally)
     if tally.boundary == 0:
         gs = _np(s)
-        same = compare_schedule(dict(ell=gs["ell"], B=gs["B"][0], tau=gs["tau"][0]), ref["sched"], tally)
+        same = compare_schedule(dict(ell=gs["ell"], B=gs["B"][0], tau=gs["tau"][0]), ref["sched"], tally,
+                                _tol(wg))
         if same:
             compare_verify(_np(v), ref["verify"], tally)
     tally.check_rate()
@@ -154,7 +155,8 @@ def test_stress_chained_rounds_match_oracle():
         compare_draft(_np(d), ref["draft"], _tol(wg), tally)
         if tally.boundary == before:
             gs = _np(s)
-            if compare_schedule(dict(ell=gs["ell"], B=gs["B"][0], tau=gs["tau"][0]), ref["sched"], tally):
+            if compare_schedule(dict(ell=gs["ell"], B=gs["B"][0], tau=gs["tau"][0]), ref["sched"], tally,
+                                _tol(wg)):
                 compare_verify(_np(v), ref["verify"], tally)
         if tally.boundary != before:
             break  # paths diverged legitimately at a boundary case; earlier rounds matched
