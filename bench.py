@@ -1,0 +1,338 @@
+#!/usr/bin/env python
+"""Benchmark of the DSpark per-round hot path (draft -> schedule -> verify) on GB300.
+
+One step = one round over one batch: the Markov-head draft of gamma positions, the
+confidence scheduler, and exact verification (with the residual / bonus token), all
+through the C ABI of libdspark.so on device-resident inputs.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload qwen3-8b]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
+
+Timing: W untimed rounds, then K rounds, each bracketed by CUDA events on the launch
+stream; the L2 is flushed (a 256 MiB write) between rounds, outside the brackets.
+value = verified draft tokens (sum of accepted lengths) over all ranks / max over ranks
+of the summed round time.  Under torchrun each rank runs its own independent batch
+(weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified draft tokens/s per round (draft+schedule+verify)"
+UNIT = "tokens/s"
+WORKLOAD_DESC = {
+    "tiny": "tiny: R=4 gamma=4 V=1024 rank=32 d=64 fp32, early-stop scheduler",
+    "qwen3-8b": "Qwen3-8B-shaped: R=32 gamma=7 V=151936 rank=256 d=4096, U/target fp32, W1/W2/h bf16, "
+                "early-stop scheduler",
+    "batch128": "batch-128 long block: R=128 gamma=16 V=151936 rank=256 d=4096, full-search scheduler",
+    "deepseek-v4": "DeepSeek-V4-shaped: R=256 gamma=5 V=129280 rank=256 d=4096, U/target bf16, capacity-K",
+    "stress": "stress: R=512 gamma=15 V=151936 rank=256 d=4096, fp32 logits, early-stop scheduler",
+}
+DRAFT_KERNEL_SOURCES = ["speculative_decoding_draft_03_gb300/csrc/draft_tc.cu",
+                        "speculative_decoding_draft_03_gb300/csrc/draft_simt.cu",
+                        "speculative_decoding_draft_03_gb300/csrc/dspark_common.cuh"]
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", default="dspark", choices=["dspark", "reference"])
+    p.add_argument("--workload", default="qwen3-8b", choices=list(WORKLOAD_DESC))
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=10)
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def source_hash():
+    h = hashlib.sha256()
+    for rel in DRAFT_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(workload):
+    """Per-launch DRAM bytes of the draft step kernel from the committed ncu summary,
+    only if it was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"draft_step_{workload}.md")
+    try:
+        txt = open(path).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in txt.splitlines():
+        if line.startswith("traffic_bytes_per_launch:") or line.startswith("source_sha:"):
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("source_sha") != source_hash() or "traffic_bytes_per_launch" not in vals:
+        return None
+    return float(vals["traffic_bytes_per_launch"])
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.index)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[3:7]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = sorted(r[0] for r in rows)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2]) if v.lower() == "active"})
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+def draft_step_bytes(w):
+    """Algorithmic bytes of one draft-step launch: the U row block of every request, the
+    whole W2 factor, and the gathered W1 rows."""
+    import torch
+    es = lambda t: torch.tensor([], dtype=t.dtype).element_size()
+    R, V, rank = w["R"], w["V"], w["rank"]
+    return R * V * es(w["U"]) + rank * V * es(w["W2"]) + R * rank * es(w["W1"])
+
+
+def launches_per_round(w):
+    g = w["gamma"]
+    return (1 if w["d"] > 0 else 0) + 1 + 2 * g + 1 + 5
+
+
+def cpu_baseline(workload, w_host, sample_rounds=1):
+    import numpy as np
+    import oracle
+    t0 = time.perf_counter()
+    acc = 0
+    for t in range(sample_rounds):
+        out = oracle.run_round(w_host, rnd=t)
+        acc += int(out["verify"]["n_acc"].sum())
+    dt = time.perf_counter() - t0
+    return {"value": acc / dt, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{sample_rounds} full round(s) of the {workload} workload ({w_host['R']} requests), "
+                      f"fp64 C oracle, OpenMP over requests; {dt:.2f} s wall",
+            "seconds": dt}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from speculative_decoding_draft_03_gb300 import workloads as wl
+    import oracle
+    oracle.build()
+    w = wl.to_numpy(wl.make(args.workload, device="cpu"))
+    total_tok, total_t = 0, 0.0
+    for t in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        out = oracle.run_round(w, rnd=t)
+        dt = time.perf_counter() - t0
+        if t >= args.warmup:
+            total_tok += int(out["verify"]["n_acc"].sum())
+            total_t += dt
+    value = total_tok / total_t
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total_t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded generator, random-init weights)",
+            "config": {"workload": WORKLOAD_DESC[args.workload]},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+                             "sample": f"each step one full round of the {args.workload} workload"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from speculative_decoding_draft_03_gb300 import binding as b
+    from speculative_decoding_draft_03_gb300 import workloads as wl
+
+    dev = torch.device("cuda", local)
+    # generated on the host: the CPU baseline and the end-to-end leg need host copies
+    w_cpu = wl.make(args.workload, device="cpu", seed=0)
+    w = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in w_cpu.items()}
+    w["req_id"] = w["req_id"] + rank * w["R"]  # each rank serves its own requests
+    rd = b.Round(w)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    n_acc_sum = torch.zeros((), dtype=torch.int64, device=dev)
+    timer = b.StepTimer(w["gamma"])
+
+    for t in range(args.warmup):
+        rd.run(rnd=t)
+    torch.cuda.synchronize()
+    assert rd.status() == 0, "device status word reports an error"
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        for t in range(args.steps):
+            flush.zero_()
+            with timer:
+                starts[t].record(stream)
+                d, s, v = rd.run(rnd=args.warmup + t)
+                ends[t].record(stream)
+            n_acc_sum += v["n_acc"].sum()
+            if (t + 1) % 16 == 0 or t == args.steps - 1:
+                torch.cuda.synchronize()  # bound the number of in-flight timer events
+                timer.collect()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        wall = time.perf_counter() - wall0
+    round_ms = sum(a.elapsed_time(e) for a, e in zip(starts, ends))
+    tokens = int(n_acc_sum.item())
+    if world > 1:
+        tt = torch.tensor([round_ms, float(tokens)], dtype=torch.float64, device=dev)
+        mx = tt.clone()
+        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+        dist.all_reduce(tt, op=dist.ReduceOp.SUM)
+        round_ms, tokens = float(mx[0]), int(tt[1])
+    value = tokens / (round_ms / 1000.0)
+    assert rd.status() == 0, "device status word reports an error"
+
+    # dominant kernel: the vocabulary-streaming draft step (one launch per draft position)
+    peaks, peak_kind = measured_peaks()
+    step_ms = sorted(timer.samples)
+    avg_step_ms = sum(step_ms) / max(1, len(step_ms))
+    step_bytes = draft_step_bytes(w)
+    achieved = step_bytes / (avg_step_ms / 1000.0) / 1e9
+    roofline = {"kernel": "draft_step (fused bias contraction + softmax stats + Gumbel-max)",
+                "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "peak_source": peak_kind,
+                "traffic": stored_traffic(args.workload), "algorithmic_bytes_per_launch": step_bytes,
+                "avg_launch_ms": avg_step_ms, "launches_timed": len(step_ms)}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(b, w, w_cpu, rd, args, stream)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.workload, wl.to_numpy(w_cpu))
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": round_ms / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+                "data": "synthetic (seeded generator, random-init weights)",
+                "config": {"workload": WORKLOAD_DESC[args.workload], "R": w["R"], "gamma": w["gamma"],
+                           "V": w["V"], "rank": w["rank"], "d": w["d"],
+                           "l2": "flushed between rounds (256 MiB write outside the timed brackets)",
+                           "parallelism": f"{world} independent batch(es), one per GPU"},
+                "rounds_per_s": 1000.0 * args.steps / round_ms,
+                "verified_tokens_per_round": tokens / args.steps / world,
+                "wall_s": wall, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": launches_per_round(w) * args.steps,
+                "clocks": clk.summary()}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def measure_e2e(b, w, w_cpu, rd, args, stream):
+    """The same metric through the public API with host buffers: every round copies its
+    inputs (U, target, h, x0) from pinned host memory and reads its result back."""
+    import torch
+    host = {k: w_cpu[k].pin_memory() for k in ("U", "target", "h", "x0")}
+    dev_in = {k: w[k] for k in host}
+    out_host = {k: torch.empty_like(rd.verify_out[k], device="cpu").pin_memory() for k in ("tokens", "n_out", "n_acc")}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in out_host.values())
+    n = max(1, args.e2e_steps)
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    tokens = 0
+    torch.cuda.synchronize()
+    s0.record(stream)
+    for t in range(n):
+        for k in host:
+            dev_in[k].copy_(host[k], non_blocking=True)
+        d, s, v = rd.run(rnd=1000 + t, x0=dev_in["x0"])
+        for k in out_host:
+            out_host[k].copy_(v[k], non_blocking=True)
+        stream.synchronize()
+        tokens += int(out_host["n_acc"].sum())
+    s1.record(stream)
+    torch.cuda.synchronize()
+    ms = s0.elapsed_time(s1)
+    return {"value": tokens / (ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms / n}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -82,6 +82,13 @@ DSPARK_API const char* dspark_last_error_message(void);
  * DSPARK_TIMEOUT otherwise.  Resets the word to 0 when reset != 0. */
 DSPARK_API dspark_status dspark_workspace_status(void* workspace, int reset, int* status, void* stream);
 
+/* Measurement hook (not part of the method).  While set, dspark_markov_draft records
+ * events[2(k-1)] just before and events[2(k-1)+1] just after the launch of draft
+ * position k's vocabulary-streaming step kernel, on the call's stream, for
+ * k = 1..min(gamma, n_events/2).  `events` holds cudaEvent_t handles owned by the
+ * caller; NULL or n_events = 0 turns recording off.  The setting is per host thread. */
+DSPARK_API void dspark_set_profile_events(void* const* events, int n_events);
+
 /* ------------------------------------------------------------------------------------
  * Stage 1: Markov-head draft loop with the confidence head.
  *

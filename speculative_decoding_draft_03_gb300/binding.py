@@ -43,6 +43,8 @@ def _load_library():
     lib.dspark_verify_workspace_size.restype = sz
     lib.dspark_verify_workspace_size.argtypes = [i32] * 5
     lib.dspark_verify.argtypes = ([i32] * 7 + [P] * 4 + [P] * 5 + [f32, P, u64, u64] + [P] * 3 + [P, sz, P])
+    lib.dspark_set_profile_events.argtypes = [P, i32]
+    lib.dspark_set_profile_events.restype = None
     for fn in ("dspark_markov_draft", "dspark_schedule", "dspark_verify", "dspark_workspace_status"):
         getattr(lib, fn).restype = i32
     return lib
@@ -185,6 +187,31 @@ def verify(target, U, W1, W2, x0, x, logq, lse_q, ell, temperature, req_id, seed
                            _p(out["tokens"]), _p(out["n_out"]), _p(ws), ws.numel(), _stream(stream))
     _check(st, "dspark_verify")
     return out
+
+
+class StepTimer:
+    """Times the draft stage's vocabulary-streaming step kernel (one launch per draft
+    position) with CUDA events the library records around each launch."""
+
+    def __init__(self, gamma: int):
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * gamma)]
+        for e in self.events:
+            e.record()  # materialise the handles
+        torch.cuda.synchronize()
+        self._arr = (ctypes.c_void_p * len(self.events))(*[e.cuda_event for e in self.events])
+        self.samples = []
+
+    def __enter__(self):
+        lib.dspark_set_profile_events(self._arr, len(self.events))
+        return self
+
+    def __exit__(self, *exc):
+        lib.dspark_set_profile_events(None, 0)
+
+    def collect(self):
+        """After the stream has synchronised: append this round's per-launch times (ms)."""
+        for k in range(len(self.events) // 2):
+            self.samples.append(self.events[2 * k].elapsed_time(self.events[2 * k + 1]))
 
 
 def device_status(ws, reset=False, stream=None) -> int:

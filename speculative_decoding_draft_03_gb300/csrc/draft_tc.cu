@@ -1,24 +1,529 @@
-// draft_tc.cu — tensor-core (tcgen05 / TMEM / TMA) draft step (placeholder until the
-// fused kernel lands: every shape runs the CUDA-core step).
+// draft_tc.cu — the fused draft step on the 5th-generation tensor cores (sm_103a).
+//
+// One launch per draft position k computes, for every request r and vocabulary id v,
+//   z[r,v] = (U[r,k,v] + (W1[x_{k-1}(r),:] . W2[:,v])) / T
+// and reduces each request's row to (max, sum exp, Gumbel-max key/id) partials, so the
+// vocabulary row is streamed exactly once per position (numb3r33 blog "DSpark:
+// confidence-scheduled speculative decoding", section "Markov sequential head";
+// DSpark 精读 §2: p_k = softmax(U_k + W1[x_{k-1}] W2), sampled left to right).
+//
+// GB300 mapping
+//   * The bias is an [R x rank] x [rank x V] contraction: tcgen05.mma kind::f16
+//     (bf16 x bf16 -> fp32), M = 128 requests (TMEM lanes), N = 128 vocabulary ids per
+//     tile (TMEM columns), K = rank.  The gathered factor rows W1[x_{k-1}] (A, K-major)
+//     stay resident in shared memory; W2 tiles (B, read in its natural [rank, V] layout,
+//     i.e. MN-major) stream through a TMA ring with 128-byte swizzle.
+//   * Accumulators live in TMEM, double-buffered (2 x 128 columns) so the MMA of tile
+//     t+1 overlaps the epilogue of tile t.
+//   * Epilogue: each thread owns one request (its TMEM lane) and a run of consecutive
+//     vocabulary ids, so softmax statistics and the Gumbel-max draw are thread-local
+//     (no shuffles per element) and one Philox block serves 4 consecutive ids.
+//   * Few requests (R <= 64): the request rows are replicated across the 4 TMEM lane
+//     quarters and each quarter takes a different part of the tile's columns, so all
+//     epilogue warps stay busy.
+//   * Many requests (R > 128): CTAs are grouped by request block; the CTAs of a group
+//     walk the same W2 tiles at the same time, so W2 comes from HBM once per position
+//     and from L2 for the other request blocks.
+//   * Warp roles: warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer, warps 2..9
+//     epilogue.  Every mbarrier wait is bounded; a wait that gives up records
+//     DSPARK_TIMEOUT in the workspace status word and the CTA winds down cleanly.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "dspark_common.cuh"
 #include "dspark_internal.h"
 
 namespace dspark {
+namespace tc {
 
-int tc_supported(int V, int rank, int dtype_w) {
-  (void)V;
-  (void)rank;
-  (void)dtype_w;
-  return 0;
+constexpr int kM = 128;           // MMA rows (requests, replicated for small batches)
+constexpr int kN = 128;           // vocabulary ids per tile
+constexpr int kKAtom = 64;        // bf16 elements per 128-byte swizzle row
+constexpr int kStages = 8;        // W2 ring stages (one 64-deep K slice of a tile each)
+constexpr int kStageBytes = kN * kKAtom * 2;  // 16 KB
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kTmemCols = 2 * kN;
+constexpr int kMaxRank = 256;
+constexpr long long kWaitCycles = 4000000000ll;  // ~2 s at 2 GHz
+
+struct Smem {
+  // offsets from the 1024-byte aligned base
+  static constexpr int a = 0;                                  // [rank/64][128 rows][128 B]
+  static constexpr int b = a + kM * kMaxRank * 2;              // [stages][2][64 rows][128 B]
+  static constexpr int red = b + kStages * kStageBytes;        // [8 warps][32] Partial
+  static constexpr int bars = red + kEpiWarps * 32 * 32;       // mbarriers
+  static constexpr int total = bars + 256;
+};
+
+// ------------------------------------------------------------------------------------
+// PTX wrappers
+// ------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
-int tc_grid_size() { return 1; }
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: gives up when another role aborted or after kWaitCycles.
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, DeviceStatus* st, int where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort_flag = 1;
+      report_timeout(st, where);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 descriptor format:
+// start >> 4 in [0,14), leading byte offset >> 4 in [16,30), stride byte offset >> 4
+// in [32,46), version 1 in [46,48), swizzle mode 2 = 128B in [61,64)).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor kind::f16: D fp32, A bf16 K-major, B bf16 MN-major, M x N.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+struct TcParams {
+  int R, gamma, V, rank;
+  int dtype_u;
+  int Rb;          // requests per block: 32, 64 or 128
+  int rblocks;     // ceil(R / Rb)
+  int ngroups;     // CTAs per request block (= partial records per request)
+  int ntiles;      // ceil(V / 128)
+  int k;           // draft position (1-based)
+  float inv_temp;
+  const void* U;
+  const int64_t* req_id;
+  uint64_t seed, round;
+  Partial* partials;  // [ngroups, R]
+  DeviceStatus* status;
+};
+
+// RB: requests per block (32, 64 or 128); the 128 MMA rows hold 128/RB copies of it.
+template <int RB>
+__global__ void __launch_bounds__(kThreads, 1)
+    draft_step_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                         TcParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int rb = blockIdx.x % p.rblocks;      // request block of this CTA
+  const int group = blockIdx.x / p.rblocks;   // vocabulary-tile group
+  const int katoms = p.rank / kKAtom;
+
+  uint32_t bar_full = sbase + Smem::bars;              // [kStages]
+  uint32_t bar_empty = bar_full + 8 * kStages;         // [kStages]
+  uint32_t bar_acc_full = bar_empty + 8 * kStages;     // [2]
+  uint32_t bar_acc_empty = bar_acc_full + 16;          // [2]
+  uint32_t bar_a = bar_acc_empty + 16;                 // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Smem::bars + 8 * (2 * kStages + 5));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Smem::bars + 8 * (2 * kStages + 5) + 8);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_acc_full + 8 * b, 1);
+      mbar_init(bar_acc_empty + 8 * b, kEpiWarps);
+    }
+    mbar_init(bar_a, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // tiles of this CTA: group, group + ngroups, ...
+  const int my_tiles = (p.ntiles > group) ? (p.ntiles - group + p.ngroups - 1) / p.ngroups : 0;
+
+  if (warp == 0) {
+    // ------------------------------ TMA producer ------------------------------
+    if (lane == 0) {
+      constexpr int rep = kM / RB;
+      mbar_arrive_expect_tx(bar_a, (uint32_t)(kM * p.rank * 2));
+      for (int j = 0; j < rep; ++j)
+        for (int ka = 0; ka < katoms; ++ka)
+          tma_load_2d(sbase + Smem::a + ka * (kM * 128) + j * RB * 128, &map_a, bar_a, ka * kKAtom, rb * RB);
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int t = 0; t < my_tiles && !*abort_flag; ++t) {
+        const int v0 = (group + t * p.ngroups) * kN;
+        for (int ka = 0; ka < katoms; ++ka) {
+          if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag, p.status, 100)) break;
+          const uint32_t dst = sbase + Smem::b + stage * kStageBytes;
+          mbar_arrive_expect_tx(bar_full + 8 * stage, kStageBytes);
+          tma_load_2d(dst, &map_b, bar_full + 8 * stage, v0, ka * kKAtom);
+          tma_load_2d(dst + kStageBytes / 2, &map_b, bar_full + 8 * stage, v0 + 64, ka * kKAtom);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer --------------------------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc(kM, kN);
+      bool ok = mbar_wait(bar_a, 0, abort_flag, p.status, 200);
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int t = 0; t < my_tiles && ok; ++t) {
+        const int buf = t & 1;
+        const uint32_t use = (uint32_t)(t >> 1) & 1u;
+        if (!mbar_wait(bar_acc_empty + 8 * buf, use ^ 1, abort_flag, p.status, 201)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * kN;
+        for (int ka = 0; ka < katoms; ++ka) {
+          if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.status, 202)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_atom = sbase + Smem::a + ka * (kM * 128);
+          const uint32_t b_stage = sbase + Smem::b + stage * kStageBytes;
+#pragma unroll
+          for (int kk = 0; kk < kKAtom / 16; ++kk) {
+            // A: K-major rows of 128 B; a 16-deep K step is 32 B further along the row.
+            const uint64_t adesc = sw128_desc(a_atom + kk * 32, 16, 1024);
+            // B: MN-major; a 16-deep K step is 16 rows (2 KB) further; the two 64-id
+            // halves of the tile are 8 KB apart (leading byte offset), 8-row groups of
+            // K are 1 KB apart (stride byte offset).
+            const uint64_t bdesc = sw128_desc(b_stage + kk * 2048, kStageBytes / 2, 1024);
+            mma_bf16(d_tmem, adesc, bdesc, idesc, (ka > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(bar_empty + 8 * stage);  // frees the ring slot once these MMAs finish
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit(bar_acc_full + 8 * buf);
+      }
+    }
+  } else {
+    // ------------------------------ epilogue ----------------------------------
+    const int ew = warp - 2;               // 0..7
+    const int quarter = warp & 3;          // TMEM lane quarter this warp may access
+    const int sub = ew >> 2;               // 0..1: which half of the quarter's columns
+    const int row0 = (quarter * 32) % RB;
+    const int replica = (quarter * 32) / RB;
+    const int r = rb * RB + row0 + lane;
+    const bool valid = r < p.R;
+    constexpr int kPass = RB / 32;         // 16-column passes per tile: 1, 2 or 4
+    const int col0 = replica * RB + sub * (RB / 2);  // RB columns per replica, half per warp
+
+    Stats st = stats_empty();
+    RngRow rng = rng_row(p.seed, valid ? __ldg(p.req_id + r) : 0, p.round, kStreamDraft, (uint32_t)p.k);
+    const size_t urow = ((size_t)(valid ? r : 0) * p.gamma + (p.k - 1)) * (size_t)p.V;
+    const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    const bool u_f32 = p.dtype_u == DSPARK_F32;
+
+    // U of the next tile is loaded into registers while the current one is processed
+    uint4 unext[kPass][4];
+    auto load_u = [&](int t, uint4 (&dst)[kPass][4]) {
+      const int vt = (group + t * p.ngroups) * kN;
+#pragma unroll
+      for (int ps = 0; ps < kPass; ++ps) {
+        const int vb = vt + col0 + ps * 16;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          // fp32: 4 ids per 16 bytes; bf16: 8 ids per 16 bytes (only q < 2 used)
+          const int v = u_f32 ? vb + 4 * q : vb + 8 * q;
+          const bool in = valid && t < my_tiles && (u_f32 || q < 2) && v < p.V;
+          dst[ps][q] = in ? (u_f32 ? __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const float*>(p.U) + urow + v))
+                                   : __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned short*>(p.U) +
+                                                                           urow + v)))
+                          : make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+    };
+    load_u(0, unext);
+
+    for (int t = 0; t < my_tiles; ++t) {
+      const int buf = t & 1;
+      const uint32_t use = (uint32_t)(t >> 1) & 1u;
+      const int vt = (group + t * p.ngroups) * kN;
+      uint4 ucur[kPass][4];
+#pragma unroll
+      for (int ps = 0; ps < kPass; ++ps)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ucur[ps][q] = unext[ps][q];
+      load_u(t + 1, unext);
+      if (!mbar_wait(bar_acc_full + 8 * buf, use, abort_flag, p.status, 300)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int ps = 0; ps < kPass; ++ps) {
+        const int c = col0 + ps * 16;
+        float bias[16];
+        tmem_ld16(tmem_base + lane_addr + buf * kN + c, bias);
+        if (ps == kPass - 1) {
+          // all of this warp's columns are in registers: hand the accumulator back
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_acc_empty + 8 * buf);
+        }
+        const int vb = vt + c;
+        if (!valid || vb >= p.V) continue;
+        float z[16];
+        if (u_f32) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            z[4 * q + 0] = __uint_as_float(ucur[ps][q].x);
+            z[4 * q + 1] = __uint_as_float(ucur[ps][q].y);
+            z[4 * q + 2] = __uint_as_float(ucur[ps][q].z);
+            z[4 * q + 3] = __uint_as_float(ucur[ps][q].w);
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const uint32_t wd[4] = {ucur[ps][q].x, ucur[ps][q].y, ucur[ps][q].z, ucur[ps][q].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              z[8 * q + 2 * e] = bf16_bits_to_float(wd[e] & 0xFFFFu);
+              z[8 * q + 2 * e + 1] = bf16_bits_to_float(wd[e] >> 16);
+            }
+          }
+        }
+        const int nvalid = min(16, p.V - vb);  // V % 8 == 0: 8 or 16
+        float cmax = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          z[i] = (z[i] + bias[i]) * p.inv_temp;
+          if (i < nvalid) cmax = fmaxf(cmax, z[i]);
+        }
+        // online softmax statistics over the 16 ids
+        const float mnew = fmaxf(st.m, cmax);
+        float acc = (st.m == -INFINITY) ? 0.f : st.s * __expf(st.m - mnew);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (i < nvalid) acc += __expf(z[i] - mnew);
+        st.m = mnew;
+        st.s = acc;
+        // Gumbel-max draw; a group of 4 ids whose best logit cannot beat the running
+        // key even with the largest possible Gumbel needs no random bits
+#pragma unroll
+        for (int g4 = 0; g4 < 4; ++g4) {
+          if (4 * g4 >= nvalid) break;
+          const float gmax = fmaxf(fmaxf(z[4 * g4], z[4 * g4 + 1]), fmaxf(z[4 * g4 + 2], z[4 * g4 + 3]));
+          if (st.idx >= 0 && gmax + kGumbelMax < st.key) continue;
+          const Philox4 bits = rng_chunk(rng, (uint32_t)((vb >> 2) + g4));
+          const uint32_t wd[4] = {bits.x, bits.y, bits.z, bits.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float zz = z[4 * g4 + e];
+            if (st.idx >= 0 && zz + kGumbelMax < st.key) continue;
+            const float key = zz + gumbel_from_bits(wd[e]);
+            if (st.idx < 0 || key > st.key) {
+              st.key = key;
+              st.idx = vb + 4 * g4 + e;
+              st.zsel = zz;
+            }
+          }
+        }
+      }
+    }
+    // merge the threads that share a request: smem slots [ew][lane]
+    Partial* red = reinterpret_cast<Partial*>(smem + Smem::red);
+    red[ew * 32 + lane] = to_partial(st);
+    asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+    const int et = threadIdx.x - 64;  // 0..255
+    if (et < RB) {
+      Stats m = stats_empty();
+      for (int w2 = 0; w2 < kEpiWarps; ++w2) {
+        const int q2 = (w2 + 2) & 3;
+        const int r0 = (q2 * 32) % RB;
+        if (et >= r0 && et < r0 + 32) stats_merge(m, from_partial(red[w2 * 32 + (et - r0)]));
+      }
+      const int rr = rb * RB + et;
+      if (rr < p.R) p.partials[(size_t)group * p.R + rr] = to_partial(m);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// Host side
+// ------------------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+static bool make_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                        uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+static int num_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return 148;
+  return sms;
+}
+
+static int block_rows(int R) { return R <= 32 ? 32 : (R <= 64 ? 64 : 128); }
+
+}  // namespace tc
+
+int tc_supported(int V, int rank, int dtype_w) {
+  return dtype_w == DSPARK_BF16 && rank % tc::kKAtom == 0 && rank >= tc::kKAtom && rank <= tc::kMaxRank &&
+         V % 8 == 0 && V >= tc::kN;
+}
+
+int tc_num_partials(int R) {
+  const int Rb = tc::block_rows(R);
+  const int rblocks = (R + Rb - 1) / Rb;
+  const int groups = tc::num_sms() / rblocks;
+  return groups > 0 ? groups : 1;
+}
 
 cudaError_t launch_draft_step_tc(const DraftArgs& a, int k, cudaStream_t s) {
-  (void)a;
-  (void)k;
-  (void)s;
-  return cudaErrorNotSupported;
+  using namespace tc;
+  TcParams p;
+  p.R = a.R;
+  p.gamma = a.gamma;
+  p.V = a.V;
+  p.rank = a.rank;
+  p.dtype_u = a.dtype_u;
+  p.Rb = block_rows(a.R);
+  p.rblocks = (a.R + p.Rb - 1) / p.Rb;
+  p.ngroups = tc_num_partials(a.R);
+  p.ntiles = (a.V + kN - 1) / kN;
+  p.k = k;
+  p.inv_temp = a.inv_temp;
+  p.U = a.U;
+  p.req_id = a.req_id;
+  p.seed = a.seed;
+  p.round = a.round;
+  p.partials = a.partials;
+  p.status = a.status;
+  CUtensorMap map_a, map_b;
+  if (!make_map_2d(&map_a, a.W1g, (uint64_t)a.rank, (uint64_t)round_up_rows(a.R), kKAtom, (uint32_t)p.Rb))
+    return cudaErrorInvalidValue;
+  if (!make_map_2d(&map_b, a.W2, (uint64_t)a.V, (uint64_t)a.rank, 64, kKAtom)) return cudaErrorInvalidValue;
+  const int smem = Smem::total + 1024;
+  auto kern = p.Rb == 32 ? draft_step_tc_kernel<32> : (p.Rb == 64 ? draft_step_tc_kernel<64> : draft_step_tc_kernel<128>);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<p.ngroups * p.rblocks, kThreads, smem, s>>>(map_a, map_b, p);
+  return cudaGetLastError();
 }
 
 }  // namespace dspark

@@ -12,6 +12,8 @@
 namespace {
 
 thread_local char g_msg[512] = "";
+thread_local void* const* g_prof_events = nullptr;
+thread_local int g_prof_n = 0;
 
 dspark_status fail(dspark_status code, const char* fmt, ...) {
   va_list ap;
@@ -44,7 +46,7 @@ DraftLayout draft_layout(int R, int gamma, int V, int rank, int dtype_w) {
   off += align256(sizeof(float) * (size_t)R * gamma);
   L.W1g = off;
   off += align256(elem_size(dtype_w) * (size_t)round_up_rows(R) * rank);
-  L.npart = draft_num_partials(V, rank, dtype_w);
+  L.npart = draft_num_partials(R, V, rank, dtype_w);
   L.partials = off;
   off += align256((size_t)32 * L.npart * R);
   L.total = off;
@@ -102,10 +104,10 @@ namespace dspark {
 
 int round_up_rows(int R) { return ((R + 127) / 128) * 128; }
 
-int draft_num_partials(int V, int rank, int dtype_w) {
+int draft_num_partials(int R, int V, int rank, int dtype_w) {
   const int simt = simt_num_chunks(V);
   if (tc_supported(V, rank, dtype_w)) {
-    const int tc = tc_grid_size();
+    const int tc = tc_num_partials(R);
     return simt > tc ? simt : tc;
   }
   return simt;
@@ -128,6 +130,11 @@ const char* dspark_status_string(int status) {
 }
 
 const char* dspark_last_error_message(void) { return g_msg; }
+
+void dspark_set_profile_events(void* const* events, int n_events) {
+  g_prof_events = (events != nullptr && n_events > 0) ? events : nullptr;
+  g_prof_n = g_prof_events ? n_events : 0;
+}
 
 dspark_status dspark_workspace_status(void* workspace, int reset, int* status, void* stream) {
   CHECK_PTR(workspace);
@@ -210,13 +217,18 @@ dspark_status dspark_markov_draft(int R, int gamma, int V, int rank, int d, int 
   const bool tc = dspark::tc_supported(V, rank, dtype_w) != 0;
   for (int k = 1; k <= gamma; ++k) {
     int npart;
+    const bool prof = 2 * k <= g_prof_n;
+    if (prof && (e = cudaEventRecord((cudaEvent_t)g_prof_events[2 * (k - 1)], s)) != cudaSuccess)
+      return cuda_fail(e, "profile event");
     if (tc) {
       if ((e = dspark::launch_draft_step_tc(a, k, s)) != cudaSuccess) return cuda_fail(e, "draft_step_tc");
-      npart = dspark::tc_grid_size();
+      npart = dspark::tc_num_partials(R);
     } else {
       if ((e = dspark::launch_draft_step_simt(a, k, s)) != cudaSuccess) return cuda_fail(e, "draft_step_simt");
       npart = dspark::simt_num_chunks(V);
     }
+    if (prof && (e = cudaEventRecord((cudaEvent_t)g_prof_events[2 * (k - 1) + 1], s)) != cudaSuccess)
+      return cuda_fail(e, "profile event");
     if ((e = dspark::launch_draft_combine(a, k, npart, s)) != cudaSuccess) return cuda_fail(e, "draft_combine");
   }
   return DSPARK_OK;

@@ -82,8 +82,8 @@ __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size
 
 int simt_num_chunks(int V);
 int tc_supported(int V, int rank, int dtype_w);
-int tc_grid_size();
-int draft_num_partials(int V, int rank, int dtype_w);
+int tc_num_partials(int R);
+int draft_num_partials(int R, int V, int rank, int dtype_w);
 int round_up_rows(int R);
 
 cudaError_t launch_conf_hdot(const DraftArgs& a, cudaStream_t s);

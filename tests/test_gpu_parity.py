@@ -169,6 +169,35 @@ def test_stress_chained_rounds_match_oracle():
     tally.check_rate()
 
 
+@pytest.mark.parametrize("R,V,rank", [(5, 2056, 64), (32, 4104, 256), (64, 1032, 128), (100, 2056, 192),
+                                      (200, 1160, 256), (513, 1032, 64)])
+def test_draft_bias_dominant(R, V, rank):
+    """Large low-rank factors (bias comparable to U), bf16: the tensor-core contraction
+    decides the tokens, so any layout/descriptor error shows as token mismatches.
+    Covers request blocks of 32/64/128 rows, several blocks, ragged R and V."""
+    import torch
+    b = _b()
+    gamma, d = 3, 16
+    g = torch.Generator().manual_seed(R * 7 + V)
+    U = torch.randn((R, gamma, V), generator=g) * 1.0
+    W1 = (torch.randn((V, rank), generator=g) * 0.35).to(torch.bfloat16)
+    W2 = (torch.randn((rank, V), generator=g) * 0.35).to(torch.bfloat16)
+    h = torch.randn((R, gamma, d), generator=g)
+    cw = torch.randn(d + rank, generator=g) * 0.1
+    x0 = torch.randint(0, V, (R,), generator=g, dtype=torch.int32)
+    ids = torch.arange(R, dtype=torch.int64) * 3 + 1
+    ct = torch.ones(gamma)
+    gd = b.markov_draft(U.cuda(), W1.cuda(), W2.cuda(), h.cuda(), cw.cuda(), 0.0, 1.0, ct.cuda(), 1.0, x0.cuda(),
+                        ids.cuda(), 5, 9)
+    torch.cuda.synchronize()
+    bits = lambda t: t.view(torch.int16).numpy().view(np.uint16)
+    od = oracle.markov_draft(U.numpy(), bits(W1), bits(W2), h.numpy(), cw.numpy(), 0.0, 1.0, ct.numpy(), 1.0,
+                             x0.numpy(), ids.numpy(), 5, 9)
+    tally = Tally()
+    compare_draft(_np(gd), od, 2e-3, tally)
+    tally.check_rate()
+
+
 def test_edge_cases():
     """Single request, gamma = 1, V not a multiple of 4/8 (scalar tails), zero-length and
     full-length verify, T != 1."""
