@@ -29,6 +29,7 @@
 //     DSPARK_TIMEOUT in the workspace status word and the CTA winds down cleanly.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <string.h>
 
 #include "dspark_common.cuh"
 #include "dspark_internal.h"
@@ -182,10 +183,22 @@ struct TcParams {
   uint64_t seed, round;
   Partial* partials;  // [ngroups, R]
   DeviceStatus* status;
+  // residual mode
+  const void* target;
+  int dtype_t;
+  const int* jstar;     // [R] rejected position (0 = none)
+  const float* lse_q;   // [R, gamma]
+  const float* lse_t;   // [R]
+  Partial* partials2;   // [ngroups, R] fallback draw
 };
 
+constexpr int kModeDraft = 0;
+constexpr int kModeResidual = 1;
+
 // RB: requests per block (32, 64 or 128); the 128 MMA rows hold 128/RB copies of it.
-template <int RB>
+// MODE: kModeDraft (one draft position for every request) or kModeResidual (the
+// rejected position j* of each request that has one).
+template <int RB, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     draft_step_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                          TcParams p) {
@@ -304,13 +317,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row0 = (quarter * 32) % RB;
     const int replica = (quarter * 32) / RB;
     const int r = rb * RB + row0 + lane;
-    const bool valid = r < p.R;
+    bool valid = r < p.R;
     constexpr int kPass = RB / 32;         // 16-column passes per tile: 1, 2 or 4
     const int col0 = replica * RB + sub * (RB / 2);  // RB columns per replica, half per warp
 
-    Stats st = stats_empty();
-    RngRow rng = rng_row(p.seed, valid ? __ldg(p.req_id + r) : 0, p.round, kStreamDraft, (uint32_t)p.k);
-    const size_t urow = ((size_t)(valid ? r : 0) * p.gamma + (p.k - 1)) * (size_t)p.V;
+    // draft: position k of every request; residual: the rejected position j* (0 = none)
+    int pos = p.k;
+    float lse_q = 0.f, lse_t = 0.f;
+    if constexpr (MODE == kModeResidual) {
+      pos = valid ? p.jstar[r] : 0;
+      valid = valid && pos > 0;
+      if (valid) {
+        lse_q = __ldg(p.lse_q + (size_t)r * p.gamma + (pos - 1));
+        lse_t = p.lse_t[r];
+      }
+    }
+    Stats st = stats_empty();  // draft: softmax stats + Gumbel-max; residual: ln(p-q)+ + g
+    Stats fb = stats_empty();  // residual only: ln p + g (the rounding fallback)
+    const PhiloxRow prow = philox_row(rng_row(p.seed, valid ? __ldg(p.req_id + r) : 0, p.round,
+                                              MODE == kModeDraft ? kStreamDraft : kStreamCorrect, (uint32_t)pos));
+    const size_t urow = ((size_t)(valid ? r : 0) * p.gamma + (valid ? pos - 1 : 0)) * (size_t)p.V;
+    const size_t trow = ((size_t)(valid ? r : 0) * (p.gamma + 1) + (valid ? pos - 1 : 0)) * (size_t)p.V;
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     const bool u_f32 = p.dtype_u == DSPARK_F32;
 
@@ -381,38 +408,102 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         const int nvalid = min(16, p.V - vb);  // V % 8 == 0: 8 or 16
-        float cmax = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          z[i] = (z[i] + bias[i]) * p.inv_temp;
-          if (i < nvalid) cmax = fmaxf(cmax, z[i]);
-        }
-        // online softmax statistics over the 16 ids
-        const float mnew = fmaxf(st.m, cmax);
-        float acc = (st.m == -INFINITY) ? 0.f : st.s * __expf(st.m - mnew);
+        for (int i = 0; i < 16; ++i) z[i] = (z[i] + bias[i]) * p.inv_temp;
+        if constexpr (MODE == kModeDraft) {
+          float cmax = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          if (i < nvalid) acc += __expf(z[i] - mnew);
-        st.m = mnew;
-        st.s = acc;
-        // Gumbel-max draw; a group of 4 ids whose best logit cannot beat the running
-        // key even with the largest possible Gumbel needs no random bits
+          for (int i = 0; i < 16; ++i)
+            if (i < nvalid) cmax = fmaxf(cmax, z[i]);
+          // online softmax statistics over the 16 ids; term_i = exp(z_i - m)
+          const float mnew = fmaxf(st.m, cmax);
+          float acc = (st.m == -INFINITY) ? 0.f : st.s * __expf(st.m - mnew);
+          float term[16];
 #pragma unroll
-        for (int g4 = 0; g4 < 4; ++g4) {
-          if (4 * g4 >= nvalid) break;
-          const float gmax = fmaxf(fmaxf(z[4 * g4], z[4 * g4 + 1]), fmaxf(z[4 * g4 + 2], z[4 * g4 + 3]));
-          if (st.idx >= 0 && gmax + kGumbelMax < st.key) continue;
-          const Philox4 bits = rng_chunk(rng, (uint32_t)((vb >> 2) + g4));
-          const uint32_t wd[4] = {bits.x, bits.y, bits.z, bits.w};
+          for (int i = 0; i < 16; ++i) {
+            term[i] = (i < nvalid) ? __expf(z[i] - mnew) : 0.f;
+            acc += term[i];
+          }
+          st.m = mnew;
+          st.s = acc;
+          // Gumbel-max draw.  The 16 ids' random words come from 4 independent Philox
+          // blocks (no branches, so they interleave).  An element is rejected without
+          // logarithms when 1-u >= exp(z - best) = term * exp(m - best) -- it then
+          // cannot beat the running key -- and only the rare survivors evaluate z + g.
+          uint32_t wd[16];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float zz = z[4 * g4 + e];
-            if (st.idx >= 0 && zz + kGumbelMax < st.key) continue;
-            const float key = zz + gumbel_from_bits(wd[e]);
+          for (int g4 = 0; g4 < 4; ++g4) {
+            const Philox4 bits = prow.block((uint32_t)((vb >> 2) + g4));
+            wd[4 * g4 + 0] = bits.x;
+            wd[4 * g4 + 1] = bits.y;
+            wd[4 * g4 + 2] = bits.z;
+            wd[4 * g4 + 3] = bits.w;
+          }
+          const float scale = (st.idx >= 0) ? __expf(mnew - st.key) * kRejectSlack : INFINITY;
+          uint32_t cand = 0;
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (i < nvalid && !gumbel_cannot_win(wd[i], term[i] * scale)) cand |= 1u << i;
+          while (cand) {
+            const int i = __ffs(cand) - 1;
+            cand &= cand - 1;
+            float zi = 0.f;
+            uint32_t wi = 0u;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)  // static register selection (no local memory)
+              if (j == i) {
+                zi = z[j];
+                wi = wd[j];
+              }
+            const float key = zi + gumbel_from_bits(wi);
             if (st.idx < 0 || key > st.key) {
               st.key = key;
-              st.idx = vb + 4 * g4 + e;
-              st.zsel = zz;
+              st.idx = vb + i;
+              st.zsel = zi;
+            }
+          }
+        } else {
+          // residual: q = exp(z - lse_q), p = exp(t/T - lse_t); draw from (p - q)+ by
+          // Gumbel-max over ln(p - q) where positive, and keep the ln p draw as fallback
+          float lp[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            lp[i] = (i < nvalid) ? load_elem(p.target, p.dtype_t, trow + vb + i) * p.inv_temp - lse_t : -INFINITY;
+#pragma unroll
+          for (int g4 = 0; g4 < 4; ++g4) {
+            if (4 * g4 >= nvalid) break;
+            const float gmax = fmaxf(fmaxf(lp[4 * g4], lp[4 * g4 + 1]), fmaxf(lp[4 * g4 + 2], lp[4 * g4 + 3]));
+            // ln(p - q) <= ln p: neither draw can improve once ln p + G_max is below both keys
+            if (st.idx >= 0 && fb.idx >= 0 && gmax + kGumbelMax < st.key && gmax + kGumbelMax < fb.key) continue;
+            const Philox4 bits = prow.block((uint32_t)((vb >> 2) + g4));
+            const uint32_t wd[4] = {bits.x, bits.y, bits.z, bits.w};
+            // rejection scales: a key c + g beats best only if 1-u < e^{c - best}
+            const float s1 = (st.idx >= 0) ? __expf(-st.key) * kRejectSlack : INFINITY;
+            const float s2 = (fb.idx >= 0) ? __expf(-fb.key) * kRejectSlack : INFINITY;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int v = vb + 4 * g4 + e;
+              const float pv = __expf(lp[4 * g4 + e]);
+              const float rho = pv - __expf(z[4 * g4 + e] - lse_q);
+              const float w = one_minus_uniform(wd[e]);
+              const bool try1 = rho > 0.f && !(w >= rho * s1);
+              const bool try2 = !(w >= pv * s2);
+              if (!try1 && !try2) continue;
+              const float g = gumbel_from_bits(wd[e]);
+              if (try2) {
+                const float k2 = lp[4 * g4 + e] + g;
+                if (fb.idx < 0 || k2 > fb.key) {
+                  fb.key = k2;
+                  fb.idx = v;
+                }
+              }
+              if (try1) {
+                const float k1 = logf(rho) + g;
+                if (st.idx < 0 || k1 > st.key) {
+                  st.key = k1;
+                  st.idx = v;
+                }
+              }
             }
           }
         }
@@ -420,18 +511,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // merge the threads that share a request: smem slots [ew][lane]
     Partial* red = reinterpret_cast<Partial*>(smem + Smem::red);
-    red[ew * 32 + lane] = to_partial(st);
-    asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
     const int et = threadIdx.x - 64;  // 0..255
-    if (et < RB) {
-      Stats m = stats_empty();
-      for (int w2 = 0; w2 < kEpiWarps; ++w2) {
-        const int q2 = (w2 + 2) & 3;
-        const int r0 = (q2 * 32) % RB;
-        if (et >= r0 && et < r0 + 32) stats_merge(m, from_partial(red[w2 * 32 + (et - r0)]));
+#pragma unroll
+    for (int which = 0; which < (MODE == kModeDraft ? 1 : 2); ++which) {
+      red[ew * 32 + lane] = to_partial(which ? fb : st);
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+      if (et < RB) {
+        Stats m = stats_empty();
+        for (int w2 = 0; w2 < kEpiWarps; ++w2) {
+          const int q2 = (w2 + 2) & 3;
+          const int r0 = (q2 * 32) % RB;
+          if (et >= r0 && et < r0 + 32) stats_merge(m, from_partial(red[w2 * 32 + (et - r0)]));
+        }
+        const int rr = rb * RB + et;
+        if (rr < p.R) (which ? p.partials2 : p.partials)[(size_t)group * p.R + rr] = to_partial(m);
       }
-      const int rr = rb * RB + et;
-      if (rr < p.R) p.partials[(size_t)group * p.R + rr] = to_partial(m);
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
     }
   }
   __syncthreads();
@@ -494,36 +589,67 @@ int tc_num_partials(int R) {
   return groups > 0 ? groups : 1;
 }
 
-cudaError_t launch_draft_step_tc(const DraftArgs& a, int k, cudaStream_t s) {
-  using namespace tc;
+namespace tc {
+
+static TcParams base_params(int R, int gamma, int V, int rank, int dtype_u, float inv_temp, const void* U,
+                            const int64_t* req_id, uint64_t seed, uint64_t round, DeviceStatus* status) {
   TcParams p;
-  p.R = a.R;
-  p.gamma = a.gamma;
-  p.V = a.V;
-  p.rank = a.rank;
-  p.dtype_u = a.dtype_u;
-  p.Rb = block_rows(a.R);
-  p.rblocks = (a.R + p.Rb - 1) / p.Rb;
-  p.ngroups = tc_num_partials(a.R);
-  p.ntiles = (a.V + kN - 1) / kN;
-  p.k = k;
-  p.inv_temp = a.inv_temp;
-  p.U = a.U;
-  p.req_id = a.req_id;
-  p.seed = a.seed;
-  p.round = a.round;
-  p.partials = a.partials;
-  p.status = a.status;
+  memset(&p, 0, sizeof p);
+  p.R = R;
+  p.gamma = gamma;
+  p.V = V;
+  p.rank = rank;
+  p.dtype_u = dtype_u;
+  p.Rb = block_rows(R);
+  p.rblocks = (R + p.Rb - 1) / p.Rb;
+  p.ngroups = tc_num_partials(R);
+  p.ntiles = (V + kN - 1) / kN;
+  p.inv_temp = inv_temp;
+  p.U = U;
+  p.req_id = req_id;
+  p.seed = seed;
+  p.round = round;
+  p.status = status;
+  return p;
+}
+
+template <int MODE>
+static cudaError_t launch(const TcParams& p, const void* W1g, const void* W2, cudaStream_t s) {
   CUtensorMap map_a, map_b;
-  if (!make_map_2d(&map_a, a.W1g, (uint64_t)a.rank, (uint64_t)round_up_rows(a.R), kKAtom, (uint32_t)p.Rb))
+  if (!make_map_2d(&map_a, W1g, (uint64_t)p.rank, (uint64_t)round_up_rows(p.R), kKAtom, (uint32_t)p.Rb))
     return cudaErrorInvalidValue;
-  if (!make_map_2d(&map_b, a.W2, (uint64_t)a.V, (uint64_t)a.rank, 64, kKAtom)) return cudaErrorInvalidValue;
+  if (!make_map_2d(&map_b, W2, (uint64_t)p.V, (uint64_t)p.rank, 64, kKAtom)) return cudaErrorInvalidValue;
   const int smem = Smem::total + 1024;
-  auto kern = p.Rb == 32 ? draft_step_tc_kernel<32> : (p.Rb == 64 ? draft_step_tc_kernel<64> : draft_step_tc_kernel<128>);
+  auto kern = p.Rb == 32 ? draft_step_tc_kernel<32, MODE>
+                         : (p.Rb == 64 ? draft_step_tc_kernel<64, MODE> : draft_step_tc_kernel<128, MODE>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   kern<<<p.ngroups * p.rblocks, kThreads, smem, s>>>(map_a, map_b, p);
   return cudaGetLastError();
+}
+
+}  // namespace tc
+
+cudaError_t launch_draft_step_tc(const DraftArgs& a, int k, cudaStream_t s) {
+  tc::TcParams p = tc::base_params(a.R, a.gamma, a.V, a.rank, a.dtype_u, a.inv_temp, a.U, a.req_id, a.seed,
+                                   a.round, a.status);
+  p.k = k;
+  p.partials = a.partials;
+  return tc::launch<tc::kModeDraft>(p, a.W1g, a.W2, s);
+}
+
+cudaError_t launch_residual_tc(const VerifyArgs& a, cudaStream_t s) {
+  tc::TcParams p = tc::base_params(a.R, a.gamma, a.V, a.rank, a.dtype_u, a.inv_temp, a.U, a.req_id, a.seed,
+                                   a.round, a.status);
+  p.k = 1;
+  p.partials = a.res_part;
+  p.partials2 = a.res_part2;
+  p.target = a.target;
+  p.dtype_t = a.dtype_t;
+  p.jstar = a.jstar;
+  p.lse_q = a.lse_q;
+  p.lse_t = a.lse_t;
+  return tc::launch<tc::kModeResidual>(p, a.W1g, a.W2, s);
 }
 
 }  // namespace dspark

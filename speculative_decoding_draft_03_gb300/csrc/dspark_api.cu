@@ -63,7 +63,7 @@ VerifyLayout verify_layout(int R, int gamma, int V, int rank, int dtype_w) {
   VerifyLayout L;
   const size_t rows = (size_t)R * (gamma + 1);
   L.nchunk = (V + kVerifyChunk - 1) / kVerifyChunk;
-  L.npart = simt_num_chunks(V);
+  L.npart = residual_num_partials(R, V, rank, dtype_w);
   size_t off = 256;
   L.counters = off;
   off += 256;

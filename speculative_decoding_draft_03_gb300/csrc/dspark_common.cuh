@@ -34,16 +34,15 @@ __device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint3
                                                  uint32_t k0, uint32_t k1) {
 #pragma unroll
   for (int i = 0; i < 10; ++i) {
-    const uint32_t lo_a = 0xD2511F53u * c0;
-    const uint32_t hi_a = __umulhi(0xD2511F53u, c0);
-    const uint32_t lo_b = 0xCD9E8D57u * c2;
-    const uint32_t hi_b = __umulhi(0xCD9E8D57u, c2);
-    const uint32_t n0 = hi_b ^ c1 ^ k0;
-    const uint32_t n2 = hi_a ^ c3 ^ k1;
+    // one 32x32->64 product each (a single wide multiply), then the xor mix
+    const unsigned long long pa = 0xD2511F53ull * (unsigned long long)c0;
+    const unsigned long long pb = 0xCD9E8D57ull * (unsigned long long)c2;
+    const uint32_t n0 = (uint32_t)(pb >> 32) ^ c1 ^ k0;
+    const uint32_t n2 = (uint32_t)(pa >> 32) ^ c3 ^ k1;
     c0 = n0;
-    c1 = lo_b;
+    c1 = (uint32_t)pb;
     c2 = n2;
-    c3 = lo_a;
+    c3 = (uint32_t)pa;
     k0 += 0x9E3779B9u;
     k1 += 0xBB67AE85u;
   }
@@ -72,6 +71,57 @@ __device__ __forceinline__ Philox4 rng_chunk(const RngRow& r, uint32_t chunk) {
   return philox4x32_10(r.c0, r.c1, r.c2, chunk, r.k0, r.k1);
 }
 
+// The same generator specialised to one row: only the 4th counter word (the chunk)
+// varies, so the first round's products and half of the second round's are per-row
+// constants.  philox_row(...).block(chunk) == rng_chunk(row, chunk) bit for bit.
+struct PhiloxRow {
+  uint32_t p;     // round 1 input word 2 without the chunk:  hi(M_A c0) ^ k1
+  uint32_t g;     // round 2 output word 0 partial:          lo(M_B c2) ^ (k0 + W_A)
+  uint32_t e, f;  // round 2 output words 2, 3 (constant)
+  uint32_t k0, k1;
+
+  __device__ __forceinline__ Philox4 block(uint32_t chunk) const {
+    const uint32_t x2 = p ^ chunk;
+    const unsigned long long pb = 0xCD9E8D57ull * (unsigned long long)x2;
+    uint32_t c0 = (uint32_t)(pb >> 32) ^ g, c1 = (uint32_t)pb, c2 = e, c3 = f;
+    uint32_t a = k0 + 2u * 0x9E3779B9u, b = k1 + 2u * 0xBB67AE85u;
+#pragma unroll
+    for (int i = 2; i < 10; ++i) {
+      const unsigned long long qa = 0xD2511F53ull * (unsigned long long)c0;
+      const unsigned long long qb = 0xCD9E8D57ull * (unsigned long long)c2;
+      const uint32_t n0 = (uint32_t)(qb >> 32) ^ c1 ^ a;
+      const uint32_t n2 = (uint32_t)(qa >> 32) ^ c3 ^ b;
+      c0 = n0;
+      c1 = (uint32_t)qb;
+      c2 = n2;
+      c3 = (uint32_t)qa;
+      a += 0x9E3779B9u;
+      b += 0xBB67AE85u;
+    }
+    return Philox4{c0, c1, c2, c3};
+  }
+};
+
+__device__ __forceinline__ PhiloxRow philox_row(const RngRow& r) {
+  // round 1 with (c0, c1, c2, chunk): outputs (hi(pb)^c1^k0, lo(pb), hi(pa)^chunk^k1, lo(pa))
+  const unsigned long long pa = 0xD2511F53ull * (unsigned long long)r.c0;
+  const unsigned long long pb = 0xCD9E8D57ull * (unsigned long long)r.c2;
+  const uint32_t y0 = (uint32_t)(pb >> 32) ^ r.c1 ^ r.k0;
+  const uint32_t y1 = (uint32_t)pb;
+  const uint32_t y3 = (uint32_t)pa;
+  // round 2 (key + W): its A-product uses y0 only, a per-row constant
+  const uint32_t ka = r.k0 + 0x9E3779B9u, kb = r.k1 + 0xBB67AE85u;
+  const unsigned long long qa = 0xD2511F53ull * (unsigned long long)y0;
+  PhiloxRow o;
+  o.p = (uint32_t)(pa >> 32) ^ r.k1;
+  o.g = y1 ^ ka;
+  o.e = (uint32_t)(qa >> 32) ^ y3 ^ kb;
+  o.f = (uint32_t)qa;
+  o.k0 = r.k0;
+  o.k1 = r.k1;
+  return o;
+}
+
 // u = ((bits >> 8) + 0.5) * 2^-24 = (2b+1) * 2^-25 with b = bits >> 8, strictly inside
 // (0,1).  binary64 holds it exactly; binary32 holds u exactly for b < 2^23 (u < 1/2)
 // and 1-u = (2^25-2b-1) * 2^-25 exactly for b >= 2^23.
@@ -94,6 +144,22 @@ __device__ __forceinline__ float neg_log_uniform(uint32_t bits) {
 
 // Standard Gumbel g = -ln(-ln u) = -ln E.
 __device__ __forceinline__ float gumbel_from_bits(uint32_t bits) { return -logf(neg_log_uniform(bits)); }
+
+// 1 - u in binary32 (exact for u >= 1/2, within one rounding below).  Since
+// E = -ln u = -ln(1 - w) >= w, an element with w >= t has E >= t.
+__device__ __forceinline__ float one_minus_uniform(uint32_t bits) {
+  return __uint2float_rn((1u << 25) - 2u * (bits >> 8) - 1u) * 0x1.0p-25f;
+}
+
+// Exact rejection test of the Gumbel-max race.  key = z + g beats `best` only if
+// E < exp(z - best).  `t` must be an upper bound of exp(z - best); callers inflate
+// it by a small factor to cover the rounding of exp and of w.  Returns true when the
+// element certainly cannot beat `best`, without evaluating any logarithm.
+__device__ __forceinline__ bool gumbel_cannot_win(uint32_t bits, float t) { return one_minus_uniform(bits) >= t; }
+
+// Relative inflation of exp(z - best) in the rejection test: covers the error of the
+// fast exponential (a few ulp), the rounding of w, and leaves a wide margin (e^0.002).
+constexpr float kRejectSlack = 1.002f;
 
 // ---------------------------------------------------------------------------------
 // Loads

@@ -98,5 +98,7 @@ cudaError_t launch_schedule(int R, int gamma, const float* conf, const double* s
 size_t schedule_smem_bytes(int R, int gamma);
 
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s);
+cudaError_t launch_residual_tc(const VerifyArgs& a, cudaStream_t s);
+int residual_num_partials(int R, int V, int rank, int dtype_w);
 
 }  // namespace dspark

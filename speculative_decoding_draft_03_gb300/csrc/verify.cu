@@ -360,17 +360,32 @@ cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s) {
   const int wblocks = (a.R * 32 + 255) / 256;
   verify_accept_kernel<<<wblocks, 256, 0, s>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  dim3 rgrid(simt_num_chunks(a.V), (a.R + kSimtRB - 1) / kSimtRB);
-  const size_t smem = sizeof(float) * kSimtRB * a.rank;
-  if (smem > 48 * 1024) {
-    e = cudaFuncSetAttribute(residual_step_simt_kernel<kSimtRB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-    if (e != cudaSuccess) return e;
+  int npart;
+  if (tc_supported(a.V, a.rank, a.dtype_w)) {
+    // the residual recomputes one bias row per rejected request on the tensor cores
+    if ((e = launch_residual_tc(a, s)) != cudaSuccess) return e;
+    npart = tc_num_partials(a.R);
+  } else {
+    dim3 rgrid(simt_num_chunks(a.V), (a.R + kSimtRB - 1) / kSimtRB);
+    const size_t smem = sizeof(float) * kSimtRB * a.rank;
+    if (smem > 48 * 1024) {
+      e = cudaFuncSetAttribute(residual_step_simt_kernel<kSimtRB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem);
+      if (e != cudaSuccess) return e;
+    }
+    residual_step_simt_kernel<kSimtRB><<<rgrid, kSimtThreads, smem, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    npart = (int)rgrid.x;
   }
-  residual_step_simt_kernel<kSimtRB><<<rgrid, kSimtThreads, smem, s>>>(a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  residual_combine_kernel<<<wblocks, 256, 0, s>>>(a, (int)rgrid.x);
+  residual_combine_kernel<<<wblocks, 256, 0, s>>>(a, npart);
   return cudaGetLastError();
+}
+
+int residual_num_partials(int R, int V, int rank, int dtype_w) {
+  const int simt = simt_num_chunks(V);
+  if (!tc_supported(V, rank, dtype_w)) return simt;
+  const int tc = tc_num_partials(R);
+  return simt > tc ? simt : tc;
 }
 
 }  // namespace dspark

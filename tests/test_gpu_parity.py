@@ -195,6 +195,19 @@ def test_draft_bias_dominant(R, V, rank):
                              x0.numpy(), ids.numpy(), 5, 9)
     tally = Tally()
     compare_draft(_np(gd), od, 2e-3, tally)
+    # verification of the oracle's drafts: the residual recomputes the same bias rows
+    target = torch.cat([U, U[:, -1:]], 1) + torch.randn((R, gamma + 1, V), generator=g) * 0.8
+    ell = torch.randint(0, gamma + 1, (R,), generator=g, dtype=torch.int32)
+    logq = od["logq"].astype(np.float32)
+    lse = od["lse"].astype(np.float32)
+    ov = oracle.verify(target.numpy(), U.numpy(), bits(W1), bits(W2), x0.numpy(), od["x"], logq, lse, ell.numpy(),
+                       1.0, ids.numpy(), 5, 9)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    gv = b.verify(target.cuda(), U.cuda(), W1.cuda(), W2.cuda(), x0.cuda(), t(od["x"]), t(logq), t(lse), ell.cuda(),
+                  1.0, ids.cuda(), 5, 9)
+    torch.cuda.synchronize()
+    compare_verify(_np(gv), ov, tally)
+    assert (ov["corr_kind"] == 1).sum() >= min(R, 3)  # residual draws were exercised
     tally.check_rate()
 
 
