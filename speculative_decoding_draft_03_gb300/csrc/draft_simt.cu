@@ -9,19 +9,26 @@
 //                  statistics and Gumbel-max draw, one partial record per
 //                  (vocabulary chunk, request)
 //   draft_combine  merges the partials of a position into x_k, lse_k, logq_k and
-//                  prepares position k+1.
+//                  prepares position k+1 (one CTA per request).
 //
 // Method: numb3r33 blog "DSpark: confidence-scheduled speculative decoding", sections
 // "Markov sequential head" (p_k(v|x_{k-1}) = softmax(U_k(v) + W1[x_{k-1}] W2)) and
 // "Confidence head"; DSpark 精读 §2 and §4 (confidence on [h_k ; W1[x_{k-1}]]).
+//
+// Every kernel is launched with programmatic dependent launch and waits for its
+// predecessor (griddep_wait) before its first dependent access.
 #include "dspark_common.cuh"
 #include "dspark_internal.h"
 
 namespace dspark {
 
+constexpr int kCombineThreads = 128;
+
 // One warp per (r,k) row of h.
 __global__ void conf_hdot_kernel(int rows, int d, int dtype_h, const void* __restrict__ h,
                                  const float* __restrict__ w_h, float* __restrict__ s_h) {
+  griddep_allow_next();
+  griddep_wait();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= rows) return;
@@ -46,8 +53,23 @@ __global__ void conf_hdot_kernel(int rows, int d, int dtype_h, const void* __res
   if (lane == 0) s_h[warp] = acc;
 }
 
-// Gather W1[x_prev] into W1g[r] and write c_k; executed by one full warp.
-__device__ __forceinline__ void prepare_position(const DraftArgs& a, int r, int k, int x_prev, int lane) {
+// Block-wide sum over kCombineThreads threads (result valid in every thread).
+__device__ __forceinline__ float block_sum(float v, float* scratch) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < kCombineThreads / 32; ++w) t += scratch[w];
+  return t;
+}
+
+// Gather W1[x_prev] into W1g[r] and write c_k; executed by a whole CTA of
+// kCombineThreads threads.
+__device__ void prepare_position_block(const DraftArgs& a, int r, int k, int x_prev, float* scratch) {
   const size_t src = (size_t)x_prev * a.rank;
   const size_t dst = (size_t)r * a.rank;
   float acc = 0.f;
@@ -55,7 +77,7 @@ __device__ __forceinline__ void prepare_position(const DraftArgs& a, int r, int 
   if (a.dtype_w == DSPARK_BF16) {
     const unsigned short* w1 = reinterpret_cast<const unsigned short*>(a.W1);
     unsigned short* g = reinterpret_cast<unsigned short*>(a.W1g);
-    for (int i = lane; i < a.rank; i += 32) {
+    for (int i = threadIdx.x; i < a.rank; i += blockDim.x) {
       const unsigned short b = __ldg(w1 + src + i);
       g[dst + i] = b;
       acc = fmaf(__ldg(w_e + i), bf16_bits_to_float(b), acc);
@@ -63,28 +85,32 @@ __device__ __forceinline__ void prepare_position(const DraftArgs& a, int r, int 
   } else {
     const float* w1 = reinterpret_cast<const float*>(a.W1);
     float* g = reinterpret_cast<float*>(a.W1g);
-    for (int i = lane; i < a.rank; i += 32) {
+    for (int i = threadIdx.x; i < a.rank; i += blockDim.x) {
       const float b = __ldg(w1 + src + i);
       g[dst + i] = b;
       acc = fmaf(__ldg(w_e + i), b, acc);
     }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) {
+  acc = block_sum(acc, scratch);
+  if (threadIdx.x == 0) {
     const size_t row = (size_t)r * a.gamma + (k - 1);
     const float logit = a.conf_scale * (a.s_h[row] + acc + a.conf_b);
     a.conf_out[row] = sigmoidf_dev(logit / __ldg(a.conf_temp + (k - 1)));
+    // no Gumbel key of position k has been seen yet: the running bound starts at -inf
+    // (the order-preserving int code of -inf)
+    a.hint[r] = __float_as_int(-INFINITY) ^ 0x7FFFFFFF;
   }
 }
 
-__global__ void draft_prepare_kernel(DraftArgs a, int k) {
-  const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (r >= a.R) return;
+// One CTA per request.
+__global__ void __launch_bounds__(kCombineThreads) draft_prepare_kernel(DraftArgs a, int k) {
+  griddep_allow_next();
+  griddep_wait();
+  __shared__ float scratch[kCombineThreads / 32];
+  const int r = blockIdx.x;
   const int raw = (k == 1) ? __ldg(a.x0 + r) : a.x_out[(size_t)r * a.gamma + (k - 2)];
   const int x_prev = checked_token(raw, a.V, a.status, 1);
-  prepare_position(a, r, k, x_prev, lane);
+  prepare_position_block(a, r, k, x_prev, scratch);
 }
 
 // ---------------------------------------------------------------------------------
@@ -94,6 +120,7 @@ __global__ void draft_prepare_kernel(DraftArgs a, int k) {
 // ---------------------------------------------------------------------------------
 template <int RB>
 __global__ void __launch_bounds__(kSimtThreads) draft_step_simt_kernel(DraftArgs a, int k) {
+  griddep_wait();
   extern __shared__ float w1s[];  // [RB][rank]
   const int r0 = blockIdx.y * RB;
   for (int i = threadIdx.x; i < RB * a.rank; i += blockDim.x) {
@@ -184,23 +211,34 @@ __global__ void __launch_bounds__(kSimtThreads) draft_step_simt_kernel(DraftArgs
   }
 }
 
-// One warp per request: merge npart partials of position k; then prepare position k+1.
-__global__ void draft_combine_kernel(DraftArgs a, int k, int npart) {
-  const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (r >= a.R) return;
+// One CTA per request: merge npart partials of position k; then prepare position k+1.
+__global__ void __launch_bounds__(kCombineThreads) draft_combine_kernel(DraftArgs a, int k, int npart) {
+  griddep_allow_next();
+  griddep_wait();
+  __shared__ Partial red[kCombineThreads / 32];
+  __shared__ float scratch[kCombineThreads / 32];
+  __shared__ int xk_s;
+  const int r = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   Stats st = stats_empty();
-  for (int p = lane; p < npart; p += 32) stats_merge(st, from_partial(a.partials[(size_t)p * a.R + r]));
+  for (int p = threadIdx.x; p < npart; p += blockDim.x) stats_merge(st, from_partial(a.partials[(size_t)p * a.R + r]));
   st = warp_reduce_stats(st);
-  const int xk = st.idx;
-  if (lane == 0) {
-    const size_t row = (size_t)r * a.gamma + (k - 1);
-    const float lse = st.m + logf(st.s);
-    a.x_out[row] = xk;
-    a.lse_out[row] = lse;
-    a.logq_out[row] = st.zsel - lse;
+  if (lane == 0) red[warp] = to_partial(st);
+  __syncthreads();
+  if (warp == 0) {
+    Stats b = (lane < kCombineThreads / 32) ? from_partial(red[lane]) : stats_empty();
+    b = warp_reduce_stats(b);
+    if (lane == 0) {
+      const size_t row = (size_t)r * a.gamma + (k - 1);
+      const float lse = b.m + logf(b.s);
+      a.x_out[row] = b.idx;
+      a.lse_out[row] = lse;
+      a.logq_out[row] = b.zsel - lse;
+      xk_s = checked_token(b.idx, a.V, a.status, 2);
+    }
   }
-  if (k < a.gamma) prepare_position(a, r, k + 1, checked_token(xk, a.V, a.status, 2), lane);
+  __syncthreads();
+  if (k < a.gamma) prepare_position_block(a, r, k + 1, xk_s, scratch);
 }
 
 // ---------------------------------------------------------------------------------
@@ -210,15 +248,12 @@ cudaError_t launch_conf_hdot(const DraftArgs& a, cudaStream_t s) {
   const int rows = a.R * a.gamma;
   const int threads = 256;
   const int blocks = (rows * 32 + threads - 1) / threads;
-  conf_hdot_kernel<<<blocks, threads, 0, s>>>(rows, a.d, a.dtype_h, a.h, a.conf_w, a.s_h);
-  return cudaGetLastError();
+  return launch_pdl(conf_hdot_kernel, dim3(blocks), dim3(threads), 0, s, rows, a.d, a.dtype_h, a.h, a.conf_w,
+                    a.s_h);
 }
 
 cudaError_t launch_draft_prepare(const DraftArgs& a, int k, cudaStream_t s) {
-  const int threads = 256;
-  const int blocks = (a.R * 32 + threads - 1) / threads;
-  draft_prepare_kernel<<<blocks, threads, 0, s>>>(a, k);
-  return cudaGetLastError();
+  return launch_pdl(draft_prepare_kernel, dim3(a.R), dim3(kCombineThreads), 0, s, a, k);
 }
 
 int simt_num_chunks(int V) {
@@ -235,15 +270,11 @@ cudaError_t launch_draft_step_simt(const DraftArgs& a, int k, cudaStream_t s) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  draft_step_simt_kernel<kSimtRB><<<grid, kSimtThreads, smem, s>>>(a, k);
-  return cudaGetLastError();
+  return launch_pdl(draft_step_simt_kernel<kSimtRB>, grid, dim3(kSimtThreads), smem, s, a, k);
 }
 
 cudaError_t launch_draft_combine(const DraftArgs& a, int k, int npart, cudaStream_t s) {
-  const int threads = 256;
-  const int blocks = (a.R * 32 + threads - 1) / threads;
-  draft_combine_kernel<<<blocks, threads, 0, s>>>(a, k, npart);
-  return cudaGetLastError();
+  return launch_pdl(draft_combine_kernel, dim3(a.R), dim3(kCombineThreads), 0, s, a, k, npart);
 }
 
 }  // namespace dspark

@@ -5,26 +5,31 @@
 // and reduces each request's row to (max, sum exp, Gumbel-max key/id) partials, so the
 // vocabulary row is streamed exactly once per position (numb3r33 blog "DSpark:
 // confidence-scheduled speculative decoding", section "Markov sequential head";
-// DSpark 精读 §2: p_k = softmax(U_k + W1[x_{k-1}] W2), sampled left to right).
+// DSpark 精读 §2: p_k = softmax(U_k + W1[x_{k-1}] W2), sampled left to right).  A
+// second epilogue mode recomputes the rejected position's row for the (p - q)+
+// residual draw of verification.
 //
 // GB300 mapping
 //   * The bias is an [R x rank] x [rank x V] contraction: tcgen05.mma kind::f16
 //     (bf16 x bf16 -> fp32), M = 128 requests (TMEM lanes), N = 128 vocabulary ids per
 //     tile (TMEM columns), K = rank.  The gathered factor rows W1[x_{k-1}] (A, K-major)
 //     stay resident in shared memory; W2 tiles (B, read in its natural [rank, V] layout,
-//     i.e. MN-major) stream through a TMA ring with 128-byte swizzle.
+//     i.e. MN-major) stream through a TMA ring with 128-byte swizzle, marked to stay in
+//     L2 across the draft positions of a round.
 //   * Accumulators live in TMEM, double-buffered (2 x 128 columns) so the MMA of tile
 //     t+1 overlaps the epilogue of tile t.
-//   * Epilogue: each thread owns one request (its TMEM lane) and a run of consecutive
-//     vocabulary ids, so softmax statistics and the Gumbel-max draw are thread-local
-//     (no shuffles per element) and one Philox block serves 4 consecutive ids.
+//   * Epilogue (16 warps, 4 per TMEM lane quarter): each thread owns one request (its
+//     TMEM lane) and runs of 8 consecutive vocabulary ids, so softmax statistics and the
+//     Gumbel-max draw are thread-local and one Philox block serves 4 consecutive ids.
+//     Random words are only turned into Gumbel keys for elements that survive an exact
+//     log-free rejection test against the best key known so far.
 //   * Few requests (R <= 64): the request rows are replicated across the 4 TMEM lane
 //     quarters and each quarter takes a different part of the tile's columns, so all
 //     epilogue warps stay busy.
 //   * Many requests (R > 128): CTAs are grouped by request block; the CTAs of a group
 //     walk the same W2 tiles at the same time, so W2 comes from HBM once per position
 //     and from L2 for the other request blocks.
-//   * Warp roles: warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer, warps 2..9
+//   * Warp roles: warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer, warps 2..17
 //     epilogue.  Every mbarrier wait is bounded; a wait that gives up records
 //     DSPARK_TIMEOUT in the workspace status word and the CTA winds down cleanly.
 #include <cuda.h>
@@ -42,17 +47,20 @@ constexpr int kN = 128;           // vocabulary ids per tile
 constexpr int kKAtom = 64;        // bf16 elements per 128-byte swizzle row
 constexpr int kStages = 8;        // W2 ring stages (one 64-deep K slice of a tile each)
 constexpr int kStageBytes = kN * kKAtom * 2;  // 16 KB
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;
+constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kCols = 8;          // vocabulary ids per epilogue pass
 constexpr int kTmemCols = 2 * kN;
 constexpr int kMaxRank = 256;
 constexpr long long kWaitCycles = 4000000000ll;  // ~2 s at 2 GHz
+constexpr int kPublishTiles = 2;  // tiles after which a CTA publishes its best keys
 
 struct Smem {
   // offsets from the 1024-byte aligned base
   static constexpr int a = 0;                                  // [rank/64][128 rows][128 B]
   static constexpr int b = a + kM * kMaxRank * 2;              // [stages][2][64 rows][128 B]
-  static constexpr int red = b + kStages * kStageBytes;        // [8 warps][32] Partial
+  static constexpr int red = b + kStages * kStageBytes;        // [16 warps][32] Partial
   static constexpr int bars = red + kEpiWarps * 32 * 32;       // mbarriers
   static constexpr int total = bars + 256;
 };
@@ -101,13 +109,35 @@ __device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_fla
   }
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+// 2-D tensor load with an L2 eviction-priority policy.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                            uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
-          dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, "
+      "%4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
       : "memory");
 }
+
+// The W2 factor is re-read at every draft position of a round: keep it resident.
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// Order-preserving int encoding of a float (for atomicMax on keys of any sign).
+__device__ __forceinline__ int ordered_key(float f) {
+  const int i = __float_as_int(f);
+  return i >= 0 ? i : i ^ 0x7FFFFFFF;
+}
+__device__ __forceinline__ float key_from_ordered(int i) { return __int_as_float(i >= 0 ? i : i ^ 0x7FFFFFFF); }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
@@ -136,19 +166,16 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// 16 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
+// 8 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[kCols]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 descriptor format:
@@ -182,6 +209,7 @@ struct TcParams {
   const int64_t* req_id;
   uint64_t seed, round;
   Partial* partials;  // [ngroups, R]
+  int* hint;          // [R] published best keys (draft mode)
   DeviceStatus* status;
   // residual mode
   const void* target;
@@ -194,6 +222,38 @@ struct TcParams {
 
 constexpr int kModeDraft = 0;
 constexpr int kModeResidual = 1;
+
+// 8 consecutive ids of U (fp32 or bf16) as fp32; ids at or beyond V read as 0 (V % 8 == 0,
+// so a run of 8 is either entirely inside the row or entirely outside).
+__device__ __forceinline__ void load_run8(const void* base, int dtype, size_t row, int v, int V, bool valid,
+                                          uint4 (&raw)[2]) {
+  if (!valid || v >= V) {
+    raw[0] = raw[1] = make_uint4(0u, 0u, 0u, 0u);
+  } else if (dtype == DSPARK_F32) {
+    const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const float*>(base) + row + v);
+    raw[0] = __ldg(src);
+    raw[1] = __ldg(src + 1);
+  } else {
+    raw[0] = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned short*>(base) + row + v));
+    raw[1] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+__device__ __forceinline__ void decode_run8(int dtype, const uint4 (&raw)[2], float (&x)[kCols]) {
+  if (dtype == DSPARK_F32) {
+    x[0] = __uint_as_float(raw[0].x); x[1] = __uint_as_float(raw[0].y);
+    x[2] = __uint_as_float(raw[0].z); x[3] = __uint_as_float(raw[0].w);
+    x[4] = __uint_as_float(raw[1].x); x[5] = __uint_as_float(raw[1].y);
+    x[6] = __uint_as_float(raw[1].z); x[7] = __uint_as_float(raw[1].w);
+  } else {
+    const uint32_t wd[4] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      x[2 * e] = bf16_bits_to_float(wd[e] & 0xFFFFu);
+      x[2 * e + 1] = bf16_bits_to_float(wd[e] >> 16);
+    }
+  }
+}
 
 // RB: requests per block (32, 64 or 128); the 128 MMA rows hold 128/RB copies of it.
 // MODE: kModeDraft (one draft position for every request) or kModeResidual (the
@@ -246,27 +306,42 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------
     if (lane == 0) {
-      constexpr int rep = kM / RB;
-      mbar_arrive_expect_tx(bar_a, (uint32_t)(kM * p.rank * 2));
-      for (int j = 0; j < rep; ++j)
-        for (int ka = 0; ka < katoms; ++ka)
-          tma_load_2d(sbase + Smem::a + ka * (kM * 128) + j * RB * 128, &map_a, bar_a, ka * kKAtom, rb * RB);
+      // The factor rows (A) are written by the preceding kernel; W2 (B) is an input.
+      // So the first ring's worth of W2 stages is issued before waiting for the
+      // predecessor, and A right after.
+      const uint64_t w2_policy = policy_evict_last();
+      const uint64_t a_policy = policy_evict_normal();
+      auto load_a = [&]() {
+        griddep_wait();
+        constexpr int rep = kM / RB;
+        mbar_arrive_expect_tx(bar_a, (uint32_t)(kM * p.rank * 2));
+        for (int j = 0; j < rep; ++j)
+          for (int ka = 0; ka < katoms; ++ka)
+            tma_load_2d(sbase + Smem::a + ka * (kM * 128) + j * RB * 128, &map_a, bar_a, ka * kKAtom, rb * RB,
+                        a_policy);
+      };
+      const int total = my_tiles * katoms;
+      bool a_issued = false;
       int stage = 0;
       uint32_t phase = 0;
-      for (int t = 0; t < my_tiles && !*abort_flag; ++t) {
+      for (int it = 0; it < total && !*abort_flag; ++it) {
+        if (it == kStages) {
+          load_a();
+          a_issued = true;
+        }
+        const int t = it / katoms, ka = it % katoms;
         const int v0 = (group + t * p.ngroups) * kN;
-        for (int ka = 0; ka < katoms; ++ka) {
-          if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag, p.status, 100)) break;
-          const uint32_t dst = sbase + Smem::b + stage * kStageBytes;
-          mbar_arrive_expect_tx(bar_full + 8 * stage, kStageBytes);
-          tma_load_2d(dst, &map_b, bar_full + 8 * stage, v0, ka * kKAtom);
-          tma_load_2d(dst + kStageBytes / 2, &map_b, bar_full + 8 * stage, v0 + 64, ka * kKAtom);
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1;
-          }
+        if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag, p.status, 100)) break;
+        const uint32_t dst = sbase + Smem::b + stage * kStageBytes;
+        mbar_arrive_expect_tx(bar_full + 8 * stage, kStageBytes);
+        tma_load_2d(dst, &map_b, bar_full + 8 * stage, v0, ka * kKAtom, w2_policy);
+        tma_load_2d(dst + kStageBytes / 2, &map_b, bar_full + 8 * stage, v0 + 64, ka * kKAtom, w2_policy);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1;
         }
       }
+      if (!a_issued) load_a();
     }
   } else if (warp == 1) {
     // ------------------------------ MMA issuer --------------------------------
@@ -311,16 +386,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------ epilogue ----------------------------------
-    const int ew = warp - 2;               // 0..7
+    const int ew = warp - 2;               // 0..15
     const int quarter = warp & 3;          // TMEM lane quarter this warp may access
-    const int sub = ew >> 2;               // 0..1: which half of the quarter's columns
+    const int sub = ew >> 2;               // 0..3: which quarter of the replica's columns
     const int row0 = (quarter * 32) % RB;
     const int replica = (quarter * 32) / RB;
     const int r = rb * RB + row0 + lane;
     bool valid = r < p.R;
-    constexpr int kPass = RB / 32;         // 16-column passes per tile: 1, 2 or 4
-    const int col0 = replica * RB + sub * (RB / 2);  // RB columns per replica, half per warp
+    constexpr int kPass = RB / 32;         // 8-column passes per tile: 1, 2 or 4
+    const int col0 = replica * RB + sub * (RB / 4);  // RB columns per replica, a quarter per warp
 
+    // the residual's positions and normalisers come from the preceding kernel
+    if constexpr (MODE == kModeResidual) griddep_wait();
     // draft: position k of every request; residual: the rejected position j* (0 = none)
     int pos = p.k;
     float lse_q = 0.f, lse_t = 0.f;
@@ -339,46 +416,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     const size_t urow = ((size_t)(valid ? r : 0) * p.gamma + (valid ? pos - 1 : 0)) * (size_t)p.V;
     const size_t trow = ((size_t)(valid ? r : 0) * (p.gamma + 1) + (valid ? pos - 1 : 0)) * (size_t)p.V;
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-    const bool u_f32 = p.dtype_u == DSPARK_F32;
 
     // U of the next tile is loaded into registers while the current one is processed
-    uint4 unext[kPass][4];
-    auto load_u = [&](int t, uint4 (&dst)[kPass][4]) {
+    uint4 unext[kPass][2];
+    auto load_u = [&](int t, uint4 (&dst)[kPass][2]) {
       const int vt = (group + t * p.ngroups) * kN;
 #pragma unroll
-      for (int ps = 0; ps < kPass; ++ps) {
-        const int vb = vt + col0 + ps * 16;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          // fp32: 4 ids per 16 bytes; bf16: 8 ids per 16 bytes (only q < 2 used)
-          const int v = u_f32 ? vb + 4 * q : vb + 8 * q;
-          const bool in = valid && t < my_tiles && (u_f32 || q < 2) && v < p.V;
-          dst[ps][q] = in ? (u_f32 ? __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const float*>(p.U) + urow + v))
-                                   : __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned short*>(p.U) +
-                                                                           urow + v)))
-                          : make_uint4(0u, 0u, 0u, 0u);
-        }
-      }
+      for (int ps = 0; ps < kPass; ++ps)
+        load_run8(p.U, p.dtype_u, urow, vt + col0 + ps * kCols, p.V, valid && t < my_tiles, dst[ps]);
     };
     load_u(0, unext);
+    // U is an input: its first tile is in flight before waiting for the predecessor,
+    // which still reads the partial records this kernel overwrites at the end
+    if constexpr (MODE == kModeDraft) griddep_wait();
+
+    // Draft mode: the best key any CTA has published for this request at this position.
+    // Every published value is the key of an actual element, so it is a lower bound of
+    // the final winner's key and elements that cannot reach it can be skipped.
+    float published = -INFINITY;
+    float bound = -INFINITY;
 
     for (int t = 0; t < my_tiles; ++t) {
       const int buf = t & 1;
       const uint32_t use = (uint32_t)(t >> 1) & 1u;
       const int vt = (group + t * p.ngroups) * kN;
-      uint4 ucur[kPass][4];
-#pragma unroll
-      for (int ps = 0; ps < kPass; ++ps)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) ucur[ps][q] = unext[ps][q];
-      load_u(t + 1, unext);
-      if (!mbar_wait(bar_acc_full + 8 * buf, use, abort_flag, p.status, 300)) break;
-      tc_fence_after();
+      uint4 ucur[kPass][2];
 #pragma unroll
       for (int ps = 0; ps < kPass; ++ps) {
-        const int c = col0 + ps * 16;
-        float bias[16];
-        tmem_ld16(tmem_base + lane_addr + buf * kN + c, bias);
+        ucur[ps][0] = unext[ps][0];
+        ucur[ps][1] = unext[ps][1];
+      }
+      load_u(t + 1, unext);
+      // On an abandoned wait the warp keeps iterating without touching TMEM, so that
+      // every epilogue warp still meets the same named barriers.
+      const bool acc_ready = mbar_wait(bar_acc_full + 8 * buf, use, abort_flag, p.status, 300);
+      if (acc_ready) tc_fence_after();
+#pragma unroll
+      for (int ps = 0; ps < kPass; ++ps) {
+        if (!acc_ready) break;
+        const int c = col0 + ps * kCols;
+        float bias[kCols];
+        tmem_ld8(tmem_base + lane_addr + buf * kN + c, bias);
         if (ps == kPass - 1) {
           // all of this warp's columns are in registers: hand the accumulator back
           tc_fence_before();
@@ -387,76 +465,78 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int vb = vt + c;
         if (!valid || vb >= p.V) continue;
-        float z[16];
-        if (u_f32) {
+        float z[kCols];
+        decode_run8(p.dtype_u, ucur[ps], z);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            z[4 * q + 0] = __uint_as_float(ucur[ps][q].x);
-            z[4 * q + 1] = __uint_as_float(ucur[ps][q].y);
-            z[4 * q + 2] = __uint_as_float(ucur[ps][q].z);
-            z[4 * q + 3] = __uint_as_float(ucur[ps][q].w);
-          }
-        } else {
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const uint32_t wd[4] = {ucur[ps][q].x, ucur[ps][q].y, ucur[ps][q].z, ucur[ps][q].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              z[8 * q + 2 * e] = bf16_bits_to_float(wd[e] & 0xFFFFu);
-              z[8 * q + 2 * e + 1] = bf16_bits_to_float(wd[e] >> 16);
-            }
-          }
-        }
-        const int nvalid = min(16, p.V - vb);  // V % 8 == 0: 8 or 16
-#pragma unroll
-        for (int i = 0; i < 16; ++i) z[i] = (z[i] + bias[i]) * p.inv_temp;
+        for (int i = 0; i < kCols; ++i) z[i] = (z[i] + bias[i]) * p.inv_temp;
         if constexpr (MODE == kModeDraft) {
-          float cmax = -INFINITY;
+          float cmax = z[0];
+          int imax = 0;
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (i < nvalid) cmax = fmaxf(cmax, z[i]);
-          // online softmax statistics over the 16 ids; term_i = exp(z_i - m)
+          for (int i = 1; i < kCols; ++i)
+            if (z[i] > cmax) {
+              cmax = z[i];
+              imax = i;
+            }
+          // online softmax statistics over the 8 ids; term_i = exp(z_i - m)
           const float mnew = fmaxf(st.m, cmax);
           float acc = (st.m == -INFINITY) ? 0.f : st.s * __expf(st.m - mnew);
-          float term[16];
+          float term[kCols];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            term[i] = (i < nvalid) ? __expf(z[i] - mnew) : 0.f;
+          for (int i = 0; i < kCols; ++i) {
+            term[i] = __expf(z[i] - mnew);
             acc += term[i];
           }
           st.m = mnew;
           st.s = acc;
-          // Gumbel-max draw.  The 16 ids' random words come from 4 independent Philox
-          // blocks (no branches, so they interleave).  An element is rejected without
-          // logarithms when 1-u >= exp(z - best) = term * exp(m - best) -- it then
-          // cannot beat the running key -- and only the rare survivors evaluate z + g.
-          uint32_t wd[16];
+          // Gumbel-max draw against the best key known so far (own record or published).
+          // A run whose largest logit cannot reach it even with the largest possible
+          // Gumbel needs no random bits.  Otherwise the 8 ids' words come from two
+          // independent Philox blocks; an element is rejected without logarithms when
+          // 1-u >= exp(z - best) = term * exp(m - best), and only survivors evaluate
+          // their key.  Without any known key, the run's largest logit is keyed first so
+          // that the others are tested against it.
+          float thr = fmaxf(st.idx >= 0 ? st.key : -INFINITY, bound);
+          if (thr > -INFINITY && cmax + kGumbelMax < thr) continue;
+          uint32_t wd[kCols];
 #pragma unroll
-          for (int g4 = 0; g4 < 4; ++g4) {
+          for (int g4 = 0; g4 < 2; ++g4) {
             const Philox4 bits = prow.block((uint32_t)((vb >> 2) + g4));
             wd[4 * g4 + 0] = bits.x;
             wd[4 * g4 + 1] = bits.y;
             wd[4 * g4 + 2] = bits.z;
             wd[4 * g4 + 3] = bits.w;
           }
-          const float scale = (st.idx >= 0) ? __expf(mnew - st.key) * kRejectSlack : INFINITY;
+          if (thr == -INFINITY) {
+            uint32_t wm = wd[0];
+#pragma unroll
+            for (int i = 1; i < kCols; ++i)
+              if (i == imax) wm = wd[i];
+            const float key = cmax + gumbel_from_bits(wm);
+            st.key = key;
+            st.idx = vb + imax;
+            st.zsel = cmax;
+            thr = key;
+          }
+          const float scale = __expf(mnew - thr) * kRejectSlack;
           uint32_t cand = 0;
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (i < nvalid && !gumbel_cannot_win(wd[i], term[i] * scale)) cand |= 1u << i;
+          for (int i = 0; i < kCols; ++i)
+            if (!gumbel_cannot_win(wd[i], term[i] * scale)) cand |= 1u << i;
           while (cand) {
             const int i = __ffs(cand) - 1;
             cand &= cand - 1;
             float zi = 0.f;
             uint32_t wi = 0u;
 #pragma unroll
-            for (int j = 0; j < 16; ++j)  // static register selection (no local memory)
+            for (int j = 0; j < kCols; ++j)  // static register selection (no local memory)
               if (j == i) {
                 zi = z[j];
                 wi = wd[j];
               }
+            if (vb + i == st.idx) continue;  // already keyed above
             const float key = zi + gumbel_from_bits(wi);
-            if (st.idx < 0 || key > st.key) {
+            if (key > st.key || (key == st.key && vb + i < st.idx)) {
               st.key = key;
               st.idx = vb + i;
               st.zsel = zi;
@@ -465,16 +545,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           // residual: q = exp(z - lse_q), p = exp(t/T - lse_t); draw from (p - q)+ by
           // Gumbel-max over ln(p - q) where positive, and keep the ln p draw as fallback
-          float lp[16];
+          uint4 traw[2];
+          load_run8(p.target, p.dtype_t, trow, vb, p.V, true, traw);
+          float lp[kCols];
+          decode_run8(p.dtype_t, traw, lp);
+          float gmax = -INFINITY;
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            lp[i] = (i < nvalid) ? load_elem(p.target, p.dtype_t, trow + vb + i) * p.inv_temp - lse_t : -INFINITY;
+          for (int i = 0; i < kCols; ++i) {
+            lp[i] = lp[i] * p.inv_temp - lse_t;
+            gmax = fmaxf(gmax, lp[i]);
+          }
+          // ln(p - q) <= ln p: neither draw can improve once ln p + G_max is below both keys
+          if (st.idx >= 0 && fb.idx >= 0 && gmax + kGumbelMax < st.key && gmax + kGumbelMax < fb.key) continue;
 #pragma unroll
-          for (int g4 = 0; g4 < 4; ++g4) {
-            if (4 * g4 >= nvalid) break;
-            const float gmax = fmaxf(fmaxf(lp[4 * g4], lp[4 * g4 + 1]), fmaxf(lp[4 * g4 + 2], lp[4 * g4 + 3]));
-            // ln(p - q) <= ln p: neither draw can improve once ln p + G_max is below both keys
-            if (st.idx >= 0 && fb.idx >= 0 && gmax + kGumbelMax < st.key && gmax + kGumbelMax < fb.key) continue;
+          for (int g4 = 0; g4 < 2; ++g4) {
             const Philox4 bits = prow.block((uint32_t)((vb >> 2) + g4));
             const uint32_t wd[4] = {bits.x, bits.y, bits.z, bits.w};
             // rejection scales: a key c + g beats best only if 1-u < e^{c - best}
@@ -508,14 +592,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      if constexpr (MODE == kModeDraft) {
+        // After the first tiles, publish the CTA's best key per request (one atomic per
+        // request per CTA), so that CTAs still streaming can skip more of their draws.
+        if (t < kPublishTiles) {
+          float* pub = reinterpret_cast<float*>(smem + Smem::red);
+          pub[ew * 32 + lane] = (valid && st.idx >= 0) ? st.key : -INFINITY;
+          asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+          const int et = threadIdx.x - 64;
+          if (et < RB && rb * RB + et < p.R) {
+            float best = -INFINITY;
+            for (int w2 = 0; w2 < kEpiWarps; ++w2) {
+              const int r0 = (((w2 + 2) & 3) * 32) % RB;
+              if (et >= r0 && et < r0 + 32) best = fmaxf(best, pub[w2 * 32 + (et - r0)]);
+            }
+            if (best > published) {
+              atomicMax(p.hint + rb * RB + et, ordered_key(best));
+              published = best;
+            }
+          }
+          asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+        }
+        // the bound for the next tile (its latency overlaps the next tile's wait)
+        if (valid) bound = key_from_ordered(__ldcg(p.hint + r));
+      }
     }
     // merge the threads that share a request: smem slots [ew][lane]
     Partial* red = reinterpret_cast<Partial*>(smem + Smem::red);
-    const int et = threadIdx.x - 64;  // 0..255
+    const int et = threadIdx.x - 64;  // 0..511
 #pragma unroll
     for (int which = 0; which < (MODE == kModeDraft ? 1 : 2); ++which) {
       red[ew * 32 + lane] = to_partial(which ? fb : st);
-      asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
       if (et < RB) {
         Stats m = stats_empty();
         for (int w2 = 0; w2 < kEpiWarps; ++w2) {
@@ -526,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rr = rb * RB + et;
         if (rr < p.R) (which ? p.partials2 : p.partials)[(size_t)group * p.R + rr] = to_partial(m);
       }
-      asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
     }
   }
   __syncthreads();
@@ -624,8 +732,7 @@ static cudaError_t launch(const TcParams& p, const void* W1g, const void* W2, cu
                          : (p.Rb == 64 ? draft_step_tc_kernel<64, MODE> : draft_step_tc_kernel<128, MODE>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<p.ngroups * p.rblocks, kThreads, smem, s>>>(map_a, map_b, p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(p.ngroups * p.rblocks), dim3(kThreads), (size_t)smem, s, map_a, map_b, p);
 }
 
 }  // namespace tc
@@ -635,6 +742,7 @@ cudaError_t launch_draft_step_tc(const DraftArgs& a, int k, cudaStream_t s) {
                                    a.round, a.status);
   p.k = k;
   p.partials = a.partials;
+  p.hint = a.hint;
   return tc::launch<tc::kModeDraft>(p, a.W1g, a.W2, s);
 }
 

@@ -34,7 +34,7 @@ constexpr int kMaxGamma = 64;
 constexpr int kVerifyChunk = 8192;
 
 struct DraftLayout {
-  size_t s_h, W1g, partials, total;
+  size_t s_h, W1g, partials, hint, total;
   int npart;
 };
 
@@ -49,6 +49,8 @@ DraftLayout draft_layout(int R, int gamma, int V, int rank, int dtype_w) {
   L.npart = draft_num_partials(R, V, rank, dtype_w);
   L.partials = off;
   off += align256((size_t)32 * L.npart * R);
+  L.hint = off;
+  off += align256(sizeof(int) * (size_t)R);
   L.total = off;
   return L;
 }
@@ -204,6 +206,7 @@ dspark_status dspark_markov_draft(int R, int gamma, int V, int rank, int d, int 
   a.s_h = reinterpret_cast<float*>(ws + L.s_h);
   a.W1g = ws + L.W1g;
   a.partials = reinterpret_cast<dspark::Partial*>(ws + L.partials);
+  a.hint = reinterpret_cast<int*>(ws + L.hint);
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;

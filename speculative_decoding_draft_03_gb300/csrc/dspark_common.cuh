@@ -296,4 +296,12 @@ __device__ __forceinline__ int checked_token(int x, int V, DeviceStatus* st, int
 
 __device__ __forceinline__ float sigmoidf_dev(float x) { return 1.0f / (1.0f + __expf(-x)); }
 
+// Programmatic dependent launch: every kernel of the round is launched so that it may
+// start while its predecessor drains.  griddep_wait() returns once the preceding grid
+// has completed and its memory is visible; a kernel calls it before touching anything
+// a predecessor writes or reads.  griddep_allow_next() lets the next grid start its own
+// prologue early (it will still wait before its first dependent access).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_allow_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 }  // namespace dspark

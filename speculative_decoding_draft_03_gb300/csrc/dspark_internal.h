@@ -39,6 +39,7 @@ struct DraftArgs {
   float* s_h;        // [R*gamma]
   void* W1g;         // [Rpad, rank] gathered factor rows (dtype_w)
   Partial* partials; // [npart, R]
+  int* hint;         // [R] best Gumbel key found so far at the current position (ordered int)
 };
 
 struct VerifyArgs {
@@ -76,6 +77,24 @@ struct VerifyArgs {
   Partial* res_part;  // [npart, R] residual partials: key = ln rho + g
   Partial* res_part2; // [npart, R] fallback partials: key = ln p + g
 };
+
+// Launch with programmatic stream serialization (the kernel must call griddep_wait()
+// before its first dependent memory access).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 // Workspace layout: a 256-byte status block, then 256-byte aligned pieces.
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }

@@ -200,6 +200,8 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
     schedule_kernel(int R, int gamma, const float* __restrict__ conf, const double* __restrict__ sps, int mode,
                     const float* __restrict__ conf_hist, int fixed_len, int32_t* __restrict__ ell_out,
                     int32_t* __restrict__ B_out, double* __restrict__ tau_out) {
+  griddep_allow_next();
+  griddep_wait();
   extern __shared__ __align__(256) unsigned char smem[];
   const int N = R * gamma;
   int npad = 2;
@@ -284,9 +286,8 @@ cudaError_t launch_schedule(int R, int gamma, const float* conf, const double* s
   const size_t smem = schedule_smem_bytes(R, gamma);
   cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  schedule_kernel<<<1, kSchedThreads, smem, s>>>(R, gamma, conf, sps, mode, conf_hist, fixed_len, ell_out,
-                                                 B_out, tau_out);
-  return cudaGetLastError();
+  return launch_pdl(schedule_kernel, dim3(1), dim3(kSchedThreads), smem, s, R, gamma, conf, sps, mode, conf_hist,
+                    fixed_len, ell_out, B_out, tau_out);
 }
 
 }  // namespace dspark

@@ -38,6 +38,8 @@ __device__ __forceinline__ int clamp_ell(const VerifyArgs& a, int r) {
 }
 
 __global__ void __launch_bounds__(kPlanThreads) verify_plan_kernel(VerifyArgs a) {
+  griddep_allow_next();
+  griddep_wait();
   __shared__ int wsum[32];
   const int per = (a.R + blockDim.x - 1) / blockDim.x;
   const int lo = threadIdx.x * per, hi = min(lo + per, a.R);
@@ -80,6 +82,8 @@ __global__ void __launch_bounds__(kPlanThreads) verify_plan_kernel(VerifyArgs a)
 // Per (row, chunk): online (max, sum exp) of t/T; on the bonus row also the
 // Gumbel-max record of t/T + g (stream 2, position ell+1).
 __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyArgs a) {
+  griddep_allow_next();
+  griddep_wait();
   const int n_items = (*a.n_rows) * a.nchunk;
   __shared__ Partial red[kRowThreads / 32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -90,8 +94,8 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyArgs a) 
     const size_t rbase = ((size_t)r * (a.gamma + 1) + t) * a.V;
     const int v0 = c * a.chunk, v1 = min(v0 + a.chunk, a.V);
     Stats st = stats_empty();
-    RngRow rng;
-    if (bonus) rng = rng_row(a.seed, __ldg(a.req_id + r), a.round, kStreamCorrect, (uint32_t)(t + 1));
+    PhiloxRow prow;
+    if (bonus) prow = philox_row(rng_row(a.seed, __ldg(a.req_id + r), a.round, kStreamCorrect, (uint32_t)(t + 1)));
     // groups of 4 consecutive ids (chunk starts are multiples of 4)
     for (int g = v0 / 4 + threadIdx.x; 4 * g < v1; g += blockDim.x) {
       float x[4];
@@ -107,25 +111,38 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyArgs a) 
 #pragma unroll
         for (int e = 0; e < 4; ++e) x[e] = (vb + e < v1) ? load_elem(a.target, a.dtype_t, rbase + vb + e) : 0.f;
       }
-      Philox4 bits;
-      if (bonus) bits = rng_chunk(rng, (uint32_t)g);
-      const uint32_t wd[4] = {bits.x, bits.y, bits.z, bits.w};
+      const int nv = min(4, v1 - vb);
+      float z[4], term[4];
+      float cmax = -INFINITY;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        if (vb + e >= v1) break;
-        const float z = x[e] * a.inv_temp;
-        if (z > st.m) {
-          st.s = st.s * __expf(st.m - z) + 1.f;
-          st.m = z;
-        } else {
-          st.s += __expf(z - st.m);
-        }
-        if (bonus && (z + kGumbelMax >= st.key || st.idx < 0)) {
-          const float key = z + gumbel_from_bits(wd[e]);
+        z[e] = x[e] * a.inv_temp;
+        if (e < nv) cmax = fmaxf(cmax, z[e]);
+      }
+      // online (max, sum exp) with term_e = exp(z_e - m)
+      const float mnew = fmaxf(st.m, cmax);
+      float s = (st.m == -INFINITY) ? 0.f : st.s * __expf(st.m - mnew);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        term[e] = (e < nv) ? __expf(z[e] - mnew) : 0.f;
+        s += term[e];
+      }
+      st.m = mnew;
+      st.s = s;
+      if (bonus) {
+        // Gumbel-max with the exact log-free rejection of elements that cannot beat
+        // the running key (1-u >= exp(z - best))
+        const Philox4 bits = prow.block((uint32_t)g);
+        const uint32_t wd[4] = {bits.x, bits.y, bits.z, bits.w};
+        const float scale = (st.idx >= 0) ? __expf(mnew - st.key) * kRejectSlack : INFINITY;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (e >= nv || (st.idx >= 0 && gumbel_cannot_win(wd[e], term[e] * scale))) continue;
+          const float key = z[e] + gumbel_from_bits(wd[e]);
           if (key > st.key || st.idx < 0) {
             st.key = key;
             st.idx = vb + e;
-            st.zsel = z;
+            st.zsel = z[e];
           }
         }
       }
@@ -144,6 +161,8 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyArgs a) 
 
 // One warp per request.
 __global__ void verify_accept_kernel(VerifyArgs a) {
+  griddep_allow_next();
+  griddep_wait();
   const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (r >= a.R) return;
@@ -214,6 +233,8 @@ __global__ void verify_accept_kernel(VerifyArgs a) {
 // CUDA-core residual pass.  blockIdx.x: vocabulary chunk; blockIdx.y: request block.
 template <int RB>
 __global__ void __launch_bounds__(kSimtThreads) residual_step_simt_kernel(VerifyArgs a) {
+  griddep_allow_next();
+  griddep_wait();
   extern __shared__ float w1s[];  // [RB][rank]
   const int r0 = blockIdx.y * RB;
   int js[RB];
@@ -331,6 +352,8 @@ __global__ void __launch_bounds__(kSimtThreads) residual_step_simt_kernel(Verify
 }
 
 __global__ void residual_combine_kernel(VerifyArgs a, int npart) {
+  griddep_allow_next();
+  griddep_wait();
   const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (r >= a.R) return;
@@ -347,19 +370,16 @@ __global__ void residual_combine_kernel(VerifyArgs a, int npart) {
 }
 
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s) {
-  verify_plan_kernel<<<1, kPlanThreads, 0, s>>>(a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(verify_plan_kernel, dim3(1), dim3(kPlanThreads), 0, s, a);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int max_items = a.R * (a.gamma + 1) * a.nchunk;
   const int grid = min(max_items, sms * 8);
-  verify_rows_kernel<<<grid, kRowThreads, 0, s>>>(a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_pdl(verify_rows_kernel, dim3(grid), dim3(kRowThreads), 0, s, a)) != cudaSuccess) return e;
   const int wblocks = (a.R * 32 + 255) / 256;
-  verify_accept_kernel<<<wblocks, 256, 0, s>>>(a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_pdl(verify_accept_kernel, dim3(wblocks), dim3(256), 0, s, a)) != cudaSuccess) return e;
   int npart;
   if (tc_supported(a.V, a.rank, a.dtype_w)) {
     // the residual recomputes one bias row per rejected request on the tensor cores
@@ -373,12 +393,11 @@ cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s) {
                                (int)smem);
       if (e != cudaSuccess) return e;
     }
-    residual_step_simt_kernel<kSimtRB><<<rgrid, kSimtThreads, smem, s>>>(a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_pdl(residual_step_simt_kernel<kSimtRB>, rgrid, dim3(kSimtThreads), smem, s, a)) != cudaSuccess)
+      return e;
     npart = (int)rgrid.x;
   }
-  residual_combine_kernel<<<wblocks, 256, 0, s>>>(a, npart);
-  return cudaGetLastError();
+  return launch_pdl(residual_combine_kernel, dim3(wblocks), dim3(256), 0, s, a, npart);
 }
 
 int residual_num_partials(int R, int V, int rank, int dtype_w) {
