@@ -200,6 +200,28 @@ DSPARK_API dspark_status dspark_verify(
     int32_t* n_acc_out, int32_t* tokens_out, int32_t* n_out,
     void* workspace, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------------------------------------
+ * Stage 3 for callers that cannot allocate device memory.  (The paper has no
+ * counterpart: this is a deployment convenience of this library.)
+ *
+ * Same arguments, results and limits as dspark_verify, without `workspace`/`ws_bytes`:
+ * the scratch is an 8 MiB array inside the library (one copy per GPU that loads the
+ * library, held until the process exits).  Shapes whose dspark_verify_workspace_size()
+ * exceeds 8 MiB are rejected with DSPARK_UNSUPPORTED_SHAPE.  Allocates nothing.
+ *   - The first call on a device looks up the array's device address (with that device
+ *     current); make that first call before any stream capture.
+ *   - All calls share the array: calls that may overlap on the GPU (other streams, other
+ *     host threads on the same device) race and must be ordered by the caller.
+ *   - The status block that must start at zero is cleared on `stream` at every call, so
+ *     device-side input reports of earlier calls are not kept.
+ * ---------------------------------------------------------------------------------- */
+DSPARK_API dspark_status dspark_verify_static(
+    int R, int gamma, int V, int rank, int dtype_t, int dtype_u, int dtype_w,
+    const void* target, const void* U, const void* W1, const void* W2,
+    const int32_t* x0, const int32_t* x, const float* logq, const float* lse_q,
+    const int32_t* ell, float temperature, const int64_t* req_id, uint64_t seed, uint64_t round,
+    int32_t* n_acc_out, int32_t* tokens_out, int32_t* n_out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -104,6 +104,8 @@ bool aligned256(const void* p) { return ((uintptr_t)p & 255u) == 0; }
 
 namespace dspark {
 
+dspark_status record_error(dspark_status code, const char* msg) { return fail(code, "%s", msg); }
+
 int round_up_rows(int R) { return ((R + 127) / 128) * 128; }
 
 int draft_num_partials(int R, int V, int rank, int dtype_w) {

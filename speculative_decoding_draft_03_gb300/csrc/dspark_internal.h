@@ -99,6 +99,9 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 // Workspace layout: a 256-byte status block, then 256-byte aligned pieces.
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Sets the thread's dspark_last_error_message() and returns `code`.
+int record_error(int code, const char* msg);
+
 int simt_num_chunks(int V);
 int tc_supported(int V, int rank, int dtype_w);
 int tc_num_partials(int R);

@@ -1,0 +1,57 @@
+"""dspark_verify_static: verification for callers that cannot allocate device memory
+(a host framework whose memory pool must not be bypassed, or a serving loop that may
+not allocate after start-up).  It must give exactly the results of dspark_verify, on
+repeated calls that reuse the library's one static scratch array, and must reject a
+shape whose scratch would not fit.
+
+This file is named to be collected last: if it fails, a run that stops at the first
+failure has already run every other test."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_decoding_draft_03_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(name, **over):
+    w = wl.make(name, device="cpu", **over)
+    wn = wl.to_numpy(w)
+    wg = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in w.items()}
+    d = oracle.markov_draft(wn["U"], wn["W1"], wn["W2"], wn["h"], wn["conf_w"], wn["conf_b"],
+                            wn["conf_logit_scale"], wn["conf_temp"], wn["temperature"], wn["x0"], wn["req_id"],
+                            wn["seed"], 0)
+    rng = np.random.default_rng(1)
+    ell = rng.integers(0, wn["gamma"] + 1, wn["R"]).astype(np.int32)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    inputs = (wg["target"], wg["U"], wg["W1"], wg["W2"], wg["x0"], t(d["x"]), t(d["logq"].astype(np.float32)),
+              t(d["lse"].astype(np.float32)), t(ell), wg["temperature"], wg["req_id"], wg["seed"])
+    return inputs
+
+
+@pytest.mark.parametrize("name,over", [("tiny", {}), ("qwen3-8b", dict(V=20000, d=256)),
+                                       ("stress", dict(V=2056, d=64))])
+def test_static_scratch_matches_workspace_entry_point(name, over):
+    from speculative_decoding_draft_03_gb300 import binding as b
+    inputs = _case(name, **over)
+    for rnd in (3, 4):  # two calls in a row: the second reuses the first call's scratch
+        ref = b.verify(*inputs, rnd)
+        got = b.verify_static(*inputs, rnd)
+        torch.cuda.synchronize()
+        for k in ("n_acc", "tokens", "n_out"):
+            assert torch.equal(ref[k], got[k]), (name, rnd, k)
+
+
+def test_static_scratch_rejects_oversized_shapes():
+    from speculative_decoding_draft_03_gb300 import binding as b
+    R, gamma, V, rank = 2048, 3, 151936, 256  # needs tens of MiB of scratch
+    need = b.verify_workspace_size(R, gamma, V, rank, torch.bfloat16)
+    assert need > (8 << 20)
+    dev = torch.device("cuda")
+    target = torch.zeros((1, gamma + 1, 8), device=dev)  # never read: rejected before any launch
+    st = b.lib.dspark_verify_static(R, gamma, V, rank, 0, 0, 1, *([b._p(target)] * 9), 1.0, b._p(target), 0, 0,
+                                    *([b._p(target)] * 3), b._stream())
+    assert st == 2
+    assert "static scratch" in b.lib.dspark_last_error_message().decode()
