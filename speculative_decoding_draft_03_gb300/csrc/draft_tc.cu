@@ -29,9 +29,12 @@
 //   * Many requests (R > 128): CTAs are grouped by request block; the CTAs of a group
 //     walk the same W2 tiles at the same time, so W2 comes from HBM once per position
 //     and from L2 for the other request blocks.
-//   * Warp roles: warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer, warps 2..17
-//     epilogue.  Every mbarrier wait is bounded; a wait that gives up records
-//     DSPARK_TIMEOUT in the workspace status word and the CTA winds down cleanly.
+//   * U (draft mode) also arrives by TMA: 128-byte-wide boxes of request rows at the
+//     current position, 128B-swizzled so that each thread's row reads are bank-conflict
+//     free, several tiles ahead of the epilogue.  Epilogue threads issue no global loads.
+//   * Warp roles: warp 0 W2/A TMA producer, warp 1 TMEM allocator + MMA issuer, warp 2 U
+//     TMA producer, warps 3..18 epilogue.  Every mbarrier wait is bounded; a wait that
+//     gives up records DSPARK_TIMEOUT in the workspace status word and the CTA winds down.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <string.h>
@@ -45,24 +48,39 @@ namespace tc {
 constexpr int kM = 128;           // MMA rows (requests, replicated for small batches)
 constexpr int kN = 128;           // vocabulary ids per tile
 constexpr int kKAtom = 64;        // bf16 elements per 128-byte swizzle row
-constexpr int kStages = 8;        // W2 ring stages (one 64-deep K slice of a tile each)
-constexpr int kStageBytes = kN * kKAtom * 2;  // 16 KB
+constexpr int kStageBytes = kN * kKAtom * 2;  // 16 KB per W2 ring stage (one 64-deep K slice)
+constexpr int kMaxUBoxes = 16;
 constexpr int kEpiWarps = 16;
 constexpr int kEpiThreads = 32 * kEpiWarps;
-constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kFirstEpiWarp = 3;  // warps 0..2: W2/A producer, MMA issuer, U producer
+constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
 constexpr int kCols = 8;          // vocabulary ids per epilogue pass
 constexpr int kTmemCols = 2 * kN;
 constexpr int kMaxRank = 256;
 constexpr long long kWaitCycles = 4000000000ll;  // ~2 s at 2 GHz
 constexpr int kPublishTiles = 2;  // tiles after which a CTA publishes its best keys
 
+// Shared-memory plan per request-block size RB.  The U ring (draft mode) holds boxes of
+// 128 bytes x RB request rows (32 fp32 or 64 bf16 vocabulary ids); the kernel uses a
+// whole number of tiles' worth of them (four fp32 or two bf16 boxes per tile), so it
+// needs room for at least four.  RB = 64 and 128 trade one W2 stage for a 64 KB ring.
+template <int RB>
 struct Smem {
+  static constexpr int stages = RB == 32 ? 6 : 5;                 // W2 ring stages
+  static constexpr int ubytes = RB == 32 ? 56 * 1024 : 64 * 1024;  // U ring
+  static constexpr int uboxes = ubytes / (RB * 128);
   // offsets from the 1024-byte aligned base
   static constexpr int a = 0;                                  // [rank/64][128 rows][128 B]
   static constexpr int b = a + kM * kMaxRank * 2;              // [stages][2][64 rows][128 B]
-  static constexpr int red = b + kStages * kStageBytes;        // [16 warps][32] Partial
-  static constexpr int bars = red + kEpiWarps * 32 * 32;       // mbarriers
-  static constexpr int total = bars + 256;
+  static constexpr int u = b + stages * kStageBytes;           // [boxes][rows][128 B]
+  static constexpr int pub = u + ubytes;                       // [16 warps][32] float
+  static constexpr int bars = pub + kEpiWarps * 32 * 4;        // mbarriers
+  static constexpr int total = bars + 512;
+  // the final merge ([16 warps][32] Partial = 16 KB) reuses the idle W2 ring
+  static constexpr int red = b;
+  static_assert(kEpiWarps * 32 * 32 <= stages * kStageBytes, "merge scratch must fit in the W2 ring");
+  static_assert(uboxes >= 4 && uboxes <= kMaxUBoxes, "U ring must hold one tile of fp32 boxes");
+  static_assert(total + 1024 <= 232448, "shared memory plan exceeds 227 KB");
 };
 
 // ------------------------------------------------------------------------------------
@@ -117,6 +135,28 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "%4}], [%2], %5;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
       : "memory");
+}
+
+// 3-D tensor load (U viewed as [R][gamma][V]: a box of request rows at one position).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y, int z,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, "
+      "%4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
 }
 
 // The W2 factor is re-read at every draft position of a round: keep it resident.
@@ -204,6 +244,7 @@ struct TcParams {
   int ngroups;     // CTAs per request block (= partial records per request)
   int ntiles;      // ceil(V / 128)
   int k;           // draft position (1-based)
+  int ubox_cols;   // draft mode: vocabulary ids per 128-byte U box (32 fp32, 64 bf16)
   float inv_temp;
   const void* U;
   const int64_t* req_id;
@@ -261,23 +302,37 @@ __device__ __forceinline__ void decode_run8(int dtype, const uint4 (&raw)[2], fl
 template <int RB, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     draft_step_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                         TcParams p) {
+                         const __grid_constant__ CUtensorMap map_u, TcParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  using SM = Smem<RB>;
+  constexpr int kStages = SM::stages;
   const int rb = blockIdx.x % p.rblocks;      // request block of this CTA
   const int group = blockIdx.x / p.rblocks;   // vocabulary-tile group
   const int katoms = p.rank / kKAtom;
 
-  uint32_t bar_full = sbase + Smem::bars;              // [kStages]
+  uint32_t bar_full = sbase + SM::bars;              // [kStages]
   uint32_t bar_empty = bar_full + 8 * kStages;         // [kStages]
   uint32_t bar_acc_full = bar_empty + 8 * kStages;     // [2]
   uint32_t bar_acc_empty = bar_acc_full + 16;          // [2]
   uint32_t bar_a = bar_acc_empty + 16;                 // [1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Smem::bars + 8 * (2 * kStages + 5));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Smem::bars + 8 * (2 * kStages + 5) + 8);
+  uint32_t bar_ufull = bar_a + 8;                      // [kMaxUBoxes]
+  uint32_t bar_uempty = bar_ufull + 8 * kMaxUBoxes;    // [kMaxUBoxes]
+  constexpr int kBarBytes = 8 * (2 * kStages + 5 + 2 * kMaxUBoxes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::bars + kBarBytes);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM::bars + kBarBytes + 8);
+  // U boxes of a tile: 128/ubox_cols of them, each read by the 16/(128/ubox_cols) warps
+  // whose columns fall inside it
+  const int uboxes_per_tile = kN / p.ubox_cols;
+  const int warps_per_ubox = kEpiWarps / uboxes_per_tile;
+  // Ring capacity: a whole number of tiles, so that slot i % n_uboxes is always read by
+  // the same warps.  Each of them has consumed the slot's previous fill before it waits
+  // for the next one, which keeps every parity wait at most one phase ahead.
+  const int n_uboxes = (SM::uboxes / uboxes_per_tile) * uboxes_per_tile;
+  const int ubox_bytes = RB * 128;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -289,6 +344,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_acc_empty + 8 * b, kEpiWarps);
     }
     mbar_init(bar_a, 1);
+    for (int s = 0; s < kMaxUBoxes; ++s) {
+      mbar_init(bar_ufull + 8 * s, 1);
+      mbar_init(bar_uempty + 8 * s, warps_per_ubox);
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -317,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(bar_a, (uint32_t)(kM * p.rank * 2));
         for (int j = 0; j < rep; ++j)
           for (int ka = 0; ka < katoms; ++ka)
-            tma_load_2d(sbase + Smem::a + ka * (kM * 128) + j * RB * 128, &map_a, bar_a, ka * kKAtom, rb * RB,
+            tma_load_2d(sbase + SM::a + ka * (kM * 128) + j * RB * 128, &map_a, bar_a, ka * kKAtom, rb * RB,
                         a_policy);
       };
       const int total = my_tiles * katoms;
@@ -332,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = it / katoms, ka = it % katoms;
         const int v0 = (group + t * p.ngroups) * kN;
         if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag, p.status, 100)) break;
-        const uint32_t dst = sbase + Smem::b + stage * kStageBytes;
+        const uint32_t dst = sbase + SM::b + stage * kStageBytes;
         mbar_arrive_expect_tx(bar_full + 8 * stage, kStageBytes);
         tma_load_2d(dst, &map_b, bar_full + 8 * stage, v0, ka * kKAtom, w2_policy);
         tma_load_2d(dst + kStageBytes / 2, &map_b, bar_full + 8 * stage, v0 + 64, ka * kKAtom, w2_policy);
@@ -362,8 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_atom = sbase + Smem::a + ka * (kM * 128);
-          const uint32_t b_stage = sbase + Smem::b + stage * kStageBytes;
+          const uint32_t a_atom = sbase + SM::a + ka * (kM * 128);
+          const uint32_t b_stage = sbase + SM::b + stage * kStageBytes;
 #pragma unroll
           for (int kk = 0; kk < kKAtom / 16; ++kk) {
             // A: K-major rows of 128 B; a 16-deep K step is 32 B further along the row.
@@ -384,9 +443,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar_acc_full + 8 * buf);
       }
     }
+  } else if (warp == 2) {
+    // ------------------------------ U producer (draft mode) -------------------
+    // U is an input of the round: its boxes stream ahead of the epilogue through a
+    // ring of n_uboxes slots, read once (evict-first in L2).
+    if (MODE == kModeDraft && lane == 0) {
+      const uint64_t u_policy = policy_evict_first();
+      const int total = my_tiles * uboxes_per_tile;
+      for (int i = 0; i < total && !*abort_flag; ++i) {
+        const int slot = i % n_uboxes;
+        const uint32_t ph = (uint32_t)(i / n_uboxes) & 1u;
+        if (!mbar_wait(bar_uempty + 8 * slot, ph ^ 1, abort_flag, p.status, 400)) break;
+        const int t = i / uboxes_per_tile, bx = i % uboxes_per_tile;
+        const int v0 = (group + t * p.ngroups) * kN + bx * p.ubox_cols;
+        mbar_arrive_expect_tx(bar_ufull + 8 * slot, (uint32_t)ubox_bytes);
+        tma_load_3d(sbase + SM::u + slot * ubox_bytes, &map_u, bar_ufull + 8 * slot, v0, p.k - 1, rb * RB,
+                    u_policy);
+      }
+    }
   } else {
     // ------------------------------ epilogue ----------------------------------
-    const int ew = warp - 2;               // 0..15
+    const int ew = warp - kFirstEpiWarp;   // 0..15
     const int quarter = warp & 3;          // TMEM lane quarter this warp may access
     const int sub = ew >> 2;               // 0..3: which quarter of the replica's columns
     const int row0 = (quarter * 32) % RB;
@@ -417,7 +494,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const size_t trow = ((size_t)(valid ? r : 0) * (p.gamma + 1) + (valid ? pos - 1 : 0)) * (size_t)p.V;
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
 
-    // U of the next tile is loaded into registers while the current one is processed
+    // Residual mode: U of the next tile is loaded into registers while the current one is
+    // processed (each request reads its own position).  Draft mode: U arrives through
+    // the TMA ring; this warp reads box my_box of each tile, from column box_col on.
     uint4 unext[kPass][2];
     auto load_u = [&](int t, uint4 (&dst)[kPass][2]) {
       const int vt = (group + t * p.ngroups) * kN;
@@ -425,9 +504,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ps = 0; ps < kPass; ++ps)
         load_run8(p.U, p.dtype_u, urow, vt + col0 + ps * kCols, p.V, valid && t < my_tiles, dst[ps]);
     };
-    load_u(0, unext);
-    // U is an input: its first tile is in flight before waiting for the predecessor,
-    // which still reads the partial records this kernel overwrites at the end
+    const int my_box = col0 / p.ubox_cols;
+    const int box_col = col0 % p.ubox_cols;
+    const int box_row = row0 + lane;
+    const bool u_f32 = p.dtype_u == DSPARK_F32;
+    if constexpr (MODE == kModeResidual) load_u(0, unext);
+    // the predecessor still reads the partial records this kernel overwrites at the end
     if constexpr (MODE == kModeDraft) griddep_wait();
 
     // Draft mode: the best key any CTA has published for this request at this position.
@@ -441,15 +523,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t use = (uint32_t)(t >> 1) & 1u;
       const int vt = (group + t * p.ngroups) * kN;
       uint4 ucur[kPass][2];
+      int uslot = 0;
+      bool u_ready = true;
+      if constexpr (MODE == kModeResidual) {
 #pragma unroll
-      for (int ps = 0; ps < kPass; ++ps) {
-        ucur[ps][0] = unext[ps][0];
-        ucur[ps][1] = unext[ps][1];
+        for (int ps = 0; ps < kPass; ++ps) {
+          ucur[ps][0] = unext[ps][0];
+          ucur[ps][1] = unext[ps][1];
+        }
+        load_u(t + 1, unext);
+      } else {
+        const int i = t * uboxes_per_tile + my_box;
+        uslot = i % n_uboxes;
+        u_ready = mbar_wait(bar_ufull + 8 * uslot, (uint32_t)(i / n_uboxes) & 1u, abort_flag, p.status, 301);
+        // this thread's 8-id runs from its request row of the 128B-swizzled box
+        const uint32_t row_addr = sbase + SM::u + uslot * ubox_bytes + box_row * 128;
+#pragma unroll
+        for (int ps = 0; ps < kPass; ++ps) {
+          const int cb = box_col + ps * kCols;
+          if (!u_ready) {
+            ucur[ps][0] = ucur[ps][1] = make_uint4(0u, 0u, 0u, 0u);
+          } else if (u_f32) {
+            const int c0 = cb >> 2;  // two 16-byte chunks
+            ucur[ps][0] = lds128(row_addr + ((c0 ^ (box_row & 7)) << 4));
+            ucur[ps][1] = lds128(row_addr + (((c0 + 1) ^ (box_row & 7)) << 4));
+          } else {
+            const int c0 = cb >> 3;  // one 16-byte chunk
+            ucur[ps][0] = lds128(row_addr + ((c0 ^ (box_row & 7)) << 4));
+            ucur[ps][1] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        // the box slot can be refilled once every reader has its values in registers
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_uempty + 8 * uslot);
       }
-      load_u(t + 1, unext);
       // On an abandoned wait the warp keeps iterating without touching TMEM, so that
       // every epilogue warp still meets the same named barriers.
-      const bool acc_ready = mbar_wait(bar_acc_full + 8 * buf, use, abort_flag, p.status, 300);
+      const bool acc_ready = mbar_wait(bar_acc_full + 8 * buf, use, abort_flag, p.status, 300) && u_ready;
       if (acc_ready) tc_fence_after();
 #pragma unroll
       for (int ps = 0; ps < kPass; ++ps) {
@@ -596,14 +706,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // After the first tiles, publish the CTA's best key per request (one atomic per
         // request per CTA), so that CTAs still streaming can skip more of their draws.
         if (t < kPublishTiles) {
-          float* pub = reinterpret_cast<float*>(smem + Smem::red);
+          float* pub = reinterpret_cast<float*>(smem + SM::pub);
           pub[ew * 32 + lane] = (valid && st.idx >= 0) ? st.key : -INFINITY;
           asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
-          const int et = threadIdx.x - 64;
+          const int et = threadIdx.x - 32 * kFirstEpiWarp;
           if (et < RB && rb * RB + et < p.R) {
             float best = -INFINITY;
             for (int w2 = 0; w2 < kEpiWarps; ++w2) {
-              const int r0 = (((w2 + 2) & 3) * 32) % RB;
+              const int r0 = (((w2 + kFirstEpiWarp) & 3) * 32) % RB;
               if (et >= r0 && et < r0 + 32) best = fmaxf(best, pub[w2 * 32 + (et - r0)]);
             }
             if (best > published) {
@@ -618,8 +728,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // merge the threads that share a request: smem slots [ew][lane]
-    Partial* red = reinterpret_cast<Partial*>(smem + Smem::red);
-    const int et = threadIdx.x - 64;  // 0..511
+    Partial* red = reinterpret_cast<Partial*>(smem + SM::red);
+    const int et = threadIdx.x - 32 * kFirstEpiWarp;  // 0..511
 #pragma unroll
     for (int which = 0; which < (MODE == kModeDraft ? 1 : 2); ++which) {
       red[ew * 32 + lane] = to_partial(which ? fb : st);
@@ -627,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (et < RB) {
         Stats m = stats_empty();
         for (int w2 = 0; w2 < kEpiWarps; ++w2) {
-          const int q2 = (w2 + 2) & 3;
+          const int q2 = (w2 + kFirstEpiWarp) & 3;
           const int r0 = (q2 * 32) % RB;
           if (et >= r0 && et < r0 + 32) stats_merge(m, from_partial(red[w2 * 32 + (et - r0)]));
         }
@@ -671,6 +781,23 @@ static bool make_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uint
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// U as a 3-D tensor [R][gamma][V] (fp32 or bf16): boxes of 128 bytes of ids by `rows`
+// request rows at one position.
+static bool make_map_u(CUtensorMap* map, const void* base, int dtype, uint64_t V, uint64_t gamma, uint64_t R,
+                       uint32_t rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const uint64_t es = dtype == DSPARK_F32 ? 4 : 2;
+  cuuint64_t dims[3] = {V, gamma, R};
+  cuuint64_t strides[2] = {V * es, gamma * V * es};
+  cuuint32_t box[3] = {(cuuint32_t)(128 / es), 1, rows};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, dtype == DSPARK_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -722,17 +849,24 @@ static TcParams base_params(int R, int gamma, int V, int rank, int dtype_u, floa
 }
 
 template <int MODE>
-static cudaError_t launch(const TcParams& p, const void* W1g, const void* W2, cudaStream_t s) {
-  CUtensorMap map_a, map_b;
+static cudaError_t launch(TcParams p, const void* W1g, const void* W2, cudaStream_t s) {
+  CUtensorMap map_a, map_b, map_u;
   if (!make_map_2d(&map_a, W1g, (uint64_t)p.rank, (uint64_t)round_up_rows(p.R), kKAtom, (uint32_t)p.Rb))
     return cudaErrorInvalidValue;
   if (!make_map_2d(&map_b, W2, (uint64_t)p.V, (uint64_t)p.rank, 64, kKAtom)) return cudaErrorInvalidValue;
-  const int smem = Smem::total + 1024;
+  p.ubox_cols = p.dtype_u == DSPARK_F32 ? 32 : 64;
+  if (MODE == kModeDraft) {
+    if (!make_map_u(&map_u, p.U, p.dtype_u, (uint64_t)p.V, (uint64_t)p.gamma, (uint64_t)p.R, (uint32_t)p.Rb))
+      return cudaErrorInvalidValue;
+  } else {
+    map_u = map_b;  // unused: the residual reads each request's own position directly
+  }
+  const int smem = (p.Rb == 32 ? Smem<32>::total : (p.Rb == 64 ? Smem<64>::total : Smem<128>::total)) + 1024;
   auto kern = p.Rb == 32 ? draft_step_tc_kernel<32, MODE>
                          : (p.Rb == 64 ? draft_step_tc_kernel<64, MODE> : draft_step_tc_kernel<128, MODE>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(p.ngroups * p.rblocks), dim3(kThreads), (size_t)smem, s, map_a, map_b, p);
+  return launch_pdl(kern, dim3(p.ngroups * p.rblocks), dim3(kThreads), (size_t)smem, s, map_a, map_b, map_u, p);
 }
 
 }  // namespace tc
