@@ -154,6 +154,9 @@ def draft_step_bytes(w):
 
 
 def launches_per_round(w):
+    """Kernels of one round: confidence h-part, first-position prepare, a step and a
+    combine per draft position, the scheduler, and verify's plan / rows / accept /
+    residual step / residual combine."""
     g = w["gamma"]
     return (1 if w["d"] > 0 else 0) + 1 + 2 * g + 1 + 5
 
@@ -232,6 +235,17 @@ def main():
     torch.cuda.synchronize()
     assert rd.status() == 0, "device status word reports an error"
 
+    # Each timed round is one CUDA graph (its own round index, so its own random draws),
+    # captured and replayed once before timing.  Every 4th graph also records the
+    # step-kernel events; those sit between kernels that otherwise overlap through
+    # programmatic dependent launch, so the other rounds run without them.
+    profiled = [t % 4 == 0 for t in range(args.steps)]
+    graphs = [rd.capture(rnd=args.warmup + t, timer=timer if profiled[t] else None) for t in range(args.steps)]
+    for g in graphs:
+        g.replay()
+    torch.cuda.synchronize()
+    assert rd.status() == 0, "device status word reports an error"
+
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     if world > 1:
@@ -241,19 +255,13 @@ def main():
         wall0 = time.perf_counter()
         for t in range(args.steps):
             flush.zero_()
-            # The step-kernel events sit between kernels that otherwise overlap through
-            # programmatic dependent launch, so they are recorded on every 4th round only.
-            timed_steps = (t % 4 == 0)
-            if timed_steps:
-                timer.__enter__()
             starts[t].record(stream)
-            d, s, v = rd.run(rnd=args.warmup + t)
+            graphs[t].replay()
             ends[t].record(stream)
-            if timed_steps:
-                timer.__exit__()
-                torch.cuda.synchronize()  # the timer's events are reused by the next timed round
+            if profiled[t]:
+                torch.cuda.synchronize()  # the step events are shared by the profiled graphs
                 timer.collect()
-            n_acc_sum += v["n_acc"].sum()
+            n_acc_sum += rd.verify_out["n_acc"].sum()
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
@@ -297,6 +305,7 @@ def main():
                 "config": {"workload": WORKLOAD_DESC[args.workload], "R": w["R"], "gamma": w["gamma"],
                            "V": w["V"], "rank": w["rank"], "d": w["d"],
                            "l2": "flushed between rounds (256 MiB write outside the timed brackets)",
+                           "launch": "each round one CUDA graph, captured and replayed once before timing",
                            "parallelism": f"{world} independent batch(es), one per GPU"},
                 "rounds_per_s": 1000.0 * args.steps / round_ms,
                 "verified_tokens_per_round": tokens / args.steps / world,

@@ -18,7 +18,9 @@
  * Conventions for every entry point
  *   - All array pointers are DEVICE pointers owned by the caller, C-contiguous,
  *     row-major.  "U[R,gamma,V]" means element U[(r*gamma + k-1)*V + v] for request r,
- *     draft position k (1-based) and vocabulary id v.
+ *     draft position k (1-based) and vocabulary id v.  The logit and weight arrays (U,
+ *     target, W1, W2, h) must start on a 16-byte boundary (they are read with 16-byte
+ *     vector loads and the Tensor Memory Accelerator); others need natural alignment.
  *   - The library never allocates device memory: scratch comes from the caller's
  *     `workspace` (at least the size the matching *_workspace_size() returns, 256-byte
  *     aligned).  A workspace may be reused by later calls on the same stream; calls that
@@ -86,7 +88,9 @@ DSPARK_API dspark_status dspark_workspace_status(void* workspace, int reset, int
  * events[2(k-1)] just before and events[2(k-1)+1] just after the launch of draft
  * position k's vocabulary-streaming step kernel, on the call's stream, for
  * k = 1..min(gamma, n_events/2).  `events` holds cudaEvent_t handles owned by the
- * caller; NULL or n_events = 0 turns recording off.  The setting is per host thread. */
+ * caller; NULL or n_events = 0 turns recording off.  The setting is per host thread.
+ * While the stream is being captured into a CUDA graph, the events become external
+ * event-record nodes of the graph, so every replay records them. */
 DSPARK_API void dspark_set_profile_events(void* const* events, int n_events);
 
 /* ------------------------------------------------------------------------------------

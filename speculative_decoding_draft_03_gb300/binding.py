@@ -291,6 +291,22 @@ class Round:
                    stream=stream)
         return d, s, v
 
+    def capture(self, rnd=0, x0=None, timer=None):
+        """Capture one round (round index ``rnd``) as a CUDA graph.  Replaying it launches
+        the round's kernels with no host work; it writes the same output tensors as
+        ``run``.  With ``timer`` (a StepTimer) the graph also records its step events."""
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(device=self.w["U"].device)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(g, stream=side):
+            if timer is not None:
+                with timer:
+                    self.run(rnd, x0)
+            else:
+                self.run(rnd, x0)
+        torch.cuda.current_stream().wait_stream(side)
+        return g
+
     def status(self) -> int:
         codes = [device_status(ws) for ws in (self.ws_draft, self.ws_sched, self.ws_verify)]
         return max(codes)

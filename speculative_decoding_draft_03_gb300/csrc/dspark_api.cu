@@ -98,6 +98,13 @@ VerifyLayout verify_layout(int R, int gamma, int V, int rank, int dtype_w) {
     if ((p) == nullptr) return fail(DSPARK_INVALID_ARG, "null pointer: %s", #p); \
   } while (0)
 
+// logit and weight arrays are read with 16-byte vector loads and the TMA
+#define CHECK_ALIGN16(p)                                                                     \
+  do {                                                                                       \
+    if ((reinterpret_cast<uintptr_t>(p) & 15u) != 0)                                         \
+      return fail(DSPARK_INVALID_ARG, "%s must start on a 16-byte boundary", #p);            \
+  } while (0)
+
 bool aligned256(const void* p) { return ((uintptr_t)p & 255u) == 0; }
 
 }  // namespace
@@ -134,6 +141,16 @@ const char* dspark_status_string(int status) {
 }
 
 const char* dspark_last_error_message(void) { return g_msg; }
+
+// A profiling event recorded while the stream is being captured must become an event
+// record node of the graph (not only a capture-ordering marker), so that replays time it.
+static cudaError_t record_profile_event(void* ev, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &cs);
+  if (e != cudaSuccess) return e;
+  return cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags((cudaEvent_t)ev, s, cudaEventRecordExternal)
+                                             : cudaEventRecord((cudaEvent_t)ev, s);
+}
 
 void dspark_set_profile_events(void* const* events, int n_events) {
   g_prof_events = (events != nullptr && n_events > 0) ? events : nullptr;
@@ -190,6 +207,10 @@ dspark_status dspark_markov_draft(int R, int gamma, int V, int rank, int d, int 
   CHECK_PTR(lse_out);
   CHECK_PTR(conf_out);
   CHECK_PTR(workspace);
+  CHECK_ALIGN16(U);
+  CHECK_ALIGN16(W1);
+  CHECK_ALIGN16(W2);
+  if (d > 0) CHECK_ALIGN16(h);
   if (!aligned256(workspace)) return fail(DSPARK_INVALID_ARG, "workspace must be 256-byte aligned");
   const DraftLayout L = draft_layout(R, gamma, V, rank, dtype_w);
   if (ws_bytes < L.total)
@@ -223,7 +244,7 @@ dspark_status dspark_markov_draft(int R, int gamma, int V, int rank, int d, int 
   for (int k = 1; k <= gamma; ++k) {
     int npart;
     const bool prof = 2 * k <= g_prof_n;
-    if (prof && (e = cudaEventRecord((cudaEvent_t)g_prof_events[2 * (k - 1)], s)) != cudaSuccess)
+    if (prof && (e = record_profile_event(g_prof_events[2 * (k - 1)], s)) != cudaSuccess)
       return cuda_fail(e, "profile event");
     if (tc) {
       if ((e = dspark::launch_draft_step_tc(a, k, s)) != cudaSuccess) return cuda_fail(e, "draft_step_tc");
@@ -232,8 +253,10 @@ dspark_status dspark_markov_draft(int R, int gamma, int V, int rank, int d, int 
       if ((e = dspark::launch_draft_step_simt(a, k, s)) != cudaSuccess) return cuda_fail(e, "draft_step_simt");
       npart = dspark::simt_num_chunks(V);
     }
-    if (prof && (e = cudaEventRecord((cudaEvent_t)g_prof_events[2 * (k - 1) + 1], s)) != cudaSuccess)
+    if (prof && (e = record_profile_event(g_prof_events[2 * (k - 1) + 1], s)) != cudaSuccess)
       return cuda_fail(e, "profile event");
+    // the merge runs as its own kernel: launched early (programmatic dependent launch),
+    // it overlaps the next step's prologue and W2 prefetch
     if ((e = dspark::launch_draft_combine(a, k, npart, s)) != cudaSuccess) return cuda_fail(e, "draft_combine");
   }
   return DSPARK_OK;
@@ -307,6 +330,10 @@ dspark_status dspark_verify(int R, int gamma, int V, int rank, int dtype_t, int 
   CHECK_PTR(tokens_out);
   CHECK_PTR(n_out);
   CHECK_PTR(workspace);
+  CHECK_ALIGN16(target);
+  CHECK_ALIGN16(U);
+  CHECK_ALIGN16(W1);
+  CHECK_ALIGN16(W2);
   if (!aligned256(workspace)) return fail(DSPARK_INVALID_ARG, "workspace must be 256-byte aligned");
   const VerifyLayout L = verify_layout(R, gamma, V, rank, dtype_w);
   if (ws_bytes < L.total) return fail(DSPARK_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, L.total);

@@ -19,6 +19,8 @@
 //                    (U + W1[x_{j*-1}] W2), q = exp(z - lse_q), p = exp(t/T - lse_t),
 //                    Gumbel-max of ln(p - q)+ (and of ln p, the rounding fallback)
 //   residual_combine merges the residual partials into the correction token.
+#include <climits>
+
 #include "dspark_common.cuh"
 #include "dspark_internal.h"
 
@@ -79,70 +81,136 @@ __global__ void __launch_bounds__(kPlanThreads) verify_plan_kernel(VerifyArgs a)
   if (threadIdx.x == 0) *a.n_res = 0;
 }
 
-// Per (row, chunk): online (max, sum exp) of t/T; on the bonus row also the
-// Gumbel-max record of t/T + g (stream 2, position ell+1).
-__global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyArgs a) {
+// Per (row, chunk): (max, sum exp) of t/T and, on the bonus row, the Gumbel-max record
+// of t/T + g (stream 2, position ell+1).  Every thread keeps its kRowPer ids in
+// registers, so the chunk's maximum M is known before any exponential and before any
+// random draw.  The bonus draw first keys the chunk's (lowest-id) maximum exactly,
+// L = M + g; every other id then needs its Philox word only for the log-free test
+// 1-u >= exp(z - L), and evaluates its key only when it survives (a handful per chunk).
+constexpr int kRowPer = 32;
+
+__device__ __forceinline__ float block_max(float v, float* sm) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if ((threadIdx.x & 31) == 0) sm[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float r = sm[0];
+#pragma unroll
+  for (int w = 1; w < kRowThreads / 32; ++w) r = fmaxf(r, sm[w]);
+  __syncthreads();
+  return r;
+}
+
+__device__ __forceinline__ int block_min(int v, int* sm) {
+  v = __reduce_min_sync(0xffffffffu, v);
+  if ((threadIdx.x & 31) == 0) sm[threadIdx.x >> 5] = v;
+  __syncthreads();
+  int r = sm[0];
+#pragma unroll
+  for (int w = 1; w < kRowThreads / 32; ++w) r = min(r, sm[w]);
+  __syncthreads();
+  return r;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kRowThreads, 4) verify_rows_kernel(VerifyArgs a) {
   griddep_allow_next();
   griddep_wait();
-  const int n_items = (*a.n_rows) * a.nchunk;
+  constexpr int EPV = DT == DSPARK_F32 ? 4 : 8;  // ids per 16-byte vector
+  constexpr int NV = kRowPer / EPV;              // vectors per thread per item
+  __shared__ float sm_f[kRowThreads / 32];
+  __shared__ int sm_i[kRowThreads / 32];
   __shared__ Partial red[kRowThreads / 32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int n_items = (*a.n_rows) * a.nchunk;
+  const bool vec_ok = (a.V % EPV) == 0 && (reinterpret_cast<uintptr_t>(a.target) & 15u) == 0;
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
     const int row = item / a.nchunk, c = item % a.nchunk;
     const int r = a.row_req[row], t = a.row_t[row];
     const bool bonus = (t == clamp_ell(a, r));
     const size_t rbase = ((size_t)r * (a.gamma + 1) + t) * a.V;
     const int v0 = c * a.chunk, v1 = min(v0 + a.chunk, a.V);
-    Stats st = stats_empty();
-    PhiloxRow prow;
-    if (bonus) prow = philox_row(rng_row(a.seed, __ldg(a.req_id + r), a.round, kStreamCorrect, (uint32_t)(t + 1)));
-    // groups of 4 consecutive ids (chunk starts are multiples of 4)
-    for (int g = v0 / 4 + threadIdx.x; 4 * g < v1; g += blockDim.x) {
-      float x[4];
-      const int vb = 4 * g;
-      if (a.dtype_t == DSPARK_F32 && (a.V % 4) == 0) {
-        const float4 q = __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.target) + rbase) + g);
-        x[0] = q.x; x[1] = q.y; x[2] = q.z; x[3] = q.w;
-      } else if (a.dtype_t == DSPARK_BF16 && (a.V % 4) == 0) {
-        const uint2 q = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const unsigned short*>(a.target) + rbase) + g);
-        x[0] = bf16_bits_to_float(q.x & 0xFFFFu); x[1] = bf16_bits_to_float(q.x >> 16);
-        x[2] = bf16_bits_to_float(q.y & 0xFFFFu); x[3] = bf16_bits_to_float(q.y >> 16);
+    // thread's ids: vector i covers v0 + (threadIdx.x + i*kRowThreads)*EPV + [0, EPV)
+    float z[kRowPer];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int vb = v0 + (threadIdx.x + i * kRowThreads) * EPV;
+      if (vec_ok && vb + EPV <= v1) {
+        if constexpr (DT == DSPARK_F32) {
+          const float4 q = __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.target) + rbase + vb));
+          z[i * 4 + 0] = q.x;
+          z[i * 4 + 1] = q.y;
+          z[i * 4 + 2] = q.z;
+          z[i * 4 + 3] = q.w;
+        } else {
+          const uint4 q =
+              __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned short*>(a.target) + rbase + vb));
+          const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            z[i * 8 + 2 * e] = bf16_bits_to_float(wd[e] & 0xFFFFu);
+            z[i * 8 + 2 * e + 1] = bf16_bits_to_float(wd[e] >> 16);
+          }
+        }
       } else {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) x[e] = (vb + e < v1) ? load_elem(a.target, a.dtype_t, rbase + vb + e) : 0.f;
+        for (int e = 0; e < EPV; ++e) z[i * EPV + e] = (vb + e < v1) ? load_elem(a.target, DT, rbase + vb + e) : -INFINITY;
       }
-      const int nv = min(4, v1 - vb);
-      float z[4], term[4];
-      float cmax = -INFINITY;
+    }
+    float m = -INFINITY;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        z[e] = x[e] * a.inv_temp;
-        if (e < nv) cmax = fmaxf(cmax, z[e]);
+    for (int k = 0; k < kRowPer; ++k) {
+      z[k] *= a.inv_temp;
+      m = fmaxf(m, z[k]);
+    }
+    const float M = block_max(m, sm_f);
+    Stats st = stats_empty();
+    st.m = M;
+    st.s = 0.f;
+#pragma unroll
+    for (int k = 0; k < kRowPer; ++k) st.s += __expf(z[k] - M);
+    if (bonus) {
+      int mi = INT_MAX;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const int vb = v0 + (threadIdx.x + i * kRowThreads) * EPV;
+#pragma unroll
+        for (int e = 0; e < EPV; ++e)
+          if (z[i * EPV + e] == M) mi = min(mi, vb + e);
       }
-      // online (max, sum exp) with term_e = exp(z_e - m)
-      const float mnew = fmaxf(st.m, cmax);
-      float s = (st.m == -INFINITY) ? 0.f : st.s * __expf(st.m - mnew);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        term[e] = (e < nv) ? __expf(z[e] - mnew) : 0.f;
-        s += term[e];
+      mi = block_min(mi, sm_i);
+      if (mi == INT_MAX) {  // no finite maximum: NaN logits
+        report_bad_input(a.status, 12);
+        mi = v0;
       }
-      st.m = mnew;
-      st.s = s;
-      if (bonus) {
-        // Gumbel-max with the exact log-free rejection of elements that cannot beat
-        // the running key (1-u >= exp(z - best))
-        const Philox4 bits = prow.block((uint32_t)g);
-        const uint32_t wd[4] = {bits.x, bits.y, bits.z, bits.w};
-        const float scale = (st.idx >= 0) ? __expf(mnew - st.key) * kRejectSlack : INFINITY;
+      const PhiloxRow prow =
+          philox_row(rng_row(a.seed, __ldg(a.req_id + r), a.round, kStreamCorrect, (uint32_t)(t + 1)));
+      const Philox4 wb = prow.block((uint32_t)mi >> 2);
+      const uint32_t wm = (mi & 3) == 0 ? wb.x : ((mi & 3) == 1 ? wb.y : ((mi & 3) == 2 ? wb.z : wb.w));
+      const float L = M + gumbel_from_bits(wm);
+      st.key = L;
+      st.idx = mi;
+      st.zsel = M;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          if (e >= nv || (st.idx >= 0 && gumbel_cannot_win(wd[e], term[e] * scale))) continue;
-          const float key = z[e] + gumbel_from_bits(wd[e]);
-          if (key > st.key || st.idx < 0) {
-            st.key = key;
-            st.idx = vb + e;
-            st.zsel = z[e];
+      for (int i = 0; i < NV; ++i) {
+        const int vb = v0 + (threadIdx.x + i * kRowThreads) * EPV;
+#pragma unroll
+        for (int q = 0; q < EPV / 4; ++q) {
+          const int vq = vb + 4 * q;
+          if (vq >= v1) continue;
+          const Philox4 bits = prow.block((uint32_t)vq >> 2);
+          const uint32_t wd[4] = {bits.x, bits.y, bits.z, bits.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float zz = z[i * EPV + 4 * q + e];
+            if (gumbel_cannot_win(wd[e], __expf(zz - L) * kRejectSlack)) continue;
+            const int id = vq + e;
+            const float key = zz + gumbel_from_bits(wd[e]);
+            if (key > st.key || (key == st.key && id < st.idx)) {
+              st.key = key;
+              st.idx = id;
+              st.zsel = zz;
+            }
           }
         }
       }
@@ -151,7 +219,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyArgs a) 
     if (lane == 0) red[warp] = to_partial(w);
     __syncthreads();
     if (warp == 0) {
-      Stats b = (lane < (int)(blockDim.x >> 5)) ? from_partial(red[lane]) : stats_empty();
+      Stats b = (lane < kRowThreads / 32) ? from_partial(red[lane]) : stats_empty();
       b = warp_reduce_stats(b);
       if (lane == 0) a.row_part[(size_t)row * a.nchunk + c] = to_partial(b);
     }
@@ -376,8 +444,11 @@ cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s) {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int max_items = a.R * (a.gamma + 1) * a.nchunk;
-  const int grid = min(max_items, sms * 8);
-  if ((e = launch_pdl(verify_rows_kernel, dim3(grid), dim3(kRowThreads), 0, s, a)) != cudaSuccess) return e;
+  const int grid = min(max_items, sms * 4);
+  if (a.chunk != kRowThreads * kRowPer) return cudaErrorInvalidValue;
+  e = a.dtype_t == DSPARK_F32 ? launch_pdl(verify_rows_kernel<DSPARK_F32>, dim3(grid), dim3(kRowThreads), 0, s, a)
+                              : launch_pdl(verify_rows_kernel<DSPARK_BF16>, dim3(grid), dim3(kRowThreads), 0, s, a);
+  if (e != cudaSuccess) return e;
   const int wblocks = (a.R * 32 + 255) / 256;
   if ((e = launch_pdl(verify_accept_kernel, dim3(wblocks), dim3(256), 0, s, a)) != cudaSuccess) return e;
   int npart;

@@ -52,6 +52,8 @@ def _draft_call(b, **kw):
     P = _fake(13)
     for k in kw.get("null", []):
         P[k] = None
+    for k in kw.get("misalign", []):
+        P[k] = ctypes.c_void_p(P[k].value + 8)
     return b.lib.dspark_markov_draft(args["R"], args["gamma"], args["V"], args["rank"], args["d"], args["du"],
                                      args["dw"], args["dh"], P[0], P[1], P[2], P[3], P[4], 0.0, 1.0, P[5],
                                      args["T"], P[6], P[7], 0, 0, P[8], P[9], P[10], P[11], P[12],
@@ -70,6 +72,9 @@ def test_draft_validation(b):
         assert _draft_call(b, null=[k]) == 1, k
     assert _draft_call(b, ws_bytes=16) == 3
     assert "workspace" in b.lib.dspark_last_error_message().decode()
+    for k in (0, 1, 2, 3):  # U, W1, W2, h: 16-byte vector loads and TMA
+        assert _draft_call(b, misalign=[k]) == 1, k
+        assert "16-byte" in b.lib.dspark_last_error_message().decode()
 
 
 def test_schedule_validation(b):
@@ -94,6 +99,8 @@ def test_verify_validation(b):
         p = list(P)
         for k in kw.get("null", []):
             p[k] = None
+        for k in kw.get("misalign", []):
+            p[k] = ctypes.c_void_p(p[k].value + 4)
         return L(a["R"], a["g"], a["V"], a["rank"], a["dt"], 0, 0, p[0], p[1], p[2], p[3], p[4], p[5], p[6],
                  p[7], p[8], a["T"], p[9], 0, 0, p[10], p[11], p[12], p[13], a["ws"], None)
 
@@ -104,6 +111,9 @@ def test_verify_validation(b):
     for k in range(14):
         assert call(null=[k]) == 1, k
     assert call(ws=100) == 3
+    for k in (0, 1, 2, 3):  # target, U, W1, W2
+        assert call(misalign=[k]) == 1, k
+        assert "16-byte" in b.lib.dspark_last_error_message().decode()
 
 
 def test_workspace_sizes_grow_with_shape(b):
