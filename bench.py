@@ -144,6 +144,26 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+def rank_request_ids(req_id, rank, R):
+    """Each rank serves its own independent batch: request ids rank*R .. rank*R + R-1, so
+    no two ranks share a random stream."""
+    return req_id + rank * R
+
+
+def combine_ranks(round_ms, tokens, device):
+    """Whole-job figures over the ranks: the slowest rank's time (max) and the tokens of
+    all ranks (sum).  Single-process runs return their own values."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return round_ms, tokens
+    t = torch.tensor([round_ms], dtype=torch.float64, device=device)
+    n = torch.tensor([float(tokens)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(n.item())
+
+
 def draft_step_bytes(w):
     """Algorithmic bytes of one draft-step launch: the U row block of every request, the
     whole W2 factor, and the gathered W1 rows."""
@@ -223,7 +243,7 @@ def main():
     # generated on the host: the CPU baseline and the end-to-end leg need host copies
     w_cpu = wl.make(args.workload, device="cpu", seed=0)
     w = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in w_cpu.items()}
-    w["req_id"] = w["req_id"] + rank * w["R"]  # each rank serves its own requests
+    w["req_id"] = rank_request_ids(w["req_id"], rank, w["R"])
     rd = b.Round(w)
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -268,12 +288,7 @@ def main():
         wall = time.perf_counter() - wall0
     round_ms = sum(a.elapsed_time(e) for a, e in zip(starts, ends))
     tokens = int(n_acc_sum.item())
-    if world > 1:
-        tt = torch.tensor([round_ms, float(tokens)], dtype=torch.float64, device=dev)
-        mx = tt.clone()
-        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
-        dist.all_reduce(tt, op=dist.ReduceOp.SUM)
-        round_ms, tokens = float(mx[0]), int(tt[1])
+    round_ms, tokens = combine_ranks(round_ms, tokens, dev)
     value = tokens / (round_ms / 1000.0)
     assert rd.status() == 0, "device status word reports an error"
 
