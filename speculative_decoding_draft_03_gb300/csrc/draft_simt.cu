@@ -24,75 +24,111 @@ namespace dspark {
 
 constexpr int kCombineThreads = 128;
 
-// One warp per (r,k) row of h.
-__global__ void conf_hdot_kernel(int rows, int d, int dtype_h, const void* __restrict__ h,
-                                 const float* __restrict__ w_h, float* __restrict__ s_h) {
+// s_h[row] = w_h . h[row,:] for the R*gamma rows of h.  A CTA of 256 threads takes two
+// rows, four warps per row; each lane issues all of its 16-byte loads of an iteration
+// before using them, and the four warp sums are added in a fixed order (deterministic).
+constexpr int kHdotThreads = 256;
+constexpr int kHdotWarpsPerRow = 4;
+constexpr int kHdotRowsPerCta = kHdotThreads / 32 / kHdotWarpsPerRow;
+constexpr int kHdotUnroll = 4;
+
+__global__ void __launch_bounds__(kHdotThreads) conf_hdot_kernel(int rows, int d, int dtype_h,
+                                                                 const void* __restrict__ h,
+                                                                 const float* __restrict__ w_h,
+                                                                 float* __restrict__ s_h) {
   griddep_allow_next();
   griddep_wait();
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (warp >= rows) return;
+  __shared__ float part[kHdotRowsPerCta][kHdotWarpsPerRow];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int local = warp / kHdotWarpsPerRow, sub = warp % kHdotWarpsPerRow;
+  const int row = blockIdx.x * kHdotRowsPerCta + local;
+  constexpr int kStride = 32 * kHdotWarpsPerRow;  // lanes per row
   float acc = 0.f;
-  const size_t base = (size_t)warp * d;
-  if (dtype_h == DSPARK_BF16 && (d % 8) == 0) {
-    const uint4* hp = reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned short*>(h) + base);
-    for (int c = lane; c < d / 8; c += 32) {
-      const uint4 q = __ldg(hp + c);
-      const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+  if (row < rows) {
+    const size_t base = (size_t)row * d;
+    const bool vec = dtype_h == DSPARK_BF16 && (d % 8) == 0 && (reinterpret_cast<uintptr_t>(h) & 15u) == 0;
+    if (vec) {
+      const int n8 = d / 8;
+      const uint4* hp = reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned short*>(h) + base);
+      for (int c0 = sub * 32 + lane; c0 < n8; c0 += kHdotUnroll * kStride) {
+        uint4 q[kHdotUnroll];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        acc = fmaf(__ldg(w_h + c * 8 + 2 * e), bf16_bits_to_float(wd[e] & 0xFFFFu), acc);
-        acc = fmaf(__ldg(w_h + c * 8 + 2 * e + 1), bf16_bits_to_float(wd[e] >> 16), acc);
+        for (int u = 0; u < kHdotUnroll; ++u) {
+          const int c = c0 + u * kStride;
+          q[u] = (c < n8) ? __ldg(hp + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kHdotUnroll; ++u) {
+          const int c = c0 + u * kStride;
+          if (c >= n8) break;
+          const uint32_t wd[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            acc = fmaf(__ldg(w_h + c * 8 + 2 * e), bf16_bits_to_float(wd[e] & 0xFFFFu), acc);
+            acc = fmaf(__ldg(w_h + c * 8 + 2 * e + 1), bf16_bits_to_float(wd[e] >> 16), acc);
+          }
+        }
       }
+    } else {
+      for (int i = sub * 32 + lane; i < d; i += kStride) acc = fmaf(__ldg(w_h + i), load_elem(h, dtype_h, base + i), acc);
     }
-  } else {
-    for (int i = lane; i < d; i += 32) acc = fmaf(__ldg(w_h + i), load_elem(h, dtype_h, base + i), acc);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) s_h[warp] = acc;
+  if (lane == 0) part[local][sub] = acc;
+  __syncthreads();
+  if (threadIdx.x < kHdotRowsPerCta) {
+    const int rr = blockIdx.x * kHdotRowsPerCta + threadIdx.x;
+    if (rr < rows) {
+      float t = 0.f;
+#pragma unroll
+      for (int w = 0; w < kHdotWarpsPerRow; ++w) t += part[threadIdx.x][w];
+      s_h[rr] = t;
+    }
+  }
 }
 
-// Block-wide sum over kCombineThreads threads (result valid in every thread).
-__device__ __forceinline__ float block_sum(float v, float* scratch) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  __syncthreads();
-  if (lane == 0) scratch[warp] = v;
-  __syncthreads();
-  float t = 0.f;
-#pragma unroll
-  for (int w = 0; w < kCombineThreads / 32; ++w) t += scratch[w];
-  return t;
-}
-
-// Gather W1[x_prev] into W1g[r] and write c_k; executed by a whole CTA of
-// kCombineThreads threads.
-__device__ void prepare_position_block(const DraftArgs& a, int r, int k, int x_prev, float* scratch) {
+// Gather W1[x_prev] into W1g[r] and write c_k; executed by one warp.  Lane l covers the
+// factor ids [8l, 8l+8) with one 16-byte load (bf16 rows of rank <= 256), so the whole
+// row arrives after one memory latency.
+__device__ void prepare_position_warp(const DraftArgs& a, int r, int k, int x_prev, int lane) {
   const size_t src = (size_t)x_prev * a.rank;
   const size_t dst = (size_t)r * a.rank;
-  float acc = 0.f;
   const float* w_e = a.conf_w + a.d;
-  if (a.dtype_w == DSPARK_BF16) {
+  float acc = 0.f;
+  if (a.dtype_w == DSPARK_BF16 && (a.rank % 8) == 0) {
+    const uint4* w1 = reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned short*>(a.W1) + src);
+    uint4* g = reinterpret_cast<uint4*>(reinterpret_cast<unsigned short*>(a.W1g) + dst);
+    for (int c = lane; c < a.rank / 8; c += 32) {
+      const uint4 q = __ldg(w1 + c);
+      g[c] = q;
+      const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc = fmaf(__ldg(w_e + 8 * c + 2 * e), bf16_bits_to_float(wd[e] & 0xFFFFu), acc);
+        acc = fmaf(__ldg(w_e + 8 * c + 2 * e + 1), bf16_bits_to_float(wd[e] >> 16), acc);
+      }
+    }
+  } else if (a.dtype_w == DSPARK_BF16) {
     const unsigned short* w1 = reinterpret_cast<const unsigned short*>(a.W1);
     unsigned short* g = reinterpret_cast<unsigned short*>(a.W1g);
-    for (int i = threadIdx.x; i < a.rank; i += blockDim.x) {
-      const unsigned short b = __ldg(w1 + src + i);
-      g[dst + i] = b;
-      acc = fmaf(__ldg(w_e + i), bf16_bits_to_float(b), acc);
+    for (int i = lane; i < a.rank; i += 32) {
+      const unsigned short bits = __ldg(w1 + src + i);
+      g[dst + i] = bits;
+      acc = fmaf(__ldg(w_e + i), bf16_bits_to_float(bits), acc);
     }
   } else {
     const float* w1 = reinterpret_cast<const float*>(a.W1);
     float* g = reinterpret_cast<float*>(a.W1g);
-    for (int i = threadIdx.x; i < a.rank; i += blockDim.x) {
-      const float b = __ldg(w1 + src + i);
-      g[dst + i] = b;
-      acc = fmaf(__ldg(w_e + i), b, acc);
+    for (int i = lane; i < a.rank; i += 32) {
+      const float v = __ldg(w1 + src + i);
+      g[dst + i] = v;
+      acc = fmaf(__ldg(w_e + i), v, acc);
     }
   }
-  acc = block_sum(acc, scratch);
-  if (threadIdx.x == 0) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) {
     const size_t row = (size_t)r * a.gamma + (k - 1);
     const float logit = a.conf_scale * (a.s_h[row] + acc + a.conf_b);
     a.conf_out[row] = sigmoidf_dev(logit / __ldg(a.conf_temp + (k - 1)));
@@ -102,15 +138,14 @@ __device__ void prepare_position_block(const DraftArgs& a, int r, int k, int x_p
   }
 }
 
-// One CTA per request.
-__global__ void __launch_bounds__(kCombineThreads) draft_prepare_kernel(DraftArgs a, int k) {
+// Position 1: one warp per request.
+__global__ void __launch_bounds__(32) draft_prepare_kernel(DraftArgs a, int k) {
   griddep_allow_next();
   griddep_wait();
-  __shared__ float scratch[kCombineThreads / 32];
   const int r = blockIdx.x;
   const int raw = (k == 1) ? __ldg(a.x0 + r) : a.x_out[(size_t)r * a.gamma + (k - 2)];
   const int x_prev = checked_token(raw, a.V, a.status, 1);
-  prepare_position_block(a, r, k, x_prev, scratch);
+  prepare_position_warp(a, r, k, x_prev, threadIdx.x & 31);
 }
 
 // ---------------------------------------------------------------------------------
@@ -215,30 +250,37 @@ __global__ void __launch_bounds__(kSimtThreads) draft_step_simt_kernel(DraftArgs
 __global__ void __launch_bounds__(kCombineThreads) draft_combine_kernel(DraftArgs a, int k, int npart) {
   griddep_allow_next();
   griddep_wait();
+  constexpr int kBatch = 4;
   __shared__ Partial red[kCombineThreads / 32];
-  __shared__ float scratch[kCombineThreads / 32];
-  __shared__ int xk_s;
   const int r = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   Stats st = stats_empty();
-  for (int p = threadIdx.x; p < npart; p += blockDim.x) stats_merge(st, from_partial(a.partials[(size_t)p * a.R + r]));
+  // every thread's partial records are loaded before any is merged
+  for (int p0 = threadIdx.x; p0 < npart; p0 += kBatch * kCombineThreads) {
+    Partial rec[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int p = p0 + u * kCombineThreads;
+      if (p < npart) rec[u] = a.partials[(size_t)p * a.R + r];
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u)
+      if (p0 + u * kCombineThreads < npart) stats_merge(st, from_partial(rec[u]));
+  }
   st = warp_reduce_stats(st);
   if (lane == 0) red[warp] = to_partial(st);
   __syncthreads();
-  if (warp == 0) {
-    Stats b = (lane < kCombineThreads / 32) ? from_partial(red[lane]) : stats_empty();
-    b = warp_reduce_stats(b);
-    if (lane == 0) {
-      const size_t row = (size_t)r * a.gamma + (k - 1);
-      const float lse = b.m + logf(b.s);
-      a.x_out[row] = b.idx;
-      a.lse_out[row] = lse;
-      a.logq_out[row] = b.zsel - lse;
-      xk_s = checked_token(b.idx, a.V, a.status, 2);
-    }
+  if (warp != 0) return;
+  Stats b = (lane < kCombineThreads / 32) ? from_partial(red[lane]) : stats_empty();
+  b = warp_reduce_stats(b);
+  const size_t row = (size_t)r * a.gamma + (k - 1);
+  if (lane == 0) {
+    const float lse = b.m + logf(b.s);
+    a.x_out[row] = b.idx;
+    a.lse_out[row] = lse;
+    a.logq_out[row] = b.zsel - lse;
   }
-  __syncthreads();
-  if (k < a.gamma) prepare_position_block(a, r, k + 1, xk_s, scratch);
+  if (k < a.gamma) prepare_position_warp(a, r, k + 1, checked_token(b.idx, a.V, a.status, 2), lane);
 }
 
 // ---------------------------------------------------------------------------------
@@ -246,14 +288,13 @@ __global__ void __launch_bounds__(kCombineThreads) draft_combine_kernel(DraftArg
 // ---------------------------------------------------------------------------------
 cudaError_t launch_conf_hdot(const DraftArgs& a, cudaStream_t s) {
   const int rows = a.R * a.gamma;
-  const int threads = 256;
-  const int blocks = (rows * 32 + threads - 1) / threads;
-  return launch_pdl(conf_hdot_kernel, dim3(blocks), dim3(threads), 0, s, rows, a.d, a.dtype_h, a.h, a.conf_w,
+  const int blocks = (rows + kHdotRowsPerCta - 1) / kHdotRowsPerCta;
+  return launch_pdl(conf_hdot_kernel, dim3(blocks), dim3(kHdotThreads), 0, s, rows, a.d, a.dtype_h, a.h, a.conf_w,
                     a.s_h);
 }
 
 cudaError_t launch_draft_prepare(const DraftArgs& a, int k, cudaStream_t s) {
-  return launch_pdl(draft_prepare_kernel, dim3(a.R), dim3(kCombineThreads), 0, s, a, k);
+  return launch_pdl(draft_prepare_kernel, dim3(a.R), dim3(32), 0, s, a, k);
 }
 
 int simt_num_chunks(int V) {

@@ -58,7 +58,10 @@ constexpr int kCols = 8;          // vocabulary ids per epilogue pass
 constexpr int kTmemCols = 2 * kN;
 constexpr int kMaxRank = 256;
 constexpr long long kWaitCycles = 4000000000ll;  // ~2 s at 2 GHz
-constexpr int kPublishTiles = 2;  // tiles after which a CTA publishes its best keys
+// Tiles after which a CTA publishes its best keys: one for 32-request blocks (eight
+// tiles per CTA, where each publication is a visible share of the step), two otherwise.
+template <int RB>
+constexpr int publish_tiles() { return RB == 32 ? 1 : 2; }
 
 // Shared-memory plan per request-block size RB.  The U ring (draft mode) holds boxes of
 // 128 bytes x RB request rows (32 fp32 or 64 bf16 vocabulary ids); the kernel uses a
@@ -522,6 +525,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int buf = t & 1;
       const uint32_t use = (uint32_t)(t >> 1) & 1u;
       const int vt = (group + t * p.ngroups) * kN;
+      // the published bound is read a tile ahead of its use, so that its latency hides
+      // behind this tile's work
+      const int hint_pref = (MODE == kModeDraft && valid) ? __ldcg(p.hint + r) : 0;
       uint4 ucur[kPass][2];
       int uslot = 0;
       bool u_ready = true;
@@ -705,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (MODE == kModeDraft) {
         // After the first tiles, publish the CTA's best key per request (one atomic per
         // request per CTA), so that CTAs still streaming can skip more of their draws.
-        if (t < kPublishTiles) {
+        if (t < publish_tiles<RB>()) {
           float* pub = reinterpret_cast<float*>(smem + SM::pub);
           pub[ew * 32 + lane] = (valid && st.idx >= 0) ? st.key : -INFINITY;
           asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
@@ -723,8 +729,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
         }
-        // the bound for the next tile (its latency overlaps the next tile's wait)
-        if (valid) bound = key_from_ordered(__ldcg(p.hint + r));
+        // the bound for the next tile
+        if (valid) bound = key_from_ordered(hint_pref);
       }
     }
     // merge the threads that share a request: smem slots [ew][lane]

@@ -11,8 +11,9 @@
 // GB300 layout: R*gamma <= 8192 candidates fit one SM's shared memory.  a is formed
 // in binary64 by the same left-to-right products as the method states, so the sort
 // keys (the binary64 bit patterns of a, which order like the values for a >= 0) and
-// hence the admission order do not depend on rounding.  The sort is a bitonic network
-// over (key, candidate id) pairs; the scan and the mode's pick are block reductions.
+// hence the admission order do not depend on rounding.  Each request's chain of a's is
+// already sorted, so the global order is a merge of R sorted lists: rounds of pairwise
+// merge-path merges; the scan and the mode's pick are block reductions.
 #include "dspark_common.cuh"
 #include "dspark_internal.h"
 
@@ -20,95 +21,140 @@ namespace dspark {
 
 constexpr int kSchedThreads = 1024;  // one CTA; R*gamma <= 8192 candidates (host-checked)
 
-static int next_pow2(int n) {
-  int p = 2;
-  while (p < n) p <<= 1;
-  return p;
-}
-
 size_t schedule_smem_bytes(int R, int gamma) {
-  const int npad = next_pow2(R * gamma);
-  return align256((size_t)npad * 8) + align256((size_t)npad * 2) + align256((size_t)R * 4) +
-         align256(sizeof(double) * 64) + 256;
+  const size_t N = (size_t)R * gamma;
+  return align256(N * 8) + 2 * align256(N * 2) + align256((size_t)R * 4) + align256(sizeof(double) * 64) + 256;
 }
 
+// Shared memory (N = R*gamma <= 8192 candidates, 161 KB at most):
+//   key   [N] binary64 bits of a, indexed by candidate id; after the scan the same array
+//         holds the prefix sums in sorted order
+//   ids   two [N] buffers of candidate ids (the merge ping-pongs between them); before the
+//         sort they stage the confidences (N fp32 fill both exactly)
 struct SchedSmem {
-  unsigned long long* key;  // [npad] binary64 bits of a (0 for padding)
-  unsigned short* id;       // [npad] candidate id (j-1)*R + r (0xFFFF for padding)
-  int* ell;                 // [R]
-  double* red;              // [64] reduction scratch
-  int* misc;                // [8]
+  unsigned long long* key;
+  unsigned short* idA;
+  unsigned short* idB;
+  unsigned short* sorted;  // the buffer that holds the final order
+  int* ell;                // [R]
+  double* red;             // [64] reduction scratch
+  int* misc;               // [8]
 };
 
-// does candidate (ka, ia) come before (kb, ib)?  a desc, then id asc; the id
-// (j-1)*R + r orders by depth first, then request.
-__device__ __forceinline__ bool before(unsigned long long ka, unsigned ia, unsigned long long kb, unsigned ib) {
-  return (ka > kb) || (ka == kb && ia < ib);
+// does candidate x come before candidate y?  a desc, then id asc; the id (j-1)*R + r
+// orders by depth first, then request.
+__device__ __forceinline__ bool before(const SchedSmem& sm, unsigned x, unsigned y) {
+  const unsigned long long kx = sm.key[x], ky = sm.key[y];
+  return (kx > ky) || (kx == ky && x < y);
 }
 
-__device__ void bitonic_sort(SchedSmem& sm, int npad) {
-  for (int k = 2; k <= npad; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int p = threadIdx.x; p < (npad >> 1); p += blockDim.x) {
-        const int i = 2 * j * (p / j) + (p % j);
-        const int l = i + j;
-        const unsigned long long ki = sm.key[i], kl = sm.key[l];
-        const unsigned ii = sm.id[i], il = sm.id[l];
-        const bool up = (i & k) == 0;
-        const bool swap = up ? before(kl, il, ki, ii) : before(ki, ii, kl, il);
-        if (swap) {
-          sm.key[i] = kl;
-          sm.key[l] = ki;
-          sm.id[i] = (unsigned short)il;
-          sm.id[l] = (unsigned short)ii;
-        }
-      }
-      __syncthreads();
-    }
-  }
-}
-
-// a = prod c along each chain, into (key, id); padding sorts last.
-__device__ void build_candidates(SchedSmem& sm, const float* conf, int R, int gamma, int npad) {
+// a = prod c along each chain (binary64, left to right), keyed by candidate id.  Each
+// request's chain is already in sorted order: c <= 1 makes a non-increasing in j, and
+// on equal a the smaller depth comes first.  A confidence outside [0,1] (or NaN) is
+// reported and clamped, which keeps the chains sorted.
+__device__ void build_candidates(SchedSmem& sm, const float* conf, int R, int gamma, DeviceStatus* status) {
   const int N = R * gamma;
+  float* cf = reinterpret_cast<float*>(sm.idA);  // spans idA and idB
+  for (int i = threadIdx.x; i < N; i += blockDim.x) cf[i] = __ldg(conf + i);
+  __syncthreads();
   for (int r = threadIdx.x; r < R; r += blockDim.x) {
     double a = 1.0;
     for (int j = 1; j <= gamma; ++j) {
-      a = __dmul_rn(a, (double)__ldg(conf + (size_t)r * gamma + (j - 1)));
-      const int id = (j - 1) * R + r;
-      sm.key[id] = (unsigned long long)__double_as_longlong(a);
-      sm.id[id] = (unsigned short)id;
+      float c = cf[r * gamma + (j - 1)];
+      if (!(c >= 0.f && c <= 1.f)) {
+        report_bad_input(status, 20);
+        c = (c > 1.f) ? 1.f : 0.f;
+      }
+      a = __dmul_rn(a, (double)c);
+      sm.key[(j - 1) * R + r] = (unsigned long long)__double_as_longlong(a);
     }
   }
-  for (int i = N + threadIdx.x; i < npad; i += blockDim.x) {
-    sm.key[i] = 0ull;
-    sm.id[i] = 0xFFFFu;
+  __syncthreads();
+  // round-0 lists: chain r at positions [r*gamma, (r+1)*gamma)
+  for (int i = threadIdx.x; i < N; i += blockDim.x) {
+    const int r = i / gamma, j = i % gamma;
+    sm.idA[i] = (unsigned short)(j * R + r);
   }
   __syncthreads();
 }
 
-// Inclusive prefix sums of the sorted a's, in place into key[] as binary64 bits.
-// Each thread scans a contiguous run, then the run totals are scanned across the block.
+// Sorts the R chains into one list by rounds of pairwise merges (lists of gamma, 2 gamma,
+// 4 gamma, ... ids).  Each thread produces a contiguous run of E = ceil(N / threads)
+// outputs: a merge-path binary search finds where its run starts in the two input
+// lists, then it merges E elements sequentially.  ceil(log2 R) rounds, one barrier each.
+__device__ void merge_sort_chains(SchedSmem& sm, int N, int gamma) {
+  unsigned short* src = sm.idA;
+  unsigned short* dst = sm.idB;
+  const int E = (N + blockDim.x - 1) / blockDim.x;
+  for (int L = gamma; L < N; L <<= 1) {
+    const int p_begin = threadIdx.x * E, p_end = min(p_begin + E, N);
+    int p = p_begin;
+    while (p < p_end) {
+      const int m0 = (p / (2 * L)) * (2 * L);  // start of this pair
+      const int a0 = m0, a_len = min(L, N - m0);
+      const int b0 = m0 + a_len, b_len = max(0, min(L, N - b0));
+      const int seg_end = min(p_end, m0 + a_len + b_len);
+      const int d = p - m0;
+      // merge path: i elements of A and d - i of B make up the first d outputs
+      int lo = max(0, d - b_len), hi = min(d, a_len);
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (before(sm, src[a0 + mid], src[b0 + d - mid - 1]))
+          lo = mid + 1;
+        else
+          hi = mid;
+      }
+      int i = lo, j = d - lo;
+      for (; p < seg_end; ++p) {
+        const bool take_a = (j >= b_len) || (i < a_len && before(sm, src[a0 + i], src[b0 + j]));
+        dst[p] = take_a ? src[a0 + i++] : src[b0 + j++];
+      }
+    }
+    __syncthreads();
+    unsigned short* t = src;
+    src = dst;
+    dst = t;
+  }
+  sm.sorted = src;
+}
+
+// Inclusive prefix sums of the sorted a's, written over key[] in sorted order.  Each
+// thread gathers its run (at most 8 values) into registers before any is overwritten.
+constexpr int kScanPer = 8;  // 8192 candidates / 1024 threads
+
 __device__ void scan_sorted(SchedSmem& sm, int N) {
   const int per = (N + blockDim.x - 1) / blockDim.x;
   const int lo = threadIdx.x * per;
   const int hi = min(lo + per, N);
-  double run = 0.0;
-  for (int i = lo; i < hi; ++i) run += __longlong_as_double((long long)sm.key[i]);
-  // exclusive scan of run totals: warp shuffles, then the 32 warp totals
+  // binary64 arithmetic is a narrow pipe on this GPU: warps without candidates skip it
+  // (per and the warp's first index are uniform, so every branch below is too)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  double incl = run;
+  const bool active = (warp * 32) * per < N;
+  double v[kScanPer];
+  double run = 0.0;
+  double excl = 0.0;
+  if (active) {
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const double t = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += t;
+    for (int q = 0; q < kScanPer; ++q) {
+      if (q >= per) break;
+      v[q] = (lo + q < hi) ? __longlong_as_double((long long)sm.key[sm.sorted[lo + q]]) : 0.0;
+      run += v[q];
+    }
+    // exclusive scan of run totals within the warp
+    double incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    excl = __shfl_up_sync(0xffffffffu, incl, 1);
+    if (lane == 0) excl = 0.0;
+    if (lane == 31) sm.red[warp] = incl;
   }
-  double excl = __shfl_up_sync(0xffffffffu, incl, 1);
-  if (lane == 0) excl = 0.0;
-  if (lane == 31) sm.red[warp] = incl;
   __syncthreads();
+  const int nactive = min((int)(blockDim.x >> 5), (N + 32 * per - 1) / (32 * per));
   if (warp == 0) {
-    double w = (lane < (int)(blockDim.x >> 5)) ? sm.red[lane] : 0.0;
+    double w = (lane < nactive) ? sm.red[lane] : 0.0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const double t = __shfl_up_sync(0xffffffffu, w, o);
@@ -117,10 +163,16 @@ __device__ void scan_sorted(SchedSmem& sm, int N) {
     sm.red[32 + lane] = w;  // inclusive warp-total prefix
   }
   __syncthreads();
-  double base = excl + (warp > 0 ? sm.red[32 + warp - 1] : 0.0);
-  for (int i = lo; i < hi; ++i) {
-    base += __longlong_as_double((long long)sm.key[i]);
-    sm.key[i] = (unsigned long long)__double_as_longlong(base);
+  if (active) {
+    double base = excl + (warp > 0 ? sm.red[32 + warp - 1] : 0.0);
+#pragma unroll
+    for (int q = 0; q < kScanPer; ++q) {
+      if (q >= per) break;
+      if (lo + q < hi) {
+        base += v[q];
+        sm.key[lo + q] = (unsigned long long)__double_as_longlong(base);
+      }
+    }
   }
   __syncthreads();
 }
@@ -199,19 +251,20 @@ __device__ int early_stop(SchedSmem& sm, int R, int N, const double* sps) {
 __global__ void __launch_bounds__(kSchedThreads, 1)
     schedule_kernel(int R, int gamma, const float* __restrict__ conf, const double* __restrict__ sps, int mode,
                     const float* __restrict__ conf_hist, int fixed_len, int32_t* __restrict__ ell_out,
-                    int32_t* __restrict__ B_out, double* __restrict__ tau_out) {
+                    int32_t* __restrict__ B_out, double* __restrict__ tau_out, DeviceStatus* status) {
   griddep_allow_next();
   griddep_wait();
   extern __shared__ __align__(256) unsigned char smem[];
   const int N = R * gamma;
-  int npad = 2;
-  while (npad < N) npad <<= 1;
   SchedSmem sm;
   size_t off = 0;
   sm.key = reinterpret_cast<unsigned long long*>(smem + off);
-  off += align256((size_t)npad * 8);
-  sm.id = reinterpret_cast<unsigned short*>(smem + off);
-  off += align256((size_t)npad * 2);
+  off += align256((size_t)N * 8);
+  sm.idA = reinterpret_cast<unsigned short*>(smem + off);
+  off += align256((size_t)N * 2);
+  sm.idB = reinterpret_cast<unsigned short*>(smem + off);
+  off += align256((size_t)N * 2);
+  sm.sorted = sm.idA;
   sm.ell = reinterpret_cast<int*>(smem + off);
   off += align256((size_t)R * 4);
   sm.red = reinterpret_cast<double*>(smem + off);
@@ -249,17 +302,17 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
 
   int nstar;
   if (mode == DSPARK_CAPACITY_K) {
-    build_candidates(sm, conf_hist, R, gamma, npad);
-    bitonic_sort(sm, npad);
+    build_candidates(sm, conf_hist, R, gamma, status);
+    merge_sort_chains(sm, N, gamma);
     scan_sorted(sm, N);
     const int K = full_search(sm, R, N, sps);
     nstar = min(K, N);
   }
-  build_candidates(sm, conf, R, gamma, npad);
-  bitonic_sort(sm, npad);
+  build_candidates(sm, conf, R, gamma, status);
+  merge_sort_chains(sm, N, gamma);
   // admitted candidates -> per-request counts (before the scan overwrites the keys)
   if (mode == DSPARK_CAPACITY_K) {
-    for (int n = threadIdx.x; n < nstar; n += blockDim.x) atomicAdd(&sm.ell[sm.id[n] % R], 1);
+    for (int n = threadIdx.x; n < nstar; n += blockDim.x) atomicAdd(&sm.ell[sm.sorted[n] % R], 1);
     __syncthreads();
   }
   scan_sorted(sm, N);
@@ -269,7 +322,7 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
     nstar = full_search(sm, R, N, sps);
   }
   if (mode != DSPARK_CAPACITY_K) {
-    for (int n = threadIdx.x; n < nstar; n += blockDim.x) atomicAdd(&sm.ell[sm.id[n] % R], 1);
+    for (int n = threadIdx.x; n < nstar; n += blockDim.x) atomicAdd(&sm.ell[sm.sorted[n] % R], 1);
   }
   __syncthreads();
   for (int r = threadIdx.x; r < R; r += blockDim.x) ell_out[r] = sm.ell[r];
@@ -282,12 +335,11 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
 cudaError_t launch_schedule(int R, int gamma, const float* conf, const double* sps, int mode,
                             const float* conf_hist, int fixed_len, int32_t* ell_out, int32_t* B_out,
                             double* tau_out, DeviceStatus* status, cudaStream_t s) {
-  (void)status;
   const size_t smem = schedule_smem_bytes(R, gamma);
   cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(schedule_kernel, dim3(1), dim3(kSchedThreads), smem, s, R, gamma, conf, sps, mode, conf_hist,
-                    fixed_len, ell_out, B_out, tau_out);
+                    fixed_len, ell_out, B_out, tau_out, status);
 }
 
 }  // namespace dspark

@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(kRowThreads, 4) verify_rows_kernel(VerifyArgs 
       }
       mi = block_min(mi, sm_i);
       if (mi == INT_MAX) {  // no finite maximum: NaN logits
-        report_bad_input(a.status, 12);
+        report_bad_input(a.status, 13);
         mi = v0;
       }
       const PhiloxRow prow =
@@ -227,7 +227,12 @@ __global__ void __launch_bounds__(kRowThreads, 4) verify_rows_kernel(VerifyArgs 
   }
 }
 
-// One warp per request.
+// One warp per request.  Row t = lane + 32 s (s = 0..2, gamma <= 64) is owned by one
+// lane: its log-normaliser and bonus record come from a warp reduction over the row's
+// chunk partials, then every verified draft j = t+1 is tested by its own lane (all loads
+// of the request are issued together), and a ballot finds the first rejection.
+constexpr int kRowSlots = 3;  // rows per lane: (gamma + 1) <= 96
+
 __global__ void verify_accept_kernel(VerifyArgs a) {
   griddep_allow_next();
   griddep_wait();
@@ -236,35 +241,78 @@ __global__ void verify_accept_kernel(VerifyArgs a) {
   if (r >= a.R) return;
   const int ell = clamp_ell(a, r);
   const int base = a.row_base[r];
-  const RngRow acc_rng = rng_row(a.seed, __ldg(a.req_id + r), a.round, kStreamAccept, 0u);
-  int n_acc = 0;
-  float lse_stop = 0.f;
-  for (int t = 0; t <= ell; ++t) {
-    Stats st = stats_empty();
-    for (int c = lane; c < a.nchunk; c += 32) stats_merge(st, from_partial(a.row_part[(size_t)(base + t) * a.nchunk + c]));
-    st = warp_reduce_stats(st);
-    const float lse = st.m + logf(st.s);
-    if (t == ell) {  // every verified draft accepted: bonus token from row ell
-      if (lane == 0) a.tokens_out[(size_t)r * (a.gamma + 1) + ell] = st.idx;
-      n_acc = ell;
-      break;
-    }
-    // acceptance test of draft j = t+1 against target row t
-    const int xj = checked_token(__ldg(a.x + (size_t)r * a.gamma + t), a.V, a.status, 11);
-    const float tx = load_elem(a.target, a.dtype_t, ((size_t)r * (a.gamma + 1) + t) * a.V + xj) * a.inv_temp;
-    const double lp = (double)tx - (double)lse;
-    const double ratio = exp(lp - (double)__ldg(a.logq + (size_t)r * a.gamma + t));
-    RngRow rr = acc_rng;
-    rr.c2 = (kStreamAccept << 24) | (uint32_t)(t + 1);
-    const double u = uniform_from_bits_f64(rng_chunk(rr, 0u).x);
-    if (u < ratio) {
-      n_acc = t + 1;
-      continue;
-    }
-    n_acc = t;
-    lse_stop = lse;
-    break;
+  const int nch = a.nchunk;
+  float lse_own[kRowSlots];
+  int idx_own[kRowSlots];
+#pragma unroll
+  for (int s = 0; s < kRowSlots; ++s) {
+    lse_own[s] = 0.f;
+    idx_own[s] = -1;
   }
+  // rows 0..ell, eight at a time; each lane merges chunks lane, lane+32, ... of each row
+  for (int t0 = 0; t0 <= ell; t0 += 8) {
+    Stats acc[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[q] = stats_empty();
+    for (int c = lane; c < nch; c += 32) {
+      Partial rec[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (t0 + q <= ell) rec[q] = a.row_part[(size_t)(base + t0 + q) * nch + c];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (t0 + q <= ell) stats_merge(acc[q], from_partial(rec[q]));
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int t = t0 + q;
+      if (t > ell) break;  // uniform across the warp
+      const Stats st = warp_reduce_stats(acc[q]);
+#pragma unroll
+      for (int s = 0; s < kRowSlots; ++s)
+        if (t == lane + 32 * s) {
+          lse_own[s] = st.m + logf(st.s);
+          idx_own[s] = st.idx;
+        }
+    }
+  }
+  // acceptance test of draft j+1 (lane-owned row j < ell) against target row j
+  uint32_t rej[kRowSlots];
+  const RngRow acc_rng = rng_row(a.seed, __ldg(a.req_id + r), a.round, kStreamAccept, 0u);
+#pragma unroll
+  for (int s = 0; s < kRowSlots; ++s) {
+    const int j = lane + 32 * s;
+    bool reject = false;
+    if (j < ell) {
+      const int xj = checked_token(__ldg(a.x + (size_t)r * a.gamma + j), a.V, a.status, 11);
+      const float tx = load_elem(a.target, a.dtype_t, ((size_t)r * (a.gamma + 1) + j) * a.V + xj) * a.inv_temp;
+      const double lp = (double)tx - (double)lse_own[s];
+      const double ratio = exp(lp - (double)__ldg(a.logq + (size_t)r * a.gamma + j));
+      RngRow rr = acc_rng;
+      rr.c2 = (kStreamAccept << 24) | (uint32_t)(j + 1);
+      const double u = uniform_from_bits_f64(rng_chunk(rr, 0u).x);
+      reject = !(u < ratio);
+    }
+    rej[s] = __ballot_sync(0xffffffffu, reject);
+  }
+  int n_acc = ell;
+#pragma unroll
+  for (int s = kRowSlots - 1; s >= 0; --s)
+    if (rej[s]) n_acc = 32 * s + __ffs(rej[s]) - 1;
+  // the row that decided: n_acc (its normaliser for the residual, or its bonus record)
+  const int src_lane = n_acc & 31, src_slot = n_acc >> 5;
+  float lse_stop = 0.f;
+  int bonus = -1;
+#pragma unroll
+  for (int s = 0; s < kRowSlots; ++s) {
+    const float l = __shfl_sync(0xffffffffu, lse_own[s], src_lane);
+    const int i = __shfl_sync(0xffffffffu, idx_own[s], src_lane);
+    if (s == src_slot) {
+      lse_stop = l;
+      bonus = i;
+    }
+  }
+  if (n_acc == ell && lane == 0) a.tokens_out[(size_t)r * (a.gamma + 1) + ell] = bonus;
   const size_t orow = (size_t)r * (a.gamma + 1);
   for (int j = lane; j <= a.gamma; j += 32) {
     if (j < n_acc) a.tokens_out[orow + j] = __ldg(a.x + (size_t)r * a.gamma + j);

@@ -255,3 +255,48 @@ def test_bad_device_inputs_reported_not_faulted():
                    wg["req_id"], 0, 0, ws=ws)
     assert b.device_status(ws, reset=True) == 1
     assert b.device_status(ws) == 0
+
+
+def test_out_of_range_confidences_reported_not_faulted():
+    """The scheduler's chains are sorted because c <= 1; a confidence outside [0,1] (or
+    NaN) is reported and clamped, and the verify lengths stay valid."""
+    b = _b()
+    R, gamma = 16, 5
+    conf = torch.rand((R, gamma), device="cuda", dtype=torch.float32)
+    conf[3, 1] = 1.5
+    conf[7, 0] = float("nan")
+    conf[9, 4] = -0.25
+    sps = torch.from_numpy(1000.0 / (1.0 + np.arange(R * (gamma + 1) + 1) / 64.0)).cuda()
+    ws = b.workspace(b.schedule_workspace_size(R, gamma), conf.device)
+    for mode in (0, 1, 2):
+        out = b.schedule(conf, sps, mode, conf if mode == 2 else None, 0, ws=ws)
+        torch.cuda.synchronize()
+        assert b.device_status(ws, reset=True) == 1, mode
+        ell = out["ell"].cpu().numpy()
+        assert ((ell >= 0) & (ell <= gamma)).all()
+        assert int(out["B"].item()) == R + int(ell.sum())
+
+
+@pytest.mark.parametrize("R,gamma", [(1, 8), (3, 64), (5, 3), (100, 7), (513, 15), (700, 11), (8192, 1)])
+def test_schedule_ragged_shapes_match_oracle(R, gamma):
+    """Request counts that are not powers of two (partial merge lists), the largest
+    gamma, and the largest candidate set; confidences with exact ties (1.0 and repeated
+    values) so that the depth/request tie-break decides part of the order."""
+    b = _b()
+    rng = np.random.default_rng(R * 131 + gamma)
+    conf = rng.choice(np.array([1.0, 0.999, 0.9, 0.5], np.float32), size=(R, gamma)).astype(np.float32)
+    mix = rng.uniform(0.05, 1.0, (R, gamma)).astype(np.float32)
+    conf = np.where(rng.uniform(size=(R, gamma)) < 0.5, conf, mix).astype(np.float32)
+    hist = rng.uniform(0.0, 1.0, (R, gamma)).astype(np.float32)
+    B = np.arange(R * (gamma + 1) + 1, dtype=np.float64)
+    tally = Tally()
+    for sps in (1000.0 / (1.0 + B / 64.0), np.where(B <= 2 * R, 1000.0, 1000.0 * 2 * R / np.maximum(B, 1.0))):
+        sps = np.ascontiguousarray(sps)
+        for mode in (wl.EARLY_STOP, wl.FULL_SEARCH, wl.CAPACITY_K):
+            ref = oracle.schedule(conf, sps, mode, hist if mode == wl.CAPACITY_K else None)
+            g = b.schedule(torch.from_numpy(conf).cuda(), torch.from_numpy(sps).cuda(), mode,
+                           torch.from_numpy(hist).cuda() if mode == wl.CAPACITY_K else None)
+            torch.cuda.synchronize()
+            g = _np(g)
+            compare_schedule(dict(ell=g["ell"], B=g["B"][0], tau=g["tau"][0]), ref, tally)
+    tally.check_rate()
