@@ -56,7 +56,8 @@ DraftLayout draft_layout(int R, int gamma, int V, int rank, int dtype_w) {
 }
 
 struct VerifyLayout {
-  size_t counters, row_req, row_t, row_base, row_part, lse_t, jstar, res_list, W1g, res_part, res_part2, total;
+  size_t counters, row_req, row_t, row_base, row_order, row_part, lse_t, jstar, res_list, W1g, res_part, res_part2,
+      total;
   int nchunk, npart;
 };
 
@@ -75,6 +76,8 @@ VerifyLayout verify_layout(int R, int gamma, int V, int rank, int dtype_w) {
   off += align256(4 * rows);
   L.row_base = off;
   off += align256(4 * (size_t)R);
+  L.row_order = off;
+  off += align256(4 * rows);
   L.row_part = off;
   off += align256(32 * rows * L.nchunk);
   L.lse_t = off;
@@ -353,6 +356,8 @@ dspark_status dspark_verify(int R, int gamma, int V, int rank, int dtype_t, int 
   a.row_req = reinterpret_cast<int*>(ws + L.row_req);
   a.row_t = reinterpret_cast<int*>(ws + L.row_t);
   a.row_base = reinterpret_cast<int*>(ws + L.row_base);
+  a.row_order = reinterpret_cast<int*>(ws + L.row_order);
+  a.work_next = counters + 2;
   a.row_part = reinterpret_cast<dspark::Partial*>(ws + L.row_part);
   a.nchunk = L.nchunk;
   a.chunk = kVerifyChunk;

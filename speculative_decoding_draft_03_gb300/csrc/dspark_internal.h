@@ -66,6 +66,8 @@ struct VerifyArgs {
   int* row_req;       // [R*(gamma+1)] request of compact row
   int* row_t;         // [R*(gamma+1)] target row index (0-based) of compact row
   int* row_base;      // [R] first compact row of request r
+  int* row_order;     // [R*(gamma+1)] processing order: the R bonus rows, then the others
+  int* work_next;     // [1] next (row, chunk) item of verify_rows (a work queue)
   Partial* row_part;  // [R*(gamma+1), nchunk]
   int nchunk;         // vocabulary chunks per row
   int chunk;          // ids per chunk

@@ -11,8 +11,9 @@
 //   verify_plan      ell -> compact list of the target rows that must be read:
 //                    rows 0..ell_r of request r (sum_r (ell_r + 1) rows)
 //   verify_rows      streams those rows once, coalesced and vectorised: per
-//                    (row, vocabulary chunk) the online (max, sum exp) of t/T and, on
-//                    row ell_r, the bonus Gumbel-max draw
+//                    (row, vocabulary chunk) item, taken from a work queue that holds
+//                    the bonus rows first, the (max, sum exp) of t/T and, on row ell_r,
+//                    the bonus Gumbel-max draw
 //   verify_accept    per request: row log-normalisers, the acceptance scan, the
 //                    bonus token, and the residual position j* when a draft is rejected
 //   residual_step    per rejected request: recompute the draft logits of position j*
@@ -74,11 +75,18 @@ __global__ void __launch_bounds__(kPlanThreads) verify_plan_kernel(VerifyArgs a)
       a.row_req[base + t] = r;
       a.row_t[base + t] = t;
     }
+    // processing order: the bonus row (t = ell, which also draws a Gumbel race) of every
+    // request first, so that the heavier items start early; then rows 0..ell-1
+    a.row_order[r] = base + n - 1;
+    for (int t = 0; t + 1 < n; ++t) a.row_order[a.R + (base - r) + t] = base + t;
     a.jstar[r] = 0;
     base += n;
   }
   if (threadIdx.x == blockDim.x - 1) *a.n_rows = base;
-  if (threadIdx.x == 0) *a.n_res = 0;
+  if (threadIdx.x == 0) {
+    *a.n_res = 0;
+    *a.work_next = 0;
+  }
 }
 
 // Per (row, chunk): (max, sum exp) of t/T and, on the bonus row, the Gumbel-max record
@@ -112,22 +120,43 @@ __device__ __forceinline__ int block_min(int v, int* sm) {
   return r;
 }
 
+// Order-preserving int code of a float key (max over codes = max over keys).
+__device__ __forceinline__ int key_code(float f) {
+  const int i = __float_as_int(f);
+  return i >= 0 ? i : i ^ 0x7FFFFFFF;
+}
+
+// Work items are (row position, chunk) pairs taken from a queue in row_order: every
+// request's bonus row first.  Per item the CTA needs:
+//  - the chunk maximum M (block max; every thread then sums exp(z - M) against the same
+//    M, so the partial sums add without rescaling);
+//  - on a bonus row, the Gumbel-max record: the lowest-id maximum is keyed exactly,
+//    L = M + g, and every other id needs only the log-free test 1-u >= exp(z - L)
+//    (computed branch-free for a batch of ids); the few survivors evaluate their keys.
 template <int DT>
-__global__ void __launch_bounds__(kRowThreads, 4) verify_rows_kernel(VerifyArgs a) {
+__global__ void __launch_bounds__(kRowThreads, 3) verify_rows_kernel(VerifyArgs a) {
   griddep_allow_next();
   griddep_wait();
   constexpr int EPV = DT == DSPARK_F32 ? 4 : 8;  // ids per 16-byte vector
   constexpr int NV = kRowPer / EPV;              // vectors per thread per item
-  __shared__ float sm_f[kRowThreads / 32];
-  __shared__ int sm_i[kRowThreads / 32];
-  __shared__ Partial red[kRowThreads / 32];
+  constexpr int kWarps = kRowThreads / 32;
+  __shared__ float sm_f[kWarps];
+  __shared__ int sm_i[kWarps];
+  __shared__ int sm_key[kWarps], sm_idx[kWarps];
+  __shared__ float sm_z[kWarps];
+  __shared__ int item_s;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int n_items = (*a.n_rows) * a.nchunk;
   const bool vec_ok = (a.V % EPV) == 0 && (reinterpret_cast<uintptr_t>(a.target) & 15u) == 0;
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const int row = item / a.nchunk, c = item % a.nchunk;
+  for (;;) {
+    if (threadIdx.x == 0) item_s = atomicAdd(a.work_next, 1);
+    __syncthreads();
+    const int item = item_s;
+    if (item >= n_items) break;
+    const int pos = item / a.nchunk, c = item % a.nchunk;
+    const int row = a.row_order[pos];
     const int r = a.row_req[row], t = a.row_t[row];
-    const bool bonus = (t == clamp_ell(a, r));
+    const bool bonus = pos < a.R;  // the first R positions hold the rows t = ell_r
     const size_t rbase = ((size_t)r * (a.gamma + 1) + t) * a.V;
     const int v0 = c * a.chunk, v1 = min(v0 + a.chunk, a.V);
     // thread's ids: vector i covers v0 + (threadIdx.x + i*kRowThreads)*EPV + [0, EPV)
@@ -164,11 +193,11 @@ __global__ void __launch_bounds__(kRowThreads, 4) verify_rows_kernel(VerifyArgs 
       m = fmaxf(m, z[k]);
     }
     const float M = block_max(m, sm_f);
-    Stats st = stats_empty();
-    st.m = M;
-    st.s = 0.f;
+    float ssum = 0.f;
 #pragma unroll
-    for (int k = 0; k < kRowPer; ++k) st.s += __expf(z[k] - M);
+    for (int k = 0; k < kRowPer; ++k) ssum += __expf(z[k] - M);
+    float bkey = -INFINITY, bz = 0.f;
+    int bidx = -1;
     if (bonus) {
       int mi = INT_MAX;
 #pragma unroll
@@ -188,40 +217,92 @@ __global__ void __launch_bounds__(kRowThreads, 4) verify_rows_kernel(VerifyArgs 
       const Philox4 wb = prow.block((uint32_t)mi >> 2);
       const uint32_t wm = (mi & 3) == 0 ? wb.x : ((mi & 3) == 1 ? wb.y : ((mi & 3) == 2 ? wb.z : wb.w));
       const float L = M + gumbel_from_bits(wm);
-      st.key = L;
-      st.idx = mi;
-      st.zsel = M;
+      bkey = L;
+      bidx = mi;
+      bz = M;
+      // two batches of 16 ids: the words and the survivor mask without branches, then
+      // the (rare) survivors.  Ids past the row end have z = -inf and never survive.
+      constexpr int kHalf = kRowPer / 2;
+      constexpr int VH = NV / 2;
 #pragma unroll
-      for (int i = 0; i < NV; ++i) {
-        const int vb = v0 + (threadIdx.x + i * kRowThreads) * EPV;
+      for (int h = 0; h < 2; ++h) {
+        uint32_t wd[kHalf];
 #pragma unroll
-        for (int q = 0; q < EPV / 4; ++q) {
-          const int vq = vb + 4 * q;
-          if (vq >= v1) continue;
-          const Philox4 bits = prow.block((uint32_t)vq >> 2);
-          const uint32_t wd[4] = {bits.x, bits.y, bits.z, bits.w};
+        for (int i = 0; i < VH; ++i) {
+          const int vb = v0 + (threadIdx.x + (h * VH + i) * kRowThreads) * EPV;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float zz = z[i * EPV + 4 * q + e];
-            if (gumbel_cannot_win(wd[e], __expf(zz - L) * kRejectSlack)) continue;
-            const int id = vq + e;
-            const float key = zz + gumbel_from_bits(wd[e]);
-            if (key > st.key || (key == st.key && id < st.idx)) {
-              st.key = key;
-              st.idx = id;
-              st.zsel = zz;
+          for (int q = 0; q < EPV / 4; ++q) {
+            const Philox4 bits = prow.block((uint32_t)(vb + 4 * q) >> 2);
+            wd[i * EPV + 4 * q + 0] = bits.x;
+            wd[i * EPV + 4 * q + 1] = bits.y;
+            wd[i * EPV + 4 * q + 2] = bits.z;
+            wd[i * EPV + 4 * q + 3] = bits.w;
+          }
+        }
+        uint32_t cand = 0;
+#pragma unroll
+        for (int k = 0; k < kHalf; ++k) {
+          const bool may = !gumbel_cannot_win(wd[k], __expf(z[h * kHalf + k] - L) * kRejectSlack);
+          cand |= (uint32_t)may << k;
+        }
+        if (cand != 0) {
+#pragma unroll
+          for (int k = 0; k < kHalf; ++k) {
+            if (!((cand >> k) & 1u)) continue;
+            const int id = v0 + (threadIdx.x + (h * VH + k / EPV) * kRowThreads) * EPV + (k % EPV);
+            const float zz = z[h * kHalf + k];
+            const float key = zz + gumbel_from_bits(wd[k]);
+            if (key > bkey || (key == bkey && id < bidx)) {
+              bkey = key;
+              bidx = id;
+              bz = zz;
             }
           }
         }
       }
     }
-    Stats w = warp_reduce_stats(st);
-    if (lane == 0) red[warp] = to_partial(w);
+    // sum of exp(z - M) (one common M: no rescaling) and, on a bonus row, the best
+    // (key, lowest id) record: warp reductions, then the warps in a fixed order
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
+    if (lane == 0) sm_f[warp] = ssum;
+    if (bonus) {
+      const int code = key_code(bkey);
+      const int wmax = __reduce_max_sync(0xffffffffu, code);
+      const int widx = __reduce_min_sync(0xffffffffu, code == wmax ? bidx : INT_MAX);
+      const int src = __ffs(__ballot_sync(0xffffffffu, code == wmax && bidx == widx)) - 1;
+      const float wz = __shfl_sync(0xffffffffu, bz, src);
+      if (lane == 0) {
+        sm_key[warp] = wmax;
+        sm_idx[warp] = widx;
+        sm_z[warp] = wz;
+      }
+    }
     __syncthreads();
-    if (warp == 0) {
-      Stats b = (lane < kRowThreads / 32) ? from_partial(red[lane]) : stats_empty();
-      b = warp_reduce_stats(b);
-      if (lane == 0) a.row_part[(size_t)row * a.nchunk + c] = to_partial(b);
+    if (threadIdx.x == 0) {
+      Partial out;
+      out.m = M;
+      out.s = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) out.s += sm_f[w];
+      out.key = -INFINITY;
+      out.zsel = 0.f;
+      out.idx = -1;
+      out.pad0 = out.pad1 = out.pad2 = 0;
+      if (bonus) {
+        int bc = sm_key[0], bi = sm_idx[0];
+        float bzz = sm_z[0];
+        for (int w = 1; w < kWarps; ++w)
+          if (sm_key[w] > bc || (sm_key[w] == bc && sm_idx[w] < bi)) {
+            bc = sm_key[w];
+            bi = sm_idx[w];
+            bzz = sm_z[w];
+          }
+        out.key = __int_as_float(bc >= 0 ? bc : bc ^ 0x7FFFFFFF);
+        out.idx = bi;
+        out.zsel = bzz;
+      }
+      a.row_part[(size_t)row * a.nchunk + c] = out;
     }
     __syncthreads();
   }
@@ -492,7 +573,7 @@ cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s) {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int max_items = a.R * (a.gamma + 1) * a.nchunk;
-  const int grid = min(max_items, sms * 4);
+  const int grid = min(max_items, sms * 3);  // work queue: CTAs take items until none is left
   if (a.chunk != kRowThreads * kRowPer) return cudaErrorInvalidValue;
   e = a.dtype_t == DSPARK_F32 ? launch_pdl(verify_rows_kernel<DSPARK_F32>, dim3(grid), dim3(kRowThreads), 0, s, a)
                               : launch_pdl(verify_rows_kernel<DSPARK_BF16>, dim3(grid), dim3(kRowThreads), 0, s, a);
