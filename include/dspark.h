@@ -205,6 +205,31 @@ DSPARK_API dspark_status dspark_verify(
     void* workspace, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------------
+ * Stage 3 on a flattened target batch (numb3r33 blog "Variable-length verification
+ * without wasting kernels": the verified rows of all requests are packed back to back
+ * and metadata, not padding, keeps each request's rows apart).
+ *
+ * Same computation, results and limits as dspark_verify; only the target layout differs:
+ *   target             [n_target_rows, V] logits; request r's verify rows t = 0..ell[r]
+ *                      (row t scores draft t+1; row ell[r] gives the bonus token) are
+ *                      rows target_row_offset[r] + t.  Rows may be in any order and
+ *                      unused rows may exist; sum_r (ell[r] + 1) rows are read.
+ *   n_target_rows      number of rows of `target` (>= 1).
+ *   target_row_offset  [R] int32 device array, the first row of each request.
+ * The workspace is the one dspark_verify_workspace_size() sizes.  A row index outside
+ * [0, n_target_rows) is reported through the workspace status word (DSPARK_INVALID_ARG)
+ * and row 0 is read instead.
+ * ---------------------------------------------------------------------------------- */
+DSPARK_API dspark_status dspark_verify_ragged(
+    int R, int gamma, int V, int rank, int dtype_t, int dtype_u, int dtype_w,
+    const void* target, int n_target_rows, const int32_t* target_row_offset,
+    const void* U, const void* W1, const void* W2,
+    const int32_t* x0, const int32_t* x, const float* logq, const float* lse_q,
+    const int32_t* ell, float temperature, const int64_t* req_id, uint64_t seed, uint64_t round,
+    int32_t* n_acc_out, int32_t* tokens_out, int32_t* n_out,
+    void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------
  * Stage 3 for callers that cannot allocate device memory.  (The paper has no
  * counterpart: this is a deployment convenience of this library.)
  *

@@ -45,6 +45,9 @@ def _load_library():
     lib.dspark_verify.argtypes = ([i32] * 7 + [P] * 4 + [P] * 5 + [f32, P, u64, u64] + [P] * 3 + [P, sz, P])
     lib.dspark_set_profile_events.argtypes = [P, i32]
     lib.dspark_set_profile_events.restype = None
+    lib.dspark_verify_ragged.argtypes = ([i32] * 7 + [P, i32, P] + [P] * 3 + [P] * 5 + [f32, P, u64, u64] + [P] * 3
+                                         + [P, sz, P])
+    lib.dspark_verify_ragged.restype = i32
     lib.dspark_verify_static.argtypes = ([i32] * 7 + [P] * 4 + [P] * 5 + [f32, P, u64, u64] + [P] * 3 + [P])
     lib.dspark_verify_static.restype = i32
     for fn in ("dspark_markov_draft", "dspark_schedule", "dspark_verify", "dspark_workspace_status"):
@@ -188,6 +191,38 @@ def verify(target, U, W1, W2, x0, x, logq, lse_q, ell, temperature, req_id, seed
                            float(temperature), _p(req_id), int(seed), int(rnd), _p(out["n_acc"]),
                            _p(out["tokens"]), _p(out["n_out"]), _p(ws), ws.numel(), _stream(stream))
     _check(st, "dspark_verify")
+    return out
+
+
+def verify_ragged(target_rows, row_offset, U, W1, W2, x0, x, logq, lse_q, ell, temperature, req_id, seed, rnd,
+                  out=None, ws=None, stream=None):
+    """Stage 3 on a flattened target (dspark_verify_ragged): target_rows [n_rows, V],
+    request r's verify rows at row_offset[r] + t.  Returns dict n_acc, tokens, n_out."""
+    n_rows, V = target_rows.shape
+    R, gamma = x.shape
+    rank = W1.shape[1]
+    dev = target_rows.device
+    for t, n in ((target_rows, "target_rows"), (U, "U"), (W1, "W1"), (W2, "W2")):
+        _cuda(t, n)
+    _cuda(row_offset, "row_offset", torch.int32)
+    _cuda(x0, "x0", torch.int32)
+    _cuda(x, "x", torch.int32)
+    _cuda(logq, "logq", torch.float32)
+    _cuda(lse_q, "lse_q", torch.float32)
+    _cuda(ell, "ell", torch.int32)
+    _cuda(req_id, "req_id", torch.int64)
+    if out is None:
+        out = dict(n_acc=torch.empty(R, dtype=torch.int32, device=dev),
+                   tokens=torch.empty((R, gamma + 1), dtype=torch.int32, device=dev),
+                   n_out=torch.empty(R, dtype=torch.int32, device=dev))
+    if ws is None:
+        ws = workspace(verify_workspace_size(R, gamma, V, rank, W1.dtype), dev)
+    st = lib.dspark_verify_ragged(R, gamma, V, rank, _dt(target_rows, "target_rows"), _dt(U, "U"), _dt(W1, "W1"),
+                                  _p(target_rows), int(n_rows), _p(row_offset), _p(U), _p(W1), _p(W2), _p(x0),
+                                  _p(x), _p(logq), _p(lse_q), _p(ell), float(temperature), _p(req_id), int(seed),
+                                  int(rnd), _p(out["n_acc"]), _p(out["tokens"]), _p(out["n_out"]), _p(ws),
+                                  ws.numel(), _stream(stream))
+    _check(st, "dspark_verify_ragged")
     return out
 
 

@@ -257,6 +257,8 @@ struct TcParams {
   DeviceStatus* status;
   // residual mode
   const void* target;
+  const int32_t* t_off;  // flattened target rows (nullptr: padded [R, gamma+1, V])
+  int n_trows;
   int dtype_t;
   const int* jstar;     // [R] rejected position (0 = none)
   const float* lse_q;   // [R, gamma]
@@ -494,7 +496,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const PhiloxRow prow = philox_row(rng_row(p.seed, valid ? __ldg(p.req_id + r) : 0, p.round,
                                               MODE == kModeDraft ? kStreamDraft : kStreamCorrect, (uint32_t)pos));
     const size_t urow = ((size_t)(valid ? r : 0) * p.gamma + (valid ? pos - 1 : 0)) * (size_t)p.V;
-    const size_t trow = ((size_t)(valid ? r : 0) * (p.gamma + 1) + (valid ? pos - 1 : 0)) * (size_t)p.V;
+    const size_t trow =
+        (valid ? target_row_index(p.t_off, p.n_trows, p.gamma, r, pos - 1, p.status) : 0) * (size_t)p.V;
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
 
     // Residual mode: U of the next tile is loaded into registers while the current one is
@@ -893,6 +896,8 @@ cudaError_t launch_residual_tc(const VerifyArgs& a, cudaStream_t s) {
   p.partials = a.res_part;
   p.partials2 = a.res_part2;
   p.target = a.target;
+  p.t_off = a.t_off;
+  p.n_trows = a.n_trows;
   p.dtype_t = a.dtype_t;
   p.jstar = a.jstar;
   p.lse_q = a.lse_q;

@@ -304,12 +304,14 @@ size_t dspark_verify_workspace_size(int R, int gamma, int V, int rank, int dtype
   return verify_layout(R, gamma, V, rank, dtype_w).total;
 }
 
-dspark_status dspark_verify(int R, int gamma, int V, int rank, int dtype_t, int dtype_u, int dtype_w,
-                            const void* target, const void* U, const void* W1, const void* W2, const int32_t* x0,
-                            const int32_t* x, const float* logq, const float* lse_q, const int32_t* ell,
-                            float temperature, const int64_t* req_id, uint64_t seed, uint64_t round,
-                            int32_t* n_acc_out, int32_t* tokens_out, int32_t* n_out, void* workspace,
-                            size_t ws_bytes, void* stream) {
+// dspark_verify and dspark_verify_ragged: t_off == nullptr selects the padded target.
+static dspark_status verify_impl(int R, int gamma, int V, int rank, int dtype_t, int dtype_u, int dtype_w,
+                                 const void* target, const int32_t* t_off, int n_trows, const void* U,
+                                 const void* W1, const void* W2, const int32_t* x0, const int32_t* x,
+                                 const float* logq, const float* lse_q, const int32_t* ell, float temperature,
+                                 const int64_t* req_id, uint64_t seed, uint64_t round, int32_t* n_acc_out,
+                                 int32_t* tokens_out, int32_t* n_out, void* workspace, size_t ws_bytes,
+                                 void* stream) {
   if (R < 1 || gamma < 1 || V < 1 || rank < 1)
     return fail(DSPARK_INVALID_ARG, "sizes must be positive (R=%d gamma=%d V=%d rank=%d)", R, gamma, V, rank);
   if (gamma > kMaxGamma) return fail(DSPARK_UNSUPPORTED_SHAPE, "gamma=%d exceeds %d", gamma, kMaxGamma);
@@ -345,6 +347,7 @@ dspark_status dspark_verify(int R, int gamma, int V, int rank, int dtype_t, int 
   a.R = R; a.gamma = gamma; a.V = V; a.rank = rank;
   a.dtype_t = dtype_t; a.dtype_u = dtype_u; a.dtype_w = dtype_w;
   a.target = target; a.U = U; a.W1 = W1; a.W2 = W2;
+  a.t_off = t_off; a.n_trows = n_trows;
   a.x0 = x0; a.x = x; a.logq = logq; a.lse_q = lse_q; a.ell = ell;
   a.inv_temp = 1.0f / temperature;
   a.req_id = req_id; a.seed = seed; a.round = round;
@@ -371,6 +374,31 @@ dspark_status dspark_verify(int R, int gamma, int V, int rank, int dtype_t, int 
   cudaError_t e = dspark::launch_verify(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "verify");
   return DSPARK_OK;
+}
+
+dspark_status dspark_verify(int R, int gamma, int V, int rank, int dtype_t, int dtype_u, int dtype_w,
+                            const void* target, const void* U, const void* W1, const void* W2, const int32_t* x0,
+                            const int32_t* x, const float* logq, const float* lse_q, const int32_t* ell,
+                            float temperature, const int64_t* req_id, uint64_t seed, uint64_t round,
+                            int32_t* n_acc_out, int32_t* tokens_out, int32_t* n_out, void* workspace,
+                            size_t ws_bytes, void* stream) {
+  return verify_impl(R, gamma, V, rank, dtype_t, dtype_u, dtype_w, target, nullptr, 0, U, W1, W2, x0, x, logq,
+                     lse_q, ell, temperature, req_id, seed, round, n_acc_out, tokens_out, n_out, workspace, ws_bytes,
+                     stream);
+}
+
+dspark_status dspark_verify_ragged(int R, int gamma, int V, int rank, int dtype_t, int dtype_u, int dtype_w,
+                                   const void* target, int n_target_rows, const int32_t* target_row_offset,
+                                   const void* U, const void* W1, const void* W2, const int32_t* x0,
+                                   const int32_t* x, const float* logq, const float* lse_q, const int32_t* ell,
+                                   float temperature, const int64_t* req_id, uint64_t seed, uint64_t round,
+                                   int32_t* n_acc_out, int32_t* tokens_out, int32_t* n_out, void* workspace,
+                                   size_t ws_bytes, void* stream) {
+  if (n_target_rows < 1) return fail(DSPARK_INVALID_ARG, "n_target_rows must be positive (%d)", n_target_rows);
+  CHECK_PTR(target_row_offset);
+  return verify_impl(R, gamma, V, rank, dtype_t, dtype_u, dtype_w, target, target_row_offset, n_target_rows, U, W1,
+                     W2, x0, x, logq, lse_q, ell, temperature, req_id, seed, round, n_acc_out, tokens_out, n_out,
+                     workspace, ws_bytes, stream);
 }
 
 }  // extern "C"

@@ -296,6 +296,21 @@ __device__ __forceinline__ int checked_token(int x, int V, DeviceStatus* st, int
 
 __device__ __forceinline__ float sigmoidf_dev(float x) { return 1.0f / (1.0f + __expf(-x)); }
 
+// Row of the target logits holding request r's verify row t: the padded layout
+// [R, gamma+1, V] (t_off == nullptr), or the flattened layout with request r's rows at
+// t_off[r], t_off[r]+1, ... of n_trows rows.  An offset outside the array is reported
+// and row 0 is used instead (every access stays in bounds).
+__device__ __forceinline__ size_t target_row_index(const int32_t* t_off, int n_trows, int gamma, int r, int t,
+                                                   DeviceStatus* st) {
+  if (t_off == nullptr) return (size_t)r * (gamma + 1) + t;
+  const long long row = (long long)__ldg(t_off + r) + t;
+  if (row < 0 || row >= n_trows) {
+    report_bad_input(st, 14);
+    return 0;
+  }
+  return (size_t)row;
+}
+
 // Programmatic dependent launch: every kernel of the round is launched so that it may
 // start while its predecessor drains.  griddep_wait() returns once the preceding grid
 // has completed and its memory is visible; a kernel calls it before touching anything

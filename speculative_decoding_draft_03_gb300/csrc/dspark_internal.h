@@ -46,6 +46,8 @@ struct VerifyArgs {
   int R, gamma, V, rank;
   int dtype_t, dtype_u, dtype_w;
   const void* target;
+  const int32_t* t_off;  // flattened target layout: request r's first row (nullptr: padded)
+  int n_trows;           // rows of the flattened target
   const void* U;
   const void* W1;
   const void* W2;

@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(kRowThreads, 3) verify_rows_kernel(VerifyArgs 
     const int row = a.row_order[pos];
     const int r = a.row_req[row], t = a.row_t[row];
     const bool bonus = pos < a.R;  // the first R positions hold the rows t = ell_r
-    const size_t rbase = ((size_t)r * (a.gamma + 1) + t) * a.V;
+    const size_t rbase = target_row_index(a.t_off, a.n_trows, a.gamma, r, t, a.status) * a.V;
     const int v0 = c * a.chunk, v1 = min(v0 + a.chunk, a.V);
     // thread's ids: vector i covers v0 + (threadIdx.x + i*kRowThreads)*EPV + [0, EPV)
     float z[kRowPer];
@@ -366,7 +366,9 @@ __global__ void verify_accept_kernel(VerifyArgs a) {
     bool reject = false;
     if (j < ell) {
       const int xj = checked_token(__ldg(a.x + (size_t)r * a.gamma + j), a.V, a.status, 11);
-      const float tx = load_elem(a.target, a.dtype_t, ((size_t)r * (a.gamma + 1) + j) * a.V + xj) * a.inv_temp;
+      const float tx =
+          load_elem(a.target, a.dtype_t, target_row_index(a.t_off, a.n_trows, a.gamma, r, j, a.status) * a.V + xj) *
+          a.inv_temp;
       const double lp = (double)tx - (double)lse_own[s];
       const double ratio = exp(lp - (double)__ldg(a.logq + (size_t)r * a.gamma + j));
       RngRow rr = acc_rng;
@@ -502,7 +504,7 @@ __global__ void __launch_bounds__(kSimtThreads) residual_step_simt_kernel(Verify
       const Philox4 bits = rng_chunk(rng[rr], (uint32_t)g);
       const uint32_t wd[4] = {bits.x, bits.y, bits.z, bits.w};
       const size_t urow = ((size_t)r * a.gamma + (js[rr] - 1)) * a.V;
-      const size_t trow = ((size_t)r * (a.gamma + 1) + (js[rr] - 1)) * a.V;
+      const size_t trow = target_row_index(a.t_off, a.n_trows, a.gamma, r, js[rr] - 1, a.status) * a.V;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int v = 4 * g + e;

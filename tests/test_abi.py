@@ -123,3 +123,27 @@ def test_workspace_sizes_grow_with_shape(b):
     assert 256 < s1 < s2
     assert b.verify_workspace_size(4, 4, 1024, 32, torch.float32) > 256
     assert b.schedule_workspace_size(512, 15) >= 256
+
+
+def test_verify_ragged_validation(b):
+    P = _fake(18)
+    L = b.lib.dspark_verify_ragged
+
+    def call(**kw):
+        a = dict(R=4, g=4, V=1024, rank=32, nrows=10, ws=1 << 30)
+        a.update(kw)
+        p = list(P)
+        for k in kw.get("null", []):
+            p[k] = None
+        for k in kw.get("misalign", []):
+            p[k] = ctypes.c_void_p(p[k].value + 4)
+        return L(a["R"], a["g"], a["V"], a["rank"], 0, 0, 0, p[0], a["nrows"], p[1], p[2], p[3], p[4], p[5], p[6],
+                 p[7], p[8], p[9], 1.0, p[10], 0, 0, p[11], p[12], p[13], p[14], a["ws"], None)
+
+    assert call(nrows=0) == 1
+    assert call(null=[1]) == 1  # row offsets
+    assert "target_row_offset" in b.lib.dspark_last_error_message().decode()
+    assert call(null=[0]) == 1
+    assert call(misalign=[0]) == 1
+    assert call(R=0) == 1
+    assert call(ws=100) == 3
