@@ -66,6 +66,8 @@ def _load():
             lib.orc_schedule_path.argtypes = [i32, i32, P, P, P, P, P, P]
             lib.orc_schedule_many.argtypes = [i32, i32, i32, P, P, i32, i32, P, i32, P]
             lib.orc_schedule_many.restype = ctypes.c_int
+            lib.orc_schedule_threshold.argtypes = [i32, i32, P, f64, P, P, P]
+            lib.orc_schedule_threshold.restype = ctypes.c_int
             lib.orc_verify.argtypes = ([i32] * 7 + [P] * 4 + [P, P, P, P, P, f64, P, u64, u64]
                                        + [P] * 3 + [P] * 4 + [i32])
             lib.orc_max_threads.restype = i32
@@ -192,6 +194,22 @@ def schedule(conf, sps, mode, conf_hist=None, fixed_len=0):
     if rc != 0:
         raise ValueError("oracle schedule rejected its arguments")
     return dict(ell=ell, B=int(B[0]), tau=float(tau[0]), gap=float(diag[0]), tie=float(diag[1]))
+
+
+def schedule_threshold(conf, threshold):
+    """Verify lengths from a fixed confidence cutoff: each request keeps its leading drafts
+    with c >= threshold (vllmbangkok "Verify smarter, not longer").  Returns ell, B, tau."""
+    lib = _load()
+    conf = _c(conf, np.float32)
+    R, gamma = conf.shape
+    ell = np.zeros(R, np.int32)
+    B = np.zeros(1, np.int32)
+    tau = np.zeros(1)
+    rc = lib.orc_schedule_threshold(R, gamma, _ptr(conf), ctypes.c_double(float(threshold)), _ptr(ell), _ptr(B),
+                                    _ptr(tau))
+    if rc != 0:
+        raise ValueError("oracle schedule_threshold rejected its arguments")
+    return dict(ell=ell, B=int(B[0]), tau=float(tau[0]))
 
 
 def schedule_many(conf, sps, mode, conf_hist=None, fixed_len=0):

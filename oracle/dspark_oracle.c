@@ -502,6 +502,33 @@ int orc_verify(int R, int gamma, int V, int rank, int dtype_t, int dtype_u, int 
 
 /* Many independent scheduler problems of the same shape, one after another (used by
  * the law tests, which run 10^6 small batches). */
+/* Fixed confidence cutoff ([VLLM] "Verify smarter, not longer: the role of confidence
+ * scheduling": draft tokens whose confidence is below a fixed cutoff are dropped before
+ * verification).  Verification needs a prefix, so request r keeps its leading tokens
+ * with c >= threshold: l_r = the first j with c_{r,j} < threshold, minus one (gamma if
+ * none).  B and tau as in every mode: B = R + sum l_r, tau = R + sum_r sum_{j<=l_r} a_{r,j}
+ * with a the left-to-right product of the confidences. */
+int orc_schedule_threshold(int R, int gamma, const float* conf, double threshold, int32_t* ell_out,
+                           int32_t* B_out, double* tau_out) {
+    if (R < 0 || gamma < 1) return 1;
+    double t = (double)R;
+    long long B = R;
+    for (int r = 0; r < R; ++r) {
+        double a = 1.0;
+        int l = 0;
+        while (l < gamma && (double)conf[(size_t)r * gamma + l] >= threshold) {
+            a = a * (double)conf[(size_t)r * gamma + l];
+            t += a;
+            ++l;
+        }
+        ell_out[r] = l;
+        B += l;
+    }
+    *B_out = (int32_t)B;
+    *tau_out = t;
+    return 0;
+}
+
 int orc_schedule_many(int nbatch, int R, int gamma, const float* conf, const double* sps,
                       int sps_len, int mode, const float* conf_hist, int fixed_len,
                       int32_t* ell_out) {

@@ -5,6 +5,7 @@ import json
 import os
 
 import numpy as np
+import pytest
 
 import oracle
 from tests.conftest import GOLDEN
@@ -189,3 +190,35 @@ def test_fixed_mode_and_zero_length():
         Le = min(L, 4)
         assert (s["ell"] == Le).all() and s["B"] == 3 * (1 + Le)
         assert abs(s["tau"] - 3 * (1 + sum(0.5 ** j for j in range(1, Le + 1)))) < 1e-12
+
+
+def test_threshold_mode_worked_example():
+    """Fixed confidence cutoff (vllmbangkok "Verify smarter, not longer"): each request keeps
+    its leading drafts with c >= threshold; a token at exactly the cutoff is kept."""
+    conf = np.array([[0.9, 0.8, 0.3],
+                     [0.2, 0.95, 0.9],
+                     [1.0, 1.0, 1.0],
+                     [0.5, 0.5, 0.49]], np.float32)
+    out = oracle.schedule_threshold(conf, 0.5)
+    assert out["ell"].tolist() == [2, 0, 3, 2]
+    assert out["B"] == 4 + 7
+    a = lambda *c: np.cumprod(np.array(c, np.float64)).sum()
+    tau = 4 + a(np.float32(0.9), np.float32(0.8)) + a(1.0, 1.0, 1.0) + a(0.5, 0.5)
+    assert out["tau"] == pytest.approx(tau, rel=1e-15)
+    # cutoffs above 1 keep nothing, cutoffs at or below 0 keep everything
+    assert oracle.schedule_threshold(conf, 1.01)["ell"].tolist() == [0, 0, 0, 0]
+    assert oracle.schedule_threshold(conf, 0.0)["ell"].tolist() == [3, 3, 3, 3]
+
+
+def test_threshold_mode_is_prefix_closed_and_monotone():
+    rng = np.random.default_rng(11)
+    conf = rng.uniform(0, 1, (64, 9)).astype(np.float32)
+    prev = None
+    for th in (0.9, 0.7, 0.5, 0.3, 0.1):
+        ell = oracle.schedule_threshold(conf, th)["ell"]
+        for r in range(64):
+            assert (conf[r, :ell[r]] >= th).all()
+            assert ell[r] == 9 or conf[r, ell[r]] < th
+        if prev is not None:
+            assert (ell >= prev).all()  # lowering the cutoff never shortens a prefix
+        prev = ell
