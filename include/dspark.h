@@ -172,6 +172,21 @@ DSPARK_API dspark_status dspark_schedule(
     void* workspace, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------------
+ * Stage 2 with a fixed confidence cutoff (vllmbangkok "Verify smarter, not longer: the
+ * role of confidence scheduling": drafts whose confidence is below a fixed cutoff are not
+ * verified).  Verification needs a prefix, so request r keeps its leading drafts with
+ * c >= threshold:
+ *   ell[r] = max { j : c[r,i] >= threshold for every i <= j }   (0 if c[r,1] < threshold)
+ *   B      = R + sum_r ell[r];   tau = R + sum_r sum_{j <= ell[r]} prod_{i <= j} c[r,i]
+ * (products in binary64, left to right).  A NaN confidence ends the prefix.
+ * Arguments as dspark_schedule; threshold is a finite double; the workspace is the one
+ * dspark_schedule_workspace_size() sizes.  Limits: 1 <= R, 1 <= gamma <= 64.
+ * ---------------------------------------------------------------------------------- */
+DSPARK_API dspark_status dspark_schedule_threshold(int R, int gamma, const float* conf, double threshold,
+                                                   int32_t* ell_out, int32_t* B_out, double* tau_out,
+                                                   void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------
  * Stage 3: exact speculative-sampling verification.
  *
  * Defines (numb3r33 blog "One-token exactness", "Why only the longest accepted prefix

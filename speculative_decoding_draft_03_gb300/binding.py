@@ -40,6 +40,8 @@ def _load_library():
     lib.dspark_schedule_workspace_size.restype = sz
     lib.dspark_schedule_workspace_size.argtypes = [i32, i32]
     lib.dspark_schedule.argtypes = [i32, i32, P, P, i32, i32, P, i32, P, P, P, P, sz, P]
+    lib.dspark_schedule_threshold.argtypes = [i32, i32, P, ctypes.c_double, P, P, P, P, sz, P]
+    lib.dspark_schedule_threshold.restype = i32
     lib.dspark_verify_workspace_size.restype = sz
     lib.dspark_verify_workspace_size.argtypes = [i32] * 5
     lib.dspark_verify.argtypes = ([i32] * 7 + [P] * 4 + [P] * 5 + [f32, P, u64, u64] + [P] * 3 + [P, sz, P])
@@ -162,6 +164,24 @@ def schedule(conf, sps, mode, conf_hist=None, fixed_len=0, out=None, ws=None, st
                              _p(conf_hist), int(fixed_len), _p(out["ell"]), _p(out["B"]), _p(out["tau"]),
                              _p(ws), ws.numel(), _stream(stream))
     _check(st, "dspark_schedule")
+    return out
+
+
+def schedule_threshold(conf, threshold, out=None, ws=None, stream=None):
+    """Stage 2 with a fixed confidence cutoff (dspark_schedule_threshold).  Returns dict
+    ell [R] int32, B [1] int32, tau [1] float64."""
+    _cuda(conf, "conf", torch.float32)
+    R, gamma = conf.shape
+    dev = conf.device
+    if out is None:
+        out = dict(ell=torch.empty(R, dtype=torch.int32, device=dev),
+                   B=torch.empty(1, dtype=torch.int32, device=dev),
+                   tau=torch.empty(1, dtype=torch.float64, device=dev))
+    if ws is None:
+        ws = workspace(schedule_workspace_size(R, gamma), dev)
+    st = lib.dspark_schedule_threshold(R, gamma, _p(conf), float(threshold), _p(out["ell"]), _p(out["B"]),
+                                       _p(out["tau"]), _p(ws), ws.numel(), _stream(stream))
+    _check(st, "dspark_schedule_threshold")
     return out
 
 

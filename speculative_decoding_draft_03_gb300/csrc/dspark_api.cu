@@ -299,6 +299,28 @@ dspark_status dspark_schedule(int R, int gamma, const float* conf, const double*
   return DSPARK_OK;
 }
 
+dspark_status dspark_schedule_threshold(int R, int gamma, const float* conf, double threshold, int32_t* ell_out,
+                                        int32_t* B_out, double* tau_out, void* workspace, size_t ws_bytes,
+                                        void* stream) {
+  if (R < 1 || gamma < 1) return fail(DSPARK_INVALID_ARG, "sizes must be positive (R=%d gamma=%d)", R, gamma);
+  if (gamma > kMaxGamma) return fail(DSPARK_UNSUPPORTED_SHAPE, "gamma=%d exceeds %d", gamma, kMaxGamma);
+  if ((long long)R * gamma > (1ll << 24)) return fail(DSPARK_UNSUPPORTED_SHAPE, "R*gamma too large");
+  if (!isfinite(threshold)) return fail(DSPARK_INVALID_ARG, "threshold must be finite");
+  CHECK_PTR(conf);
+  CHECK_PTR(ell_out);
+  CHECK_PTR(B_out);
+  CHECK_PTR(tau_out);
+  CHECK_PTR(workspace);
+  if (!aligned256(workspace)) return fail(DSPARK_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (ws_bytes < dspark_schedule_workspace_size(R, gamma))
+    return fail(DSPARK_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes,
+                dspark_schedule_workspace_size(R, gamma));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = dspark::launch_schedule_threshold(R, gamma, conf, threshold, ell_out, B_out, tau_out, s);
+  if (e != cudaSuccess) return cuda_fail(e, "schedule_threshold");
+  return DSPARK_OK;
+}
+
 size_t dspark_verify_workspace_size(int R, int gamma, int V, int rank, int dtype_w) {
   if (R < 1 || gamma < 1 || V < 1 || rank < 1) return 0;
   return verify_layout(R, gamma, V, rank, dtype_w).total;

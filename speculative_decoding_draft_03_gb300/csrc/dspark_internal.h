@@ -118,6 +118,8 @@ cudaError_t launch_draft_step_simt(const DraftArgs& a, int k, cudaStream_t s);
 cudaError_t launch_draft_combine(const DraftArgs& a, int k, int npart, cudaStream_t s);
 cudaError_t launch_draft_step_tc(const DraftArgs& a, int k, cudaStream_t s);
 
+cudaError_t launch_schedule_threshold(int R, int gamma, const float* conf, double threshold, int32_t* ell_out,
+                                      int32_t* B_out, double* tau_out, cudaStream_t s);
 cudaError_t launch_schedule(int R, int gamma, const float* conf, const double* sps, int mode,
                             const float* conf_hist, int fixed_len, int32_t* ell_out, int32_t* B_out,
                             double* tau_out, DeviceStatus* status, cudaStream_t s);

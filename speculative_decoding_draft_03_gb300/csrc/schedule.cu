@@ -342,4 +342,62 @@ cudaError_t launch_schedule(int R, int gamma, const float* conf, const double* s
                     fixed_len, ell_out, B_out, tau_out, status);
 }
 
+// Fixed confidence cutoff (vllmbangkok "Verify smarter, not longer: the role of
+// confidence scheduling": drafts below a fixed confidence cutoff are not verified).
+// Verification needs a prefix, so request r keeps its leading drafts with c >= threshold.
+// B and tau as in the other modes; a is the same left-to-right binary64 product.
+__global__ void __launch_bounds__(kSchedThreads) schedule_threshold_kernel(int R, int gamma,
+                                                                           const float* __restrict__ conf,
+                                                                           double threshold,
+                                                                           int32_t* __restrict__ ell_out,
+                                                                           int32_t* __restrict__ B_out,
+                                                                           double* __restrict__ tau_out) {
+  griddep_allow_next();
+  griddep_wait();
+  __shared__ double red_t[kSchedThreads / 32];
+  __shared__ long long red_b[kSchedThreads / 32];
+  double part = 0.0;
+  long long bsum = 0;
+  for (int r = threadIdx.x; r < R; r += blockDim.x) {
+    double a = 1.0;
+    int l = 0;
+    while (l < gamma) {
+      const double c = (double)__ldg(conf + (size_t)r * gamma + l);
+      if (!(c >= threshold)) break;
+      a = __dmul_rn(a, c);
+      part += a;
+      ++l;
+    }
+    ell_out[r] = l;
+    bsum += l;
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    part += __shfl_xor_sync(0xffffffffu, part, o);
+    bsum += __shfl_xor_sync(0xffffffffu, bsum, o);
+  }
+  if (lane == 0) {
+    red_t[warp] = part;
+    red_b[warp] = bsum;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double t = (double)R;
+    long long b = R;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+      t += red_t[w];
+      b += red_b[w];
+    }
+    *B_out = (int32_t)b;
+    *tau_out = t;
+  }
+}
+
+cudaError_t launch_schedule_threshold(int R, int gamma, const float* conf, double threshold, int32_t* ell_out,
+                                      int32_t* B_out, double* tau_out, cudaStream_t s) {
+  return launch_pdl(schedule_threshold_kernel, dim3(1), dim3(kSchedThreads), 0, s, R, gamma, conf, threshold, ell_out,
+                    B_out, tau_out);
+}
+
 }  // namespace dspark

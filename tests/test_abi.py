@@ -147,3 +147,17 @@ def test_verify_ragged_validation(b):
     assert call(misalign=[0]) == 1
     assert call(R=0) == 1
     assert call(ws=100) == 3
+
+
+def test_schedule_threshold_validation(b):
+    P = _fake(5)
+    L = b.lib.dspark_schedule_threshold
+    call = lambda R=4, g=4, th=0.5, ws=1 << 20, null=(): L(R, g, *([None if k in null else P[k] for k in range(1)]),
+                                                           th, *([None if k in null else P[k] for k in range(1, 5)]),
+                                                           ws, None)
+    assert call(R=0) == 1
+    assert call(g=65) == 2
+    assert call(th=float("nan")) == 1
+    for k in range(5):
+        assert call(null=(k,)) == 1, k
+    assert call(ws=16) == 3

@@ -300,3 +300,21 @@ def test_schedule_ragged_shapes_match_oracle(R, gamma):
             g = _np(g)
             compare_schedule(dict(ell=g["ell"], B=g["B"][0], tau=g["tau"][0]), ref, tally)
     tally.check_rate()
+
+
+@pytest.mark.parametrize("R,gamma", [(1, 1), (4, 4), (32, 7), (513, 15), (8192, 1)])
+def test_schedule_threshold_matches_oracle(R, gamma):
+    """Fixed confidence cutoff: verify lengths and B bit-exact, tau within the fp64
+    summation-order tolerance; cutoffs at, between and beyond the confidence values."""
+    b = _b()
+    rng = np.random.default_rng(R + 7 * gamma)
+    conf = rng.choice(np.array([1.0, 0.75, 0.5, 0.25], np.float32), size=(R, gamma)).astype(np.float32)
+    conf = np.where(rng.uniform(size=(R, gamma)) < 0.5, conf, rng.uniform(0, 1, (R, gamma))).astype(np.float32)
+    conf[0, 0] = np.float32(np.nan) if R > 1 else conf[0, 0]
+    for th in (0.0, 0.25, 0.5, 0.6, 0.75, 1.0, 1.5):
+        ref = oracle.schedule_threshold(conf, th)
+        g = _np(b.schedule_threshold(torch.from_numpy(conf).cuda(), th))
+        torch.cuda.synchronize()
+        assert np.array_equal(g["ell"], ref["ell"]), th
+        assert int(g["B"][0]) == ref["B"], th
+        assert abs(g["tau"][0] - ref["tau"]) <= 1e-12 * ref["tau"], th
