@@ -173,12 +173,21 @@ def draft_step_bytes(w):
     return R * V * es(w["U"]) + rank * V * es(w["W2"]) + R * rank * es(w["W1"])
 
 
+def tensor_core_path(w):
+    """The bf16 shapes the library runs on tcgen05 (the others run on CUDA cores)."""
+    import torch
+    return (w["W1"].dtype == torch.bfloat16 and w["rank"] % 64 == 0 and 64 <= w["rank"] <= 256
+            and w["V"] % 8 == 0 and w["V"] >= 128)
+
+
 def launches_per_round(w):
-    """Kernels of one round: confidence h-part, first-position prepare, a step and a
-    combine per draft position, the scheduler, and verify's plan / rows / accept /
-    residual step / residual combine."""
+    """Kernels of one round: confidence h-part, first-position prepare, the draft (a step
+    per position and one final merge on the tensor-core path; a step and a merge per
+    position on CUDA cores), the scheduler, and verify's plan / rows / accept / residual
+    step / residual combine."""
     g = w["gamma"]
-    return (1 if w["d"] > 0 else 0) + 1 + 2 * g + 1 + 5
+    draft = g + 1 if tensor_core_path(w) else 2 * g
+    return (1 if w["d"] > 0 else 0) + 1 + draft + 1 + 5
 
 
 def cpu_baseline(workload, w_host, sample_rounds=1):

@@ -136,6 +136,12 @@ __device__ void prepare_position_warp(const DraftArgs& a, int r, int k, int x_pr
     // (the order-preserving int code of -inf)
     a.hint[r] = __float_as_int(-INFINITY) ^ 0x7FFFFFFF;
   }
+  // tensor-core path: every position's bound and winner start empty
+  if (k == 1)
+    for (int i = lane; i < a.gamma; i += 32) {
+      a.hint[(size_t)i * a.R + r] = __float_as_int(-INFINITY) ^ 0x7FFFFFFF;
+      a.win[(size_t)i * a.R + r] = 0ull;
+    }
 }
 
 // Position 1: one warp per request.
@@ -283,6 +289,38 @@ __global__ void __launch_bounds__(kCombineThreads) draft_combine_kernel(DraftArg
   if (k < a.gamma) prepare_position_warp(a, r, k + 1, checked_token(b.idx, a.V, a.status, 2), lane);
 }
 
+// After the last tensor-core position: one warp per (request, position) merges that
+// position's partial records into x_k, lse_k and logq_k (the same merge the per-position
+// combine does; the steps themselves only needed the winner).
+__global__ void __launch_bounds__(256) draft_finalize_kernel(DraftArgs a, int npart) {
+  griddep_allow_next();
+  griddep_wait();
+  constexpr int kRecs = 5;  // records per lane and batch
+  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= a.R * a.gamma) return;
+  const int r = wid / a.gamma, k = wid % a.gamma + 1;
+  const Partial* part = a.partials + (size_t)(k - 1) * npart * a.R;
+  Stats st = stats_empty();
+  for (int g0 = lane; g0 < npart; g0 += 32 * kRecs) {
+    Partial rec[kRecs];
+#pragma unroll
+    for (int q = 0; q < kRecs; ++q)
+      if (g0 + 32 * q < npart) rec[q] = part[(size_t)(g0 + 32 * q) * a.R + r];
+#pragma unroll
+    for (int q = 0; q < kRecs; ++q)
+      if (g0 + 32 * q < npart) stats_merge(st, from_partial(rec[q]));
+  }
+  st = warp_reduce_stats(st);
+  if (lane == 0) {
+    const size_t row = (size_t)r * a.gamma + (k - 1);
+    const float lse = st.m + logf(st.s);
+    a.x_out[row] = st.idx;
+    a.lse_out[row] = lse;
+    a.logq_out[row] = st.zsel - lse;
+  }
+}
+
 // ---------------------------------------------------------------------------------
 // Host-side launchers
 // ---------------------------------------------------------------------------------
@@ -312,6 +350,11 @@ cudaError_t launch_draft_step_simt(const DraftArgs& a, int k, cudaStream_t s) {
     if (e != cudaSuccess) return e;
   }
   return launch_pdl(draft_step_simt_kernel<kSimtRB>, grid, dim3(kSimtThreads), smem, s, a, k);
+}
+
+cudaError_t launch_draft_finalize(const DraftArgs& a, int npart, cudaStream_t s) {
+  const int warps = a.R * a.gamma;
+  return launch_pdl(draft_finalize_kernel, dim3((warps * 32 + 255) / 256), dim3(256), 0, s, a, npart);
 }
 
 cudaError_t launch_draft_combine(const DraftArgs& a, int k, int npart, cudaStream_t s) {

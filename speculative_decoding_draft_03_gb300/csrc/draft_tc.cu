@@ -264,6 +264,18 @@ struct TcParams {
   const float* lse_q;   // [R, gamma]
   const float* lse_t;   // [R]
   Partial* partials2;   // [ngroups, R] fallback draw
+  // draft mode: the factor rows of position k come from the previous position's winner
+  // (x0 at k = 1); each CTA publishes its per-request winner into win (64-bit maximum of
+  // (key code, ~id)); group-0 CTAs write the confidence c_k for k >= 2
+  const int32_t* x0;
+  const unsigned long long* win_prev;  // [R] winners of position k-1 (k >= 2)
+  unsigned long long* win;             // [R] winners of position k
+  const void* W1;                      // [V, rank] bf16
+  const float* w_e;                    // [rank]
+  const float* s_h;                    // [R, gamma]
+  const float* conf_temp;              // [gamma]
+  float* conf_out;                     // [R, gamma]
+  float conf_b, conf_scale;
 };
 
 constexpr int kModeDraft = 0;
@@ -323,10 +335,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t bar_empty = bar_full + 8 * kStages;         // [kStages]
   uint32_t bar_acc_full = bar_empty + 8 * kStages;     // [2]
   uint32_t bar_acc_empty = bar_acc_full + 16;          // [2]
-  uint32_t bar_a = bar_acc_empty + 16;                 // [1]
-  uint32_t bar_ufull = bar_a + 8;                      // [kMaxUBoxes]
+  uint32_t bar_a = bar_acc_empty + 16;                 // [1] A rows landed (residual: TMA)
+  uint32_t bar_a2 = bar_a + 8;                         // [1] A rows written (draft: epilogue)
+  uint32_t bar_ufull = bar_a2 + 8;                     // [kMaxUBoxes]
   uint32_t bar_uempty = bar_ufull + 8 * kMaxUBoxes;    // [kMaxUBoxes]
-  constexpr int kBarBytes = 8 * (2 * kStages + 5 + 2 * kMaxUBoxes);
+  constexpr int kBarBytes = 8 * (2 * kStages + 6 + 2 * kMaxUBoxes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::bars + kBarBytes);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM::bars + kBarBytes + 8);
   // U boxes of a tile: 128/ubox_cols of them, each read by the 16/(128/ubox_cols) warps
@@ -349,6 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_acc_empty + 8 * b, kEpiWarps);
     }
     mbar_init(bar_a, 1);
+    mbar_init(bar_a2, 1);
     for (int s = 0; s < kMaxUBoxes; ++s) {
       mbar_init(bar_ufull + 8 * s, 1);
       mbar_init(bar_uempty + 8 * s, warps_per_ubox);
@@ -388,8 +402,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool a_issued = false;
       int stage = 0;
       uint32_t phase = 0;
+      if (MODE == kModeDraft) a_issued = true;  // draft: the epilogue writes A itself
       for (int it = 0; it < total && !*abort_flag; ++it) {
-        if (it == kStages) {
+        if (it == kStages && !a_issued) {
           load_a();
           a_issued = true;
         }
@@ -411,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------ MMA issuer --------------------------------
     if (lane == 0) {
       constexpr uint32_t idesc = make_idesc(kM, kN);
-      bool ok = mbar_wait(bar_a, 0, abort_flag, p.status, 200);
+      bool ok = mbar_wait(MODE == kModeDraft ? bar_a2 : bar_a, 0, abort_flag, p.status, 200);
       int stage = 0;
       uint32_t phase = 0;
       for (int t = 0; t < my_tiles && ok; ++t) {
@@ -516,7 +531,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool u_f32 = p.dtype_u == DSPARK_F32;
     if constexpr (MODE == kModeResidual) load_u(0, unext);
     // the predecessor still reads the partial records this kernel overwrites at the end
-    if constexpr (MODE == kModeDraft) griddep_wait();
+    if constexpr (MODE == kModeDraft) {
+      griddep_wait();
+      // A rows of this position: W1[x_{k-1}] for the request block, x_{k-1} from x0 or
+      // the previous position's winner.  Lane l moves 16-byte chunk l of the row (rank
+      // <= 256) into the 128-byte swizzled K-atom rows of every replica.  Group-0 CTAs
+      // also write c_k (k >= 2).
+      const int et0 = threadIdx.x - 32 * kFirstEpiWarp;
+      for (int rr = ew; rr < RB; rr += kEpiWarps) {
+        const int rq = rb * RB + rr;
+        int xp = 0;
+        if (rq < p.R) {
+          const int raw = p.k == 1 ? __ldg(p.x0 + rq) : (int)~(uint32_t)(__ldcg(p.win_prev + rq) & 0xFFFFFFFFull);
+          xp = checked_token(raw, p.V, p.status, 3);
+        }
+        const bool has = lane * 8 < p.rank;
+        uint4 q = make_uint4(0u, 0u, 0u, 0u);
+        if (rq < p.R && has)
+          q = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned short*>(p.W1) + (size_t)xp * p.rank) +
+                    lane);
+        if (has) {
+          const int ka = lane >> 3, c = lane & 7;
+          const uint32_t dst = sbase + SM::a + ka * (kM * 128) + rr * 128 + ((c ^ (rr & 7)) << 4);
+#pragma unroll
+          for (int j = 0; j < kM / RB; ++j)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + j * RB * 128), "r"(q.x), "r"(q.y),
+                         "r"(q.z), "r"(q.w)
+                         : "memory");
+        }
+        if (group == 0 && p.k >= 2 && rq < p.R) {
+          const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+          float acc = 0.f;
+          if (has) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              acc = fmaf(__ldg(p.w_e + lane * 8 + 2 * e), bf16_bits_to_float(wd[e] & 0xFFFFu), acc);
+              acc = fmaf(__ldg(p.w_e + lane * 8 + 2 * e + 1), bf16_bits_to_float(wd[e] >> 16), acc);
+            }
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+          if (lane == 0) {
+            const size_t row = (size_t)rq * p.gamma + (p.k - 1);
+            const float logit = p.conf_scale * (p.s_h[row] + acc + p.conf_b);
+            p.conf_out[row] = sigmoidf_dev(logit / __ldg(p.conf_temp + (p.k - 1)));
+          }
+        }
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // read next by the tensor cores
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+      if (et0 == 0) mbar_arrive(bar_a2);
+    }
 
     // Draft mode: the best key any CTA has published for this request at this position.
     // Every published value is the key of an actual element, so it is a lower bound of
@@ -752,6 +817,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int rr = rb * RB + et;
         if (rr < p.R) (which ? p.partials2 : p.partials)[(size_t)group * p.R + rr] = to_partial(m);
+        // draft: this CTA's winner for the request, as one 64-bit maximum (key code in the
+        // high half, sign-flipped so that the order is unsigned; ~id in the low half, so the
+        // lowest id wins equal keys)
+        if (MODE == kModeDraft && rr < p.R && m.idx >= 0) {
+          const unsigned long long packed =
+              ((unsigned long long)((uint32_t)ordered_key(m.key) ^ 0x80000000u) << 32) | (uint32_t)~(uint32_t)m.idx;
+          atomicMax(p.win + rr, packed);
+        }
       }
       asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
     }
@@ -884,8 +957,18 @@ cudaError_t launch_draft_step_tc(const DraftArgs& a, int k, cudaStream_t s) {
   tc::TcParams p = tc::base_params(a.R, a.gamma, a.V, a.rank, a.dtype_u, a.inv_temp, a.U, a.req_id, a.seed,
                                    a.round, a.status);
   p.k = k;
-  p.partials = a.partials;
-  p.hint = a.hint;
+  p.partials = a.partials + (size_t)(k - 1) * tc_num_partials(a.R) * a.R;
+  p.hint = a.hint + (size_t)(k - 1) * a.R;
+  p.x0 = a.x0;
+  p.win_prev = k >= 2 ? a.win + (size_t)(k - 2) * a.R : nullptr;
+  p.win = a.win + (size_t)(k - 1) * a.R;
+  p.W1 = a.W1;
+  p.w_e = a.conf_w + a.d;
+  p.s_h = a.s_h;
+  p.conf_temp = a.conf_temp;
+  p.conf_out = a.conf_out;
+  p.conf_b = a.conf_b;
+  p.conf_scale = a.conf_scale;
   return tc::launch<tc::kModeDraft>(p, a.W1g, a.W2, s);
 }
 

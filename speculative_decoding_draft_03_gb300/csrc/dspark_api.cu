@@ -34,7 +34,7 @@ constexpr int kMaxGamma = 64;
 constexpr int kVerifyChunk = 8192;
 
 struct DraftLayout {
-  size_t s_h, W1g, partials, hint, total;
+  size_t s_h, W1g, partials, hint, win, total;
   int npart;
 };
 
@@ -48,9 +48,11 @@ DraftLayout draft_layout(int R, int gamma, int V, int rank, int dtype_w) {
   off += align256(elem_size(dtype_w) * (size_t)round_up_rows(R) * rank);
   L.npart = draft_num_partials(R, V, rank, dtype_w);
   L.partials = off;
-  off += align256((size_t)32 * L.npart * R);
+  off += align256((size_t)32 * L.npart * R * gamma);  // one set per draft position
   L.hint = off;
-  off += align256(sizeof(int) * (size_t)R);
+  off += align256(sizeof(int) * (size_t)R * gamma);
+  L.win = off;
+  off += align256(sizeof(unsigned long long) * (size_t)R * gamma);
   L.total = off;
   return L;
 }
@@ -233,6 +235,7 @@ dspark_status dspark_markov_draft(int R, int gamma, int V, int rank, int d, int 
   a.W1g = ws + L.W1g;
   a.partials = reinterpret_cast<dspark::Partial*>(ws + L.partials);
   a.hint = reinterpret_cast<int*>(ws + L.hint);
+  a.win = reinterpret_cast<unsigned long long*>(ws + L.win);
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
@@ -258,10 +261,14 @@ dspark_status dspark_markov_draft(int R, int gamma, int V, int rank, int d, int 
     }
     if (prof && (e = record_profile_event(g_prof_events[2 * (k - 1) + 1], s)) != cudaSuccess)
       return cuda_fail(e, "profile event");
-    // the merge runs as its own kernel: launched early (programmatic dependent launch),
-    // it overlaps the next step's prologue and W2 prefetch
-    if ((e = dspark::launch_draft_combine(a, k, npart, s)) != cudaSuccess) return cuda_fail(e, "draft_combine");
+    // Tensor-core path: each step publishes its per-request winner (one 64-bit maximum),
+    // from which the next step gathers its own factor rows, so the partial records are
+    // merged once, after the last position.  CUDA-core path: a merge kernel per position.
+    if (!tc && (e = dspark::launch_draft_combine(a, k, npart, s)) != cudaSuccess)
+      return cuda_fail(e, "draft_combine");
   }
+  if (tc && (e = dspark::launch_draft_finalize(a, dspark::tc_num_partials(R), s)) != cudaSuccess)
+    return cuda_fail(e, "draft_finalize");
   return DSPARK_OK;
 }
 

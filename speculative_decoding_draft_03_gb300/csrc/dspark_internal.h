@@ -38,8 +38,9 @@ struct DraftArgs {
   DeviceStatus* status;
   float* s_h;        // [R*gamma]
   void* W1g;         // [Rpad, rank] gathered factor rows (dtype_w)
-  Partial* partials; // [npart, R]
-  int* hint;         // [R] best Gumbel key found so far at the current position (ordered int)
+  Partial* partials; // [gamma, npart, R] (the CUDA-core path uses the first [npart, R])
+  int* hint;         // [gamma, R] best Gumbel key published so far per position (ordered int)
+  unsigned long long* win;  // [gamma, R] tensor-core path: (key code, ~id) maximum per position
 };
 
 struct VerifyArgs {
@@ -117,6 +118,8 @@ cudaError_t launch_draft_prepare(const DraftArgs& a, int k, cudaStream_t s);
 cudaError_t launch_draft_step_simt(const DraftArgs& a, int k, cudaStream_t s);
 cudaError_t launch_draft_combine(const DraftArgs& a, int k, int npart, cudaStream_t s);
 cudaError_t launch_draft_step_tc(const DraftArgs& a, int k, cudaStream_t s);
+// After the last tensor-core position: every position's partial records -> x, lse, logq.
+cudaError_t launch_draft_finalize(const DraftArgs& a, int npart, cudaStream_t s);
 
 cudaError_t launch_schedule_threshold(int R, int gamma, const float* conf, double threshold, int32_t* ell_out,
                                       int32_t* B_out, double* tau_out, cudaStream_t s);
