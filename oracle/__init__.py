@@ -71,6 +71,8 @@ def _load():
             lib.orc_verify.argtypes = ([i32] * 7 + [P] * 4 + [P, P, P, P, P, f64, P, u64, u64]
                                        + [P] * 3 + [P] * 4 + [i32])
             lib.orc_max_threads.restype = i32
+            lib.orc_acceptance_overlap.argtypes = [i32] * 7 + [P] * 7 + [f64, P, i32]
+            lib.orc_acceptance_overlap.restype = ctypes.c_int
             for name in ("orc_markov_draft", "orc_draft_distribution", "orc_schedule",
                          "orc_schedule_path", "orc_verify", "orc_philox4x32_10"):
                 getattr(lib, name).restype = ctypes.c_int if name != "orc_philox4x32_10" else None
@@ -274,6 +276,32 @@ def verify(target, U, W1, W2, x0, x, logq, lse_q, ell, temperature, req_id, seed
                         _ptr(out["corr_rho"]), _ptr(out["corr_kind"]), int(nthreads))
     if rc != 0:
         raise ValueError("oracle verify rejected its arguments")
+    return out
+
+
+def acceptance_overlap(target, U, W1, W2, x0, x, ell=None, temperature=1.0, nthreads=0):
+    """Expected acceptance of each drafted position, c*_j = sum_v min(q_j(v), p_j(v))
+    (numb3r33 blog, "Total variation label").
+
+    target [R,gamma+1,V]; U [R,gamma,V]; x [R,gamma]; ell [R] or None (every position).
+    Returns float64 [R,gamma], NaN at positions past ell[r].
+    """
+    lib = _load()
+    dt, target = _dtype_code(np.ascontiguousarray(target))
+    du, U = _dtype_code(np.ascontiguousarray(U))
+    dw, W1 = _dtype_code(np.ascontiguousarray(W1))
+    _, W2 = _dtype_code(np.ascontiguousarray(W2))
+    R, g1, V = target.shape
+    gamma = g1 - 1
+    x0 = _c(x0, np.int32)
+    x = _c(x, np.int32)
+    ell_c = None if ell is None else _c(ell, np.int32)
+    out = np.zeros((R, gamma))
+    rc = lib.orc_acceptance_overlap(R, gamma, V, W1.shape[1], dt, du, dw, _ptr(target), _ptr(U), _ptr(W1),
+                                    _ptr(W2), _ptr(x0), _ptr(x), _ptr(ell_c), float(temperature), _ptr(out),
+                                    int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle acceptance_overlap rejected its arguments")
     return out
 
 

@@ -544,4 +544,54 @@ int orc_schedule_many(int nbatch, int R, int gamma, const float* conf, const dou
     return 0;
 }
 
+/* ------------------------------------------------------------------------- */
+/* Acceptance-overlap diagnostic.                                             */
+/* ------------------------------------------------------------------------- */
+/* For request r and drafted position j (1-based) the expected acceptance of the
+ * draft token is the overlap of the two distributions ([EXPL] "Total variation
+ * label"; [EXPL] "Speculative sampling in one picture"):
+ *   c*_j = sum_v min(q_j(v), p_j(v)) = 1 - (1/2) ||q_j - p_j||_1
+ * with q_j = softmax((U[r,j-1,:] + W1[x_{j-1},:] W2)/T) the draft distribution at
+ * position j (x_0 the anchor) and p_j = softmax(target[r,j-1,:]/T) the target
+ * distribution that verifies position j.  Positions j <= n_r are evaluated, n_r =
+ * ell[r] (ell == NULL: every position); the others are set to NaN. */
+int orc_acceptance_overlap(int R, int gamma, int V, int rank, int dtype_t, int dtype_u, int dtype_w,
+                           const void* target, const void* U, const void* W1, const void* W2,
+                           const int32_t* x0, const int32_t* x, const int32_t* ell,
+                           double temperature, double* out, int nthreads) {
+    if (R < 0 || gamma < 1 || V < 1 || rank < 1 || temperature <= 0.0) return 1;
+    if (ell)
+        for (int r = 0; r < R; ++r)
+            if (ell[r] < 0 || ell[r] > gamma) return 1;
+    int nt = orc_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
+    for (int r = 0; r < R; ++r) {
+        double* z = (double*)malloc(sizeof(double) * (size_t)V);
+        double* t = (double*)malloc(sizeof(double) * (size_t)V);
+        const int n = ell ? ell[r] : gamma;
+        for (int j = 1; j <= gamma; ++j) {
+            const size_t row = (size_t)r * gamma + (j - 1);
+            if (j > n) {
+                out[row] = NAN;
+                continue;
+            }
+            const int xprev = (j == 1) ? x0[r] : x[(size_t)r * gamma + (j - 2)];
+            orc_draft_logits(V, rank, dtype_u, dtype_w, U, row * (size_t)V, W1, W2, xprev, temperature, z);
+            const double lq = orc_logsumexp(z, V);
+            const size_t trow = ((size_t)r * (gamma + 1) + (j - 1)) * (size_t)V;
+            for (int v = 0; v < V; ++v) t[v] = orc_load(target, dtype_t, trow + v) / temperature;
+            const double lt = orc_logsumexp(t, V);
+            double c = 0.0;
+            for (int v = 0; v < V; ++v) {
+                const double q = exp(z[v] - lq), p = exp(t[v] - lt);
+                c += q < p ? q : p;
+            }
+            out[row] = c;
+        }
+        free(z);
+        free(t);
+    }
+    return 0;
+}
+
 int orc_max_threads(void) { return orc_threads(0); }
