@@ -266,6 +266,38 @@ DSPARK_API dspark_status dspark_verify_static(
     const int32_t* ell, float temperature, const int64_t* req_id, uint64_t seed, uint64_t round,
     int32_t* n_acc_out, int32_t* tokens_out, int32_t* n_out, void* stream);
 
+/* ------------------------------------------------------------------------------------
+ * Acceptance-overlap diagnostic of a drafted block.
+ *
+ * Defines (numb3r33 blog "DSpark: confidence-scheduled speculative decoding", sections
+ * "Total variation label" and "Speculative sampling in one picture"): for every request
+ * r and drafted position j = 1..n_r,
+ *   c*[r,j] = sum_v min(q_j(v), p_j(v)) = 1 - ||q_j - p_j||_1 / 2,
+ *   q_j = exp(z - lse_q[r,j]), z = (U[r,j,:] + W1[x_{j-1},:] W2) / T (x_0 = x0[r]),
+ *   p_j = softmax(target row j-1 / T)  (0-based row of target[r]),
+ * the probability that the draft token of position j is accepted given its prefix (the
+ * expectation of min(1, p/q) under q), i.e. the label the confidence head c_j predicts.
+ * n_r = ell[r] when ell is given (the verified positions), gamma when ell is NULL.
+ * Arguments
+ *   target [R,gamma+1,V] (dtype_t), U [R,gamma,V] (dtype_u), W1 [V,rank], W2 [rank,V]
+ *     (dtype_w): as in stages 1 and 3; 16-byte aligned.
+ *   x0 [R], x [R,gamma] int32: the drafted tokens (stage 1 output).
+ *   lse_q [R,gamma] fp32: the draft log-normalisers (stage 1 output).
+ *   ell [R] int32 in [0,gamma], or NULL.
+ * Output: overlap_out [R,gamma] fp32; NaN at positions j > n_r.
+ * Token ids or lengths outside their range are reported through the workspace status
+ * word (DSPARK_INVALID_ARG) and clamped.  Workspace: the size
+ * dspark_acceptance_overlap_workspace_size() returns (0 for unsupported sizes).
+ * Limits: R*gamma <= 2^24, gamma <= 64.
+ * ---------------------------------------------------------------------------------- */
+DSPARK_API size_t dspark_acceptance_overlap_workspace_size(int R, int gamma, int V, int rank, int dtype_w);
+
+DSPARK_API dspark_status dspark_acceptance_overlap(
+    int R, int gamma, int V, int rank, int dtype_t, int dtype_u, int dtype_w,
+    const void* target, const void* U, const void* W1, const void* W2,
+    const int32_t* x0, const int32_t* x, const float* lse_q, const int32_t* ell,
+    float temperature, float* overlap_out, void* workspace, size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

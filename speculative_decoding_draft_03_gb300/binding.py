@@ -52,6 +52,10 @@ def _load_library():
     lib.dspark_verify_ragged.restype = i32
     lib.dspark_verify_static.argtypes = ([i32] * 7 + [P] * 4 + [P] * 5 + [f32, P, u64, u64] + [P] * 3 + [P])
     lib.dspark_verify_static.restype = i32
+    lib.dspark_acceptance_overlap_workspace_size.restype = sz
+    lib.dspark_acceptance_overlap_workspace_size.argtypes = [i32] * 5
+    lib.dspark_acceptance_overlap.argtypes = [i32] * 7 + [P] * 4 + [P] * 4 + [f32, P, P, sz, P]
+    lib.dspark_acceptance_overlap.restype = i32
     for fn in ("dspark_markov_draft", "dspark_schedule", "dspark_verify", "dspark_workspace_status"):
         getattr(lib, fn).restype = i32
     return lib
@@ -243,6 +247,36 @@ def verify_ragged(target_rows, row_offset, U, W1, W2, x0, x, logq, lse_q, ell, t
                                   int(rnd), _p(out["n_acc"]), _p(out["tokens"]), _p(out["n_out"]), _p(ws),
                                   ws.numel(), _stream(stream))
     _check(st, "dspark_verify_ragged")
+    return out
+
+
+def acceptance_overlap_workspace_size(R, gamma, V, rank, w_dtype) -> int:
+    return int(lib.dspark_acceptance_overlap_workspace_size(R, gamma, V, rank, _DT[w_dtype]))
+
+
+def acceptance_overlap(target, U, W1, W2, x0, x, lse_q, ell, temperature, out=None, ws=None, stream=None):
+    """Expected acceptance c*[r,j] = sum_v min(q_j, p_j) of every drafted position
+    (dspark_acceptance_overlap); ell None evaluates all positions.  Returns [R,gamma]
+    float32, NaN past ell[r]."""
+    R, g1, V = target.shape
+    gamma = g1 - 1
+    rank = W1.shape[1]
+    dev = target.device
+    for t, n in ((target, "target"), (U, "U"), (W1, "W1"), (W2, "W2")):
+        _cuda(t, n)
+    _cuda(x0, "x0", torch.int32)
+    _cuda(x, "x", torch.int32)
+    _cuda(lse_q, "lse_q", torch.float32)
+    if ell is not None:
+        _cuda(ell, "ell", torch.int32)
+    if out is None:
+        out = torch.empty((R, gamma), dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = workspace(acceptance_overlap_workspace_size(R, gamma, V, rank, W1.dtype), dev)
+    st = lib.dspark_acceptance_overlap(R, gamma, V, rank, _dt(target, "target"), _dt(U, "U"), _dt(W1, "W1"),
+                                       _p(target), _p(U), _p(W1), _p(W2), _p(x0), _p(x), _p(lse_q), _p(ell),
+                                       float(temperature), _p(out), _p(ws), ws.numel(), _stream(stream))
+    _check(st, "dspark_acceptance_overlap")
     return out
 
 

@@ -276,10 +276,16 @@ struct TcParams {
   const float* conf_temp;              // [gamma]
   float* conf_out;                     // [R, gamma]
   float conf_b, conf_scale;
+  // overlap mode: rows are the flattened [R*gamma] positions (R above counts rows);
+  // row i is request i / gamma at position i % gamma + 1, evaluated when that position
+  // is at most ell[request] (every position without ell)
+  const int32_t* ell;
+  float* ovl_part;  // [ngroups, rows] partial sums of min(q, p)
 };
 
 constexpr int kModeDraft = 0;
 constexpr int kModeResidual = 1;
+constexpr int kModeOverlap = 2;
 
 // 8 consecutive ids of U (fp32 or bf16) as fp32; ids at or beyond V read as 0 (V % 8 == 0,
 // so a run of 8 is either entirely inside the row or entirely outside).
@@ -314,8 +320,9 @@ __device__ __forceinline__ void decode_run8(int dtype, const uint4 (&raw)[2], fl
 }
 
 // RB: requests per block (32, 64 or 128); the 128 MMA rows hold 128/RB copies of it.
-// MODE: kModeDraft (one draft position for every request) or kModeResidual (the
-// rejected position j* of each request that has one).
+// MODE: kModeDraft (one draft position for every request), kModeResidual (the
+// rejected position j* of each request that has one) or kModeOverlap (every drafted
+// position: sum_v min(q, p), the expected acceptance).
 template <int RB, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     draft_step_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
@@ -494,9 +501,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int col0 = replica * RB + sub * (RB / 4);  // RB columns per replica, a quarter per warp
 
     // the residual's positions and normalisers come from the preceding kernel
-    if constexpr (MODE == kModeResidual) griddep_wait();
-    // draft: position k of every request; residual: the rejected position j* (0 = none)
+    if constexpr (MODE != kModeDraft) griddep_wait();
+    // draft: position k of every request; residual: the rejected position j* (0 = none);
+    // overlap: row r is position r % gamma + 1 of request r / gamma
     int pos = p.k;
+    int req = r;
     float lse_q = 0.f, lse_t = 0.f;
     if constexpr (MODE == kModeResidual) {
       pos = valid ? p.jstar[r] : 0;
@@ -506,13 +515,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         lse_t = p.lse_t[r];
       }
     }
+    if constexpr (MODE == kModeOverlap) {
+      req = r / p.gamma;
+      pos = r % p.gamma + 1;
+      if (valid && p.ell != nullptr) valid = pos <= min(max(__ldg(p.ell + req), 0), p.gamma);
+      if (valid) {
+        lse_q = __ldg(p.lse_q + r);
+        lse_t = p.lse_t[r];
+      }
+    }
     Stats st = stats_empty();  // draft: softmax stats + Gumbel-max; residual: ln(p-q)+ + g
     Stats fb = stats_empty();  // residual only: ln p + g (the rounding fallback)
-    const PhiloxRow prow = philox_row(rng_row(p.seed, valid ? __ldg(p.req_id + r) : 0, p.round,
-                                              MODE == kModeDraft ? kStreamDraft : kStreamCorrect, (uint32_t)pos));
-    const size_t urow = ((size_t)(valid ? r : 0) * p.gamma + (valid ? pos - 1 : 0)) * (size_t)p.V;
+    float ovl = 0.f;           // overlap only: this thread's sum of min(q, p)
+    const PhiloxRow prow =
+        philox_row(rng_row(p.seed, (MODE != kModeOverlap && valid) ? __ldg(p.req_id + r) : 0, p.round,
+                           MODE == kModeDraft ? kStreamDraft : kStreamCorrect, (uint32_t)pos));
+    const size_t urow = MODE == kModeOverlap
+                            ? (size_t)(valid ? r : 0) * (size_t)p.V
+                            : ((size_t)(valid ? r : 0) * p.gamma + (valid ? pos - 1 : 0)) * (size_t)p.V;
     const size_t trow =
-        (valid ? target_row_index(p.t_off, p.n_trows, p.gamma, r, pos - 1, p.status) : 0) * (size_t)p.V;
+        (valid ? target_row_index(p.t_off, p.n_trows, p.gamma, req, pos - 1, p.status) : 0) * (size_t)p.V;
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
 
     // Residual mode: U of the next tile is loaded into registers while the current one is
@@ -529,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int box_col = col0 % p.ubox_cols;
     const int box_row = row0 + lane;
     const bool u_f32 = p.dtype_u == DSPARK_F32;
-    if constexpr (MODE == kModeResidual) load_u(0, unext);
+    if constexpr (MODE != kModeDraft) load_u(0, unext);
     // the predecessor still reads the partial records this kernel overwrites at the end
     if constexpr (MODE == kModeDraft) {
       griddep_wait();
@@ -599,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint4 ucur[kPass][2];
       int uslot = 0;
       bool u_ready = true;
-      if constexpr (MODE == kModeResidual) {
+      if constexpr (MODE != kModeDraft) {
 #pragma unroll
         for (int ps = 0; ps < kPass; ++ps) {
           ucur[ps][0] = unext[ps][0];
@@ -726,6 +748,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               st.zsel = zi;
             }
           }
+        } else if constexpr (MODE == kModeOverlap) {
+          // overlap: min(q, p) with q = exp(z - lse_q), p = exp(t/T - lse_t)
+          uint4 traw[2];
+          load_run8(p.target, p.dtype_t, trow, vb, p.V, true, traw);
+          float tl[kCols];
+          decode_run8(p.dtype_t, traw, tl);
+#pragma unroll
+          for (int i = 0; i < kCols; ++i)
+            ovl += fminf(__expf(fmaf(tl[i], p.inv_temp, -lse_t)), __expf(z[i] - lse_q));
         } else {
           // residual: q = exp(z - lse_q), p = exp(t/T - lse_t); draw from (p - q)+ by
           // Gumbel-max over ln(p - q) where positive, and keep the ln p draw as fallback
@@ -804,8 +835,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // merge the threads that share a request: smem slots [ew][lane]
     Partial* red = reinterpret_cast<Partial*>(smem + SM::red);
     const int et = threadIdx.x - 32 * kFirstEpiWarp;  // 0..511
+    if constexpr (MODE == kModeOverlap) {
+      // the warps holding a row add their sums in a fixed order (deterministic)
+      float* redf = reinterpret_cast<float*>(smem + SM::red);
+      redf[ew * 32 + lane] = ovl;
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+      if (et < RB) {
+        float sum = 0.f;
+        for (int w2 = 0; w2 < kEpiWarps; ++w2) {
+          const int r0 = (((w2 + kFirstEpiWarp) & 3) * 32) % RB;
+          if (et >= r0 && et < r0 + 32) sum += redf[w2 * 32 + (et - r0)];
+        }
+        const int rr = rb * RB + et;
+        if (rr < p.R) p.ovl_part[(size_t)group * p.R + rr] = sum;
+      }
+    }
 #pragma unroll
-    for (int which = 0; which < (MODE == kModeDraft ? 1 : 2); ++which) {
+    for (int which = 0; which < (MODE == kModeDraft ? 1 : (MODE == kModeResidual ? 2 : 0)); ++which) {
       red[ew * 32 + lane] = to_partial(which ? fb : st);
       asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
       if (et < RB) {
@@ -970,6 +1016,19 @@ cudaError_t launch_draft_step_tc(const DraftArgs& a, int k, cudaStream_t s) {
   p.conf_b = a.conf_b;
   p.conf_scale = a.conf_scale;
   return tc::launch<tc::kModeDraft>(p, a.W1g, a.W2, s);
+}
+
+cudaError_t launch_overlap_tc(const OverlapArgs& a, cudaStream_t s) {
+  const int rows = a.R * a.gamma;
+  tc::TcParams p = tc::base_params(rows, a.gamma, a.V, a.rank, a.dtype_u, a.inv_temp, a.U, nullptr, 0, 0, a.status);
+  p.k = 1;
+  p.target = a.target;
+  p.dtype_t = a.dtype_t;
+  p.lse_q = a.lse_q;
+  p.lse_t = a.lse_t;
+  p.ell = a.ell;
+  p.ovl_part = a.part;
+  return tc::launch<tc::kModeOverlap>(p, a.W1g, a.W2, s);
 }
 
 cudaError_t launch_residual_tc(const VerifyArgs& a, cudaStream_t s) {

@@ -98,6 +98,27 @@ VerifyLayout verify_layout(int R, int gamma, int V, int rank, int dtype_w) {
   return L;
 }
 
+struct OverlapLayout {
+  size_t W1g, lse_t, part, total;
+  int npart;
+};
+
+OverlapLayout overlap_layout(int R, int gamma, int V, int rank, int dtype_w) {
+  using namespace dspark;
+  OverlapLayout L;
+  const size_t rows = (size_t)R * gamma;
+  L.npart = overlap_num_partials(R, gamma, V, rank, dtype_w);
+  size_t off = 256;
+  L.W1g = off;
+  off += align256(elem_size(dtype_w) * (size_t)round_up_rows((int)rows) * rank);
+  L.lse_t = off;
+  off += align256(4 * rows);
+  L.part = off;
+  off += align256(4 * rows * (size_t)L.npart);
+  L.total = off;
+  return L;
+}
+
 #define CHECK_PTR(p)                                                              \
   do {                                                                            \
     if ((p) == nullptr) return fail(DSPARK_INVALID_ARG, "null pointer: %s", #p); \
@@ -428,6 +449,64 @@ dspark_status dspark_verify_ragged(int R, int gamma, int V, int rank, int dtype_
   return verify_impl(R, gamma, V, rank, dtype_t, dtype_u, dtype_w, target, target_row_offset, n_target_rows, U, W1,
                      W2, x0, x, logq, lse_q, ell, temperature, req_id, seed, round, n_acc_out, tokens_out, n_out,
                      workspace, ws_bytes, stream);
+}
+
+size_t dspark_acceptance_overlap_workspace_size(int R, int gamma, int V, int rank, int dtype_w) {
+  if (R < 1 || gamma < 1 || V < 1 || rank < 1) return 0;
+  if ((long long)R * gamma > (1ll << 24)) return 0;
+  return overlap_layout(R, gamma, V, rank, dtype_w).total;
+}
+
+dspark_status dspark_acceptance_overlap(int R, int gamma, int V, int rank, int dtype_t, int dtype_u, int dtype_w,
+                                        const void* target, const void* U, const void* W1, const void* W2,
+                                        const int32_t* x0, const int32_t* x, const float* lse_q, const int32_t* ell,
+                                        float temperature, float* overlap_out, void* workspace, size_t ws_bytes,
+                                        void* stream) {
+  if (R < 1 || gamma < 1 || V < 1 || rank < 1)
+    return fail(DSPARK_INVALID_ARG, "sizes must be positive (R=%d gamma=%d V=%d rank=%d)", R, gamma, V, rank);
+  if (gamma > kMaxGamma) return fail(DSPARK_UNSUPPORTED_SHAPE, "gamma=%d exceeds %d", gamma, kMaxGamma);
+  if ((long long)V > (1ll << 30)) return fail(DSPARK_UNSUPPORTED_SHAPE, "V=%d too large", V);
+  if ((long long)R * gamma > (1ll << 24)) return fail(DSPARK_UNSUPPORTED_SHAPE, "R*gamma too large");
+  // the CUDA-core bias pass takes blocks of 4 positions along the grid's y dimension
+  if (!dspark::tc_supported(V, rank, dtype_w) && ((long long)R * gamma + 3) / 4 > 65535)
+    return fail(DSPARK_UNSUPPORTED_SHAPE, "R*gamma=%lld exceeds 262140 without the tensor-core path",
+                (long long)R * gamma);
+  if (!valid_dtype(dtype_t) || !valid_dtype(dtype_u) || !valid_dtype(dtype_w))
+    return fail(DSPARK_INVALID_ARG, "dtype codes must be DSPARK_F32 or DSPARK_BF16");
+  if (!(temperature > 0.f) || !isfinite(temperature))
+    return fail(DSPARK_INVALID_ARG, "temperature must be finite and > 0");
+  CHECK_PTR(target);
+  CHECK_PTR(U);
+  CHECK_PTR(W1);
+  CHECK_PTR(W2);
+  CHECK_PTR(x0);
+  CHECK_PTR(x);
+  CHECK_PTR(lse_q);
+  CHECK_PTR(overlap_out);
+  CHECK_PTR(workspace);
+  CHECK_ALIGN16(target);
+  CHECK_ALIGN16(U);
+  CHECK_ALIGN16(W1);
+  CHECK_ALIGN16(W2);
+  if (!aligned256(workspace)) return fail(DSPARK_INVALID_ARG, "workspace must be 256-byte aligned");
+  const OverlapLayout L = overlap_layout(R, gamma, V, rank, dtype_w);
+  if (ws_bytes < L.total) return fail(DSPARK_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, L.total);
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  dspark::OverlapArgs a;
+  a.R = R; a.gamma = gamma; a.V = V; a.rank = rank;
+  a.dtype_t = dtype_t; a.dtype_u = dtype_u; a.dtype_w = dtype_w;
+  a.target = target; a.U = U; a.W1 = W1; a.W2 = W2;
+  a.x0 = x0; a.x = x; a.lse_q = lse_q; a.ell = ell;
+  a.inv_temp = 1.0f / temperature;
+  a.out = overlap_out;
+  a.status = reinterpret_cast<dspark::DeviceStatus*>(ws);
+  a.W1g = ws + L.W1g;
+  a.lse_t = reinterpret_cast<float*>(ws + L.lse_t);
+  a.part = reinterpret_cast<float*>(ws + L.part);
+  a.npart = L.npart;
+  cudaError_t e = dspark::launch_overlap(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "acceptance_overlap");
+  return DSPARK_OK;
 }
 
 }  // extern "C"

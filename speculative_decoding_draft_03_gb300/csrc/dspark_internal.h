@@ -83,6 +83,30 @@ struct VerifyArgs {
   Partial* res_part2; // [npart, R] fallback partials: key = ln p + g
 };
 
+// Acceptance-overlap diagnostic: c*[r, j-1] = sum_v min(q_j(v), p_j(v)) for the drafted
+// positions j <= n_r of every request (n_r = ell[r], or gamma without ell).  Row i of
+// the flattened [R*gamma] positions is request i / gamma at position i % gamma + 1.
+struct OverlapArgs {
+  int R, gamma, V, rank;
+  int dtype_t, dtype_u, dtype_w;
+  const void* target;   // [R, gamma+1, V]
+  const void* U;        // [R, gamma, V]
+  const void* W1;
+  const void* W2;
+  const int32_t* x0;
+  const int32_t* x;
+  const float* lse_q;   // [R, gamma] draft log-normalisers
+  const int32_t* ell;   // [R] or nullptr
+  float inv_temp;
+  float* out;           // [R, gamma]
+  // workspace pieces
+  DeviceStatus* status;
+  void* W1g;            // [round_up_rows(R*gamma), rank] factor rows W1[x_{j-1}] (zero where unused)
+  float* lse_t;         // [R*gamma] target log-normaliser of row j-1 (/T)
+  float* part;          // [npart, R*gamma] partial sums of min(q, p)
+  int npart;
+};
+
 // Launch with programmatic stream serialization (the kernel must call griddep_wait()
 // before its first dependent memory access).
 template <typename... KArgs, typename... Args>
@@ -131,5 +155,9 @@ size_t schedule_smem_bytes(int R, int gamma);
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s);
 cudaError_t launch_residual_tc(const VerifyArgs& a, cudaStream_t s);
 int residual_num_partials(int R, int V, int rank, int dtype_w);
+
+cudaError_t launch_overlap(const OverlapArgs& a, cudaStream_t s);
+cudaError_t launch_overlap_tc(const OverlapArgs& a, cudaStream_t s);
+int overlap_num_partials(int R, int gamma, int V, int rank, int dtype_w);
 
 }  // namespace dspark

@@ -1,0 +1,278 @@
+// overlap.cu — acceptance-overlap diagnostic of a drafted block.
+//
+//   c*_j = sum_v min(q_j(v), p_j(v)) = 1 - ||q_j - p_j||_1 / 2
+//
+// for every drafted position j <= n_r of request r, with q_j = softmax((U_j +
+// W1[x_{j-1}] W2)/T) the draft distribution of position j and p_j = softmax(target row
+// j-1 / T) the target distribution that verifies it.  It is the probability that the
+// draft token of position j is accepted given its prefix: the expectation of
+// min(1, p/q) under q (numb3r33 blog "DSpark: confidence-scheduled speculative
+// decoding", sections "Total variation label" and "Speculative sampling in one
+// picture").  The confidence head is trained against this label; evaluating it on
+// verified rounds measures how well c_j is calibrated.
+//
+//   overlap_prepare   one CTA per flattened position: the factor row W1[x_{j-1}] (the A
+//                     operand of the bias contraction) and lse of target row j-1 / T
+//   bias pass         the bias rows W1[x_{j-1}] W2 for all positions at once, on the
+//                     tensor cores (draft_step_tc_kernel in overlap mode) or on CUDA
+//                     cores (overlap_step_simt below); each CTA writes one partial sum
+//                     of min(q, p) per position
+//   overlap_combine   partial sums -> c*, in a fixed order (deterministic); NaN for the
+//                     positions that are not evaluated
+#include "dspark_common.cuh"
+#include "dspark_internal.h"
+
+namespace dspark {
+
+constexpr int kOvlThreads = 512;
+
+// 8 consecutive entries of a logit row as fp32 (V % 8 == 0: the run is inside the row).
+__device__ __forceinline__ void load8(const void* base, int dtype, size_t idx, float (&x)[8]) {
+  if (dtype == DSPARK_F32) {
+    const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const float*>(base) + idx);
+    const uint4 a = __ldg(src), b = __ldg(src + 1);
+    x[0] = __uint_as_float(a.x); x[1] = __uint_as_float(a.y); x[2] = __uint_as_float(a.z); x[3] = __uint_as_float(a.w);
+    x[4] = __uint_as_float(b.x); x[5] = __uint_as_float(b.y); x[6] = __uint_as_float(b.z); x[7] = __uint_as_float(b.w);
+  } else {
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned short*>(base) + idx));
+    const uint32_t wd[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      x[2 * e] = bf16_bits_to_float(wd[e] & 0xFFFFu);
+      x[2 * e + 1] = bf16_bits_to_float(wd[e] >> 16);
+    }
+  }
+}
+
+// Verify length of request r for this diagnostic: ell[r] clamped to [0, gamma] (gamma
+// without ell).  An out-of-range length is reported by overlap_prepare.
+__device__ __forceinline__ int overlap_len(const OverlapArgs& a, int r) {
+  if (a.ell == nullptr) return a.gamma;
+  return min(max(__ldg(a.ell + r), 0), a.gamma);
+}
+
+__device__ __forceinline__ void online_add(float& m, float& s, float x) {
+  if (x > m) {
+    s = s * __expf(m - x) + 1.f;
+    m = x;
+  } else {
+    s += __expf(x - m);
+  }
+}
+
+__global__ void __launch_bounds__(kOvlThreads) overlap_prepare_kernel(OverlapArgs a) {
+  griddep_allow_next();
+  griddep_wait();
+  const int i = blockIdx.x;
+  const int r = i / a.gamma, j = i % a.gamma + 1;
+  if (a.ell != nullptr && j == 1 && threadIdx.x == 0) {
+    const int l = __ldg(a.ell + r);
+    if (l < 0 || l > a.gamma) report_bad_input(a.status, 31);
+  }
+  const bool valid = j <= overlap_len(a, r);
+  if (threadIdx.x < 32) {
+    // factor row of the position (zero where the position is not evaluated)
+    int xp = 0;
+    if (valid) {
+      const int raw = j == 1 ? __ldg(a.x0 + r) : __ldg(a.x + (size_t)r * a.gamma + (j - 2));
+      xp = checked_token(raw, a.V, a.status, 30);
+    }
+    const size_t src = (size_t)xp * a.rank, dst = (size_t)i * a.rank;
+    if (a.dtype_w == DSPARK_F32) {
+      const float* w1 = reinterpret_cast<const float*>(a.W1);
+      float* g = reinterpret_cast<float*>(a.W1g);
+      for (int c = threadIdx.x; c < a.rank; c += 32) g[dst + c] = valid ? __ldg(w1 + src + c) : 0.f;
+    } else {
+      const unsigned short* w1 = reinterpret_cast<const unsigned short*>(a.W1);
+      unsigned short* g = reinterpret_cast<unsigned short*>(a.W1g);
+      for (int c = threadIdx.x; c < a.rank; c += 32) g[dst + c] = valid ? __ldg(w1 + src + c) : (unsigned short)0;
+    }
+  }
+  if (!valid) {
+    if (threadIdx.x == 0) a.lse_t[i] = NAN;
+    return;  // uniform across the CTA
+  }
+  // log-sum-exp of target row j-1 scaled by 1/T: per-thread online statistics, two
+  // 8-element runs in flight per iteration
+  const size_t trow = ((size_t)r * (a.gamma + 1) + (j - 1)) * (size_t)a.V;
+  float m = -INFINITY, s = 0.f;
+  if (a.V % 8 == 0) {
+    const int step = kOvlThreads * 8;
+    for (int v = threadIdx.x * 8; v < a.V; v += 2 * step) {
+      float x0[8], x1[8];
+      const bool two = v + step < a.V;
+      load8(a.target, a.dtype_t, trow + v, x0);
+      if (two) load8(a.target, a.dtype_t, trow + v + step, x1);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) online_add(m, s, x0[e] * a.inv_temp);
+      if (two) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) online_add(m, s, x1[e] * a.inv_temp);
+      }
+    }
+  } else {
+    for (int v = threadIdx.x; v < a.V; v += kOvlThreads) online_add(m, s, load_elem(a.target, a.dtype_t, trow + v) * a.inv_temp);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    lse_merge(m, s, m2, s2);
+  }
+  __shared__ float wm[kOvlThreads / 32], ws[kOvlThreads / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) {
+    wm[warp] = m;
+    ws[warp] = s;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    m = lane < kOvlThreads / 32 ? wm[lane] : -INFINITY;
+    s = lane < kOvlThreads / 32 ? ws[lane] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+      lse_merge(m, s, m2, s2);
+    }
+    if (lane == 0) a.lse_t[i] = m + logf(s);
+  }
+}
+
+// CUDA-core bias pass (fp32 weights or shapes the tensor-core path does not take).
+// blockIdx.x: vocabulary chunk; blockIdx.y: block of RB flattened positions.
+template <int RB>
+__global__ void __launch_bounds__(kSimtThreads) overlap_step_simt_kernel(OverlapArgs a) {
+  griddep_allow_next();
+  griddep_wait();
+  extern __shared__ float w1s[];  // [RB][rank]
+  const int rows = a.R * a.gamma;
+  const int i0 = blockIdx.y * RB;
+  bool ok[RB];
+  float lq[RB], lt[RB];
+  bool any = false;
+#pragma unroll
+  for (int rr = 0; rr < RB; ++rr) {
+    const int i = i0 + rr;
+    ok[rr] = i < rows && (i % a.gamma) + 1 <= overlap_len(a, i / a.gamma);
+    lq[rr] = ok[rr] ? __ldg(a.lse_q + i) : 0.f;
+    lt[rr] = ok[rr] ? a.lse_t[i] : 0.f;
+    any |= ok[rr];
+  }
+  if (!any) {
+    if (threadIdx.x < RB && i0 + (int)threadIdx.x < rows) a.part[(size_t)blockIdx.x * rows + i0 + threadIdx.x] = 0.f;
+    return;
+  }
+  for (int e = threadIdx.x; e < RB * a.rank; e += blockDim.x) {
+    const int rr = e / a.rank, c = e % a.rank;
+    w1s[e] = ok[rr] ? load_elem(a.W1g, a.dtype_w, (size_t)(i0 + rr) * a.rank + c) : 0.f;
+  }
+  __syncthreads();
+  float sum[RB];
+#pragma unroll
+  for (int rr = 0; rr < RB; ++rr) sum[rr] = 0.f;
+  const int groups_total = (a.V + 3) / 4;
+  const int g0 = blockIdx.x * kSimtGroups * blockDim.x;
+  for (int t = 0; t < kSimtGroups; ++t) {
+    const int g = g0 + t * blockDim.x + threadIdx.x;
+    if (g >= groups_total) break;
+    float acc[RB][4];
+#pragma unroll
+    for (int rr = 0; rr < RB; ++rr)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[rr][e] = 0.f;
+    for (int k = 0; k < a.rank; ++k) {
+      float w2[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int v = 4 * g + e;
+        w2[e] = (v < a.V) ? load_elem(a.W2, a.dtype_w, (size_t)k * a.V + v) : 0.f;
+      }
+#pragma unroll
+      for (int rr = 0; rr < RB; ++rr) {
+        const float w1 = w1s[rr * a.rank + k];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[rr][e] = fmaf(w1, w2[e], acc[rr][e]);
+      }
+    }
+#pragma unroll
+    for (int rr = 0; rr < RB; ++rr) {
+      if (!ok[rr]) continue;
+      const int i = i0 + rr;
+      const int r = i / a.gamma, j = i % a.gamma + 1;
+      const size_t urow = (size_t)i * a.V;
+      const size_t trow = ((size_t)r * (a.gamma + 1) + (j - 1)) * (size_t)a.V;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int v = 4 * g + e;
+        if (v >= a.V) break;
+        const float z = (load_elem(a.U, a.dtype_u, urow + v) + acc[rr][e]) * a.inv_temp;
+        const float lp = load_elem(a.target, a.dtype_t, trow + v) * a.inv_temp - lt[rr];
+        sum[rr] += fminf(__expf(lp), __expf(z - lq[rr]));
+      }
+    }
+  }
+  // block sums per position, added in a fixed order
+  __shared__ float red[kSimtThreads / 32][RB];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int rr = 0; rr < RB; ++rr) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum[rr] += __shfl_xor_sync(0xffffffffu, sum[rr], o);
+    if (lane == 0) red[warp][rr] = sum[rr];
+  }
+  __syncthreads();
+  if (threadIdx.x < RB && i0 + (int)threadIdx.x < rows) {
+    float t = 0.f;
+    for (int w = 0; w < kSimtThreads / 32; ++w) t += red[w][threadIdx.x];
+    a.part[(size_t)blockIdx.x * rows + i0 + threadIdx.x] = t;
+  }
+}
+
+// One warp per flattened position: c* = sum of the npart partial sums.
+__global__ void overlap_combine_kernel(OverlapArgs a, int npart) {
+  griddep_allow_next();
+  griddep_wait();
+  const int rows = a.R * a.gamma;
+  const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (i >= rows) return;
+  const bool ok = (i % a.gamma) + 1 <= overlap_len(a, i / a.gamma);
+  float t = 0.f;
+  if (ok)
+    for (int q = lane; q < npart; q += 32) t += a.part[(size_t)q * rows + i];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+  if (lane == 0) a.out[i] = ok ? t : NAN;
+}
+
+int overlap_num_partials(int R, int gamma, int V, int rank, int dtype_w) {
+  const int simt = simt_num_chunks(V);
+  if (!tc_supported(V, rank, dtype_w)) return simt;
+  const int tc = tc_num_partials(R * gamma);
+  return simt > tc ? simt : tc;
+}
+
+cudaError_t launch_overlap(const OverlapArgs& a, cudaStream_t s) {
+  const int rows = a.R * a.gamma;
+  cudaError_t e = launch_pdl(overlap_prepare_kernel, dim3(rows), dim3(kOvlThreads), 0, s, a);
+  if (e != cudaSuccess) return e;
+  int npart;
+  if (tc_supported(a.V, a.rank, a.dtype_w)) {
+    if ((e = launch_overlap_tc(a, s)) != cudaSuccess) return e;
+    npart = tc_num_partials(rows);
+  } else {
+    dim3 grid(simt_num_chunks(a.V), (rows + kSimtRB - 1) / kSimtRB);
+    const size_t smem = sizeof(float) * kSimtRB * a.rank;
+    if (smem > 48 * 1024) {
+      e = cudaFuncSetAttribute(overlap_step_simt_kernel<kSimtRB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem);
+      if (e != cudaSuccess) return e;
+    }
+    if ((e = launch_pdl(overlap_step_simt_kernel<kSimtRB>, grid, dim3(kSimtThreads), smem, s, a)) != cudaSuccess)
+      return e;
+    npart = (int)grid.x;
+  }
+  if (npart > a.npart) return cudaErrorInvalidValue;
+  return launch_pdl(overlap_combine_kernel, dim3((rows * 32 + 255) / 256), dim3(256), 0, s, a, npart);
+}
+
+}  // namespace dspark

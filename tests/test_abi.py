@@ -161,3 +161,32 @@ def test_schedule_threshold_validation(b):
     for k in range(5):
         assert call(null=(k,)) == 1, k
     assert call(ws=16) == 3
+
+
+def test_acceptance_overlap_validation(b):
+    P = _fake(10)
+    L = b.lib.dspark_acceptance_overlap
+
+    def call(**kw):
+        a = dict(R=4, g=4, V=1024, rank=32, dt=0, T=1.0, ws=1 << 30)
+        a.update(kw)
+        p = list(P)
+        for k in kw.get("null", []):
+            p[k] = None
+        for k in kw.get("misalign", []):
+            p[k] = ctypes.c_void_p(p[k].value + 4)
+        return L(a["R"], a["g"], a["V"], a["rank"], a["dt"], 0, 0, p[0], p[1], p[2], p[3], p[4], p[5], p[6], p[7],
+                 a["T"], p[8], p[9], a["ws"], None)
+
+    assert call(R=0) == 1
+    assert call(g=100) == 2
+    assert call(dt=3) == 1
+    assert call(T=0.0) == 1
+    for k in (0, 1, 2, 3, 4, 5, 6, 8, 9):  # every pointer but ell (optional)
+        assert call(null=[k]) == 1, k
+    for k in (0, 1, 2, 3):
+        assert call(misalign=[k]) == 1, k
+    assert call(ws=100) == 3
+    assert call(null=[7], ws=100) == 3  # a missing ell is allowed: the next check fails
+    assert b.acceptance_overlap_workspace_size(4, 4, 1024, 32, __import__("torch").float32) > 256
+    assert b.acceptance_overlap_workspace_size(0, 4, 1024, 32, __import__("torch").float32) == 0
