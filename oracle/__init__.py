@@ -69,7 +69,14 @@ def _load():
             lib.orc_schedule_threshold.argtypes = [i32, i32, P, f64, P, P, P]
             lib.orc_schedule_threshold.restype = ctypes.c_int
             lib.orc_verify.argtypes = ([i32] * 7 + [P] * 4 + [P, P, P, P, P, f64, P, u64, u64]
-                                       + [P] * 3 + [P] * 4 + [i32])
+                                       + [P] * 3 + [P] * 4 + [P, i32])
+            lib.orc_rnn_cell.argtypes = [i32] * 5 + [P, i32] + [P] * 5 + [ctypes.c_size_t, P]
+            lib.orc_rnn_cell.restype = ctypes.c_int
+            lib.orc_draft_row.argtypes = [i32] * 4 + [P, P, P, f64, u64, u64, u64, u32] + [P] * 5
+            lib.orc_draft_row.restype = ctypes.c_int
+            lib.orc_rnn_draft.argtypes = ([i32] * 9 + [P] * 7 + [P, f64, f64, P, f64, P, P, u64, u64]
+                                          + [P] * 7 + [i32])
+            lib.orc_rnn_draft.restype = ctypes.c_int
             lib.orc_max_threads.restype = i32
             lib.orc_acceptance_overlap.argtypes = [i32] * 7 + [P] * 7 + [f64, P, i32]
             lib.orc_acceptance_overlap.restype = ctypes.c_int
@@ -247,10 +254,11 @@ def schedule_path(conf, sps):
 # ---------------------------------------------------------------------------
 # Stage 3: exact verification
 # ---------------------------------------------------------------------------
-def verify(target, U, W1, W2, x0, x, logq, lse_q, ell, temperature, req_id, seed, rnd, nthreads=0):
+def verify(target, U, W1, W2, x0, x, logq, lse_q, ell, temperature, req_id, seed, rnd, nthreads=0, state=None):
     """min(1,p/q) acceptance, (p-q)+ residual, bonus token (numb3r33 blog "One-token exactness").
 
     target [R,gamma+1,V]; x [R,gamma]; logq, lse_q [R,gamma] (float64 or float32); ell [R].
+    state [R,gamma,rank] (recurrent head): the residual's factor rows (W1 is then unused).
     Returns dict n_acc, tokens [R,gamma+1], n_out, acc_margin, corr_margin, corr_rho, corr_kind.
     """
     lib = _load()
@@ -266,16 +274,91 @@ def verify(target, U, W1, W2, x0, x, logq, lse_q, ell, temperature, req_id, seed
     lse_q = _c(lse_q, np.float64)
     ell = _c(ell, np.int32)
     req_id = _c(req_id, np.int64)
+    st = None if state is None else _c(state, np.float64)
+    rank = W1.shape[1] if st is None else st.shape[2]
     out = dict(n_acc=np.zeros(R, np.int32), tokens=np.zeros((R, gamma + 1), np.int32),
                n_out=np.zeros(R, np.int32), acc_margin=np.zeros((R, gamma)),
                corr_margin=np.zeros(R), corr_rho=np.zeros((R, 2)), corr_kind=np.zeros(R, np.int32))
-    rc = lib.orc_verify(R, gamma, V, W1.shape[1], dt, du, dw, _ptr(target), _ptr(U), _ptr(W1), _ptr(W2),
+    rc = lib.orc_verify(R, gamma, V, rank, dt, du, dw, _ptr(target), _ptr(U), _ptr(W1), _ptr(W2),
                         _ptr(x0), _ptr(x), _ptr(logq), _ptr(lse_q), _ptr(ell), float(temperature),
                         _ptr(req_id), int(seed), int(rnd), _ptr(out["n_acc"]), _ptr(out["tokens"]),
                         _ptr(out["n_out"]), _ptr(out["acc_margin"]), _ptr(out["corr_margin"]),
-                        _ptr(out["corr_rho"]), _ptr(out["corr_kind"]), int(nthreads))
+                        _ptr(out["corr_rho"]), _ptr(out["corr_kind"]), _ptr(st), int(nthreads))
     if rc != 0:
         raise ValueError("oracle verify rejected its arguments")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Stage 1, recurrent head (numb3r33 blog "RNN sequential head"; DSpark 精读 §2)
+# ---------------------------------------------------------------------------
+def rnn_cell(s_prev, x_prev, E, Wse, Wh, bgc, h_row):
+    """One gated state update s = (1-g) s_prev + g tanh(.) on [s_prev; E[x_prev]; h_row],
+    rounded to the weights' storage type.  s_prev float64 [ns] (stored values)."""
+    lib = _load()
+    dw, E = _dtype_code(np.ascontiguousarray(E))
+    _, Wse = _dtype_code(np.ascontiguousarray(Wse))
+    _, Wh = _dtype_code(np.ascontiguousarray(Wh))
+    dh, h_row = _dtype_code(np.ascontiguousarray(h_row))
+    ns = Wse.shape[1] // 2
+    ne = E.shape[1]
+    d = h_row.shape[-1]
+    s_prev = _c(s_prev, np.float64)
+    bgc = _c(bgc, np.float32)
+    out = np.zeros(ns)
+    rc = lib.orc_rnn_cell(ns, ne, d, dw, dh, _ptr(s_prev), int(x_prev), _ptr(E), _ptr(Wse), _ptr(Wh), _ptr(bgc),
+                          _ptr(h_row), 0, _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle rnn_cell rejected its arguments")
+    return out
+
+
+def draft_row(U_row, arow, W2, temperature, seed, req_id, rnd, position):
+    """One draft position given its factor row: (x, lse, logq, runner_up, margin)."""
+    lib = _load()
+    du, U_row = _dtype_code(np.ascontiguousarray(U_row))
+    dw, W2 = _dtype_code(np.ascontiguousarray(W2))
+    arow = _c(arow, np.float64)
+    x = np.zeros(1, np.int32)
+    ru = np.zeros(1, np.int32)
+    lse, logq, mg = np.zeros(1), np.zeros(1), np.zeros(1)
+    lib.orc_draft_row(U_row.shape[-1], arow.shape[0], du, dw, _ptr(U_row), _ptr(arow), _ptr(W2), float(temperature),
+                      int(seed), int(req_id), int(rnd), int(position), _ptr(x), _ptr(lse), _ptr(logq), _ptr(ru),
+                      _ptr(mg))
+    return dict(x=int(x[0]), lse=float(lse[0]), logq=float(logq[0]), runner_up=int(ru[0]), margin=float(mg[0]))
+
+
+def rnn_draft(U, E, Wse, Wh, bgc, Wo, h, conf_w, conf_b, conf_logit_scale, conf_temp, temperature, x0, req_id,
+              seed, rnd, nthreads=0):
+    """Draft loop with the recurrent head.  U [R,gamma,V]; E [V,ne]; Wse [ns+ne,2ns];
+    Wh [d,2ns]; bgc [2ns]; Wo [ns,V]; h [R,gamma,d]; conf_w [d+ns].
+    Returns dict x, logq, lse, conf, state [R,gamma,ns], runner_up, margin."""
+    lib = _load()
+    du, U = _dtype_code(np.ascontiguousarray(U))
+    dw, E = _dtype_code(np.ascontiguousarray(E))
+    _, Wse = _dtype_code(np.ascontiguousarray(Wse))
+    _, Wh = _dtype_code(np.ascontiguousarray(Wh))
+    _, Wo = _dtype_code(np.ascontiguousarray(Wo))
+    dh, h = _dtype_code(np.ascontiguousarray(h))
+    R, gamma, V = U.shape
+    ns = Wse.shape[1] // 2
+    ne = E.shape[1]
+    d = h.shape[2]
+    bgc = _c(bgc, np.float32)
+    conf_w = _c(conf_w, np.float32)
+    conf_temp = _c(conf_temp, np.float32)
+    x0 = _c(x0, np.int32)
+    req_id = _c(req_id, np.int64)
+    out = dict(x=np.zeros((R, gamma), np.int32), logq=np.zeros((R, gamma)), lse=np.zeros((R, gamma)),
+               conf=np.zeros((R, gamma)), state=np.zeros((R, gamma, ns)), runner_up=np.zeros((R, gamma), np.int32),
+               margin=np.zeros((R, gamma)))
+    rc = lib.orc_rnn_draft(R, gamma, V, ns, ne, d, du, dw, dh, _ptr(U), _ptr(E), _ptr(Wse), _ptr(Wh), _ptr(bgc),
+                           _ptr(Wo), _ptr(h), _ptr(conf_w), float(conf_b), float(conf_logit_scale), _ptr(conf_temp),
+                           float(temperature), _ptr(x0), _ptr(req_id), int(seed), int(rnd), _ptr(out["x"]),
+                           _ptr(out["logq"]), _ptr(out["lse"]), _ptr(out["conf"]), _ptr(out["state"]),
+                           _ptr(out["runner_up"]), _ptr(out["margin"]), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rnn_draft rejected its arguments")
     return out
 
 

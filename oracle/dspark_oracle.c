@@ -126,6 +126,17 @@ static void orc_draft_logits(int V, int rank, int dtype_u, int dtype_w, const vo
     for (int v = 0; v < V; ++v) z[v] = (orc_load(U, dtype_u, u_row + v) + z[v]) / temperature;
 }
 
+/* z = (U_row + a W2) / T for an explicit factor row a[rank] (the head's state). */
+static void orc_row_logits(int V, int rank, int dtype_u, int dtype_w, const void* U, size_t u_row,
+                           const double* arow, const void* W2, double temperature, double* z) {
+    for (int v = 0; v < V; ++v) z[v] = 0.0;
+    for (int i = 0; i < rank; ++i) {
+        const double w1 = arow[i];
+        for (int v = 0; v < V; ++v) z[v] += w1 * orc_load(W2, dtype_w, (size_t)i * V + v);
+    }
+    for (int v = 0; v < V; ++v) z[v] = (orc_load(U, dtype_u, u_row + v) + z[v]) / temperature;
+}
+
 static double orc_logsumexp(const double* z, int V) {
     double m = -INFINITY;
     for (int v = 0; v < V; ++v)
@@ -406,14 +417,16 @@ int orc_schedule_path(int R, int gamma, const float* conf, const double* sps, do
  *   tokens = x_1..x_{n_acc}, y;  n_out = n_acc + 1.
  * Diagnostics per request: acc_margin[r*gamma + j-1] = u_j - ratio_j for tested j;
  * corr_margin[r] = Gumbel key margin of the correction draw; corr_rho[r*2 + 0/1] =
- * rho/max(p,q) of winner/runner-up for a residual draw (1 for a bonus draw). */
+ * rho/max(p,q) of winner/runner-up for a residual draw (1 for a bonus draw).
+ * With the recurrent head (state != NULL, [R,gamma,rank] stored states), the residual's
+ * bias row is state[r,j*-1,:] W2 instead of W1[x_{j*-1},:] W2. */
 int orc_verify(int R, int gamma, int V, int rank, int dtype_t, int dtype_u, int dtype_w,
                const void* target, const void* U, const void* W1, const void* W2,
                const int32_t* x0, const int32_t* x, const double* logq, const double* lse_q,
                const int32_t* ell, double temperature, const int64_t* req_id, uint64_t seed,
                uint64_t round, int32_t* n_acc_out, int32_t* tokens_out, int32_t* n_out,
                double* acc_margin, double* corr_margin, double* corr_rho, int32_t* corr_kind,
-               int nthreads) {
+               const double* state, int nthreads) {
     if (R < 0 || gamma < 1 || V < 1 || temperature <= 0.0) return 1;
     for (int r = 0; r < R; ++r)
         if (ell[r] < 0 || ell[r] > gamma) return 1;
@@ -447,7 +460,11 @@ int orc_verify(int R, int gamma, int V, int rank, int dtype_t, int dtype_u, int 
             int js = n_acc + 1;
             int xprev = (js == 1) ? x0[r] : x[(size_t)r * gamma + (js - 2)];
             size_t urow = ((size_t)r * gamma + (js - 1)) * (size_t)V;
-            orc_draft_logits(V, rank, dtype_u, dtype_w, U, urow, W1, W2, xprev, temperature, z);
+            if (state)
+                orc_row_logits(V, rank, dtype_u, dtype_w, U, urow, state + ((size_t)r * gamma + (js - 1)) * rank, W2,
+                               temperature, z);
+            else
+                orc_draft_logits(V, rank, dtype_u, dtype_w, U, urow, W1, W2, xprev, temperature, z);
             double lq = lse_q[(size_t)r * gamma + (js - 1)];
             size_t trow = ((size_t)r * (gamma + 1) + (js - 1)) * (size_t)V;
             for (int v = 0; v < V; ++v) t[v] = orc_load(target, dtype_t, trow + v) / temperature;
@@ -540,6 +557,125 @@ int orc_schedule_many(int nbatch, int R, int gamma, const float* conf, const dou
                               conf_hist ? conf_hist + off : NULL, fixed_len,
                               ell_out + (size_t)b * R, &B, &tau, NULL);
         if (rc) return rc;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Stage 1, RNN variant — recurrent sequential head.                          */
+/* ------------------------------------------------------------------------- */
+/* [EXPL] "RNN sequential head": s_k = f(s_{k-1}, E(x_{k-1}), h_k), z_k = U_k + W_o s_k;
+ * [KB] §2: f concatenates the recurrent state, the previous token's embedding and the
+ * position's backbone hidden state and accumulates the block prefix with a gated
+ * update.  The gate's form is not printed; read as the update-gate cell
+ *   a       = [s_{k-1}; E[x_{k-1}]] Wse + h_k Wh + b          (2*ns pre-activations)
+ *   g       = sigmoid(a[0:ns]),  c = tanh(a[ns:2ns])
+ *   s_k     = (1 - g) * s_{k-1} + g * c
+ * with s_0 = 0.  The state is kept in the weights' storage type (fp32, or bf16 rounded to
+ * nearest-even), so s_k here is the exact cell output rounded once to that type.       */
+static double orc_round_bf16(double v) {
+    if (v == 0.0 || !isfinite(v)) return v;
+    int e;
+    frexp(v, &e);                       /* |v| in [2^(e-1), 2^e) */
+    const double ulp = ldexp(1.0, e - 8); /* 8 significant bits */
+    return rint(v / ulp) * ulp;         /* default rounding: to nearest, ties to even */
+}
+
+static double orc_round_storage(double v, int dtype) {
+    return dtype == ORC_BF16 ? orc_round_bf16(v) : (double)(float)v;
+}
+
+/* One cell update.  s_prev [ns] (stored values), Wse [(ns+ne), 2ns], Wh [d, 2ns]
+ * (dtype_w), bgc [2ns], h row of d elements at h_row (dtype_h) -> s_out [ns]. */
+int orc_rnn_cell(int ns, int ne, int d, int dtype_w, int dtype_h, const double* s_prev, int x_prev,
+                 const void* E, const void* Wse, const void* Wh, const float* bgc, const void* h,
+                 size_t h_row, double* s_out) {
+    if (ns < 1 || ne < 0 || d < 0) return 1;
+    const int n2 = 2 * ns;
+    double* a = (double*)malloc(sizeof(double) * (size_t)n2);
+    for (int c = 0; c < n2; ++c) {
+        double acc = (double)bgc[c];
+        for (int i = 0; i < ns; ++i) acc += s_prev[i] * orc_load(Wse, dtype_w, (size_t)i * n2 + c);
+        for (int i = 0; i < ne; ++i)
+            acc += orc_load(E, dtype_w, (size_t)x_prev * ne + i) * orc_load(Wse, dtype_w, (size_t)(ns + i) * n2 + c);
+        for (int i = 0; i < d; ++i) acc += orc_load(h, dtype_h, h_row + i) * orc_load(Wh, dtype_w, (size_t)i * n2 + c);
+        a[c] = acc;
+    }
+    for (int c = 0; c < ns; ++c) {
+        const double g = orc_sigmoid(a[c]);
+        const double cand = tanh(a[ns + c]);
+        s_out[c] = orc_round_storage((1.0 - g) * s_prev[c] + g * cand, dtype_w);
+    }
+    free(a);
+    return 0;
+}
+
+/* One draft position given its factor row: x = Gumbel-max draw of softmax(z) (stream 0 at
+ * `position`), lse, logq = z_x - lse, and the runner-up / key margin of the draw. */
+int orc_draft_row(int V, int rank, int dtype_u, int dtype_w, const void* U_row, const double* arow,
+                  const void* W2, double temperature, uint64_t seed, uint64_t req_id, uint64_t round,
+                  uint32_t position, int32_t* x_out, double* lse_out, double* logq_out, int32_t* runner_up,
+                  double* margin) {
+    double* z = (double*)malloc(sizeof(double) * (size_t)V);
+    orc_row_logits(V, rank, dtype_u, dtype_w, U_row, 0, arow, W2, temperature, z);
+    const double lse = orc_logsumexp(z, V);
+    int ru = -1;
+    double mg = 0.0;
+    const int x = orc_gumbel_argmax(z, NULL, V, seed, req_id, round, ORC_STREAM_DRAFT, position, &ru, &mg);
+    *x_out = x;
+    *lse_out = lse;
+    *logq_out = z[x] - lse;
+    if (runner_up) *runner_up = ru;
+    if (margin) *margin = mg;
+    free(z);
+    return 0;
+}
+
+/* The draft loop with the recurrent head, per request r (x_0 = anchor, s_0 = 0):
+ *   s_k = cell(s_{k-1}, x_{k-1}, h[r,k-1,:]);  z = (U[r,k-1,:] + s_k W_o) / T;
+ *   x_k, lse_k, logq_k as for the Markov head (stream 0 at position k);
+ *   c_k = sigmoid(kappa (w_h . h[r,k-1,:] + w_s . s_k + b) / T_k)  (the state takes the
+ *   place of the Markov head's factor row in the confidence input).
+ * state_out [R,gamma,ns]: the stored states s_1..s_gamma. */
+int orc_rnn_draft(int R, int gamma, int V, int ns, int ne, int d, int dtype_u, int dtype_w, int dtype_h,
+                  const void* U, const void* E, const void* Wse, const void* Wh, const float* bgc,
+                  const void* Wo, const void* h, const float* conf_w, double conf_b, double conf_logit_scale,
+                  const float* conf_temp, double temperature, const int32_t* x0, const int64_t* req_id,
+                  uint64_t seed, uint64_t round, int32_t* x_out, double* logq_out, double* lse_out,
+                  double* conf_out, double* state_out, int32_t* runner_up_out, double* margin_out,
+                  int nthreads) {
+    if (R < 0 || gamma < 1 || V < 1 || ns < 1 || ne < 0 || d < 0 || temperature <= 0.0) return 1;
+    int nt = orc_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
+    for (int r = 0; r < R; ++r) {
+        double* s = (double*)calloc((size_t)ns, sizeof(double));
+        double* sn = (double*)malloc(sizeof(double) * (size_t)ns);
+        int x_prev = x0[r];
+        for (int k = 1; k <= gamma; ++k) {
+            const size_t row = (size_t)r * gamma + (k - 1);
+            orc_rnn_cell(ns, ne, d, dtype_w, dtype_h, s, x_prev, E, Wse, Wh, bgc, h, row * (size_t)d, sn);
+            memcpy(s, sn, sizeof(double) * (size_t)ns);
+            int32_t xk, ru;
+            double lse, logq, mg;
+            orc_draft_row(V, ns, dtype_u, dtype_w, (const char*)U + row * (size_t)V * (dtype_u == ORC_BF16 ? 2 : 4),
+                          s, Wo, temperature, seed, (uint64_t)req_id[r], round, (uint32_t)k, &xk, &lse, &logq,
+                          &ru, &mg);
+            double s_h = 0.0;
+            for (int i = 0; i < d; ++i) s_h += (double)conf_w[i] * orc_load(h, dtype_h, row * (size_t)d + i);
+            double s_s = 0.0;
+            for (int i = 0; i < ns; ++i) s_s += (double)conf_w[d + i] * s[i];
+            const double logit = conf_logit_scale * (s_h + s_s + conf_b);
+            x_out[row] = xk;
+            logq_out[row] = logq;
+            lse_out[row] = lse;
+            conf_out[row] = orc_sigmoid(logit / (double)conf_temp[k - 1]);
+            if (state_out) memcpy(state_out + row * (size_t)ns, s, sizeof(double) * (size_t)ns);
+            if (runner_up_out) runner_up_out[row] = ru;
+            if (margin_out) margin_out[row] = mg;
+            x_prev = xk;
+        }
+        free(s);
+        free(sn);
     }
     return 0;
 }
