@@ -52,6 +52,9 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--diagnostic", choices=["overlap"], default=None,
+                   help="time the acceptance-overlap diagnostic on the workload's verified positions "
+                        "instead of the round")
     return p.parse_args()
 
 
@@ -234,10 +237,65 @@ def run_reference(args):
     return 0
 
 
+def run_overlap_diagnostic(args):
+    """Times dspark_acceptance_overlap over the verified positions of one round of the
+    workload (one GPU): positions evaluated per second, and the whole call against the
+    HBM roofline.  Algorithmic bytes: the U and target rows of the evaluated positions
+    and W2 once."""
+    import torch
+    from speculative_decoding_draft_03_gb300 import binding as b
+    from speculative_decoding_draft_03_gb300 import workloads as wl
+    dev = torch.device("cuda", 0)
+    w = wl.make(args.workload, device="cuda", seed=0)
+    rd = b.Round(w)
+    d, s, _ = rd.run(rnd=1)
+    torch.cuda.synchronize()
+    R, gamma, V, rank = w["R"], w["gamma"], w["V"], w["rank"]
+    ws = b.workspace(b.acceptance_overlap_workspace_size(R, gamma, V, rank, w["W1"].dtype), dev)
+    out = torch.empty((R, gamma), dtype=torch.float32, device=dev)
+    call = lambda: b.acceptance_overlap(w["target"], w["U"], w["W1"], w["W2"], rd.x0, d["x"], d["lse"], s["ell"],
+                                        w["temperature"], out=out, ws=ws)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    assert b.device_status(ws) == 0
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(0) as clk:
+        for a, e in ev:
+            flush.zero_()
+            a.record(stream)
+            call()
+            e.record(stream)
+        torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(e) for a, e in ev) / args.steps
+    n_pos = int(s["ell"].sum().item())
+    es = lambda t: t.element_size()
+    alg = n_pos * V * (es(w["U"]) + es(w["target"])) + rank * V * es(w["W2"])
+    peaks, peak_kind = measured_peaks()
+    achieved = alg / (ms / 1000.0) / 1e9
+    line = {"metric": "acceptance-overlap positions/s", "value": n_pos / (ms / 1000.0), "unit": "positions/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded generator, random-init weights)",
+            "config": {"workload": WORKLOAD_DESC[args.workload], "positions": n_pos,
+                       "l2": "flushed between calls (256 MiB write outside the timed brackets)"},
+            "roofline": {"kernel": "dspark_acceptance_overlap (prepare + bias pass + combine)", "bound": "hbm",
+                         "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "peak_source": peak_kind, "traffic": None,
+                         "algorithmic_bytes_per_launch": alg},
+            "cpu_baseline": None, "e2e": None, "gpu_launches": 3 * args.steps, "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.diagnostic == "overlap":
+        return run_overlap_diagnostic(args)
     import torch
     import torch.distributed as dist
 

@@ -267,6 +267,59 @@ DSPARK_API dspark_status dspark_verify_static(
     int32_t* n_acc_out, int32_t* tokens_out, int32_t* n_out, void* stream);
 
 /* ------------------------------------------------------------------------------------
+ * Stage 1 with the recurrent (RNN) draft head.
+ *
+ * Defines (numb3r33 blog "DSpark: confidence-scheduled speculative decoding", section "RNN
+ * sequential head": s_k = f(s_{k-1}, E(x_{k-1}), h_k), z_k = U_k + W_o s_k; DSpark 精读
+ * §2: f is a gated update of the concatenated state, previous-token embedding and hidden
+ * state).  The gate is the update-gate cell, for k = 1..gamma (x_0 = x0[r], s_0 = 0):
+ *   a   = [s_{k-1}; E[x_{k-1},:]] Wse + h[r,k,:] Wh + bgc          (2*ns values)
+ *   s_k = (1 - sigmoid(a[0:ns])) * s_{k-1} + sigmoid(a[0:ns]) * tanh(a[ns:2ns])
+ *   s_k is stored in dtype_w (bf16: rounded to nearest even) and used as stored;
+ *   z = (U[r,k,:] + s_k Wo) / T;  x_k, lse_k, logq_k as in dspark_markov_draft
+ *   (Gumbel-max with stream 0 at position k);
+ *   c_k = sigmoid(kappa * (conf_w[0:d] . h[r,k,:] + conf_w[d:d+ns] . s_k + conf_b) / T_k).
+ * Arguments
+ *   ns        state width, a multiple of 32, <= 256 (tensor-core vocabulary pass for bf16
+ *             weights with ns a multiple of 64 and V a multiple of 8, V >= 128).
+ *   ne        embedding width (0..2048); d hidden width (0 allowed).
+ *   U [R,gamma,V] (dtype_u); E [V,ne], Wse [ns+ne, 2*ns] (gate columns first),
+ *   Wh [d, 2*ns], Wo [ns,V] (dtype_w); bgc [2*ns] fp32; h [R,gamma,d] (dtype_h).
+ *   conf_w [d+ns] fp32; conf_b, conf_logit_scale (kappa), conf_temp [gamma]; T > 0.
+ *   x0 [R], req_id [R], seed, round: as in dspark_markov_draft.
+ * Outputs: x_out, logq_out, lse_out, conf_out [R,gamma] as in dspark_markov_draft;
+ *   state_out [R,gamma,ns] (dtype_w): the stored states s_1..s_gamma, which the
+ *   verification of the round needs (dspark_verify_rnn).
+ * Workspace: dspark_rnn_draft_workspace_size().  U, Wo and h 16-byte aligned.
+ * ---------------------------------------------------------------------------------- */
+DSPARK_API size_t dspark_rnn_draft_workspace_size(int R, int gamma, int V, int ns, int d, int dtype_w);
+
+DSPARK_API dspark_status dspark_rnn_draft(
+    int R, int gamma, int V, int ns, int ne, int d, int dtype_u, int dtype_w, int dtype_h,
+    const void* U, const void* E, const void* Wse, const void* Wh, const float* bgc, const void* Wo,
+    const void* h, const float* conf_w, float conf_b, float conf_logit_scale, const float* conf_temp,
+    float temperature, const int32_t* x0, const int64_t* req_id, uint64_t seed, uint64_t round,
+    int32_t* x_out, float* logq_out, float* lse_out, float* conf_out, void* state_out,
+    void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * Stage 3 for a block drafted by the recurrent head.
+ *
+ * dspark_verify with the residual's bias row taken from the drafted state:
+ * z = (U[r,j*,:] + state[r,j*,:] Wo) / T instead of W1[x_{j*-1}] W2.  state [R,gamma,ns]
+ * (dtype_w) is dspark_rnn_draft's state_out; every other argument, result and limit is
+ * dspark_verify's, with rank = ns.  Workspace: dspark_verify_workspace_size(R, gamma, V,
+ * ns, dtype_w).
+ * ---------------------------------------------------------------------------------- */
+DSPARK_API dspark_status dspark_verify_rnn(
+    int R, int gamma, int V, int ns, int dtype_t, int dtype_u, int dtype_w,
+    const void* target, const void* U, const void* state, const void* Wo,
+    const int32_t* x0, const int32_t* x, const float* logq, const float* lse_q,
+    const int32_t* ell, float temperature, const int64_t* req_id, uint64_t seed, uint64_t round,
+    int32_t* n_acc_out, int32_t* tokens_out, int32_t* n_out,
+    void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------
  * Acceptance-overlap diagnostic of a drafted block.
  *
  * Defines (numb3r33 blog "DSpark: confidence-scheduled speculative decoding", sections

@@ -77,6 +77,8 @@ def _load():
             lib.orc_rnn_draft.argtypes = ([i32] * 9 + [P] * 7 + [P, f64, f64, P, f64, P, P, u64, u64]
                                           + [P] * 7 + [i32])
             lib.orc_rnn_draft.restype = ctypes.c_int
+            lib.orc_rnn_confidence.argtypes = [i32] * 5 + [P, P, P, f64, f64, P, P]
+            lib.orc_rnn_confidence.restype = ctypes.c_int
             lib.orc_max_threads.restype = i32
             lib.orc_acceptance_overlap.argtypes = [i32] * 7 + [P] * 7 + [f64, P, i32]
             lib.orc_acceptance_overlap.restype = ctypes.c_int
@@ -264,8 +266,10 @@ def verify(target, U, W1, W2, x0, x, logq, lse_q, ell, temperature, req_id, seed
     lib = _load()
     dt, target = _dtype_code(np.ascontiguousarray(target))
     du, U = _dtype_code(np.ascontiguousarray(U))
-    dw, W1 = _dtype_code(np.ascontiguousarray(W1))
-    _, W2 = _dtype_code(np.ascontiguousarray(W2))
+    dw1, W1 = _dtype_code(np.ascontiguousarray(W1))
+    dw, W2 = _dtype_code(np.ascontiguousarray(W2))
+    if state is None and dw1 != dw:
+        raise TypeError("W1 and W2 must have the same storage type")
     R, g1, V = target.shape
     gamma = g1 - 1
     x0 = _c(x0, np.int32)
@@ -326,6 +330,19 @@ def draft_row(U_row, arow, W2, temperature, seed, req_id, rnd, position):
                       int(seed), int(req_id), int(rnd), int(position), _ptr(x), _ptr(lse), _ptr(logq), _ptr(ru),
                       _ptr(mg))
     return dict(x=int(x[0]), lse=float(lse[0]), logq=float(logq[0]), runner_up=int(ru[0]), margin=float(mg[0]))
+
+
+def rnn_confidence(h, state, conf_w, conf_b, conf_logit_scale, conf_temp):
+    """c[r,k] = sigmoid(kappa (w_h . h[r,k] + w_s . state[r,k] + b) / T_k) for given states."""
+    lib = _load()
+    dh, h = _dtype_code(np.ascontiguousarray(h))
+    state = _c(state, np.float64)
+    R, gamma, d = h.shape
+    ns = state.shape[2]
+    out = np.zeros((R, gamma))
+    lib.orc_rnn_confidence(R, gamma, d, ns, dh, _ptr(h), _ptr(state), _ptr(_c(conf_w, np.float32)), float(conf_b),
+                           float(conf_logit_scale), _ptr(_c(conf_temp, np.float32)), _ptr(out))
+    return out
 
 
 def rnn_draft(U, E, Wse, Wh, bgc, Wo, h, conf_w, conf_b, conf_logit_scale, conf_temp, temperature, x0, req_id,

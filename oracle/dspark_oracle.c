@@ -631,6 +631,22 @@ int orc_draft_row(int V, int rank, int dtype_u, int dtype_w, const void* U_row, 
     return 0;
 }
 
+/* Confidence of the recurrent head for given states: c[r,k] = sigmoid(kappa (w_h .
+ * h[r,k-1,:] + w_s . state[r,k-1,:] + b) / T_k), conf_w = [w_h (d); w_s (ns)]. */
+int orc_rnn_confidence(int R, int gamma, int d, int ns, int dtype_h, const void* h, const double* state,
+                       const float* conf_w, double conf_b, double conf_logit_scale, const float* conf_temp,
+                       double* conf_out) {
+    for (int r = 0; r < R; ++r)
+        for (int k = 1; k <= gamma; ++k) {
+            const size_t row = (size_t)r * gamma + (k - 1);
+            double s_h = 0.0, s_s = 0.0;
+            for (int i = 0; i < d; ++i) s_h += (double)conf_w[i] * orc_load(h, dtype_h, row * (size_t)d + i);
+            for (int i = 0; i < ns; ++i) s_s += (double)conf_w[d + i] * state[row * (size_t)ns + i];
+            conf_out[row] = orc_sigmoid(conf_logit_scale * (s_h + s_s + conf_b) / (double)conf_temp[k - 1]);
+        }
+    return 0;
+}
+
 /* The draft loop with the recurrent head, per request r (x_0 = anchor, s_0 = 0):
  *   s_k = cell(s_{k-1}, x_{k-1}, h[r,k-1,:]);  z = (U[r,k-1,:] + s_k W_o) / T;
  *   x_k, lse_k, logq_k as for the Markov head (stream 0 at position k);

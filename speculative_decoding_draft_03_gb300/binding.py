@@ -56,6 +56,13 @@ def _load_library():
     lib.dspark_acceptance_overlap_workspace_size.argtypes = [i32] * 5
     lib.dspark_acceptance_overlap.argtypes = [i32] * 7 + [P] * 4 + [P] * 4 + [f32, P, P, sz, P]
     lib.dspark_acceptance_overlap.restype = i32
+    lib.dspark_rnn_draft_workspace_size.restype = sz
+    lib.dspark_rnn_draft_workspace_size.argtypes = [i32] * 6
+    lib.dspark_rnn_draft.argtypes = ([i32] * 9 + [P] * 7 + [P, f32, f32, P, f32, P, P, u64, u64] + [P] * 5
+                                     + [P, sz, P])
+    lib.dspark_rnn_draft.restype = i32
+    lib.dspark_verify_rnn.argtypes = ([i32] * 7 + [P] * 4 + [P] * 5 + [f32, P, u64, u64] + [P] * 3 + [P, sz, P])
+    lib.dspark_verify_rnn.restype = i32
     for fn in ("dspark_markov_draft", "dspark_schedule", "dspark_verify", "dspark_workspace_status"):
         getattr(lib, fn).restype = i32
     return lib
@@ -280,6 +287,78 @@ def acceptance_overlap(target, U, W1, W2, x0, x, lse_q, ell, temperature, out=No
     return out
 
 
+def rnn_draft_workspace_size(R, gamma, V, ns, d, w_dtype) -> int:
+    return int(lib.dspark_rnn_draft_workspace_size(R, gamma, V, ns, d, _DT[w_dtype]))
+
+
+def rnn_draft(U, E, Wse, Wh, bgc, Wo, h, conf_w, conf_b, conf_logit_scale, conf_temp, temperature, x0, req_id,
+              seed, rnd, out=None, ws=None, stream=None):
+    """Stage 1 with the recurrent head (dspark_rnn_draft).  Returns dict x, logq, lse, conf,
+    state [R,gamma,ns]."""
+    R, gamma, V = U.shape
+    ns = Wo.shape[0]
+    ne = E.shape[1] if E is not None else 0
+    d = h.shape[2] if h is not None else 0
+    dev = U.device
+    for t, n in ((U, "U"), (Wse, "Wse"), (Wo, "Wo")):
+        _cuda(t, n)
+    if ne:
+        _cuda(E, "E")
+    if d:
+        _cuda(Wh, "Wh")
+        _cuda(h, "h")
+    _cuda(bgc, "bgc", torch.float32)
+    _cuda(conf_w, "conf_w", torch.float32)
+    _cuda(conf_temp, "conf_temp", torch.float32)
+    _cuda(x0, "x0", torch.int32)
+    _cuda(req_id, "req_id", torch.int64)
+    if out is None:
+        out = dict(x=torch.empty((R, gamma), dtype=torch.int32, device=dev),
+                   logq=torch.empty((R, gamma), dtype=torch.float32, device=dev),
+                   lse=torch.empty((R, gamma), dtype=torch.float32, device=dev),
+                   conf=torch.empty((R, gamma), dtype=torch.float32, device=dev),
+                   state=torch.empty((R, gamma, ns), dtype=Wo.dtype, device=dev))
+    if ws is None:
+        ws = workspace(rnn_draft_workspace_size(R, gamma, V, ns, d, Wo.dtype), dev)
+    st = lib.dspark_rnn_draft(R, gamma, V, ns, ne, d, _dt(U, "U"), _dt(Wo, "Wo"), _dt(h, "h") if d else F32,
+                              _p(U), _p(E) if ne else None, _p(Wse), _p(Wh) if d else None, _p(bgc), _p(Wo),
+                              _p(h) if d else None, _p(conf_w), float(conf_b), float(conf_logit_scale),
+                              _p(conf_temp), float(temperature), _p(x0), _p(req_id), int(seed), int(rnd),
+                              _p(out["x"]), _p(out["logq"]), _p(out["lse"]), _p(out["conf"]), _p(out["state"]),
+                              _p(ws), ws.numel(), _stream(stream))
+    _check(st, "dspark_rnn_draft")
+    return out
+
+
+def verify_rnn(target, U, state, Wo, x0, x, logq, lse_q, ell, temperature, req_id, seed, rnd, out=None, ws=None,
+               stream=None):
+    """Stage 3 for a block drafted by the recurrent head (dspark_verify_rnn)."""
+    R, g1, V = target.shape
+    gamma = g1 - 1
+    ns = Wo.shape[0]
+    dev = target.device
+    for t, n in ((target, "target"), (U, "U"), (state, "state"), (Wo, "Wo")):
+        _cuda(t, n)
+    _cuda(x0, "x0", torch.int32)
+    _cuda(x, "x", torch.int32)
+    _cuda(logq, "logq", torch.float32)
+    _cuda(lse_q, "lse_q", torch.float32)
+    _cuda(ell, "ell", torch.int32)
+    _cuda(req_id, "req_id", torch.int64)
+    if out is None:
+        out = dict(n_acc=torch.empty(R, dtype=torch.int32, device=dev),
+                   tokens=torch.empty((R, gamma + 1), dtype=torch.int32, device=dev),
+                   n_out=torch.empty(R, dtype=torch.int32, device=dev))
+    if ws is None:
+        ws = workspace(verify_workspace_size(R, gamma, V, ns, Wo.dtype), dev)
+    st = lib.dspark_verify_rnn(R, gamma, V, ns, _dt(target, "target"), _dt(U, "U"), _dt(Wo, "Wo"), _p(target),
+                               _p(U), _p(state), _p(Wo), _p(x0), _p(x), _p(logq), _p(lse_q), _p(ell),
+                               float(temperature), _p(req_id), int(seed), int(rnd), _p(out["n_acc"]),
+                               _p(out["tokens"]), _p(out["n_out"]), _p(ws), ws.numel(), _stream(stream))
+    _check(st, "dspark_verify_rnn")
+    return out
+
+
 def verify_static(target, U, W1, W2, x0, x, logq, lse_q, ell, temperature, req_id, seed, rnd, out=None,
                   stream=None):
     """Stage 3 through dspark_verify_static: for callers that cannot allocate device
@@ -362,22 +441,38 @@ class Round:
         self.verify_out = dict(n_acc=torch.empty(R, dtype=torch.int32, device=dev),
                                tokens=torch.empty((R, gamma + 1), dtype=torch.int32, device=dev),
                                n_out=torch.empty(R, dtype=torch.int32, device=dev))
-        self.ws_draft = workspace(draft_workspace_size(R, gamma, V, rank, d, w["W1"].dtype), dev)
+        self.rnn = w.get("head") == "rnn"
+        if self.rnn:
+            self.draft_out["state"] = torch.empty((R, gamma, rank), dtype=w["Wo"].dtype, device=dev)
+            self.ws_draft = workspace(rnn_draft_workspace_size(R, gamma, V, rank, d, w["Wo"].dtype), dev)
+        else:
+            self.ws_draft = workspace(draft_workspace_size(R, gamma, V, rank, d, w["W1"].dtype), dev)
         self.ws_sched = workspace(schedule_workspace_size(R, gamma), dev)
-        self.ws_verify = workspace(verify_workspace_size(R, gamma, V, rank, w["W1"].dtype), dev)
+        wdt = w["Wo"].dtype if self.rnn else w["W1"].dtype
+        self.ws_verify = workspace(verify_workspace_size(R, gamma, V, rank, wdt), dev)
         self.x0 = w["x0"].clone()
 
     def run(self, rnd=0, x0=None, stream=None):
         w = self.w
         x0 = self.x0 if x0 is None else x0
-        d = markov_draft(w["U"], w["W1"], w["W2"], w["h"], w["conf_w"], w["conf_b"], w["conf_logit_scale"],
-                         w["conf_temp"], w["temperature"], x0, w["req_id"], w["seed"], rnd,
-                         out=self.draft_out, ws=self.ws_draft, stream=stream)
+        if self.rnn:
+            d = rnn_draft(w["U"], w["E"], w["Wse"], w["Wh"], w["bgc"], w["Wo"], w["h"], w["conf_w"], w["conf_b"],
+                          w["conf_logit_scale"], w["conf_temp"], w["temperature"], x0, w["req_id"], w["seed"], rnd,
+                          out=self.draft_out, ws=self.ws_draft, stream=stream)
+        else:
+            d = markov_draft(w["U"], w["W1"], w["W2"], w["h"], w["conf_w"], w["conf_b"], w["conf_logit_scale"],
+                             w["conf_temp"], w["temperature"], x0, w["req_id"], w["seed"], rnd,
+                             out=self.draft_out, ws=self.ws_draft, stream=stream)
         s = schedule(d["conf"], w["sps"], w["mode"], w.get("conf_hist"), w.get("fixed_len", 0),
                      out=self.sched_out, ws=self.ws_sched, stream=stream)
-        v = verify(w["target"], w["U"], w["W1"], w["W2"], x0, d["x"], d["logq"], d["lse"], s["ell"],
-                   w["temperature"], w["req_id"], w["seed"], rnd, out=self.verify_out, ws=self.ws_verify,
-                   stream=stream)
+        if self.rnn:
+            v = verify_rnn(w["target"], w["U"], d["state"], w["Wo"], x0, d["x"], d["logq"], d["lse"], s["ell"],
+                           w["temperature"], w["req_id"], w["seed"], rnd, out=self.verify_out, ws=self.ws_verify,
+                           stream=stream)
+        else:
+            v = verify(w["target"], w["U"], w["W1"], w["W2"], x0, d["x"], d["logq"], d["lse"], s["ell"],
+                       w["temperature"], w["req_id"], w["seed"], rnd, out=self.verify_out, ws=self.ws_verify,
+                       stream=stream)
         return d, s, v
 
     def capture(self, rnd=0, x0=None, timer=None):

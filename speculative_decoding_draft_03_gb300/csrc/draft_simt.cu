@@ -286,7 +286,8 @@ __global__ void __launch_bounds__(kCombineThreads) draft_combine_kernel(DraftArg
     a.lse_out[row] = lse;
     a.logq_out[row] = b.zsel - lse;
   }
-  if (k < a.gamma) prepare_position_warp(a, r, k + 1, checked_token(b.idx, a.V, a.status, 2), lane);
+  // Markov head: gather position k+1's factor row (the recurrent head's cell does its own)
+  if (k < a.gamma && !a.rnn) prepare_position_warp(a, r, k + 1, checked_token(b.idx, a.V, a.status, 2), lane);
 }
 
 // After the last tensor-core position: one warp per (request, position) merges that

@@ -286,6 +286,7 @@ struct TcParams {
 constexpr int kModeDraft = 0;
 constexpr int kModeResidual = 1;
 constexpr int kModeOverlap = 2;
+constexpr int kModeRnn = 3;
 
 // 8 consecutive ids of U (fp32 or bf16) as fp32; ids at or beyond V read as 0 (V % 8 == 0,
 // so a run of 8 is either entirely inside the row or entirely outside).
@@ -320,9 +321,11 @@ __device__ __forceinline__ void decode_run8(int dtype, const uint4 (&raw)[2], fl
 }
 
 // RB: requests per block (32, 64 or 128); the 128 MMA rows hold 128/RB copies of it.
-// MODE: kModeDraft (one draft position for every request), kModeResidual (the
-// rejected position j* of each request that has one) or kModeOverlap (every drafted
-// position: sum_v min(q, p), the expected acceptance).
+// MODE: kModeDraft (one draft position for every request; the factor rows W1[x_{k-1}]
+// are gathered by the epilogue), kModeRnn (one draft position with the factor rows
+// given: the recurrent head's states), kModeResidual (the rejected position j* of each
+// request that has one) or kModeOverlap (every drafted position: sum_v min(q, p), the
+// expected acceptance).
 template <int RB, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     draft_step_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
@@ -334,6 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   using SM = Smem<RB>;
   constexpr int kStages = SM::stages;
+  // draft positions: U through the TMA ring, online softmax + Gumbel-max, winners published
+  constexpr bool kDraftMath = MODE == kModeDraft || MODE == kModeRnn;
   const int rb = blockIdx.x % p.rblocks;      // request block of this CTA
   const int group = blockIdx.x / p.rblocks;   // vocabulary-tile group
   const int katoms = p.rank / kKAtom;
@@ -474,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------ U producer (draft mode) -------------------
     // U is an input of the round: its boxes stream ahead of the epilogue through a
     // ring of n_uboxes slots, read once (evict-first in L2).
-    if (MODE == kModeDraft && lane == 0) {
+    if (kDraftMath && lane == 0) {
       const uint64_t u_policy = policy_evict_first();
       const int total = my_tiles * uboxes_per_tile;
       for (int i = 0; i < total && !*abort_flag; ++i) {
@@ -529,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float ovl = 0.f;           // overlap only: this thread's sum of min(q, p)
     const PhiloxRow prow =
         philox_row(rng_row(p.seed, (MODE != kModeOverlap && valid) ? __ldg(p.req_id + r) : 0, p.round,
-                           MODE == kModeDraft ? kStreamDraft : kStreamCorrect, (uint32_t)pos));
+                           kDraftMath ? kStreamDraft : kStreamCorrect, (uint32_t)pos));
     const size_t urow = MODE == kModeOverlap
                             ? (size_t)(valid ? r : 0) * (size_t)p.V
                             : ((size_t)(valid ? r : 0) * p.gamma + (valid ? pos - 1 : 0)) * (size_t)p.V;
@@ -551,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int box_col = col0 % p.ubox_cols;
     const int box_row = row0 + lane;
     const bool u_f32 = p.dtype_u == DSPARK_F32;
-    if constexpr (MODE != kModeDraft) load_u(0, unext);
+    if constexpr (!kDraftMath) load_u(0, unext);
     // the predecessor still reads the partial records this kernel overwrites at the end
     if constexpr (MODE == kModeDraft) {
       griddep_wait();
@@ -617,11 +622,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int vt = (group + t * p.ngroups) * kN;
       // the published bound is read a tile ahead of its use, so that its latency hides
       // behind this tile's work
-      const int hint_pref = (MODE == kModeDraft && valid) ? __ldcg(p.hint + r) : 0;
+      const int hint_pref = (kDraftMath && valid) ? __ldcg(p.hint + r) : 0;
       uint4 ucur[kPass][2];
       int uslot = 0;
       bool u_ready = true;
-      if constexpr (MODE != kModeDraft) {
+      if constexpr (!kDraftMath) {
 #pragma unroll
         for (int ps = 0; ps < kPass; ++ps) {
           ucur[ps][0] = unext[ps][0];
@@ -675,7 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         decode_run8(p.dtype_u, ucur[ps], z);
 #pragma unroll
         for (int i = 0; i < kCols; ++i) z[i] = (z[i] + bias[i]) * p.inv_temp;
-        if constexpr (MODE == kModeDraft) {
+        if constexpr (kDraftMath) {
           float cmax = z[0];
           int imax = 0;
 #pragma unroll
@@ -807,7 +812,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if constexpr (MODE == kModeDraft) {
+      if constexpr (kDraftMath) {
         // After the first tiles, publish the CTA's best key per request (one atomic per
         // request per CTA), so that CTAs still streaming can skip more of their draws.
         if (t < publish_tiles<RB>()) {
@@ -851,7 +856,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
 #pragma unroll
-    for (int which = 0; which < (MODE == kModeDraft ? 1 : (MODE == kModeResidual ? 2 : 0)); ++which) {
+    for (int which = 0; which < (kDraftMath ? 1 : (MODE == kModeResidual ? 2 : 0)); ++which) {
       red[ew * 32 + lane] = to_partial(which ? fb : st);
       asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
       if (et < RB) {
@@ -866,7 +871,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // draft: this CTA's winner for the request, as one 64-bit maximum (key code in the
         // high half, sign-flipped so that the order is unsigned; ~id in the low half, so the
         // lowest id wins equal keys)
-        if (MODE == kModeDraft && rr < p.R && m.idx >= 0) {
+        if (kDraftMath && rr < p.R && m.idx >= 0) {
           const unsigned long long packed =
               ((unsigned long long)((uint32_t)ordered_key(m.key) ^ 0x80000000u) << 32) | (uint32_t)~(uint32_t)m.idx;
           atomicMax(p.win + rr, packed);
@@ -983,7 +988,7 @@ static cudaError_t launch(TcParams p, const void* W1g, const void* W2, cudaStrea
     return cudaErrorInvalidValue;
   if (!make_map_2d(&map_b, W2, (uint64_t)p.V, (uint64_t)p.rank, 64, kKAtom)) return cudaErrorInvalidValue;
   p.ubox_cols = p.dtype_u == DSPARK_F32 ? 32 : 64;
-  if (MODE == kModeDraft) {
+  if (MODE == kModeDraft || MODE == kModeRnn) {
     if (!make_map_u(&map_u, p.U, p.dtype_u, (uint64_t)p.V, (uint64_t)p.gamma, (uint64_t)p.R, (uint32_t)p.Rb))
       return cudaErrorInvalidValue;
   } else {
@@ -1016,6 +1021,17 @@ cudaError_t launch_draft_step_tc(const DraftArgs& a, int k, cudaStream_t s) {
   p.conf_b = a.conf_b;
   p.conf_scale = a.conf_scale;
   return tc::launch<tc::kModeDraft>(p, a.W1g, a.W2, s);
+}
+
+// Recurrent head: position k with the factor rows (the states s_k) already in a.W1g.
+cudaError_t launch_rnn_step_tc(const DraftArgs& a, int k, cudaStream_t s) {
+  tc::TcParams p = tc::base_params(a.R, a.gamma, a.V, a.rank, a.dtype_u, a.inv_temp, a.U, a.req_id, a.seed,
+                                   a.round, a.status);
+  p.k = k;
+  p.partials = a.partials + (size_t)(k - 1) * tc_num_partials(a.R) * a.R;
+  p.hint = a.hint + (size_t)(k - 1) * a.R;
+  p.win = a.win + (size_t)(k - 1) * a.R;
+  return tc::launch<tc::kModeRnn>(p, a.W1g, a.W2, s);
 }
 
 cudaError_t launch_overlap_tc(const OverlapArgs& a, cudaStream_t s) {

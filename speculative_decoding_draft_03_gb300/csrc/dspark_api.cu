@@ -57,6 +57,21 @@ DraftLayout draft_layout(int R, int gamma, int V, int rank, int dtype_w) {
   return L;
 }
 
+struct RnnLayout {
+  DraftLayout draft;
+  size_t hpart, total;
+  int nsplit;
+};
+
+RnnLayout rnn_layout(int R, int gamma, int V, int ns, int d, int dtype_w) {
+  RnnLayout L;
+  L.draft = draft_layout(R, gamma, V, ns, dtype_w);
+  L.nsplit = dspark::rnn_num_splits(d);
+  L.hpart = L.draft.total;
+  L.total = L.hpart + dspark::align256(sizeof(float) * (size_t)L.nsplit * R * gamma * 2 * ns);
+  return L;
+}
+
 struct VerifyLayout {
   size_t counters, row_req, row_t, row_base, row_order, row_part, lse_t, jstar, res_list, W1g, res_part, res_part2,
       total;
@@ -243,7 +258,7 @@ dspark_status dspark_markov_draft(int R, int gamma, int V, int rank, int d, int 
     return fail(DSPARK_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, L.total);
 
   unsigned char* ws = static_cast<unsigned char*>(workspace);
-  dspark::DraftArgs a;
+  dspark::DraftArgs a = {};
   a.R = R; a.gamma = gamma; a.V = V; a.rank = rank; a.d = d;
   a.dtype_u = dtype_u; a.dtype_w = dtype_w; a.dtype_h = dtype_h;
   a.U = U; a.W1 = W1; a.W2 = W2; a.h = h;
@@ -357,7 +372,8 @@ size_t dspark_verify_workspace_size(int R, int gamma, int V, int rank, int dtype
 // dspark_verify and dspark_verify_ragged: t_off == nullptr selects the padded target.
 static dspark_status verify_impl(int R, int gamma, int V, int rank, int dtype_t, int dtype_u, int dtype_w,
                                  const void* target, const int32_t* t_off, int n_trows, const void* U,
-                                 const void* W1, const void* W2, const int32_t* x0, const int32_t* x,
+                                 const void* W1, const void* state, const void* W2, const int32_t* x0,
+                                 const int32_t* x,
                                  const float* logq, const float* lse_q, const int32_t* ell, float temperature,
                                  const int64_t* req_id, uint64_t seed, uint64_t round, int32_t* n_acc_out,
                                  int32_t* tokens_out, int32_t* n_out, void* workspace, size_t ws_bytes,
@@ -373,7 +389,7 @@ static dspark_status verify_impl(int R, int gamma, int V, int rank, int dtype_t,
     return fail(DSPARK_INVALID_ARG, "temperature must be finite and > 0");
   CHECK_PTR(target);
   CHECK_PTR(U);
-  CHECK_PTR(W1);
+  if (state == nullptr) CHECK_PTR(W1);
   CHECK_PTR(W2);
   CHECK_PTR(x0);
   CHECK_PTR(x);
@@ -387,16 +403,16 @@ static dspark_status verify_impl(int R, int gamma, int V, int rank, int dtype_t,
   CHECK_PTR(workspace);
   CHECK_ALIGN16(target);
   CHECK_ALIGN16(U);
-  CHECK_ALIGN16(W1);
+  if (state == nullptr) CHECK_ALIGN16(W1);
   CHECK_ALIGN16(W2);
   if (!aligned256(workspace)) return fail(DSPARK_INVALID_ARG, "workspace must be 256-byte aligned");
   const VerifyLayout L = verify_layout(R, gamma, V, rank, dtype_w);
   if (ws_bytes < L.total) return fail(DSPARK_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, L.total);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
-  dspark::VerifyArgs a;
+  dspark::VerifyArgs a = {};
   a.R = R; a.gamma = gamma; a.V = V; a.rank = rank;
   a.dtype_t = dtype_t; a.dtype_u = dtype_u; a.dtype_w = dtype_w;
-  a.target = target; a.U = U; a.W1 = W1; a.W2 = W2;
+  a.target = target; a.U = U; a.W1 = W1; a.W2 = W2; a.state = state;
   a.t_off = t_off; a.n_trows = n_trows;
   a.x0 = x0; a.x = x; a.logq = logq; a.lse_q = lse_q; a.ell = ell;
   a.inv_temp = 1.0f / temperature;
@@ -432,9 +448,9 @@ dspark_status dspark_verify(int R, int gamma, int V, int rank, int dtype_t, int 
                             float temperature, const int64_t* req_id, uint64_t seed, uint64_t round,
                             int32_t* n_acc_out, int32_t* tokens_out, int32_t* n_out, void* workspace,
                             size_t ws_bytes, void* stream) {
-  return verify_impl(R, gamma, V, rank, dtype_t, dtype_u, dtype_w, target, nullptr, 0, U, W1, W2, x0, x, logq,
-                     lse_q, ell, temperature, req_id, seed, round, n_acc_out, tokens_out, n_out, workspace, ws_bytes,
-                     stream);
+  return verify_impl(R, gamma, V, rank, dtype_t, dtype_u, dtype_w, target, nullptr, 0, U, W1, nullptr, W2, x0, x,
+                     logq, lse_q, ell, temperature, req_id, seed, round, n_acc_out, tokens_out, n_out, workspace,
+                     ws_bytes, stream);
 }
 
 dspark_status dspark_verify_ragged(int R, int gamma, int V, int rank, int dtype_t, int dtype_u, int dtype_w,
@@ -447,8 +463,8 @@ dspark_status dspark_verify_ragged(int R, int gamma, int V, int rank, int dtype_
   if (n_target_rows < 1) return fail(DSPARK_INVALID_ARG, "n_target_rows must be positive (%d)", n_target_rows);
   CHECK_PTR(target_row_offset);
   return verify_impl(R, gamma, V, rank, dtype_t, dtype_u, dtype_w, target, target_row_offset, n_target_rows, U, W1,
-                     W2, x0, x, logq, lse_q, ell, temperature, req_id, seed, round, n_acc_out, tokens_out, n_out,
-                     workspace, ws_bytes, stream);
+                     nullptr, W2, x0, x, logq, lse_q, ell, temperature, req_id, seed, round, n_acc_out, tokens_out,
+                     n_out, workspace, ws_bytes, stream);
 }
 
 size_t dspark_acceptance_overlap_workspace_size(int R, int gamma, int V, int rank, int dtype_w) {
@@ -492,7 +508,7 @@ dspark_status dspark_acceptance_overlap(int R, int gamma, int V, int rank, int d
   const OverlapLayout L = overlap_layout(R, gamma, V, rank, dtype_w);
   if (ws_bytes < L.total) return fail(DSPARK_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, L.total);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
-  dspark::OverlapArgs a;
+  dspark::OverlapArgs a = {};
   a.R = R; a.gamma = gamma; a.V = V; a.rank = rank;
   a.dtype_t = dtype_t; a.dtype_u = dtype_u; a.dtype_w = dtype_w;
   a.target = target; a.U = U; a.W1 = W1; a.W2 = W2;
@@ -507,6 +523,118 @@ dspark_status dspark_acceptance_overlap(int R, int gamma, int V, int rank, int d
   cudaError_t e = dspark::launch_overlap(a, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "acceptance_overlap");
   return DSPARK_OK;
+}
+
+size_t dspark_rnn_draft_workspace_size(int R, int gamma, int V, int ns, int d, int dtype_w) {
+  if (R < 1 || gamma < 1 || V < 1 || ns < 1 || d < 0) return 0;
+  return rnn_layout(R, gamma, V, ns, d, dtype_w).total;
+}
+
+dspark_status dspark_rnn_draft(int R, int gamma, int V, int ns, int ne, int d, int dtype_u, int dtype_w, int dtype_h,
+                               const void* U, const void* E, const void* Wse, const void* Wh, const float* bgc,
+                               const void* Wo, const void* h, const float* conf_w, float conf_b,
+                               float conf_logit_scale, const float* conf_temp, float temperature, const int32_t* x0,
+                               const int64_t* req_id, uint64_t seed, uint64_t round, int32_t* x_out,
+                               float* logq_out, float* lse_out, float* conf_out, void* state_out, void* workspace,
+                               size_t ws_bytes, void* stream) {
+  if (R < 1 || gamma < 1 || V < 1 || ns < 1 || ne < 0 || d < 0)
+    return fail(DSPARK_INVALID_ARG, "sizes must be positive (R=%d gamma=%d V=%d ns=%d ne=%d d=%d)", R, gamma, V, ns,
+                ne, d);
+  if (gamma > kMaxGamma) return fail(DSPARK_UNSUPPORTED_SHAPE, "gamma=%d exceeds %d", gamma, kMaxGamma);
+  if ((long long)V > (1ll << 30)) return fail(DSPARK_UNSUPPORTED_SHAPE, "V=%d too large", V);
+  if ((long long)R * gamma > (1ll << 24)) return fail(DSPARK_UNSUPPORTED_SHAPE, "R*gamma too large");
+  if (ns % 32 != 0 || ns > 256) return fail(DSPARK_UNSUPPORTED_SHAPE, "ns=%d must be a multiple of 32, <= 256", ns);
+  if (ne > 2048) return fail(DSPARK_UNSUPPORTED_SHAPE, "ne=%d exceeds 2048", ne);
+  if (!valid_dtype(dtype_u) || !valid_dtype(dtype_w) || !valid_dtype(dtype_h))
+    return fail(DSPARK_INVALID_ARG, "dtype codes must be DSPARK_F32 or DSPARK_BF16");
+  if (!(temperature > 0.f) || !isfinite(temperature))
+    return fail(DSPARK_INVALID_ARG, "temperature must be finite and > 0");
+  CHECK_PTR(U);
+  if (ne > 0) CHECK_PTR(E);
+  CHECK_PTR(Wse);
+  if (d > 0) CHECK_PTR(Wh);
+  CHECK_PTR(bgc);
+  CHECK_PTR(Wo);
+  if (d > 0) CHECK_PTR(h);
+  CHECK_PTR(conf_w);
+  CHECK_PTR(conf_temp);
+  CHECK_PTR(x0);
+  CHECK_PTR(req_id);
+  CHECK_PTR(x_out);
+  CHECK_PTR(logq_out);
+  CHECK_PTR(lse_out);
+  CHECK_PTR(conf_out);
+  CHECK_PTR(state_out);
+  CHECK_PTR(workspace);
+  CHECK_ALIGN16(U);
+  CHECK_ALIGN16(Wo);
+  if (d > 0) CHECK_ALIGN16(h);
+  if (!aligned256(workspace)) return fail(DSPARK_INVALID_ARG, "workspace must be 256-byte aligned");
+  const RnnLayout L = rnn_layout(R, gamma, V, ns, d, dtype_w);
+  if (ws_bytes < L.total) return fail(DSPARK_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, L.total);
+
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  dspark::DraftArgs a = {};
+  a.R = R; a.gamma = gamma; a.V = V; a.rank = ns; a.d = d;
+  a.dtype_u = dtype_u; a.dtype_w = dtype_w; a.dtype_h = dtype_h;
+  a.U = U; a.W1 = nullptr; a.W2 = Wo; a.h = h;
+  a.conf_w = conf_w; a.conf_b = conf_b; a.conf_scale = conf_logit_scale; a.conf_temp = conf_temp;
+  a.inv_temp = 1.0f / temperature;
+  a.x0 = x0; a.req_id = req_id; a.seed = seed; a.round = round;
+  a.x_out = x_out; a.logq_out = logq_out; a.lse_out = lse_out; a.conf_out = conf_out;
+  a.status = reinterpret_cast<dspark::DeviceStatus*>(ws);
+  a.s_h = reinterpret_cast<float*>(ws + L.draft.s_h);
+  a.W1g = ws + L.draft.W1g;
+  a.partials = reinterpret_cast<dspark::Partial*>(ws + L.draft.partials);
+  a.hint = reinterpret_cast<int*>(ws + L.draft.hint);
+  a.win = reinterpret_cast<unsigned long long*>(ws + L.draft.win);
+  a.rnn = 1;
+  a.ne = ne; a.E = E; a.Wse = Wse; a.Wh = Wh; a.bgc = bgc;
+  a.state_out = state_out;
+  a.hpart = reinterpret_cast<float*>(ws + L.hpart);
+  a.nsplit = L.nsplit;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (d > 0) {
+    if ((e = dspark::launch_conf_hdot(a, s)) != cudaSuccess) return cuda_fail(e, "conf_hdot");
+    if ((e = dspark::launch_rnn_hproj(a, s)) != cudaSuccess) return cuda_fail(e, "rnn_hproj");
+  } else {
+    if ((e = cudaMemsetAsync(a.s_h, 0, sizeof(float) * (size_t)R * gamma, s)) != cudaSuccess)
+      return cuda_fail(e, "s_h clear");
+  }
+  const bool tc = dspark::tc_supported(V, ns, dtype_w) != 0;
+  for (int k = 1; k <= gamma; ++k) {
+    if ((e = dspark::launch_rnn_cell(a, k, tc, s)) != cudaSuccess) return cuda_fail(e, "rnn_cell");
+    const bool prof = 2 * k <= g_prof_n;
+    if (prof && (e = record_profile_event(g_prof_events[2 * (k - 1)], s)) != cudaSuccess)
+      return cuda_fail(e, "profile event");
+    if (tc) {
+      if ((e = dspark::launch_rnn_step_tc(a, k, s)) != cudaSuccess) return cuda_fail(e, "rnn_step_tc");
+    } else {
+      if ((e = dspark::launch_draft_step_simt(a, k, s)) != cudaSuccess) return cuda_fail(e, "draft_step_simt");
+    }
+    if (prof && (e = record_profile_event(g_prof_events[2 * (k - 1) + 1], s)) != cudaSuccess)
+      return cuda_fail(e, "profile event");
+    if (!tc && (e = dspark::launch_draft_combine(a, k, dspark::simt_num_chunks(V), s)) != cudaSuccess)
+      return cuda_fail(e, "draft_combine");
+  }
+  if (tc && (e = dspark::launch_draft_finalize(a, dspark::tc_num_partials(R), s)) != cudaSuccess)
+    return cuda_fail(e, "draft_finalize");
+  if ((e = dspark::launch_rnn_conf(a, s)) != cudaSuccess) return cuda_fail(e, "rnn_conf");
+  return DSPARK_OK;
+}
+
+dspark_status dspark_verify_rnn(int R, int gamma, int V, int ns, int dtype_t, int dtype_u, int dtype_w,
+                                const void* target, const void* U, const void* state, const void* Wo,
+                                const int32_t* x0, const int32_t* x, const float* logq, const float* lse_q,
+                                const int32_t* ell, float temperature, const int64_t* req_id, uint64_t seed,
+                                uint64_t round, int32_t* n_acc_out, int32_t* tokens_out, int32_t* n_out,
+                                void* workspace, size_t ws_bytes, void* stream) {
+  CHECK_PTR(state);
+  return verify_impl(R, gamma, V, ns, dtype_t, dtype_u, dtype_w, target, nullptr, 0, U, nullptr, state, Wo, x0, x,
+                     logq, lse_q, ell, temperature, req_id, seed, round, n_acc_out, tokens_out, n_out, workspace,
+                     ws_bytes, stream);
 }
 
 }  // extern "C"

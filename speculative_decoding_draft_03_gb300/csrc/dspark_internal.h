@@ -41,6 +41,17 @@ struct DraftArgs {
   Partial* partials; // [gamma, npart, R] (the CUDA-core path uses the first [npart, R])
   int* hint;         // [gamma, R] best Gumbel key published so far per position (ordered int)
   unsigned long long* win;  // [gamma, R] tensor-core path: (key code, ~id) maximum per position
+  // recurrent head (rnn != 0; rank is the state width ns, W1 is unused): the factor row of
+  // position k is the state s_k, written by the cell kernel into W1g and state_out
+  int rnn;
+  int ne;              // embedding width
+  const void* E;       // [V, ne]
+  const void* Wse;     // [ns+ne, 2ns]: gate columns, then candidate columns
+  const void* Wh;      // [d, 2ns]
+  const float* bgc;    // [2ns]
+  void* state_out;     // [R, gamma, ns] (dtype_w)
+  float* hpart;        // [nsplit, R*gamma, 2ns] split-K partial sums of h Wh
+  int nsplit;
 };
 
 struct VerifyArgs {
@@ -79,6 +90,7 @@ struct VerifyArgs {
   int* res_list;      // [R] requests that need a residual draw
   int* n_res;         // [1]
   void* W1g;          // [Rpad, rank] gathered factor rows of the residual positions
+  const void* state;  // recurrent head: [R, gamma, rank] states, the factor rows (nullptr: W1[x_{j-1}])
   Partial* res_part;  // [npart, R] residual partials: key = ln rho + g
   Partial* res_part2; // [npart, R] fallback partials: key = ln p + g
 };
@@ -142,6 +154,13 @@ cudaError_t launch_draft_prepare(const DraftArgs& a, int k, cudaStream_t s);
 cudaError_t launch_draft_step_simt(const DraftArgs& a, int k, cudaStream_t s);
 cudaError_t launch_draft_combine(const DraftArgs& a, int k, int npart, cudaStream_t s);
 cudaError_t launch_draft_step_tc(const DraftArgs& a, int k, cudaStream_t s);
+cudaError_t launch_rnn_step_tc(const DraftArgs& a, int k, cudaStream_t s);
+// Recurrent head: h Wh for every position (before the loop), the cell of position k
+// (after position k-1's draw), and the confidences from the states (after the loop).
+int rnn_num_splits(int d);
+cudaError_t launch_rnn_hproj(const DraftArgs& a, cudaStream_t s);
+cudaError_t launch_rnn_cell(const DraftArgs& a, int k, bool tc, cudaStream_t s);
+cudaError_t launch_rnn_conf(const DraftArgs& a, cudaStream_t s);
 // After the last tensor-core position: every position's partial records -> x, lse, logq.
 cudaError_t launch_draft_finalize(const DraftArgs& a, int npart, cudaStream_t s);
 

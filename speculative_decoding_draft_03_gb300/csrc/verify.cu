@@ -413,16 +413,24 @@ __global__ void verify_accept_kernel(VerifyArgs a) {
       const int slot = atomicAdd(a.n_res, 1);
       a.res_list[slot] = r;
     }
-    // gather W1[x_{j*-1}] for the bias recomputation
-    const int xprev = checked_token((js == 1) ? __ldg(a.x0 + r) : __ldg(a.x + (size_t)r * a.gamma + (js - 2)),
-                                    a.V, a.status, 12);
-    const size_t src = (size_t)xprev * a.rank, dst = (size_t)r * a.rank;
+    // gather the factor row of position j* for the bias recomputation: W1[x_{j*-1}], or
+    // the recurrent head's state s_{j*}
+    size_t src;
+    const void* rows = a.state != nullptr ? a.state : a.W1;
+    if (a.state != nullptr) {
+      src = ((size_t)r * a.gamma + (js - 1)) * a.rank;
+    } else {
+      const int xprev = checked_token((js == 1) ? __ldg(a.x0 + r) : __ldg(a.x + (size_t)r * a.gamma + (js - 2)),
+                                      a.V, a.status, 12);
+      src = (size_t)xprev * a.rank;
+    }
+    const size_t dst = (size_t)r * a.rank;
     if (a.dtype_w == DSPARK_BF16) {
-      const unsigned short* w1 = reinterpret_cast<const unsigned short*>(a.W1);
+      const unsigned short* w1 = reinterpret_cast<const unsigned short*>(rows);
       unsigned short* g = reinterpret_cast<unsigned short*>(a.W1g);
       for (int i = lane; i < a.rank; i += 32) g[dst + i] = __ldg(w1 + src + i);
     } else {
-      const float* w1 = reinterpret_cast<const float*>(a.W1);
+      const float* w1 = reinterpret_cast<const float*>(rows);
       float* g = reinterpret_cast<float*>(a.W1g);
       for (int i = lane; i < a.rank; i += 32) g[dst + i] = __ldg(w1 + src + i);
     }

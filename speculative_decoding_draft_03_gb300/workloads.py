@@ -28,6 +28,8 @@ Recipes (the five workloads of the draft/schedule/verify path):
                   S0*(1-0.2*B/2048) up to B=2048, half that value just past it, then
                   falling as 1/B; early-stop scheduler; 100 chained rounds.
 
+Any workload can be drafted by the recurrent head instead (``add_rnn_head``).
+
 All workloads: anchor x0 ~ U[0,V), request ids 0..R-1, sampling seed 0, T = 1, STS
 temperatures 1, confidence bias 0.  Each tensor has its own torch.Generator seed, so a
 workload is reproducible on a given device type.
@@ -177,6 +179,30 @@ def make(name: str, device="cpu", seed: int = 0, **override) -> dict:
         out["conf_hist"] = torch.sigmoid(sh.kappa * z).to(torch.float32)
     else:
         out["conf_hist"] = None
+    return out
+
+
+def add_rnn_head(w: dict, seed: int = 0) -> dict:
+    """The same workload drafted by the recurrent head: state width ns = rank, embedding
+    width ne = rank, weights in the workload's weight type.  E ~ N(0,1);
+    Wse ~ N(0, 1/(ns+ne)); Wh ~ N(0, 0.25/d); gate bias -1 (the gate starts mostly
+    shut), candidate bias 0; Wo ~ N(0, 0.02^2) like the Markov factors.  The confidence
+    weights' last ns entries apply to the state.  W1/W2 are dropped."""
+    dev = w["U"].device
+    wdt = w["W1"].dtype
+    ns = ne = w["rank"]
+    V, d = w["V"], w["d"]
+    base = 1000 * (seed + 1) + 20
+    out = dict(w)
+    out.pop("W1")
+    out.pop("W2")
+    out["head"] = "rnn"
+    out["ns"], out["ne"] = ns, ne
+    out["E"] = _normal((V, ne), 1.0, base + 1, dev, wdt)
+    out["Wse"] = _normal((ns + ne, 2 * ns), 1.0 / math.sqrt(ns + ne), base + 2, dev, wdt)
+    out["Wh"] = _normal((d, 2 * ns), 0.5 / math.sqrt(max(d, 1)), base + 3, dev, wdt)
+    out["bgc"] = torch.cat([torch.full((ns,), -1.0, device=dev), torch.zeros(ns, device=dev)])
+    out["Wo"] = _normal((ns, V), 0.02, base + 4, dev, wdt)
     return out
 
 

@@ -190,3 +190,57 @@ def test_acceptance_overlap_validation(b):
     assert call(null=[7], ws=100) == 3  # a missing ell is allowed: the next check fails
     assert b.acceptance_overlap_workspace_size(4, 4, 1024, 32, __import__("torch").float32) > 256
     assert b.acceptance_overlap_workspace_size(0, 4, 1024, 32, __import__("torch").float32) == 0
+
+
+def test_rnn_draft_validation(b):
+    P = _fake(22)
+    L = b.lib.dspark_rnn_draft
+
+    def call(**kw):
+        a = dict(R=4, g=4, V=1024, ns=32, ne=32, d=64, du=0, T=1.0, ws=1 << 30)
+        a.update(kw)
+        p = list(P)
+        for k in kw.get("null", []):
+            p[k] = None
+        for k in kw.get("misalign", []):
+            p[k] = ctypes.c_void_p(p[k].value + 4)
+        return L(a["R"], a["g"], a["V"], a["ns"], a["ne"], a["d"], a["du"], 0, 0, p[0], p[1], p[2], p[3], p[4], p[5],
+                 p[6], p[7], 0.0, 1.0, p[8], a["T"], p[9], p[10], 0, 0, p[11], p[12], p[13], p[14], p[15], p[16],
+                 a["ws"], None)
+
+    assert call(R=0) == 1
+    assert call(ne=-1) == 1
+    assert call(g=100) == 2
+    assert call(ns=48) == 2  # not a multiple of 32
+    assert call(ns=288) == 2
+    assert call(ne=4096) == 2
+    assert call(du=5) == 1
+    assert call(T=0.0) == 1
+    # U, E, Wse, Wh, bgc, Wo, h, conf_w, conf_temp, x0, req_id, outputs, state, workspace
+    for k in range(17):
+        assert call(null=[k]) == 1, k
+    assert call(null=[1], ne=0, ws=100) == 3  # no embedding: E may be missing
+    assert call(null=[3, 6], d=0, ws=100) == 3  # no hidden state: Wh and h may be missing
+    for k in (0, 5, 6):  # U, Wo, h
+        assert call(misalign=[k]) == 1, k
+    assert call(ws=100) == 3
+    import torch
+    assert b.rnn_draft_workspace_size(4, 4, 1024, 32, 64, torch.float32) > b.draft_workspace_size(
+        4, 4, 1024, 32, 64, torch.float32)
+
+
+def test_verify_rnn_validation(b):
+    P = _fake(17)
+    L = b.lib.dspark_verify_rnn
+
+    def call(**kw):
+        p = list(P)
+        for k in kw.get("null", []):
+            p[k] = None
+        return L(4, 4, 1024, 32, 0, 0, 0, p[0], p[1], p[2], p[3], p[4], p[5], p[6], p[7], p[8], 1.0, p[9], 0, 0,
+                 p[10], p[11], p[12], p[13], kw.get("ws", 1 << 30), None)
+
+    for k in range(14):
+        assert call(null=[k]) == 1, k
+    assert "state" in (call(null=[2]) and b.lib.dspark_last_error_message().decode())
+    assert call(ws=100) == 3

@@ -170,3 +170,22 @@ def test_verify_with_state_rows_equals_verify_with_the_factor_rows():
     assert (a["n_acc"] < gamma).any()  # some residual draws happen
     for k in ("n_acc", "tokens", "n_out", "corr_kind"):
         np.testing.assert_array_equal(a[k], b[k])
+
+
+def test_confidence_for_given_states_matches_the_chain():
+    R, gamma, V, ns, d = 3, 4, 32, 8, 5
+    rng, U, h, x0 = _setup(R, gamma, V, ns, d, seed=8)
+    E = rng.normal(0, 1, (V, 4)).astype(np.float32)
+    Wse = rng.normal(0, 0.5, (ns + 4, 2 * ns)).astype(np.float32)
+    Wh = rng.normal(0, 0.5, (d, 2 * ns)).astype(np.float32)
+    bgc = rng.normal(0, 0.5, 2 * ns).astype(np.float32)
+    Wo = rng.normal(0, 0.3, (ns, V)).astype(np.float32)
+    conf_w = _conf(d, ns, rng)
+    temp = rng.uniform(0.5, 1.5, gamma).astype(np.float32)
+    rn = oracle.rnn_draft(U, E, Wse, Wh, bgc, Wo, h, conf_w, 0.2, 1.5, temp, 1.0, x0, np.arange(R), 3, 0)
+    c = oracle.rnn_confidence(h, rn["state"], conf_w, 0.2, 1.5, temp)
+    np.testing.assert_allclose(c, rn["conf"], rtol=0, atol=1e-15)
+    # a zero state leaves the hidden-state part only: sigmoid(kappa (w_h . h + b) / T_k)
+    c0 = oracle.rnn_confidence(h, np.zeros_like(rn["state"]), conf_w, 0.2, 1.5, temp)
+    ref = special.expit(1.5 * (h.astype(np.float64) @ conf_w[:d].astype(np.float64) + 0.2) / temp)
+    np.testing.assert_allclose(c0, ref, rtol=1e-12)
