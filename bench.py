@@ -42,6 +42,11 @@ DRAFT_KERNEL_SOURCES = ["speculative_decoding_draft_03_gb300/csrc/draft_tc.cu",
                         "speculative_decoding_draft_03_gb300/csrc/dspark_common.cuh"]
 
 
+def workload_desc(args):
+    desc = WORKLOAD_DESC[args.workload]
+    return desc + "; recurrent draft head (ns = ne = rank)" if getattr(args, "head", "markov") == "rnn" else desc
+
+
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -52,6 +57,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--head", choices=["markov", "rnn"], default="markov",
+                   help="draft head: the Markov head, or the recurrent head on the same workload")
     p.add_argument("--diagnostic", choices=["overlap"], default=None,
                    help="time the acceptance-overlap diagnostic on the workload's verified positions "
                         "instead of the round")
@@ -173,13 +180,15 @@ def draft_step_bytes(w):
     import torch
     es = lambda t: torch.tensor([], dtype=t.dtype).element_size()
     R, V, rank = w["R"], w["V"], w["rank"]
-    return R * V * es(w["U"]) + rank * V * es(w["W2"]) + R * rank * es(w["W1"])
+    W2 = w["Wo"] if w.get("head") == "rnn" else w["W2"]  # the factor rows have the weights' type
+    return R * V * es(w["U"]) + rank * V * es(W2) + R * rank * es(W2)
 
 
 def tensor_core_path(w):
     """The bf16 shapes the library runs on tcgen05 (the others run on CUDA cores)."""
     import torch
-    return (w["W1"].dtype == torch.bfloat16 and w["rank"] % 64 == 0 and 64 <= w["rank"] <= 256
+    wdt = w["Wo"].dtype if w.get("head") == "rnn" else w["W1"].dtype
+    return (wdt == torch.bfloat16 and w["rank"] % 64 == 0 and 64 <= w["rank"] <= 256
             and w["V"] % 8 == 0 and w["V"] >= 128)
 
 
@@ -189,6 +198,11 @@ def launches_per_round(w):
     position on CUDA cores), the scheduler, and verify's plan / rows / accept / residual
     step / residual combine."""
     g = w["gamma"]
+    if w.get("head") == "rnn":
+        # h projection, then a cell and a step per position, the merge (tensor cores: once;
+        # CUDA cores: per position) and the confidences
+        draft = (1 if w["d"] > 0 else 0) + 2 * g + (1 if tensor_core_path(w) else g) + 1
+        return (1 if w["d"] > 0 else 0) + draft + 1 + 5
     draft = g + 1 if tensor_core_path(w) else 2 * g
     return (1 if w["d"] > 0 else 0) + 1 + draft + 1 + 5
 
@@ -215,7 +229,8 @@ def run_reference(args):
     from speculative_decoding_draft_03_gb300 import workloads as wl
     import oracle
     oracle.build()
-    w = wl.to_numpy(wl.make(args.workload, device="cpu"))
+    w = wl.make(args.workload, device="cpu")
+    w = wl.to_numpy(wl.add_rnn_head(w) if args.head == "rnn" else w)
     total_tok, total_t = 0, 0.0
     for t in range(args.warmup + args.steps):
         t0 = time.perf_counter()
@@ -229,7 +244,7 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total_t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded generator, random-init weights)",
-            "config": {"workload": WORKLOAD_DESC[args.workload]},
+            "config": {"workload": workload_desc(args)},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
                              "sample": f"each step one full round of the {args.workload} workload"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -309,6 +324,8 @@ def main():
     dev = torch.device("cuda", local)
     # generated on the host: the CPU baseline and the end-to-end leg need host copies
     w_cpu = wl.make(args.workload, device="cpu", seed=0)
+    if args.head == "rnn":
+        w_cpu = wl.add_rnn_head(w_cpu)
     w = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in w_cpu.items()}
     w["req_id"] = rank_request_ids(w["req_id"], rank, w["R"])
     rd = b.Round(w)
@@ -385,7 +402,7 @@ def main():
                 "warmup": args.warmup, "ms_per_step": round_ms / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32",
                 "data": "synthetic (seeded generator, random-init weights)",
-                "config": {"workload": WORKLOAD_DESC[args.workload], "R": w["R"], "gamma": w["gamma"],
+                "config": {"workload": workload_desc(args), "R": w["R"], "gamma": w["gamma"],
                            "V": w["V"], "rank": w["rank"], "d": w["d"],
                            "l2": "flushed between rounds (256 MiB write outside the timed brackets)",
                            "launch": "each round one CUDA graph, captured and replayed once before timing",

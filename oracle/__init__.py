@@ -409,13 +409,21 @@ def run_round(inp, rnd=0, x0=None, conf_hist=None, nthreads=0):
     """One full round: draft -> schedule (on float32 confidences, the type the stages
     exchange) -> verify (on float32 logq / lse, likewise).  ``inp`` is a workload dict."""
     x0 = inp["x0"] if x0 is None else x0
-    d = markov_draft(inp["U"], inp["W1"], inp["W2"], inp["h"], inp["conf_w"], inp["conf_b"],
-                     inp["conf_logit_scale"], inp["conf_temp"], inp["temperature"], x0,
-                     inp["req_id"], inp["seed"], rnd, nthreads)
+    rnn = inp.get("head") == "rnn"
+    if rnn:
+        d = rnn_draft(inp["U"], inp["E"], inp["Wse"], inp["Wh"], inp["bgc"], inp["Wo"], inp["h"], inp["conf_w"],
+                      inp["conf_b"], inp["conf_logit_scale"], inp["conf_temp"], inp["temperature"], x0,
+                      inp["req_id"], inp["seed"], rnd, nthreads)
+    else:
+        d = markov_draft(inp["U"], inp["W1"], inp["W2"], inp["h"], inp["conf_w"], inp["conf_b"],
+                         inp["conf_logit_scale"], inp["conf_temp"], inp["temperature"], x0,
+                         inp["req_id"], inp["seed"], rnd, nthreads)
     conf32 = d["conf"].astype(np.float32)
     hist = inp.get("conf_hist") if conf_hist is None else conf_hist
     s = schedule(conf32, inp["sps"], inp["mode"], hist, inp.get("fixed_len", 0))
-    v = verify(inp["target"], inp["U"], inp["W1"], inp["W2"], x0, d["x"],
+    W1 = np.zeros((1, 1), inp["Wo"].dtype) if rnn else inp["W1"]
+    W2 = inp["Wo"] if rnn else inp["W2"]
+    v = verify(inp["target"], inp["U"], W1, W2, x0, d["x"],
                d["logq"].astype(np.float32), d["lse"].astype(np.float32), s["ell"],
-               inp["temperature"], inp["req_id"], inp["seed"], rnd, nthreads)
+               inp["temperature"], inp["req_id"], inp["seed"], rnd, nthreads, state=d["state"] if rnn else None)
     return dict(draft=d, sched=s, verify=v)

@@ -39,6 +39,8 @@
 #include <cudaTypedefs.h>
 #include <string.h>
 
+#include <algorithm>
+
 #include "dspark_common.cuh"
 #include "dspark_internal.h"
 
@@ -888,6 +890,130 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------------------------
+// Recurrent head: the hidden-state projection h Wh ([R*gamma, d] x [d, 2*ns]) for every
+// position at once, as a plain tensor-core GEMM split over the hidden dimension.
+// CTA = (128-row tile, 128-column tile, split); A = h rows (K-major, TMA boxes of 64
+// hidden dimensions x 128 rows), B = Wh [d, 2*ns] (MN-major, loaded like W2); the
+// fp32 accumulator tile goes from TMEM straight to the split's partial-sum slice.
+// Warp 0: TMA producer; warp 1: TMEM allocation + MMA issue; warps 4..7: epilogue
+// (warp w reads TMEM lane quarter w % 4).
+// ------------------------------------------------------------------------------------
+constexpr int kGemmStages = 4;
+constexpr int kGemmStageBytes = kM * 128 + kStageBytes;  // A atom (16 KB) + B slice (16 KB)
+constexpr int kGemmThreads = 256;
+constexpr int kGemmSmem = kGemmStages * kGemmStageBytes + 256 + 1024;
+
+struct GemmParams {
+  int rows, d, n2;
+  int katoms;        // ceil(d / 64)
+  int per_split;     // K atoms per split
+  float* out;        // [nsplit, rows, n2]
+  DeviceStatus* status;
+};
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    hproj_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
+                    GemmParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mt = blockIdx.x, nt = blockIdx.y, sp = blockIdx.z;
+  const int ka0 = sp * p.per_split;
+  const int nk = max(0, min(p.per_split, p.katoms - ka0));
+  const uint32_t bar_full = sbase + kGemmStages * kGemmStageBytes;
+  const uint32_t bar_empty = bar_full + 8 * kGemmStages;
+  const uint32_t bar_acc = bar_empty + 8 * kGemmStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kGemmStages * kGemmStageBytes + 8 * (2 * kGemmStages + 1));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kGemmStages; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    mbar_init(bar_acc, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kN);
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  griddep_allow_next();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // h and Wh are inputs of the call: nothing earlier in the stream writes them
+      const uint64_t pol = policy_evict_normal();
+      for (int i = 0; i < nk && !*abort_flag; ++i) {
+        const int s = i % kGemmStages;
+        const uint32_t ph = (uint32_t)(i / kGemmStages) & 1u;
+        if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, abort_flag, p.status, 500)) break;
+        const uint32_t dst = sbase + s * kGemmStageBytes;
+        mbar_arrive_expect_tx(bar_full + 8 * s, (uint32_t)kGemmStageBytes);
+        const int k0 = (ka0 + i) * kKAtom;
+        tma_load_2d(dst, &map_h, bar_full + 8 * s, k0, mt * kM, pol);
+        tma_load_2d(dst + kM * 128, &map_w, bar_full + 8 * s, nt * kN, k0, pol);
+        tma_load_2d(dst + kM * 128 + kStageBytes / 2, &map_w, bar_full + 8 * s, nt * kN + 64, k0, pol);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc(kM, kN);
+      bool ok = true;
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % kGemmStages;
+        const uint32_t ph = (uint32_t)(i / kGemmStages) & 1u;
+        if (!mbar_wait(bar_full + 8 * s, ph, abort_flag, p.status, 501)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_st = sbase + s * kGemmStageBytes;
+        const uint32_t b_st = a_st + kM * 128;
+#pragma unroll
+        for (int kk = 0; kk < kKAtom / 16; ++kk) {
+          const uint64_t adesc = sw128_desc(a_st + kk * 32, 16, 1024);
+          const uint64_t bdesc = sw128_desc(b_st + kk * 2048, kStageBytes / 2, 1024);
+          mma_bf16(tmem_base, adesc, bdesc, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar_empty + 8 * s);
+      }
+      if (ok) mma_commit(bar_acc);
+    }
+  } else if (warp >= 4) {
+    const int quarter = warp & 3;
+    const bool ready = nk > 0 && mbar_wait(bar_acc, 0, abort_flag, p.status, 502);
+    if (ready) tc_fence_after();
+    // the partial sums overwrite what the previous call's cells read
+    griddep_wait();
+    const int row = mt * kM + quarter * 32 + lane;
+    float* out = p.out + ((size_t)sp * p.rows + row) * p.n2 + nt * kN;
+    for (int c = 0; c < kN; c += kCols) {
+      float v[kCols];
+      if (ready) {
+        tmem_ld8(tmem_base + ((uint32_t)(quarter * 32) << 16) + c, v);
+      } else {
+#pragma unroll
+        for (int e = 0; e < kCols; ++e) v[e] = 0.f;
+      }
+      if (row < p.rows) {
+        reinterpret_cast<float4*>(out + c)[0] = make_float4(v[0], v[1], v[2], v[3]);
+        reinterpret_cast<float4*>(out + c)[1] = make_float4(v[4], v[5], v[6], v[7]);
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kN);
+  }
+}
+
+// ------------------------------------------------------------------------------------
 // Host side
 // ------------------------------------------------------------------------------------
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1032,6 +1158,46 @@ cudaError_t launch_rnn_step_tc(const DraftArgs& a, int k, cudaStream_t s) {
   p.hint = a.hint + (size_t)(k - 1) * a.R;
   p.win = a.win + (size_t)(k - 1) * a.R;
   return tc::launch<tc::kModeRnn>(p, a.W1g, a.W2, s);
+}
+
+// The hidden-state projection of the recurrent head takes the tensor cores for bf16 h and
+// weights with 2*ns a multiple of 128 and d a multiple of 8 (16-byte TMA rows).
+int rnn_hproj_on_tc(int d, int ns, int dtype_w, int dtype_h) {
+  return d > 0 && d % 8 == 0 && ns % 64 == 0 && dtype_w == DSPARK_BF16 && dtype_h == DSPARK_BF16;
+}
+
+// Splits of the hidden dimension: enough CTAs to cover the GPU (tensor cores), or one per
+// 512 hidden dimensions (CUDA cores).
+int rnn_num_splits(int R, int gamma, int d, int ns, int dtype_w, int dtype_h) {
+  if (d <= 0) return 0;
+  if (!rnn_hproj_on_tc(d, ns, dtype_w, dtype_h)) return (d + 511) / 512;
+  const int katoms = (d + tc::kKAtom - 1) / tc::kKAtom;
+  const int tiles = ((R * gamma + tc::kM - 1) / tc::kM) * (2 * ns / tc::kN);
+  const int want = std::max(1, std::min(katoms, (tc::num_sms() + tiles - 1) / tiles));
+  const int per = (katoms + want - 1) / want;
+  return (katoms + per - 1) / per;
+}
+
+cudaError_t launch_rnn_hproj_tc(const DraftArgs& a, cudaStream_t s) {
+  const int rows = a.R * a.gamma, n2 = 2 * a.rank;
+  CUtensorMap map_h, map_w;
+  if (!tc::make_map_2d(&map_h, a.h, (uint64_t)a.d, (uint64_t)rows, tc::kKAtom, tc::kM)) return cudaErrorInvalidValue;
+  if (!tc::make_map_2d(&map_w, a.Wh, (uint64_t)n2, (uint64_t)a.d, 64, tc::kKAtom)) return cudaErrorInvalidValue;
+  tc::GemmParams p;
+  p.rows = rows;
+  p.d = a.d;
+  p.n2 = n2;
+  p.katoms = (a.d + tc::kKAtom - 1) / tc::kKAtom;
+  const int nsplit = rnn_num_splits(a.R, a.gamma, a.d, a.rank, a.dtype_w, a.dtype_h);
+  if (nsplit != a.nsplit) return cudaErrorInvalidValue;
+  p.per_split = (p.katoms + nsplit - 1) / nsplit;
+  p.out = a.hpart;
+  p.status = a.status;
+  cudaError_t e = cudaFuncSetAttribute(tc::hproj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       tc::kGemmSmem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((rows + tc::kM - 1) / tc::kM, n2 / tc::kN, nsplit);
+  return launch_pdl(tc::hproj_tc_kernel, grid, dim3(tc::kGemmThreads), (size_t)tc::kGemmSmem, s, map_h, map_w, p);
 }
 
 cudaError_t launch_overlap_tc(const OverlapArgs& a, cudaStream_t s) {

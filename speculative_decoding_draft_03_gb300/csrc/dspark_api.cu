@@ -6,6 +6,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
+
 #include "dspark_common.cuh"
 #include "dspark_internal.h"
 
@@ -63,10 +65,13 @@ struct RnnLayout {
   int nsplit;
 };
 
+// The partial sums are sized for the larger of the two projection splits (the hidden
+// state's type decides which projection runs).
 RnnLayout rnn_layout(int R, int gamma, int V, int ns, int d, int dtype_w) {
   RnnLayout L;
   L.draft = draft_layout(R, gamma, V, ns, dtype_w);
-  L.nsplit = dspark::rnn_num_splits(d);
+  L.nsplit = std::max(dspark::rnn_num_splits(R, gamma, d, ns, dtype_w, DSPARK_BF16),
+                      dspark::rnn_num_splits(R, gamma, d, ns, dtype_w, DSPARK_F32));
   L.hpart = L.draft.total;
   L.total = L.hpart + dspark::align256(sizeof(float) * (size_t)L.nsplit * R * gamma * 2 * ns);
   return L;
@@ -569,6 +574,7 @@ dspark_status dspark_rnn_draft(int R, int gamma, int V, int ns, int ne, int d, i
   CHECK_ALIGN16(U);
   CHECK_ALIGN16(Wo);
   if (d > 0) CHECK_ALIGN16(h);
+  if (d > 0) CHECK_ALIGN16(Wh);
   if (!aligned256(workspace)) return fail(DSPARK_INVALID_ARG, "workspace must be 256-byte aligned");
   const RnnLayout L = rnn_layout(R, gamma, V, ns, d, dtype_w);
   if (ws_bytes < L.total) return fail(DSPARK_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, L.total);
@@ -592,7 +598,7 @@ dspark_status dspark_rnn_draft(int R, int gamma, int V, int ns, int ne, int d, i
   a.ne = ne; a.E = E; a.Wse = Wse; a.Wh = Wh; a.bgc = bgc;
   a.state_out = state_out;
   a.hpart = reinterpret_cast<float*>(ws + L.hpart);
-  a.nsplit = L.nsplit;
+  a.nsplit = dspark::rnn_num_splits(R, gamma, d, ns, dtype_w, dtype_h);
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;

@@ -157,8 +157,10 @@ cudaError_t launch_draft_step_tc(const DraftArgs& a, int k, cudaStream_t s);
 cudaError_t launch_rnn_step_tc(const DraftArgs& a, int k, cudaStream_t s);
 // Recurrent head: h Wh for every position (before the loop), the cell of position k
 // (after position k-1's draw), and the confidences from the states (after the loop).
-int rnn_num_splits(int d);
+int rnn_hproj_on_tc(int d, int ns, int dtype_w, int dtype_h);
+int rnn_num_splits(int R, int gamma, int d, int ns, int dtype_w, int dtype_h);
 cudaError_t launch_rnn_hproj(const DraftArgs& a, cudaStream_t s);
+cudaError_t launch_rnn_hproj_tc(const DraftArgs& a, cudaStream_t s);
 cudaError_t launch_rnn_cell(const DraftArgs& a, int k, bool tc, cudaStream_t s);
 cudaError_t launch_rnn_conf(const DraftArgs& a, cudaStream_t s);
 // After the last tensor-core position: every position's partial records -> x, lse, logq.

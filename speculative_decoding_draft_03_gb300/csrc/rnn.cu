@@ -11,7 +11,8 @@
 // which makes it the A operand of the bias contraction s_k W_o.
 //
 //   rnn_hproj   h Wh for every (request, position) before the loop (it does not depend
-//               on the drafted tokens): split over the hidden dimension, partial sums
+//               on the drafted tokens): split over the hidden dimension, partial sums;
+//               a tensor-core GEMM (hproj_tc_kernel) for bf16 operands, else CUDA cores
 //   rnn_cell    position k: x_{k-1} (anchor, or position k-1's winner) -> s_k, written
 //               to the state output and to the factor-row buffer the draft step reads
 //   rnn_conf    after the loop: c_k = sigmoid(kappa (w_h . h_k + w_s . s_k + b) / T_k)
@@ -23,12 +24,13 @@
 
 namespace dspark {
 
-constexpr int kHRows = 8;        // hidden-state rows per CTA of rnn_hproj
-constexpr int kHSplit = 512;     // hidden dimensions per split
+constexpr int kHRows = 8;        // hidden-state rows per CTA of the CUDA-core projection
+constexpr int kHSplit = 512;     // hidden dimensions per split (CUDA-core projection)
 constexpr int kCellReq = 4;      // requests per CTA of rnn_cell
-constexpr int kCellCols = 64;    // state columns per CTA of rnn_cell
-
-int rnn_num_splits(int d) { return (d + kHSplit - 1) / kHSplit; }
+constexpr int kCellCols = 8;     // state columns per CTA of rnn_cell (x2: gate and candidate)
+constexpr int kCellSlices = 16;  // slices of the input vector per column
+constexpr int kCellBatch = 8;    // weights loaded per thread before they are used
+constexpr int kCellThreads = 2 * kCellCols * kCellSlices;
 
 // hpart[split][row][c] = sum over the split's hidden dimensions i of h[row][i] Wh[i][c].
 // Thread t owns the gate column t and the candidate column ns + t for kHRows rows.
@@ -51,7 +53,25 @@ __global__ void rnn_hproj_kernel(DraftArgs a) {
   float ag[kHRows], ac[kHRows];
 #pragma unroll
   for (int rr = 0; rr < kHRows; ++rr) ag[rr] = ac[rr] = 0.f;
-  for (int i = 0; i < len; ++i) {
+  // four hidden dimensions per step: their eight weights are loaded before any is used
+  int i = 0;
+  for (; i + 4 <= len; i += 4) {
+    float wg[4], wc[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const size_t w = (size_t)(i0 + i + q) * n2;
+      wg[q] = load_elem(a.Wh, a.dtype_w, w + t);
+      wc[q] = load_elem(a.Wh, a.dtype_w, w + ns + t);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int rr = 0; rr < kHRows; ++rr) {
+        ag[rr] = fmaf(hs[rr][i + q], wg[q], ag[rr]);
+        ac[rr] = fmaf(hs[rr][i + q], wc[q], ac[rr]);
+      }
+  }
+  for (; i < len; ++i) {
     const size_t w = (size_t)(i0 + i) * n2;
     const float wg = load_elem(a.Wh, a.dtype_w, w + t);
     const float wc = load_elem(a.Wh, a.dtype_w, w + ns + t);
@@ -71,6 +91,19 @@ __global__ void rnn_hproj_kernel(DraftArgs a) {
   }
 }
 
+// Sum of the projection's splits into split 0, in split order (before the position loop,
+// so that each cell reads one value per pre-activation).
+__global__ void rnn_hsum_kernel(DraftArgs a) {
+  griddep_allow_next();
+  griddep_wait();
+  const size_t n = (size_t)a.R * a.gamma * 2 * a.rank;
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  float v = a.hpart[i];
+  for (int sp = 1; sp < a.nsplit; ++sp) v += a.hpart[(size_t)sp * n + i];
+  a.hpart[i] = v;
+}
+
 __device__ __forceinline__ void store_state(void* base, int dtype, size_t idx, float v) {
   if (dtype == DSPARK_BF16)
     reinterpret_cast<__nv_bfloat16*>(base)[idx] = __float2bfloat16_rn(v);
@@ -78,15 +111,25 @@ __device__ __forceinline__ void store_state(void* base, int dtype, size_t idx, f
     reinterpret_cast<float*>(base)[idx] = v;
 }
 
-// Position k: CTA (block of kCellReq requests, block of kCellCols state columns); thread
-// (request rr, column c) forms the gate and candidate pre-activations of column c.
-__global__ void __launch_bounds__(kCellReq * kCellCols) rnn_cell_kernel(DraftArgs a, int k, int tc) {
-  griddep_allow_next();
-  griddep_wait();
+// Position k: CTA (block of kCellReq requests, block of kCellCols state columns).  Thread
+// (pre-activation column j, slice q) accumulates column j (the first kCellCols are gate
+// columns, the others the matching candidate columns) over the input entries q,
+// q + kCellSlices, ... for all the CTA's requests, so each weight is loaded once per
+// CTA; the slices are then added in a fixed order and kCellCols x kCellReq threads
+// finish the update.
+__global__ void __launch_bounds__(kCellThreads) rnn_cell_kernel(DraftArgs a, int k, int tc) {
   extern __shared__ float us[];  // [kCellReq][ns + ne]: s_{k-1}; E[x_{k-1}]
   __shared__ int xs[kCellReq];
+  __shared__ float red[kCellSlices][2 * kCellCols][kCellReq];
   const int ns = a.rank, n2 = 2 * ns, nu = ns + a.ne;
   const int r0 = blockIdx.x * kCellReq;
+  const int c0 = blockIdx.y * kCellCols;
+  const int j = threadIdx.x % (2 * kCellCols);  // pre-activation column within the CTA
+  const int q = threadIdx.x / (2 * kCellCols);  // input slice
+  const int cj = j < kCellCols ? c0 + j : ns + c0 + (j - kCellCols);  // column of Wse
+  const bool col_ok = c0 + (j % kCellCols) < ns;
+  griddep_allow_next();
+  griddep_wait();
   if (threadIdx.x < kCellReq) {
     const int r = r0 + threadIdx.x;
     int x = 0;
@@ -112,38 +155,71 @@ __global__ void __launch_bounds__(kCellReq * kCellCols) rnn_cell_kernel(DraftArg
       }
     }
   __syncthreads();
-  for (int e = threadIdx.x; e < kCellReq * nu; e += blockDim.x) {
-    const int rr = e / nu, j = e % nu;
-    const int r = r0 + rr;
-    float v = 0.f;
-    if (r < a.R) {
-      if (j < ns)
-        v = k == 1 ? 0.f : load_elem(a.state_out, a.dtype_w, ((size_t)r * a.gamma + (k - 2)) * ns + j);
-      else
-        v = load_elem(a.E, a.dtype_w, (size_t)xs[rr] * a.ne + (j - ns));
+  // four entries per thread and step, loaded before they are stored
+  for (int e0 = threadIdx.x; e0 < kCellReq * nu; e0 += 4 * blockDim.x) {
+    float v[4];
+#pragma unroll
+    for (int u4 = 0; u4 < 4; ++u4) {
+      const int e = e0 + u4 * blockDim.x;
+      v[u4] = 0.f;
+      if (e >= kCellReq * nu) continue;
+      const int rr = e / nu, j = e % nu;
+      const int r = r0 + rr;
+      if (r < a.R) {
+        if (j < ns)
+          v[u4] = k == 1 ? 0.f : load_elem(a.state_out, a.dtype_w, ((size_t)r * a.gamma + (k - 2)) * ns + j);
+        else
+          v[u4] = load_elem(a.E, a.dtype_w, (size_t)xs[rr] * a.ne + (j - ns));
+      }
     }
-    us[e] = v;
+#pragma unroll
+    for (int u4 = 0; u4 < 4; ++u4)
+      if (e0 + u4 * blockDim.x < kCellReq * nu) us[e0 + u4 * blockDim.x] = v[u4];
   }
   __syncthreads();
-  const int rr = threadIdx.x / kCellCols;
-  const int c = blockIdx.y * kCellCols + threadIdx.x % kCellCols;
+  float acc[kCellReq];
+#pragma unroll
+  for (int rr = 0; rr < kCellReq; ++rr) acc[rr] = 0.f;
+  if (col_ok) {
+    int i = q;
+    // kCellBatch input entries per step: their weights are loaded before any is used
+    for (; i + (kCellBatch - 1) * kCellSlices < nu; i += kCellBatch * kCellSlices) {
+      float w[kCellBatch];
+#pragma unroll
+      for (int u = 0; u < kCellBatch; ++u) w[u] = load_elem(a.Wse, a.dtype_w, (size_t)(i + u * kCellSlices) * n2 + cj);
+#pragma unroll
+      for (int u = 0; u < kCellBatch; ++u)
+#pragma unroll
+        for (int rr = 0; rr < kCellReq; ++rr) acc[rr] = fmaf(us[rr * nu + i + u * kCellSlices], w[u], acc[rr]);
+    }
+    for (; i < nu; i += kCellSlices) {
+      const float w = load_elem(a.Wse, a.dtype_w, (size_t)i * n2 + cj);
+#pragma unroll
+      for (int rr = 0; rr < kCellReq; ++rr) acc[rr] = fmaf(us[rr * nu + i], w, acc[rr]);
+    }
+  }
+#pragma unroll
+  for (int rr = 0; rr < kCellReq; ++rr) red[q][j][rr] = acc[rr];
+  __syncthreads();
+  if (threadIdx.x >= kCellCols * kCellReq) return;
+  const int cc = threadIdx.x % kCellCols, rr = threadIdx.x / kCellCols;
+  const int c = c0 + cc;
   const int r = r0 + rr;
   if (r >= a.R || c >= ns) return;
   const int row = r * a.gamma + (k - 1);
-  const int rows = a.R * a.gamma;
   float ag = __ldg(a.bgc + c), ac = __ldg(a.bgc + ns + c);
-  for (int sp = 0; sp < a.nsplit; ++sp) {
-    const float* hp = a.hpart + ((size_t)sp * rows + row) * n2;
+  if (a.nsplit > 0) {  // split 0 holds the sum of all splits
+    const float* hp = a.hpart + (size_t)row * n2;
     ag += hp[c];
     ac += hp[ns + c];
   }
-  const float* u = us + rr * nu;
-  for (int j = 0; j < nu; ++j) {
-    ag = fmaf(u[j], load_elem(a.Wse, a.dtype_w, (size_t)j * n2 + c), ag);
-    ac = fmaf(u[j], load_elem(a.Wse, a.dtype_w, (size_t)j * n2 + ns + c), ac);
+#pragma unroll
+  for (int qq = 0; qq < kCellSlices; ++qq) {
+    ag += red[qq][cc][rr];
+    ac += red[qq][kCellCols + cc][rr];
   }
   const float g = 1.f / (1.f + __expf(-ag));
-  const float s = (1.f - g) * u[c] + g * tanhf(ac);
+  const float s = (1.f - g) * us[rr * nu + c] + g * tanhf(ac);
   store_state(a.state_out, a.dtype_w, (size_t)row * ns + c, s);
   store_state(a.W1g, a.dtype_w, (size_t)r * ns + c, s);
 }
@@ -170,15 +246,24 @@ __global__ void rnn_conf_kernel(DraftArgs a) {
 }
 
 cudaError_t launch_rnn_hproj(const DraftArgs& a, cudaStream_t s) {
+  cudaError_t e;
   const int rows = a.R * a.gamma;
-  dim3 grid((rows + kHRows - 1) / kHRows, a.nsplit);
-  return launch_pdl(rnn_hproj_kernel, grid, dim3(a.rank), 0, s, a);
+  if (rnn_hproj_on_tc(a.d, a.rank, a.dtype_w, a.dtype_h)) {
+    e = launch_rnn_hproj_tc(a, s);
+  } else {
+    if (a.nsplit != (a.d + kHSplit - 1) / kHSplit) return cudaErrorInvalidValue;
+    dim3 grid((rows + kHRows - 1) / kHRows, a.nsplit);
+    e = launch_pdl(rnn_hproj_kernel, grid, dim3(a.rank), 0, s, a);
+  }
+  if (e != cudaSuccess || a.nsplit <= 1) return e;
+  const size_t n = (size_t)rows * 2 * a.rank;
+  return launch_pdl(rnn_hsum_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, a);
 }
 
 cudaError_t launch_rnn_cell(const DraftArgs& a, int k, bool tc, cudaStream_t s) {
   dim3 grid((a.R + kCellReq - 1) / kCellReq, (a.rank + kCellCols - 1) / kCellCols);
   const size_t smem = sizeof(float) * kCellReq * (a.rank + a.ne);
-  return launch_pdl(rnn_cell_kernel, grid, dim3(kCellReq * kCellCols), smem, s, a, k, tc ? 1 : 0);
+  return launch_pdl(rnn_cell_kernel, grid, dim3(kCellThreads), smem, s, a, k, tc ? 1 : 0);
 }
 
 cudaError_t launch_rnn_conf(const DraftArgs& a, cudaStream_t s) {

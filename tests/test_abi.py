@@ -221,7 +221,7 @@ def test_rnn_draft_validation(b):
         assert call(null=[k]) == 1, k
     assert call(null=[1], ne=0, ws=100) == 3  # no embedding: E may be missing
     assert call(null=[3, 6], d=0, ws=100) == 3  # no hidden state: Wh and h may be missing
-    for k in (0, 5, 6):  # U, Wo, h
+    for k in (0, 3, 5, 6):  # U, Wh, Wo, h
         assert call(misalign=[k]) == 1, k
     assert call(ws=100) == 3
     import torch
