@@ -79,6 +79,10 @@ def _load():
             lib.orc_rnn_draft.restype = ctypes.c_int
             lib.orc_rnn_confidence.argtypes = [i32] * 5 + [P, P, P, f64, f64, P, P]
             lib.orc_rnn_confidence.restype = ctypes.c_int
+            lib.orc_sts_ece.argtypes = [i32, i32, P, P, P, i32, f64, i32]
+            lib.orc_sts_ece.restype = f64
+            lib.orc_sts_fit.argtypes = [i32, i32, P, P, P, i32, i32, P, P]
+            lib.orc_sts_fit.restype = ctypes.c_int
             lib.orc_max_threads.restype = i32
             lib.orc_acceptance_overlap.argtypes = [i32] * 7 + [P] * 7 + [f64, P, i32]
             lib.orc_acceptance_overlap.restype = ctypes.c_int
@@ -403,6 +407,36 @@ def acceptance_overlap(target, U, W1, W2, x0, x, ell=None, temperature=1.0, nthr
     if rc != 0:
         raise ValueError("oracle acceptance_overlap rejected its arguments")
     return out
+
+
+# ---------------------------------------------------------------------------
+# Sequential temperature scaling (numb3r33 blog "Sequential temperature scaling";
+# mkdocs.reaper.mx "3 · DSpark" §3.2)
+# ---------------------------------------------------------------------------
+def sts_ece(z, acc_len, T_prev, k, T, M):
+    """ECE of the cumulative survival at position k (1-based) for temperature T, with
+    the temperatures of positions 1..k-1 frozen at T_prev."""
+    z = _c(z, np.float32)
+    N, gamma = z.shape
+    acc = _c(acc_len, np.int32)
+    tp = _c(np.asarray(T_prev, np.float64).reshape(-1) if len(T_prev) else np.zeros(1), np.float64)
+    return float(_load().orc_sts_ece(N, gamma, _ptr(z), _ptr(acc), _ptr(tp), int(k), float(T), int(M)))
+
+
+def sts_fit(z, acc_len, grid, M):
+    """Per-position temperatures fitted left to right on held-out (z, L) pairs.
+    z [N,gamma] confidence logits; acc_len [N] accepted drafts; grid [G] candidates.
+    Returns (T [gamma], ece [gamma])."""
+    z = _c(z, np.float32)
+    N, gamma = z.shape
+    acc = _c(acc_len, np.int32)
+    grid = _c(grid, np.float64)
+    T = np.zeros(gamma)
+    ece = np.zeros(gamma)
+    rc = _load().orc_sts_fit(N, gamma, _ptr(z), _ptr(acc), _ptr(grid), len(grid), int(M), _ptr(T), _ptr(ece))
+    if rc != 0:
+        raise ValueError("oracle sts_fit rejected its arguments")
+    return T, ece
 
 
 def run_round(inp, rnd=0, x0=None, conf_hist=None, nthreads=0):

@@ -697,6 +697,64 @@ int orc_rnn_draft(int R, int gamma, int V, int ns, int ne, int d, int dtype_u, i
 }
 
 /* ------------------------------------------------------------------------- */
+/* Sequential temperature scaling (STS) of the confidence head.               */
+/* ------------------------------------------------------------------------- */
+/* [EXPL] "Sequential temperature scaling": c_k = sigmoid(z_k / T_k); calibrate position 1,
+ * freeze it, then calibrate the cumulative survival through position 2, and so on left
+ * to right.  [FR] §3.2: a per-position temperature search minimising the expected
+ * calibration error of the cumulative product prod_{i<=k} c_i on held-out data.
+ * Held-out sample n: confidence logits z[n, 1..gamma] (before the temperature) and the
+ * number of accepted drafts L_n when the whole block was verified, so the survival
+ * outcome at position k is 1[L_n >= k].
+ * ECE over M equal-width bins of [0,1] (bin of p: min(floor(p M), M-1)):
+ *   ECE = sum_b |sum_{n in b} (p_n - o_n)| / N
+ * (the bin-weighted gap |mean p - mean o| of the usual definition).  T_k is the grid
+ * temperature with the smallest ECE of p_n = prod_{i<k} sigmoid(z_{n,i}/T_i) *
+ * sigmoid(z_{n,k}/T), the first one on ties.                                */
+static int orc_bin(double p, int M) {
+    int b = (int)floor(p * M);
+    if (b < 0) b = 0;
+    if (b > M - 1) b = M - 1;
+    return b;
+}
+
+/* ECE at position k (1-based) for temperature T, given the frozen T_1..T_{k-1}. */
+double orc_sts_ece(int N, int gamma, const float* z, const int32_t* acc_len, const double* T_prev, int k,
+                   double T, int M) {
+    double* gap = (double*)calloc((size_t)M, sizeof(double));
+    for (int n = 0; n < N; ++n) {
+        double p = 1.0;
+        for (int i = 1; i < k; ++i) p *= orc_sigmoid((double)z[(size_t)n * gamma + (i - 1)] / T_prev[i - 1]);
+        p *= orc_sigmoid((double)z[(size_t)n * gamma + (k - 1)] / T);
+        const double o = acc_len[n] >= k ? 1.0 : 0.0;
+        gap[orc_bin(p, M)] += p - o;
+    }
+    double e = 0.0;
+    for (int b = 0; b < M; ++b) e += fabs(gap[b]);
+    free(gap);
+    return e / N;
+}
+
+int orc_sts_fit(int N, int gamma, const float* z, const int32_t* acc_len, const double* grid, int G, int M,
+                double* T_out, double* ece_out) {
+    if (N < 1 || gamma < 1 || G < 1 || M < 1) return 1;
+    for (int k = 1; k <= gamma; ++k) {
+        int best = 0;
+        double best_e = INFINITY;
+        for (int g = 0; g < G; ++g) {
+            const double e = orc_sts_ece(N, gamma, z, acc_len, T_out, k, grid[g], M);
+            if (e < best_e) {
+                best_e = e;
+                best = g;
+            }
+        }
+        T_out[k - 1] = grid[best];
+        ece_out[k - 1] = best_e;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
 /* Acceptance-overlap diagnostic.                                             */
 /* ------------------------------------------------------------------------- */
 /* For request r and drafted position j (1-based) the expected acceptance of the

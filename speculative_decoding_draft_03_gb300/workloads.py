@@ -206,6 +206,27 @@ def add_rnn_head(w: dict, seed: int = 0) -> dict:
     return out
 
 
+def sts_heldout(N: int, gamma: int, T_true, seed: int = 0, mu: float = 1.5, sigma: float = 2.0,
+                device="cpu") -> dict:
+    """Synthetic held-out rounds for fitting the per-position temperatures: confidence
+    logits z[n,k] ~ N(mu, sigma^2) and accepted lengths drawn from a known calibration
+    law, position k surviving with probability sigmoid(z[n,k] / T_true[k]) given that
+    position k-1 survived (L = survivors before the first failure).  The fitted
+    temperatures should come out near T_true."""
+    dev = torch.device(device)
+    z = _normal((N, gamma), sigma, 7000 + seed, dev).add_(mu)
+    u = torch.rand((N, gamma), generator=_gen(dev, 7100 + seed), device=dev)
+    T = torch.as_tensor(np.asarray(T_true, np.float32), device=dev).view(1, gamma)
+    alive = (u < torch.sigmoid(z / T)).to(torch.int32)
+    L = torch.cumprod(alive, dim=1).sum(dim=1).to(torch.int32)
+    return dict(z=z, acc_len=L, T_true=np.asarray(T_true, np.float64))
+
+
+def sts_grid(G: int = 256, lo: float = 0.05, hi: float = 20.0) -> np.ndarray:
+    """Candidate temperatures, log-spaced."""
+    return np.exp(np.linspace(math.log(lo), math.log(hi), G)).astype(np.float32)
+
+
 def to_numpy(w: dict) -> dict:
     """Host copies for the oracle: bf16 tensors become their raw uint16 bit patterns."""
     out = {}
