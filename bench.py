@@ -59,9 +59,9 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--head", choices=["markov", "rnn"], default="markov",
                    help="draft head: the Markov head, or the recurrent head on the same workload")
-    p.add_argument("--diagnostic", choices=["overlap"], default=None,
-                   help="time the acceptance-overlap diagnostic on the workload's verified positions "
-                        "instead of the round")
+    p.add_argument("--diagnostic", choices=["overlap", "sts"], default=None,
+                   help="time the acceptance-overlap diagnostic on the workload's verified positions, or the "
+                        "sequential temperature fit on synthetic held-out rounds, instead of the round")
     return p.parse_args()
 
 
@@ -305,12 +305,68 @@ def run_overlap_diagnostic(args):
     return 0
 
 
+# Sequential temperature scaling: one candidate evaluation is sigmoid(z / T) times the
+# prefix, binned: one exponential and two reciprocals on the special-function units
+# (16 results per SM and clock), so the ALU roofline is 152 * 16 * 2.07 GHz / 3.
+STS_EVALS_PEAK = 152 * 16 * 2.07e9 / 3
+
+
+def run_sts_diagnostic(args):
+    """Times dspark_sts_fit on 131072 synthetic held-out samples of the workload's block
+    length, 256 log-spaced candidate temperatures and 15 bins.  Metric: candidate
+    evaluations (samples x candidates x positions) per second."""
+    import torch
+    from speculative_decoding_draft_03_gb300 import binding as b
+    from speculative_decoding_draft_03_gb300 import workloads as wl
+    dev = torch.device("cuda", 0)
+    gamma = wl.SHAPES[args.workload].gamma
+    N, G, M = 131072, 256, 15
+    T_true = [1.0 + 0.5 * ((k % 3) - 1) for k in range(gamma)]
+    d = wl.sts_heldout(N, gamma, T_true, seed=0, device="cuda")
+    grid = torch.from_numpy(wl.sts_grid(G)).to(dev)
+    ws = b.workspace(b.sts_fit_workspace_size(N, gamma, G, M), dev)
+    out = dict(T=torch.empty(gamma, device=dev), ece=torch.empty(gamma, device=dev))
+    call = lambda: b.sts_fit(d["z"], d["acc_len"], grid, M, out=out, ws=ws)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    assert b.device_status(ws) == 0
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(0) as clk:
+        for a, e in ev:
+            a.record(stream)
+            call()
+            e.record(stream)
+        torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(e) for a, e in ev) / args.steps
+    evals = N * G * gamma
+    achieved = evals / (ms / 1000.0)
+    line = {"metric": "sts candidate evaluations/s", "value": achieved, "unit": "evals/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic held-out rounds (seeded logits, outcomes from a known calibration law)",
+            "config": {"workload": f"STS fit: N={N} samples, gamma={gamma}, G={G} log-spaced temperatures, "
+                                   f"M={M} bins", "fitted_T": [round(float(t), 4) for t in out["T"].cpu()],
+                       "generating_T": T_true, "l2": "inputs (N*gamma*4 B) are L2-resident"},
+            "roofline": {"kernel": "dspark_sts_fit (all positions)", "bound": "alu", "achieved": achieved,
+                         "peak": STS_EVALS_PEAK, "unit": "evals/s", "frac": achieved / STS_EVALS_PEAK,
+                         "peak_source": "derived: 152 SMs x 16 SFU results/clk x 2.07 GHz / 3 per evaluation",
+                         "traffic": None},
+            "cpu_baseline": None, "e2e": None, "gpu_launches": (1 + 3 * gamma) * args.steps,
+            "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
     if args.diagnostic == "overlap":
         return run_overlap_diagnostic(args)
+    if args.diagnostic == "sts":
+        return run_sts_diagnostic(args)
     import torch
     import torch.distributed as dist
 

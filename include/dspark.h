@@ -351,6 +351,33 @@ DSPARK_API dspark_status dspark_acceptance_overlap(
     const int32_t* x0, const int32_t* x, const float* lse_q, const int32_t* ell,
     float temperature, float* overlap_out, void* workspace, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------------------------------------
+ * Sequential temperature scaling (STS) of the confidence head on held-out rounds.
+ *
+ * Defines (numb3r33 blog "DSpark: confidence-scheduled speculative decoding", section
+ * "Sequential temperature scaling"; mkdocs.reaper.mx "3 · DSpark" §3.2): one temperature
+ * per position, c_k = sigmoid(z_k / T_k), fitted left to right.  For k = 1..gamma, with
+ * T_1..T_{k-1} frozen, T_k is the candidate T of `grid` with the smallest
+ *   ECE_k(T) = sum_b | sum_{n in bin b} (p_n - o_n) | / N,
+ *   p_n = prod_{i<k} sigmoid(z[n,i] / T_i) * sigmoid(z[n,k] / T),  o_n = 1[acc_len[n] >= k],
+ * over M equal-width bins of [0,1] (bin of p: min(floor(p M), M-1)); the first candidate
+ * wins ties.  ece_out[k] is that smallest ECE.
+ * Arguments
+ *   z        [N, gamma] fp32: confidence logits of held-out samples before the
+ *            per-position temperature (kappa (w . [h; W1[x]] + b) of the confidence head).
+ *   acc_len  [N] int32: accepted drafts of each sample when all gamma were verified.
+ *   grid     [G] fp32 candidate temperatures (> 0; others are skipped and reported).
+ *   M        calibration bins, 1..16.
+ * Outputs: T_out [gamma], ece_out [gamma] fp32 (NaN if no candidate is usable).
+ * Deterministic (every sum in a fixed order).  Workspace:
+ * dspark_sts_fit_workspace_size().  Limits: gamma <= 64, G <= 65535, N*gamma < 2^31.
+ * ---------------------------------------------------------------------------------- */
+DSPARK_API size_t dspark_sts_fit_workspace_size(int N, int gamma, int G, int M);
+
+DSPARK_API dspark_status dspark_sts_fit(
+    int N, int gamma, const float* z, const int32_t* acc_len, const float* grid, int G, int M,
+    float* T_out, float* ece_out, void* workspace, size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -63,6 +63,10 @@ def _load_library():
     lib.dspark_rnn_draft.restype = i32
     lib.dspark_verify_rnn.argtypes = ([i32] * 7 + [P] * 4 + [P] * 5 + [f32, P, u64, u64] + [P] * 3 + [P, sz, P])
     lib.dspark_verify_rnn.restype = i32
+    lib.dspark_sts_fit_workspace_size.restype = sz
+    lib.dspark_sts_fit_workspace_size.argtypes = [i32] * 4
+    lib.dspark_sts_fit.argtypes = [i32, i32, P, P, P, i32, i32, P, P, P, sz, P]
+    lib.dspark_sts_fit.restype = i32
     for fn in ("dspark_markov_draft", "dspark_schedule", "dspark_verify", "dspark_workspace_status"):
         getattr(lib, fn).restype = i32
     return lib
@@ -356,6 +360,31 @@ def verify_rnn(target, U, state, Wo, x0, x, logq, lse_q, ell, temperature, req_i
                                float(temperature), _p(req_id), int(seed), int(rnd), _p(out["n_acc"]),
                                _p(out["tokens"]), _p(out["n_out"]), _p(ws), ws.numel(), _stream(stream))
     _check(st, "dspark_verify_rnn")
+    return out
+
+
+def sts_fit_workspace_size(N, gamma, G, M) -> int:
+    return int(lib.dspark_sts_fit_workspace_size(N, gamma, G, M))
+
+
+def sts_fit(z, acc_len, grid, M, out=None, ws=None, stream=None):
+    """Per-position confidence temperatures fitted left to right on held-out samples
+    (dspark_sts_fit).  z [N,gamma] fp32 logits, acc_len [N] int32, grid [G] fp32.
+    Returns dict T [gamma], ece [gamma]."""
+    N, gamma = z.shape
+    G = grid.shape[0]
+    _cuda(z, "z", torch.float32)
+    _cuda(acc_len, "acc_len", torch.int32)
+    _cuda(grid, "grid", torch.float32)
+    dev = z.device
+    if out is None:
+        out = dict(T=torch.empty(gamma, dtype=torch.float32, device=dev),
+                   ece=torch.empty(gamma, dtype=torch.float32, device=dev))
+    if ws is None:
+        ws = workspace(sts_fit_workspace_size(N, gamma, G, M), dev)
+    st = lib.dspark_sts_fit(N, gamma, _p(z), _p(acc_len), _p(grid), G, int(M), _p(out["T"]), _p(out["ece"]), _p(ws),
+                            ws.numel(), _stream(stream))
+    _check(st, "dspark_sts_fit")
     return out
 
 

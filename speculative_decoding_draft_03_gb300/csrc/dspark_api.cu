@@ -643,4 +643,63 @@ dspark_status dspark_verify_rnn(int R, int gamma, int V, int ns, int dtype_t, in
                      ws_bytes, stream);
 }
 
+namespace {
+struct StsLayout {
+  size_t zt, prefix, part, ece_g, total;
+  int S;
+};
+StsLayout sts_layout(int N, int gamma, int G, int M) {
+  StsLayout L;
+  L.S = dspark::sts_num_chunks(N);
+  size_t off = 256;
+  L.zt = off;
+  off += dspark::align256(sizeof(float) * (size_t)N * gamma);
+  L.prefix = off;
+  off += dspark::align256(sizeof(float) * (size_t)N);
+  L.part = off;
+  off += dspark::align256(sizeof(float) * (size_t)G * L.S * M);
+  L.ece_g = off;
+  off += dspark::align256(sizeof(double) * (size_t)G);
+  L.total = off;
+  return L;
+}
+}  // namespace
+
+size_t dspark_sts_fit_workspace_size(int N, int gamma, int G, int M) {
+  if (N < 1 || gamma < 1 || G < 1 || M < 1) return 0;
+  return sts_layout(N, gamma, G, M).total;
+}
+
+dspark_status dspark_sts_fit(int N, int gamma, const float* z, const int32_t* acc_len, const float* grid, int G,
+                             int M, float* T_out, float* ece_out, void* workspace, size_t ws_bytes, void* stream) {
+  if (N < 1 || gamma < 1 || G < 1 || M < 1)
+    return fail(DSPARK_INVALID_ARG, "sizes must be positive (N=%d gamma=%d G=%d M=%d)", N, gamma, G, M);
+  if (gamma > kMaxGamma) return fail(DSPARK_UNSUPPORTED_SHAPE, "gamma=%d exceeds %d", gamma, kMaxGamma);
+  if (M > dspark::kStsMaxBins) return fail(DSPARK_UNSUPPORTED_SHAPE, "M=%d bins exceed %d", M, dspark::kStsMaxBins);
+  if (G > 65535) return fail(DSPARK_UNSUPPORTED_SHAPE, "G=%d candidates exceed 65535", G);
+  if ((long long)N * gamma > (1ll << 31) - 1) return fail(DSPARK_UNSUPPORTED_SHAPE, "N*gamma too large");
+  CHECK_PTR(z);
+  CHECK_PTR(acc_len);
+  CHECK_PTR(grid);
+  CHECK_PTR(T_out);
+  CHECK_PTR(ece_out);
+  CHECK_PTR(workspace);
+  if (!aligned256(workspace)) return fail(DSPARK_INVALID_ARG, "workspace must be 256-byte aligned");
+  const StsLayout L = sts_layout(N, gamma, G, M);
+  if (ws_bytes < L.total) return fail(DSPARK_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, L.total);
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  dspark::StsArgs a = {};
+  a.N = N; a.gamma = gamma; a.G = G; a.M = M;
+  a.z = z; a.acc_len = acc_len; a.grid = grid; a.T_out = T_out; a.ece_out = ece_out;
+  a.status = reinterpret_cast<dspark::DeviceStatus*>(ws);
+  a.zt = reinterpret_cast<float*>(ws + L.zt);
+  a.prefix = reinterpret_cast<float*>(ws + L.prefix);
+  a.part = reinterpret_cast<float*>(ws + L.part);
+  a.ece_g = reinterpret_cast<double*>(ws + L.ece_g);
+  a.S = L.S;
+  cudaError_t e = dspark::launch_sts_fit(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "sts_fit");
+  return DSPARK_OK;
+}
+
 }  // extern "C"

@@ -119,6 +119,25 @@ struct OverlapArgs {
   int npart;
 };
 
+// Sequential temperature scaling on held-out data (N samples, gamma positions, G grid
+// candidates, M <= kStsMaxBins calibration bins).
+constexpr int kStsMaxBins = 16;
+struct StsArgs {
+  int N, gamma, G, M;
+  const float* z;          // [N, gamma] confidence logits
+  const int32_t* acc_len;  // [N]
+  const float* grid;       // [G]
+  float* T_out;            // [gamma]
+  float* ece_out;          // [gamma]
+  // workspace pieces
+  DeviceStatus* status;
+  float* zt;               // [gamma, N]
+  float* prefix;           // [N] prod_{i<k} sigmoid(z_i / T_i)
+  float* part;             // [G, S, M] per-chunk bin sums of p - o
+  double* ece_g;           // [G]
+  int S;                   // sample chunks
+};
+
 // Launch with programmatic stream serialization (the kernel must call griddep_wait()
 // before its first dependent memory access).
 template <typename... KArgs, typename... Args>
@@ -180,5 +199,8 @@ int residual_num_partials(int R, int V, int rank, int dtype_w);
 cudaError_t launch_overlap(const OverlapArgs& a, cudaStream_t s);
 cudaError_t launch_overlap_tc(const OverlapArgs& a, cudaStream_t s);
 int overlap_num_partials(int R, int gamma, int V, int rank, int dtype_w);
+
+int sts_num_chunks(int N);
+cudaError_t launch_sts_fit(const StsArgs& a, cudaStream_t s);
 
 }  // namespace dspark

@@ -244,3 +244,23 @@ def test_verify_rnn_validation(b):
         assert call(null=[k]) == 1, k
     assert "state" in (call(null=[2]) and b.lib.dspark_last_error_message().decode())
     assert call(ws=100) == 3
+
+
+def test_sts_fit_validation(b):
+    P = _fake(6)
+    L = b.lib.dspark_sts_fit
+
+    def call(N=100, g=4, G=8, M=15, ws=1 << 30, null=()):
+        p = [None if k in null else P[k] for k in range(6)]
+        return L(N, g, p[0], p[1], p[2], G, M, p[3], p[4], p[5], ws, None)
+
+    assert call(N=0) == 1
+    assert call(G=0) == 1
+    assert call(M=0) == 1
+    assert call(g=65) == 2
+    assert call(M=17) == 2
+    assert call(G=70000) == 2
+    for k in range(6):
+        assert call(null=(k,)) == 1, k
+    assert call(ws=100) == 3
+    assert b.sts_fit_workspace_size(100, 4, 8, 15) > 256
