@@ -119,8 +119,8 @@ VerifyLayout verify_layout(int R, int gamma, int V, int rank, int dtype_w) {
 }
 
 struct OverlapLayout {
-  size_t W1g, lse_t, part, total;
-  int npart;
+  size_t W1g, lse_t, lse_part, part, total;
+  int npart, nchunk;
 };
 
 OverlapLayout overlap_layout(int R, int gamma, int V, int rank, int dtype_w) {
@@ -133,6 +133,9 @@ OverlapLayout overlap_layout(int R, int gamma, int V, int rank, int dtype_w) {
   off += align256(elem_size(dtype_w) * (size_t)round_up_rows((int)rows) * rank);
   L.lse_t = off;
   off += align256(4 * rows);
+  L.nchunk = overlap_num_chunks(V);
+  L.lse_part = off;
+  off += align256(8 * rows * (size_t)L.nchunk);
   L.part = off;
   off += align256(4 * rows * (size_t)L.npart);
   L.total = off;
@@ -488,6 +491,8 @@ dspark_status dspark_acceptance_overlap(int R, int gamma, int V, int rank, int d
   if (gamma > kMaxGamma) return fail(DSPARK_UNSUPPORTED_SHAPE, "gamma=%d exceeds %d", gamma, kMaxGamma);
   if ((long long)V > (1ll << 30)) return fail(DSPARK_UNSUPPORTED_SHAPE, "V=%d too large", V);
   if ((long long)R * gamma > (1ll << 24)) return fail(DSPARK_UNSUPPORTED_SHAPE, "R*gamma too large");
+  if ((long long)R * gamma * dspark::overlap_num_chunks(V) > (1ll << 31) - 1)
+    return fail(DSPARK_UNSUPPORTED_SHAPE, "R*gamma*ceil(V/8192) exceeds 2^31-1");
   // the CUDA-core bias pass takes blocks of 4 positions along the grid's y dimension
   if (!dspark::tc_supported(V, rank, dtype_w) && ((long long)R * gamma + 3) / 4 > 65535)
     return fail(DSPARK_UNSUPPORTED_SHAPE, "R*gamma=%lld exceeds 262140 without the tensor-core path",
@@ -523,6 +528,8 @@ dspark_status dspark_acceptance_overlap(int R, int gamma, int V, int rank, int d
   a.status = reinterpret_cast<dspark::DeviceStatus*>(ws);
   a.W1g = ws + L.W1g;
   a.lse_t = reinterpret_cast<float*>(ws + L.lse_t);
+  a.lse_part = reinterpret_cast<float2*>(ws + L.lse_part);
+  a.nchunk = L.nchunk;
   a.part = reinterpret_cast<float*>(ws + L.part);
   a.npart = L.npart;
   cudaError_t e = dspark::launch_overlap(a, reinterpret_cast<cudaStream_t>(stream));

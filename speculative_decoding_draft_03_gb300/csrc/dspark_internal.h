@@ -115,6 +115,8 @@ struct OverlapArgs {
   DeviceStatus* status;
   void* W1g;            // [round_up_rows(R*gamma), rank] factor rows W1[x_{j-1}] (zero where unused)
   float* lse_t;         // [R*gamma] target log-normaliser of row j-1 (/T)
+  float2* lse_part;     // [R*gamma, nchunk] per-chunk (max, sum exp) of those rows
+  int nchunk;
   float* part;          // [npart, R*gamma] partial sums of min(q, p)
   int npart;
 };
@@ -199,6 +201,7 @@ int residual_num_partials(int R, int V, int rank, int dtype_w);
 cudaError_t launch_overlap(const OverlapArgs& a, cudaStream_t s);
 cudaError_t launch_overlap_tc(const OverlapArgs& a, cudaStream_t s);
 int overlap_num_partials(int R, int gamma, int V, int rank, int dtype_w);
+int overlap_num_chunks(int V);
 
 int sts_num_chunks(int N);
 cudaError_t launch_sts_fit(const StsArgs& a, cudaStream_t s);

@@ -11,8 +11,10 @@
 // picture").  The confidence head is trained against this label; evaluating it on
 // verified rounds measures how well c_j is calibrated.
 //
-//   overlap_prepare   one CTA per flattened position: the factor row W1[x_{j-1}] (the A
-//                     operand of the bias contraction) and lse of target row j-1 / T
+//   overlap_prepare   CTA (flattened position, 8192-id chunk): the chunk's softmax
+//                     statistics of target row j-1 / T, and the factor row W1[x_{j-1}]
+//                     (the A operand of the bias contraction)
+//   overlap_lse       the chunks' statistics -> lse of each position's target row
 //   bias pass         the bias rows W1[x_{j-1}] W2 for all positions at once, on the
 //                     tensor cores (draft_step_tc_kernel in overlap mode) or on CUDA
 //                     cores (overlap_step_simt below); each CTA writes one partial sum
@@ -24,7 +26,10 @@
 
 namespace dspark {
 
-constexpr int kOvlThreads = 512;
+constexpr int kOvlThreads = 256;
+constexpr int kOvlChunk = 8192;  // vocabulary ids per CTA of the lse pass (4 runs of 8 per thread)
+
+int overlap_num_chunks(int V) { return (V + kOvlChunk - 1) / kOvlChunk; }
 
 // 8 consecutive entries of a logit row as fp32 (V % 8 == 0: the run is inside the row).
 __device__ __forceinline__ void load8(const void* base, int dtype, size_t idx, float (&x)[8]) {
@@ -60,18 +65,19 @@ __device__ __forceinline__ void online_add(float& m, float& s, float x) {
   }
 }
 
+// CTA (position i, vocabulary chunk c): chunk c's (max, sum exp) of target row j-1 / T,
+// and for c = 0 the position's factor row (zero where the position is not evaluated).
 __global__ void __launch_bounds__(kOvlThreads) overlap_prepare_kernel(OverlapArgs a) {
   griddep_allow_next();
   griddep_wait();
-  const int i = blockIdx.x;
+  const int i = blockIdx.x / a.nchunk, c = blockIdx.x % a.nchunk;
   const int r = i / a.gamma, j = i % a.gamma + 1;
-  if (a.ell != nullptr && j == 1 && threadIdx.x == 0) {
+  if (a.ell != nullptr && j == 1 && c == 0 && threadIdx.x == 0) {
     const int l = __ldg(a.ell + r);
     if (l < 0 || l > a.gamma) report_bad_input(a.status, 31);
   }
   const bool valid = j <= overlap_len(a, r);
-  if (threadIdx.x < 32) {
-    // factor row of the position (zero where the position is not evaluated)
+  if (c == 0 && threadIdx.x < 32) {
     int xp = 0;
     if (valid) {
       const int raw = j == 1 ? __ldg(a.x0 + r) : __ldg(a.x + (size_t)r * a.gamma + (j - 2));
@@ -81,37 +87,46 @@ __global__ void __launch_bounds__(kOvlThreads) overlap_prepare_kernel(OverlapArg
     if (a.dtype_w == DSPARK_F32) {
       const float* w1 = reinterpret_cast<const float*>(a.W1);
       float* g = reinterpret_cast<float*>(a.W1g);
-      for (int c = threadIdx.x; c < a.rank; c += 32) g[dst + c] = valid ? __ldg(w1 + src + c) : 0.f;
+      for (int e = threadIdx.x; e < a.rank; e += 32) g[dst + e] = valid ? __ldg(w1 + src + e) : 0.f;
     } else {
       const unsigned short* w1 = reinterpret_cast<const unsigned short*>(a.W1);
       unsigned short* g = reinterpret_cast<unsigned short*>(a.W1g);
-      for (int c = threadIdx.x; c < a.rank; c += 32) g[dst + c] = valid ? __ldg(w1 + src + c) : (unsigned short)0;
+      for (int e = threadIdx.x; e < a.rank; e += 32) g[dst + e] = valid ? __ldg(w1 + src + e) : (unsigned short)0;
     }
   }
   if (!valid) {
-    if (threadIdx.x == 0) a.lse_t[i] = NAN;
+    if (threadIdx.x == 0) a.lse_part[(size_t)i * a.nchunk + c] = make_float2(-INFINITY, 0.f);
     return;  // uniform across the CTA
   }
-  // log-sum-exp of target row j-1 scaled by 1/T: per-thread online statistics, two
-  // 8-element runs in flight per iteration
   const size_t trow = ((size_t)r * (a.gamma + 1) + (j - 1)) * (size_t)a.V;
+  const int v0 = c * kOvlChunk, v1 = min(v0 + kOvlChunk, a.V);
   float m = -INFINITY, s = 0.f;
   if (a.V % 8 == 0) {
-    const int step = kOvlThreads * 8;
-    for (int v = threadIdx.x * 8; v < a.V; v += 2 * step) {
-      float x0[8], x1[8];
-      const bool two = v + step < a.V;
-      load8(a.target, a.dtype_t, trow + v, x0);
-      if (two) load8(a.target, a.dtype_t, trow + v + step, x1);
+    // kOvlChunk / (8 * kOvlThreads) runs of 8 per thread, all loaded before use
+    constexpr int kRuns = kOvlChunk / (8 * kOvlThreads);
+    float x[kRuns][8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) online_add(m, s, x0[e] * a.inv_temp);
-      if (two) {
+    for (int u = 0; u < kRuns; ++u) {
+      const int v = v0 + (u * kOvlThreads + threadIdx.x) * 8;
+      if (v < v1) {
+        load8(a.target, a.dtype_t, trow + v, x[u]);
+      } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) online_add(m, s, x1[e] * a.inv_temp);
+        for (int e = 0; e < 8; ++e) x[u][e] = -INFINITY;
       }
     }
+#pragma unroll
+    for (int u = 0; u < kRuns; ++u)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) m = fmaxf(m, x[u][e] * a.inv_temp);
+    if (m > -INFINITY)
+#pragma unroll
+      for (int u = 0; u < kRuns; ++u)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s += __expf(x[u][e] * a.inv_temp - m);
   } else {
-    for (int v = threadIdx.x; v < a.V; v += kOvlThreads) online_add(m, s, load_elem(a.target, a.dtype_t, trow + v) * a.inv_temp);
+    for (int v = v0 + threadIdx.x; v < v1; v += kOvlThreads)
+      online_add(m, s, load_elem(a.target, a.dtype_t, trow + v) * a.inv_temp);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -133,8 +148,27 @@ __global__ void __launch_bounds__(kOvlThreads) overlap_prepare_kernel(OverlapArg
       const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
       lse_merge(m, s, m2, s2);
     }
-    if (lane == 0) a.lse_t[i] = m + logf(s);
+    if (lane == 0) a.lse_part[(size_t)i * a.nchunk + c] = make_float2(m, s);
   }
+}
+
+// One thread per position: lse of target row j-1 / T from the chunks, in chunk order
+// (NaN where the position is not evaluated).
+__global__ void overlap_lse_kernel(OverlapArgs a) {
+  griddep_allow_next();
+  griddep_wait();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= a.R * a.gamma) return;
+  if ((i % a.gamma) + 1 > overlap_len(a, i / a.gamma)) {
+    a.lse_t[i] = NAN;
+    return;
+  }
+  float m = -INFINITY, s = 0.f;
+  for (int c = 0; c < a.nchunk; ++c) {
+    const float2 p = a.lse_part[(size_t)i * a.nchunk + c];
+    lse_merge(m, s, p.x, p.y);
+  }
+  a.lse_t[i] = m + logf(s);
 }
 
 // CUDA-core bias pass (fp32 weights or shapes the tensor-core path does not take).
@@ -253,8 +287,10 @@ int overlap_num_partials(int R, int gamma, int V, int rank, int dtype_w) {
 
 cudaError_t launch_overlap(const OverlapArgs& a, cudaStream_t s) {
   const int rows = a.R * a.gamma;
-  cudaError_t e = launch_pdl(overlap_prepare_kernel, dim3(rows), dim3(kOvlThreads), 0, s, a);
+  cudaError_t e = launch_pdl(overlap_prepare_kernel, dim3((unsigned)((size_t)rows * a.nchunk)), dim3(kOvlThreads), 0,
+                             s, a);
   if (e != cudaSuccess) return e;
+  if ((e = launch_pdl(overlap_lse_kernel, dim3((rows + 255) / 256), dim3(256), 0, s, a)) != cudaSuccess) return e;
   int npart;
   if (tc_supported(a.V, a.rank, a.dtype_w)) {
     if ((e = launch_overlap_tc(a, s)) != cudaSuccess) return e;

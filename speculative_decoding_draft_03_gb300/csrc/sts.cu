@@ -69,17 +69,28 @@ __global__ void __launch_bounds__(kStsThreads) sts_eval_kernel(StsArgs a, int k)
 #pragma unroll
     for (int b = 0; b < kStsMaxBins; ++b) gap[c][b][threadIdx.x] = 0.f;
   const float fM = (float)a.M;
-  for (int u = 0; u < kStsPerThread; ++u) {
-    const int n = s * kStsChunk + u * kStsThreads + threadIdx.x;
-    if (n >= a.N) break;
-    const float pre = k == 1 ? 1.f : a.prefix[n];
-    const float zn = zk[n];
-    const float o = __ldg(a.acc_len + n) >= k ? 1.f : 0.f;
+  // kStsBatch samples per step: their loads are issued before any is used
+  constexpr int kStsBatch = 8;
+  for (int u0 = 0; u0 < kStsPerThread; u0 += kStsBatch) {
+    float pre[kStsBatch], zn[kStsBatch], o[kStsBatch];
+    bool in[kStsBatch];
 #pragma unroll
-    for (int c = 0; c < kStsCands; ++c) {
-      const float p = pre * __frcp_rn(1.f + __expf(-zn * inv[c]));
-      const int bin = min((int)(p * fM), a.M - 1);
-      gap[c][bin][threadIdx.x] += p - o;
+    for (int u = 0; u < kStsBatch; ++u) {
+      const int n = s * kStsChunk + (u0 + u) * kStsThreads + threadIdx.x;
+      in[u] = n < a.N;
+      pre[u] = (k == 1 || !in[u]) ? 1.f : a.prefix[n];
+      zn[u] = in[u] ? zk[n] : 0.f;
+      o[u] = (in[u] && __ldg(a.acc_len + n) >= k) ? 1.f : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kStsBatch; ++u) {
+      if (!in[u]) continue;
+#pragma unroll
+      for (int c = 0; c < kStsCands; ++c) {
+        const float p = pre[u] * __frcp_rn(1.f + __expf(-zn[u] * inv[c]));
+        const int bin = min((int)(p * fM), a.M - 1);
+        gap[c][bin][threadIdx.x] += p - o[u];
+      }
     }
   }
   __shared__ float red[kStsCands][kStsThreads / 32][kStsMaxBins];
