@@ -152,23 +152,29 @@ __global__ void __launch_bounds__(kOvlThreads) overlap_prepare_kernel(OverlapArg
   }
 }
 
-// One thread per position: lse of target row j-1 / T from the chunks, in chunk order
-// (NaN where the position is not evaluated).
+// One warp per position: lse of target row j-1 / T from the chunks (lanes take the
+// chunks, merged by a fixed shuffle tree); NaN where the position is not evaluated.
 __global__ void overlap_lse_kernel(OverlapArgs a) {
   griddep_allow_next();
   griddep_wait();
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
   if (i >= a.R * a.gamma) return;
   if ((i % a.gamma) + 1 > overlap_len(a, i / a.gamma)) {
-    a.lse_t[i] = NAN;
+    if (lane == 0) a.lse_t[i] = NAN;
     return;
   }
   float m = -INFINITY, s = 0.f;
-  for (int c = 0; c < a.nchunk; ++c) {
+  for (int c = lane; c < a.nchunk; c += 32) {
     const float2 p = a.lse_part[(size_t)i * a.nchunk + c];
     lse_merge(m, s, p.x, p.y);
   }
-  a.lse_t[i] = m + logf(s);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    lse_merge(m, s, m2, s2);
+  }
+  if (lane == 0) a.lse_t[i] = m + logf(s);
 }
 
 // CUDA-core bias pass (fp32 weights or shapes the tensor-core path does not take).
@@ -290,7 +296,9 @@ cudaError_t launch_overlap(const OverlapArgs& a, cudaStream_t s) {
   cudaError_t e = launch_pdl(overlap_prepare_kernel, dim3((unsigned)((size_t)rows * a.nchunk)), dim3(kOvlThreads), 0,
                              s, a);
   if (e != cudaSuccess) return e;
-  if ((e = launch_pdl(overlap_lse_kernel, dim3((rows + 255) / 256), dim3(256), 0, s, a)) != cudaSuccess) return e;
+  if ((e = launch_pdl(overlap_lse_kernel, dim3((unsigned)(((size_t)rows * 32 + 255) / 256)), dim3(256), 0, s, a)) !=
+      cudaSuccess)
+    return e;
   int npart;
   if (tc_supported(a.V, a.rank, a.dtype_w)) {
     if ((e = launch_overlap_tc(a, s)) != cudaSuccess) return e;

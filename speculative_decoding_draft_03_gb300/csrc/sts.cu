@@ -15,7 +15,7 @@
 //
 //   sts_prepare   z -> position-major copy (coalesced reads per position)
 //   sts_eval      CTA (4 candidates, chunk of 4096 samples): per-bin sums of p - o
-//   sts_ece       warp per candidate: ECE, binary64 over the chunks
+//   sts_ece       warp per candidate: ECE (chunk sums in fp32, bins added in binary64)
 //   sts_update    argmin over the candidates (every CTA), T_k recorded, and
 //                 prefix[n] *= sigmoid(z[n,k] / T_k) for the next position
 // All sums run in a fixed order, so the fit is deterministic.
@@ -114,8 +114,9 @@ __global__ void __launch_bounds__(kStsThreads) sts_eval_kernel(StsArgs a, int k)
   }
 }
 
-// One warp per candidate: ECE = sum over bins of |sum over chunks of the bin sums| / N,
-// in binary64; lanes take the chunks, the lane sums are added by a fixed shuffle tree.
+// One warp per candidate: ECE = sum over bins of |sum over chunks of the bin sums| / N.
+// Lanes take the chunks (fp32), the lane sums are added by a fixed shuffle tree, and the
+// bins are added in binary64.
 __global__ void __launch_bounds__(kStsThreads) sts_ece_kernel(StsArgs a) {
   griddep_allow_next();
   griddep_wait();
@@ -123,22 +124,22 @@ __global__ void __launch_bounds__(kStsThreads) sts_ece_kernel(StsArgs a) {
   const int g = blockIdx.x * (kStsThreads / 32) + (threadIdx.x >> 5);
   if (g >= a.G) return;
   const float T = __ldg(a.grid + g);
-  double v[kStsMaxBins];
+  float v[kStsMaxBins];
 #pragma unroll
-  for (int b = 0; b < kStsMaxBins; ++b) v[b] = 0.0;
+  for (int b = 0; b < kStsMaxBins; ++b) v[b] = 0.f;
   for (int s = lane; s < a.S; s += 32) {
     const float* pp = a.part + ((size_t)g * a.S + s) * a.M;
 #pragma unroll
     for (int b = 0; b < kStsMaxBins; ++b)
-      if (b < a.M) v[b] += (double)pp[b];
+      if (b < a.M) v[b] += pp[b];
   }
   double e = 0.0;
 #pragma unroll
   for (int b = 0; b < kStsMaxBins; ++b) {
-    double x = v[b];
+    float x = v[b];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    e += fabs(x);
+    e += fabs((double)x);
   }
   if (lane == 0) a.ece_g[g] = (T > 0.f && isfinite(T)) ? e / (double)a.N : INFINITY;
 }
