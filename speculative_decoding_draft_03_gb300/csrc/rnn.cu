@@ -29,7 +29,6 @@ constexpr int kHSplit = 512;     // hidden dimensions per split (CUDA-core proje
 constexpr int kCellReq = 4;      // requests per CTA of rnn_cell
 constexpr int kCellCols = 8;     // state columns per CTA of rnn_cell (x2: gate and candidate)
 constexpr int kCellSlices = 16;  // slices of the input vector per column
-constexpr int kCellBatch = 8;    // weights loaded per thread before they are used
 constexpr int kCellThreads = 2 * kCellCols * kCellSlices;
 
 // hpart[split][row][c] = sum over the split's hidden dimensions i of h[row][i] Wh[i][c].
@@ -117,6 +116,10 @@ __device__ __forceinline__ void store_state(void* base, int dtype, size_t idx, f
 // q + kCellSlices, ... for all the CTA's requests, so each weight is loaded once per
 // CTA; the slices are then added in a fixed order and kCellCols x kCellReq threads
 // finish the update.
+// BATCH: weights loaded per thread before any is used; STAGE: input entries per thread and
+// step.  Small batches issue every load at once (the cell is a chain of L2 round trips);
+// large batches use fewer registers across their thousands of CTAs.
+template <int BATCH, int STAGE>
 __global__ void __launch_bounds__(kCellThreads) rnn_cell_kernel(DraftArgs a, int k, int tc) {
   extern __shared__ float us[];  // [kCellReq][ns + ne]: s_{k-1}; E[x_{k-1}]
   __shared__ int xs[kCellReq];
@@ -130,6 +133,20 @@ __global__ void __launch_bounds__(kCellThreads) rnn_cell_kernel(DraftArgs a, int
   const bool col_ok = c0 + (j % kCellCols) < ns;
   griddep_allow_next();
   griddep_wait();
+  // the finishing threads' bias and hidden-state projection, loaded ahead of the rest
+  float hb_g = 0.f, hb_c = 0.f;
+  {
+    const int cc = threadIdx.x % kCellCols, rr = threadIdx.x / kCellCols;
+    if (threadIdx.x < kCellCols * kCellReq && r0 + rr < a.R && c0 + cc < ns) {
+      hb_g = __ldg(a.bgc + c0 + cc);
+      hb_c = __ldg(a.bgc + ns + c0 + cc);
+      if (a.nsplit > 0) {  // split 0 holds the sum of all splits
+        const float* hp = a.hpart + (size_t)((r0 + rr) * a.gamma + (k - 1)) * n2;
+        hb_g += hp[c0 + cc];
+        hb_c += hp[ns + c0 + cc];
+      }
+    }
+  }
   if (threadIdx.x < kCellReq) {
     const int r = r0 + threadIdx.x;
     int x = 0;
@@ -155,11 +172,11 @@ __global__ void __launch_bounds__(kCellThreads) rnn_cell_kernel(DraftArgs a, int
       }
     }
   __syncthreads();
-  // four entries per thread and step, loaded before they are stored
-  for (int e0 = threadIdx.x; e0 < kCellReq * nu; e0 += 4 * blockDim.x) {
-    float v[4];
+  // STAGE entries per thread and step, loaded before they are stored
+  for (int e0 = threadIdx.x; e0 < kCellReq * nu; e0 += STAGE * blockDim.x) {
+    float v[STAGE];
 #pragma unroll
-    for (int u4 = 0; u4 < 4; ++u4) {
+    for (int u4 = 0; u4 < STAGE; ++u4) {
       const int e = e0 + u4 * blockDim.x;
       v[u4] = 0.f;
       if (e >= kCellReq * nu) continue;
@@ -173,7 +190,7 @@ __global__ void __launch_bounds__(kCellThreads) rnn_cell_kernel(DraftArgs a, int
       }
     }
 #pragma unroll
-    for (int u4 = 0; u4 < 4; ++u4)
+    for (int u4 = 0; u4 < STAGE; ++u4)
       if (e0 + u4 * blockDim.x < kCellReq * nu) us[e0 + u4 * blockDim.x] = v[u4];
   }
   __syncthreads();
@@ -182,13 +199,13 @@ __global__ void __launch_bounds__(kCellThreads) rnn_cell_kernel(DraftArgs a, int
   for (int rr = 0; rr < kCellReq; ++rr) acc[rr] = 0.f;
   if (col_ok) {
     int i = q;
-    // kCellBatch input entries per step: their weights are loaded before any is used
-    for (; i + (kCellBatch - 1) * kCellSlices < nu; i += kCellBatch * kCellSlices) {
-      float w[kCellBatch];
+    // BATCH input entries per step: their weights are loaded before any is used
+    for (; i + (BATCH - 1) * kCellSlices < nu; i += BATCH * kCellSlices) {
+      float w[BATCH];
 #pragma unroll
-      for (int u = 0; u < kCellBatch; ++u) w[u] = load_elem(a.Wse, a.dtype_w, (size_t)(i + u * kCellSlices) * n2 + cj);
+      for (int u = 0; u < BATCH; ++u) w[u] = load_elem(a.Wse, a.dtype_w, (size_t)(i + u * kCellSlices) * n2 + cj);
 #pragma unroll
-      for (int u = 0; u < kCellBatch; ++u)
+      for (int u = 0; u < BATCH; ++u)
 #pragma unroll
         for (int rr = 0; rr < kCellReq; ++rr) acc[rr] = fmaf(us[rr * nu + i + u * kCellSlices], w[u], acc[rr]);
     }
@@ -207,12 +224,7 @@ __global__ void __launch_bounds__(kCellThreads) rnn_cell_kernel(DraftArgs a, int
   const int r = r0 + rr;
   if (r >= a.R || c >= ns) return;
   const int row = r * a.gamma + (k - 1);
-  float ag = __ldg(a.bgc + c), ac = __ldg(a.bgc + ns + c);
-  if (a.nsplit > 0) {  // split 0 holds the sum of all splits
-    const float* hp = a.hpart + (size_t)row * n2;
-    ag += hp[c];
-    ac += hp[ns + c];
-  }
+  float ag = hb_g, ac = hb_c;
 #pragma unroll
   for (int qq = 0; qq < kCellSlices; ++qq) {
     ag += red[qq][cc][rr];
@@ -263,7 +275,9 @@ cudaError_t launch_rnn_hproj(const DraftArgs& a, cudaStream_t s) {
 cudaError_t launch_rnn_cell(const DraftArgs& a, int k, bool tc, cudaStream_t s) {
   dim3 grid((a.R + kCellReq - 1) / kCellReq, (a.rank + kCellCols - 1) / kCellCols);
   const size_t smem = sizeof(float) * kCellReq * (a.rank + a.ne);
-  return launch_pdl(rnn_cell_kernel, grid, dim3(kCellThreads), smem, s, a, k, tc ? 1 : 0);
+  // few requests: every weight load at once; many: smaller batches (measured both ways)
+  if (a.R <= 64) return launch_pdl(rnn_cell_kernel<32, 8>, grid, dim3(kCellThreads), smem, s, a, k, tc ? 1 : 0);
+  return launch_pdl(rnn_cell_kernel<8, 4>, grid, dim3(kCellThreads), smem, s, a, k, tc ? 1 : 0);
 }
 
 cudaError_t launch_rnn_conf(const DraftArgs& a, cudaStream_t s) {
