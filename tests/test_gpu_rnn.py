@@ -152,3 +152,43 @@ def test_rnn_full_size_sampled_requests():
     R = w["R"]
     _check_positions(w, d, 2, np.array([0, R // 2, R - 1]), tally, 2e-3)
     tally.check_rate()
+
+
+@pytest.mark.parametrize("name,over", [("tiny", {}), ("qwen3-8b", dict(R=6, gamma=3, V=2056, d=64))])
+def test_rnn_without_hidden_state_or_embedding(name, over):
+    # d = 0 (no hidden-state path, no projection) and ne = 0 (no embedding): the cell runs
+    # on the state alone; each position checked given the GPU's previous state
+    from speculative_decoding_draft_03_gb300 import binding as b
+    w = _rnn_workload(name, **over)
+    R, gamma, ns = w["R"], w["gamma"], w["ns"]
+    dev = w["U"].device
+    Wse = w["Wse"][:ns].contiguous()  # state rows only
+    h0 = torch.zeros((R, gamma, 0), dtype=w["h"].dtype, device=dev)
+    Wh0 = torch.zeros((0, 2 * ns), dtype=w["Wse"].dtype, device=dev)
+    conf_w = w["conf_w"][w["d"]:].contiguous()  # the state part only
+    x0 = w["x0"]
+    out = b.rnn_draft(w["U"], None, Wse, Wh0, w["bgc"], w["Wo"], h0, conf_w, w["conf_b"], w["conf_logit_scale"],
+                      w["conf_temp"], w["temperature"], x0, w["req_id"], w["seed"], 7)
+    torch.cuda.synchronize()
+    bf16 = w["Wo"].dtype == torch.bfloat16
+    sg = _f64(_host(out["state"]))
+    x = _host(out["x"])
+    E0 = np.zeros((w["V"], 0), np.uint16 if bf16 else np.float32)
+    hrow = np.zeros(0, np.uint16 if bf16 else np.float32)
+    U = _host(w["U"])
+    conf = oracle.rnn_confidence(np.zeros((R, gamma, 0), np.float32), sg, _host(conf_w), w["conf_b"],
+                                 w["conf_logit_scale"], _host(w["conf_temp"]))
+    tol = 2e-3 if bf16 else 1e-5
+    boundary = 0
+    for r in range(R):
+        for k in range(1, gamma + 1):
+            s_prev = np.zeros(ns) if k == 1 else sg[r, k - 2]
+            s_ref = oracle.rnn_cell(s_prev, 0, E0, _host(Wse), _host(Wh0), _host(w["bgc"]), hrow)
+            lim = np.maximum(1.01 * _ulp(s_ref, True), 1e-6) if bf16 else 1e-6
+            assert (np.abs(sg[r, k - 1] - s_ref) <= lim).all(), (r, k)
+            ref = oracle.draft_row(U[r, k - 1], sg[r, k - 1], _host(w["Wo"]), w["temperature"], w["seed"], r, 7, k)
+            if x[r, k - 1] != ref["x"]:
+                assert ref["margin"] < BOUNDARY and x[r, k - 1] == ref["runner_up"]
+                boundary += 1
+            assert abs(_host(out["conf"])[r, k - 1] - conf[r, k - 1]) <= tol * max(conf[r, k - 1], 1e-12)
+    assert boundary <= 1

@@ -81,3 +81,34 @@ def test_sts_fit_zero_logits_closed_form():
     Tg, eg = _fit(z, L, np.array([0.5, 1.0, 2.0, 4.0], np.float32), 10)
     np.testing.assert_array_equal(Tg, [0.5, 0.5])
     np.testing.assert_allclose(eg, [0.0, 0.05], atol=1e-6)
+
+
+@pytest.mark.slow
+def test_sts_fit_full_size_local_optimality():
+    # the configuration the benchmark times (131072 samples, 7 positions, 256 candidates):
+    # at every position the GPU's temperature is at least as good as its grid neighbours
+    # (given the GPU's earlier temperatures) and its reported ECE is the oracle's there
+    N, gamma = 131072, 7
+    T_true = [1.0 + 0.5 * ((k % 3) - 1) for k in range(gamma)]
+    d = wl.sts_heldout(N, gamma, T_true, seed=0)
+    z, L = d["z"].numpy(), d["acc_len"].numpy()
+    grid = wl.sts_grid(256)
+    Tg, eg = _fit(z, L, grid, 15)
+    tol = 4.0 / N + 1e-6
+    g64 = grid.astype(np.float64)
+    for k in range(1, gamma + 1):
+        gi = int(np.argmin(np.abs(g64 - Tg[k - 1])))
+        e = oracle.sts_ece(z, L, Tg[:k - 1], k, g64[gi], 15)
+        for nb in (gi - 1, gi + 1):
+            if 0 <= nb < len(g64):
+                assert e <= oracle.sts_ece(z, L, Tg[:k - 1], k, g64[nb], 15) + tol, (k, nb)
+        assert abs(eg[k - 1] - e) <= tol, (k, eg[k - 1], e)
+
+
+def test_sts_fit_single_candidate():
+    d = wl.sts_heldout(3000, 2, (1.0, 2.0), seed=2)
+    z, L = d["z"].numpy(), d["acc_len"].numpy()
+    grid = np.array([1.7], np.float32)
+    Tg, eg = _fit(z, L, grid, 12)
+    np.testing.assert_array_equal(Tg, [grid[0], grid[0]])
+    _check(z, L, grid, 12, Tg, eg)
