@@ -1,14 +1,18 @@
 /*
  * dspark.h — C ABI of the DSpark per-round speculative-decoding hot path on GB300
- * (sm_103a): Markov-head draft -> confidence scheduler -> exact verification.
+ * (sm_103a): Markov-head draft -> confidence scheduler -> exact verification, with the
+ * recurrent-head draft, verification on a flattened target batch, the fixed-cutoff
+ * scheduler, the acceptance-overlap diagnostic and sequential temperature scaling.
  *
  * The method is the one described on the pages about DSpark (Cheng, Yu, Shao et al.,
  * "DSpark: Confidence-Scheduled Speculative Decoding with Semi-Autoregressive
  * Generation", arXiv 2607.05147):
  *   - numb3r33 blog "DSpark: confidence-scheduled speculative decoding" (sections
  *     "One-token exactness", "Prefix survival and accepted length", "Markov sequential
- *     head", "Confidence head", "Sequential temperature scaling", "Scheduler
- *     objective", "Greedy prefix allocation", "Async scheduler in practice");
+ *     head", "RNN sequential head", "Confidence head", "Total variation label",
+ *     "Sequential temperature scaling", "Scheduler objective", "Greedy prefix
+ *     allocation", "Async scheduler in practice", "Variable-length verification without
+ *     wasting kernels");
  *   - vllmbangkok blog "DSpark: Confidence-Scheduled Speculative Decoding with
  *     Semi-Autoregressive Generation" (§4.1, §4.2.1, §4.2.2);
  *   - edgeai1 knowledge base "DSpark 精读" (§2 proposal law, §4 confidence head and

@@ -264,3 +264,12 @@ def test_sts_fit_validation(b):
         assert call(null=(k,)) == 1, k
     assert call(ws=100) == 3
     assert b.sts_fit_workspace_size(100, 4, 8, 15) > 256
+
+
+def test_header_is_plain_c(tmp_path):
+    # the boundary carries no C++ or CUDA types: the header compiles as C99 on its own
+    src = tmp_path / "use.c"
+    src.write_text('#include "dspark.h"\nint main(void) { return DSPARK_OK + (int)sizeof(dspark_status); }\n')
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), "-fsyntax-only",
+                        str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
