@@ -338,7 +338,10 @@ cudaError_t launch_schedule(int R, int gamma, const float* conf, const double* s
   const size_t smem = schedule_smem_bytes(R, gamma);
   cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(schedule_kernel, dim3(1), dim3(kSchedThreads), smem, s, R, gamma, conf, sps, mode, conf_hist,
+  // up to 4096 candidates, 512 threads (at most 8 per thread, as the scan needs): fewer
+  // warps meet at every barrier (1% faster at 2048 candidates)
+  const int threads = (R * gamma <= 4096) ? 512 : kSchedThreads;
+  return launch_pdl(schedule_kernel, dim3(1), dim3(threads), smem, s, R, gamma, conf, sps, mode, conf_hist,
                     fixed_len, ell_out, B_out, tau_out, status);
 }
 
