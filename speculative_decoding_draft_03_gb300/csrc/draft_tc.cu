@@ -514,11 +514,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     int pos = p.k;
     int req = r;
     float lse_q = 0.f, lse_t = 0.f;
+    // residual mode: a negative position marks a bonus draw (every verified draft
+    // survived): Gumbel-max of ln p alone, no draft law, and no U row (the position can
+    // lie one past the block)
+    bool bonus_row = false;
     if constexpr (MODE == kModeResidual) {
-      pos = valid ? p.jstar[r] : 0;
+      const int raw = valid ? p.jstar[r] : 0;
+      bonus_row = raw < 0;
+      pos = raw < 0 ? -raw : raw;
       valid = valid && pos > 0;
       if (valid) {
-        lse_q = __ldg(p.lse_q + (size_t)r * p.gamma + (pos - 1));
+        lse_q = bonus_row ? 0.f : __ldg(p.lse_q + (size_t)r * p.gamma + (pos - 1));
         lse_t = p.lse_t[r];
       }
     }
@@ -537,9 +543,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const PhiloxRow prow =
         philox_row(rng_row(p.seed, (MODE != kModeOverlap && valid) ? __ldg(p.req_id + r) : 0, p.round,
                            kDraftMath ? kStreamDraft : kStreamCorrect, (uint32_t)pos));
+    const bool u_valid = valid && !bonus_row;
     const size_t urow = MODE == kModeOverlap
                             ? (size_t)(valid ? r : 0) * (size_t)p.V
-                            : ((size_t)(valid ? r : 0) * p.gamma + (valid ? pos - 1 : 0)) * (size_t)p.V;
+                            : ((size_t)(u_valid ? r : 0) * p.gamma + (u_valid ? pos - 1 : 0)) * (size_t)p.V;
     const size_t trow =
         (valid ? target_row_index(p.t_off, p.n_trows, p.gamma, req, pos - 1, p.status) : 0) * (size_t)p.V;
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
@@ -552,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int vt = (group + t * p.ngroups) * kN;
 #pragma unroll
       for (int ps = 0; ps < kPass; ++ps)
-        load_run8(p.U, p.dtype_u, urow, vt + col0 + ps * kCols, p.V, valid && t < my_tiles, dst[ps]);
+        load_run8(p.U, p.dtype_u, urow, vt + col0 + ps * kCols, p.V, u_valid && t < my_tiles, dst[ps]);
     };
     const int my_box = col0 / p.ubox_cols;
     const int box_col = col0 % p.ubox_cols;
@@ -778,7 +785,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             gmax = fmaxf(gmax, lp[i]);
           }
           // ln(p - q) <= ln p: neither draw can improve once ln p + G_max is below both keys
-          if (st.idx >= 0 && fb.idx >= 0 && gmax + kGumbelMax < st.key && gmax + kGumbelMax < fb.key) continue;
+          // (a bonus row keeps only the ln p record)
+          if (fb.idx >= 0 && gmax + kGumbelMax < fb.key &&
+              (bonus_row || (st.idx >= 0 && gmax + kGumbelMax < st.key)))
+            continue;
 #pragma unroll
           for (int g4 = 0; g4 < 2; ++g4) {
             const Philox4 bits = prow.block((uint32_t)((vb >> 2) + g4));
@@ -792,7 +802,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float pv = __expf(lp[4 * g4 + e]);
               const float rho = pv - __expf(z[4 * g4 + e] - lse_q);
               const float w = one_minus_uniform(wd[e]);
-              const bool try1 = rho > 0.f && !(w >= rho * s1);
+              const bool try1 = !bonus_row && rho > 0.f && !(w >= rho * s1);
               const bool try2 = !(w >= pv * s2);
               if (!try1 && !try2) continue;
               const float g = gumbel_from_bits(wd[e]);

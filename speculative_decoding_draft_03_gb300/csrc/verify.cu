@@ -11,15 +11,20 @@
 //   verify_plan      ell -> compact list of the target rows that must be read:
 //                    rows 0..ell_r of request r (sum_r (ell_r + 1) rows)
 //   verify_rows      streams those rows once, coalesced and vectorised: per
-//                    (row, vocabulary chunk) item, taken from a work queue that holds
-//                    the bonus rows first, the (max, sum exp) of t/T and, on row ell_r,
-//                    the bonus Gumbel-max draw
-//   verify_accept    per request: row log-normalisers, the acceptance scan, the
-//                    bonus token, and the residual position j* when a draft is rejected
-//   residual_step    per rejected request: recompute the draft logits of position j*
-//                    (U + W1[x_{j*-1}] W2), q = exp(z - lse_q), p = exp(t/T - lse_t),
-//                    Gumbel-max of ln(p - q)+ (and of ln p, the rounding fallback)
-//   residual_combine merges the residual partials into the correction token.
+//                    (row, vocabulary chunk) item, taken from a work queue, the
+//                    (max, sum exp) of t/T
+//   verify_accept    per request: row log-normalisers, the acceptance scan, and the
+//                    position of the correction draw, n_acc + 1 (a residual draw after a
+//                    rejection, the bonus draw when every verified draft survived)
+//   residual_step    per request: the correction draw at n_acc + 1 from target row
+//                    n_acc.  After a rejection: recompute the draft logits of that
+//                    position (U + W1[x_{j*-1}] W2), q = exp(z - lse_q), p = exp(t/T -
+//                    lse_t), Gumbel-max of ln(p - q)+ (and of ln p, the rounding
+//                    fallback).  Bonus: the Gumbel-max of ln p alone, which has the
+//                    same winner as t/T + g.  Either way one pass over one target row
+//                    per request, so the bonus rows of requests that reject are never
+//                    sampled.
+//   residual_combine merges the correction partials into the emitted token.
 #include <climits>
 
 #include "dspark_common.cuh"
@@ -75,8 +80,8 @@ __global__ void __launch_bounds__(kPlanThreads) verify_plan_kernel(VerifyArgs a)
       a.row_req[base + t] = r;
       a.row_t[base + t] = t;
     }
-    // processing order: the bonus row (t = ell, which also draws a Gumbel race) of every
-    // request first, so that the heavier items start early; then rows 0..ell-1
+    // processing order: row t = ell of every request first (the correction draw reads
+    // it again), then rows 0..ell-1
     a.row_order[r] = base + n - 1;
     for (int t = 0; t + 1 < n; ++t) a.row_order[a.R + (base - r) + t] = base + t;
     a.jstar[r] = 0;
@@ -89,12 +94,8 @@ __global__ void __launch_bounds__(kPlanThreads) verify_plan_kernel(VerifyArgs a)
   }
 }
 
-// Per (row, chunk): (max, sum exp) of t/T and, on the bonus row, the Gumbel-max record
-// of t/T + g (stream 2, position ell+1).  Every thread keeps its kRowPer ids in
-// registers, so the chunk's maximum M is known before any exponential and before any
-// random draw.  The bonus draw first keys the chunk's (lowest-id) maximum exactly,
-// L = M + g; every other id then needs its Philox word only for the log-free test
-// 1-u >= exp(z - L), and evaluates its key only when it survives (a handful per chunk).
+// Per (row, chunk): (max, sum exp) of t/T.  Every thread keeps its kRowPer ids in
+// registers, so the chunk's maximum M is known before any exponential.
 constexpr int kRowPer = 32;
 
 __device__ __forceinline__ float block_max(float v, float* sm) {
@@ -109,30 +110,9 @@ __device__ __forceinline__ float block_max(float v, float* sm) {
   return r;
 }
 
-__device__ __forceinline__ int block_min(int v, int* sm) {
-  v = __reduce_min_sync(0xffffffffu, v);
-  if ((threadIdx.x & 31) == 0) sm[threadIdx.x >> 5] = v;
-  __syncthreads();
-  int r = sm[0];
-#pragma unroll
-  for (int w = 1; w < kRowThreads / 32; ++w) r = min(r, sm[w]);
-  __syncthreads();
-  return r;
-}
-
-// Order-preserving int code of a float key (max over codes = max over keys).
-__device__ __forceinline__ int key_code(float f) {
-  const int i = __float_as_int(f);
-  return i >= 0 ? i : i ^ 0x7FFFFFFF;
-}
-
-// Work items are (row position, chunk) pairs taken from a queue in row_order: every
-// request's bonus row first.  Per item the CTA needs:
-//  - the chunk maximum M (block max; every thread then sums exp(z - M) against the same
-//    M, so the partial sums add without rescaling);
-//  - on a bonus row, the Gumbel-max record: the lowest-id maximum is keyed exactly,
-//    L = M + g, and every other id needs only the log-free test 1-u >= exp(z - L)
-//    (computed branch-free for a batch of ids); the few survivors evaluate their keys.
+// Work items are (row position, chunk) pairs taken from a queue in row_order.  Per item
+// the CTA needs the chunk maximum M (block max; every thread then sums exp(z - M) against
+// the same M, so the partial sums add without rescaling).
 template <int DT>
 __global__ void __launch_bounds__(kRowThreads, 3) verify_rows_kernel(VerifyArgs a) {
   griddep_allow_next();
@@ -141,9 +121,6 @@ __global__ void __launch_bounds__(kRowThreads, 3) verify_rows_kernel(VerifyArgs 
   constexpr int NV = kRowPer / EPV;              // vectors per thread per item
   constexpr int kWarps = kRowThreads / 32;
   __shared__ float sm_f[kWarps];
-  __shared__ int sm_i[kWarps];
-  __shared__ int sm_key[kWarps], sm_idx[kWarps];
-  __shared__ float sm_z[kWarps];
   __shared__ int item_s;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int n_items = (*a.n_rows) * a.nchunk;
@@ -156,7 +133,6 @@ __global__ void __launch_bounds__(kRowThreads, 3) verify_rows_kernel(VerifyArgs 
     const int pos = item / a.nchunk, c = item % a.nchunk;
     const int row = a.row_order[pos];
     const int r = a.row_req[row], t = a.row_t[row];
-    const bool bonus = pos < a.R;  // the first R positions hold the rows t = ell_r
     const size_t rbase = target_row_index(a.t_off, a.n_trows, a.gamma, r, t, a.status) * a.V;
     const int v0 = c * a.chunk, v1 = min(v0 + a.chunk, a.V);
     // thread's ids: vector i covers v0 + (threadIdx.x + i*kRowThreads)*EPV + [0, EPV)
@@ -196,88 +172,11 @@ __global__ void __launch_bounds__(kRowThreads, 3) verify_rows_kernel(VerifyArgs 
     float ssum = 0.f;
 #pragma unroll
     for (int k = 0; k < kRowPer; ++k) ssum += __expf(z[k] - M);
-    float bkey = -INFINITY, bz = 0.f;
-    int bidx = -1;
-    if (bonus) {
-      int mi = INT_MAX;
-#pragma unroll
-      for (int i = 0; i < NV; ++i) {
-        const int vb = v0 + (threadIdx.x + i * kRowThreads) * EPV;
-#pragma unroll
-        for (int e = 0; e < EPV; ++e)
-          if (z[i * EPV + e] == M) mi = min(mi, vb + e);
-      }
-      mi = block_min(mi, sm_i);
-      if (mi == INT_MAX) {  // no finite maximum: NaN logits
-        report_bad_input(a.status, 13);
-        mi = v0;
-      }
-      const PhiloxRow prow =
-          philox_row(rng_row(a.seed, __ldg(a.req_id + r), a.round, kStreamCorrect, (uint32_t)(t + 1)));
-      const Philox4 wb = prow.block((uint32_t)mi >> 2);
-      const uint32_t wm = (mi & 3) == 0 ? wb.x : ((mi & 3) == 1 ? wb.y : ((mi & 3) == 2 ? wb.z : wb.w));
-      const float L = M + gumbel_from_bits(wm);
-      bkey = L;
-      bidx = mi;
-      bz = M;
-      // two batches of 16 ids: the words and the survivor mask without branches, then
-      // the (rare) survivors.  Ids past the row end have z = -inf and never survive.
-      constexpr int kHalf = kRowPer / 2;
-      constexpr int VH = NV / 2;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t wd[kHalf];
-#pragma unroll
-        for (int i = 0; i < VH; ++i) {
-          const int vb = v0 + (threadIdx.x + (h * VH + i) * kRowThreads) * EPV;
-#pragma unroll
-          for (int q = 0; q < EPV / 4; ++q) {
-            const Philox4 bits = prow.block((uint32_t)(vb + 4 * q) >> 2);
-            wd[i * EPV + 4 * q + 0] = bits.x;
-            wd[i * EPV + 4 * q + 1] = bits.y;
-            wd[i * EPV + 4 * q + 2] = bits.z;
-            wd[i * EPV + 4 * q + 3] = bits.w;
-          }
-        }
-        uint32_t cand = 0;
-#pragma unroll
-        for (int k = 0; k < kHalf; ++k) {
-          const bool may = !gumbel_cannot_win(wd[k], __expf(z[h * kHalf + k] - L) * kRejectSlack);
-          cand |= (uint32_t)may << k;
-        }
-        if (cand != 0) {
-#pragma unroll
-          for (int k = 0; k < kHalf; ++k) {
-            if (!((cand >> k) & 1u)) continue;
-            const int id = v0 + (threadIdx.x + (h * VH + k / EPV) * kRowThreads) * EPV + (k % EPV);
-            const float zz = z[h * kHalf + k];
-            const float key = zz + gumbel_from_bits(wd[k]);
-            if (key > bkey || (key == bkey && id < bidx)) {
-              bkey = key;
-              bidx = id;
-              bz = zz;
-            }
-          }
-        }
-      }
-    }
-    // sum of exp(z - M) (one common M: no rescaling) and, on a bonus row, the best
-    // (key, lowest id) record: warp reductions, then the warps in a fixed order
+    // sum of exp(z - M) (one common M: no rescaling): warp reductions, then the warps in
+    // a fixed order
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
     if (lane == 0) sm_f[warp] = ssum;
-    if (bonus) {
-      const int code = key_code(bkey);
-      const int wmax = __reduce_max_sync(0xffffffffu, code);
-      const int widx = __reduce_min_sync(0xffffffffu, code == wmax ? bidx : INT_MAX);
-      const int src = __ffs(__ballot_sync(0xffffffffu, code == wmax && bidx == widx)) - 1;
-      const float wz = __shfl_sync(0xffffffffu, bz, src);
-      if (lane == 0) {
-        sm_key[warp] = wmax;
-        sm_idx[warp] = widx;
-        sm_z[warp] = wz;
-      }
-    }
     __syncthreads();
     if (threadIdx.x == 0) {
       Partial out;
@@ -289,19 +188,6 @@ __global__ void __launch_bounds__(kRowThreads, 3) verify_rows_kernel(VerifyArgs 
       out.zsel = 0.f;
       out.idx = -1;
       out.pad0 = out.pad1 = out.pad2 = 0;
-      if (bonus) {
-        int bc = sm_key[0], bi = sm_idx[0];
-        float bzz = sm_z[0];
-        for (int w = 1; w < kWarps; ++w)
-          if (sm_key[w] > bc || (sm_key[w] == bc && sm_idx[w] < bi)) {
-            bc = sm_key[w];
-            bi = sm_idx[w];
-            bzz = sm_z[w];
-          }
-        out.key = __int_as_float(bc >= 0 ? bc : bc ^ 0x7FFFFFFF);
-        out.idx = bi;
-        out.zsel = bzz;
-      }
       a.row_part[(size_t)row * a.nchunk + c] = out;
     }
     __syncthreads();
@@ -309,7 +195,7 @@ __global__ void __launch_bounds__(kRowThreads, 3) verify_rows_kernel(VerifyArgs 
 }
 
 // One warp per request.  Row t = lane + 32 s (s = 0..2, gamma <= 64) is owned by one
-// lane: its log-normaliser and bonus record come from a warp reduction over the row's
+// lane: its log-normaliser comes from a warp reduction over the row's
 // chunk partials, then every verified draft j = t+1 is tested by its own lane (all loads
 // of the request are issued together), and a ballot finds the first rejection.
 constexpr int kRowSlots = 3;  // rows per lane: (gamma + 1) <= 96
@@ -324,12 +210,8 @@ __global__ void verify_accept_kernel(VerifyArgs a) {
   const int base = a.row_base[r];
   const int nch = a.nchunk;
   float lse_own[kRowSlots];
-  int idx_own[kRowSlots];
 #pragma unroll
-  for (int s = 0; s < kRowSlots; ++s) {
-    lse_own[s] = 0.f;
-    idx_own[s] = -1;
-  }
+  for (int s = 0; s < kRowSlots; ++s) lse_own[s] = 0.f;
   // rows 0..ell, eight at a time; each lane merges chunks lane, lane+32, ... of each row
   for (int t0 = 0; t0 <= ell; t0 += 8) {
     Stats acc[8];
@@ -351,10 +233,7 @@ __global__ void verify_accept_kernel(VerifyArgs a) {
       const Stats st = warp_reduce_stats(acc[q]);
 #pragma unroll
       for (int s = 0; s < kRowSlots; ++s)
-        if (t == lane + 32 * s) {
-          lse_own[s] = st.m + logf(st.s);
-          idx_own[s] = st.idx;
-        }
+        if (t == lane + 32 * s) lse_own[s] = st.m + logf(st.s);
     }
   }
   // acceptance test of draft j+1 (lane-owned row j < ell) against target row j
@@ -382,20 +261,14 @@ __global__ void verify_accept_kernel(VerifyArgs a) {
 #pragma unroll
   for (int s = kRowSlots - 1; s >= 0; --s)
     if (rej[s]) n_acc = 32 * s + __ffs(rej[s]) - 1;
-  // the row that decided: n_acc (its normaliser for the residual, or its bonus record)
+  // the row that decides the correction draw: row n_acc (its log-normaliser)
   const int src_lane = n_acc & 31, src_slot = n_acc >> 5;
   float lse_stop = 0.f;
-  int bonus = -1;
 #pragma unroll
   for (int s = 0; s < kRowSlots; ++s) {
     const float l = __shfl_sync(0xffffffffu, lse_own[s], src_lane);
-    const int i = __shfl_sync(0xffffffffu, idx_own[s], src_lane);
-    if (s == src_slot) {
-      lse_stop = l;
-      bonus = i;
-    }
+    if (s == src_slot) lse_stop = l;
   }
-  if (n_acc == ell && lane == 0) a.tokens_out[(size_t)r * (a.gamma + 1) + ell] = bonus;
   const size_t orow = (size_t)r * (a.gamma + 1);
   for (int j = lane; j <= a.gamma; j += 32) {
     if (j < n_acc) a.tokens_out[orow + j] = __ldg(a.x + (size_t)r * a.gamma + j);
@@ -405,11 +278,15 @@ __global__ void verify_accept_kernel(VerifyArgs a) {
     a.n_acc_out[r] = n_acc;
     a.n_out[r] = n_acc + 1;
   }
+  // the correction draw at position n_acc + 1 from target row n_acc: a residual draw after
+  // a rejection (jstar = n_acc + 1), the bonus draw otherwise (jstar = -(n_acc + 1))
+  if (lane == 0) {
+    a.jstar[r] = n_acc < ell ? n_acc + 1 : -(n_acc + 1);
+    a.lse_t[r] = lse_stop;
+  }
   if (n_acc < ell) {
     const int js = n_acc + 1;
     if (lane == 0) {
-      a.jstar[r] = js;
-      a.lse_t[r] = lse_stop;
       const int slot = atomicAdd(a.n_res, 1);
       a.res_list[slot] = r;
     }
@@ -444,12 +321,16 @@ __global__ void __launch_bounds__(kSimtThreads) residual_step_simt_kernel(Verify
   griddep_wait();
   extern __shared__ float w1s[];  // [RB][rank]
   const int r0 = blockIdx.y * RB;
+  // correction position (0 = none) and whether it is a bonus draw (no draft law)
   int js[RB];
+  bool bon[RB];
   bool any = false;
 #pragma unroll
   for (int rr = 0; rr < RB; ++rr) {
     const int r = r0 + rr;
-    js[rr] = (r < a.R) ? a.jstar[r] : 0;
+    const int raw = (r < a.R) ? a.jstar[r] : 0;
+    js[rr] = raw < 0 ? -raw : raw;
+    bon[rr] = raw < 0;
     any |= js[rr] > 0;
   }
   if (!any) {
@@ -465,7 +346,7 @@ __global__ void __launch_bounds__(kSimtThreads) residual_step_simt_kernel(Verify
   for (int i = threadIdx.x; i < RB * a.rank; i += blockDim.x) {
     const int rr = i / a.rank, c = i % a.rank;
     const int r = r0 + rr;
-    w1s[i] = (r < a.R && js[rr] > 0) ? load_elem(a.W1g, a.dtype_w, (size_t)r * a.rank + c) : 0.f;
+    w1s[i] = (r < a.R && js[rr] > 0 && !bon[rr]) ? load_elem(a.W1g, a.dtype_w, (size_t)r * a.rank + c) : 0.f;
   }
   __syncthreads();
   Stats st[RB], fb[RB];
@@ -478,7 +359,7 @@ __global__ void __launch_bounds__(kSimtThreads) residual_step_simt_kernel(Verify
     const int r = min(r0 + rr, a.R - 1);
     const int j = max(js[rr], 1);
     rng[rr] = rng_row(a.seed, __ldg(a.req_id + r), a.round, kStreamCorrect, (uint32_t)j);
-    lq[rr] = __ldg(a.lse_q + (size_t)r * a.gamma + (j - 1));
+    lq[rr] = bon[rr] ? 0.f : __ldg(a.lse_q + (size_t)r * a.gamma + (j - 1));
     lt[rr] = a.lse_t[r];
   }
   const int groups_total = (a.V + 3) / 4;
@@ -511,17 +392,20 @@ __global__ void __launch_bounds__(kSimtThreads) residual_step_simt_kernel(Verify
       if (r >= a.R || js[rr] == 0) continue;
       const Philox4 bits = rng_chunk(rng[rr], (uint32_t)g);
       const uint32_t wd[4] = {bits.x, bits.y, bits.z, bits.w};
-      const size_t urow = ((size_t)r * a.gamma + (js[rr] - 1)) * a.V;
+      // a bonus row has no draft law (and position n_acc + 1 may lie past the block)
+      const size_t urow = bon[rr] ? 0 : ((size_t)r * a.gamma + (js[rr] - 1)) * a.V;
       const size_t trow = target_row_index(a.t_off, a.n_trows, a.gamma, r, js[rr] - 1, a.status) * a.V;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int v = 4 * g + e;
         if (v >= a.V) break;
-        const float z = (load_elem(a.U, a.dtype_u, urow + v) + acc[rr][e]) * a.inv_temp;
         const float lp = load_elem(a.target, a.dtype_t, trow + v) * a.inv_temp - lt[rr];
         const float p = __expf(lp);
-        const float q = __expf(z - lq[rr]);
-        const float rho = p - q;
+        float rho = 0.f;
+        if (!bon[rr]) {
+          const float z = (load_elem(a.U, a.dtype_u, urow + v) + acc[rr][e]) * a.inv_temp;
+          rho = p - __expf(z - lq[rr]);
+        }
         const float g_ = gumbel_from_bits(wd[e]);
         if (rho > 0.f) {
           const float key = __logf(rho) + g_;
@@ -564,8 +448,9 @@ __global__ void residual_combine_kernel(VerifyArgs a, int npart) {
   const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (r >= a.R) return;
-  const int js = a.jstar[r];
-  if (js == 0) return;
+  const int raw = a.jstar[r];
+  if (raw == 0) return;
+  const int js = raw < 0 ? -raw : raw;
   Stats st = stats_empty(), fb = stats_empty();
   for (int p = lane; p < npart; p += 32) {
     stats_merge(st, from_partial(a.res_part[(size_t)p * a.R + r]));
@@ -573,7 +458,9 @@ __global__ void residual_combine_kernel(VerifyArgs a, int npart) {
   }
   st = warp_reduce_stats(st);
   fb = warp_reduce_stats(fb);
-  if (lane == 0) a.tokens_out[(size_t)r * (a.gamma + 1) + (js - 1)] = (st.idx >= 0) ? st.idx : fb.idx;
+  // a bonus row has only the ln p record; a residual row falls back to it only when no
+  // p - q was positive (rounding)
+  if (lane == 0) a.tokens_out[(size_t)r * (a.gamma + 1) + (js - 1)] = (raw > 0 && st.idx >= 0) ? st.idx : fb.idx;
 }
 
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s) {
