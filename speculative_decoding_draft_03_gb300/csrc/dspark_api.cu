@@ -78,7 +78,7 @@ RnnLayout rnn_layout(int R, int gamma, int V, int ns, int d, int dtype_w) {
 }
 
 struct VerifyLayout {
-  size_t counters, row_req, row_t, row_base, row_order, row_part, lse_t, jstar, res_list, W1g, res_part, res_part2,
+  size_t counters, row_req, row_t, row_base, row_order, row_part, lse_t, jstar, W1g, res_part, res_part2,
       total;
   int nchunk, npart;
 };
@@ -105,8 +105,6 @@ VerifyLayout verify_layout(int R, int gamma, int V, int rank, int dtype_w) {
   L.lse_t = off;
   off += align256(4 * (size_t)R);
   L.jstar = off;
-  off += align256(4 * (size_t)R);
-  L.res_list = off;
   off += align256(4 * (size_t)R);
   L.W1g = off;
   off += align256(elem_size(dtype_w) * (size_t)round_up_rows(R) * rank);
@@ -429,7 +427,6 @@ static dspark_status verify_impl(int R, int gamma, int V, int rank, int dtype_t,
   a.status = reinterpret_cast<dspark::DeviceStatus*>(ws);
   int* counters = reinterpret_cast<int*>(ws + L.counters);
   a.n_rows = counters;
-  a.n_res = counters + 1;
   a.row_req = reinterpret_cast<int*>(ws + L.row_req);
   a.row_t = reinterpret_cast<int*>(ws + L.row_t);
   a.row_base = reinterpret_cast<int*>(ws + L.row_base);
@@ -440,7 +437,6 @@ static dspark_status verify_impl(int R, int gamma, int V, int rank, int dtype_t,
   a.chunk = kVerifyChunk;
   a.lse_t = reinterpret_cast<float*>(ws + L.lse_t);
   a.jstar = reinterpret_cast<int*>(ws + L.jstar);
-  a.res_list = reinterpret_cast<int*>(ws + L.res_list);
   a.W1g = ws + L.W1g;
   a.res_part = reinterpret_cast<dspark::Partial*>(ws + L.res_part);
   a.res_part2 = reinterpret_cast<dspark::Partial*>(ws + L.res_part2);

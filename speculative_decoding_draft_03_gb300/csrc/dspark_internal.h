@@ -87,8 +87,6 @@ struct VerifyArgs {
   int chunk;          // ids per chunk
   float* lse_t;       // [R] target log-normaliser of the residual row
   int* jstar;         // [R] residual position (0 = none)
-  int* res_list;      // [R] requests that need a residual draw
-  int* n_res;         // [1]
   void* W1g;          // [Rpad, rank] gathered factor rows of the residual positions
   const void* state;  // recurrent head: [R, gamma, rank] states, the factor rows (nullptr: W1[x_{j-1}])
   Partial* res_part;  // [npart, R] residual partials: key = ln rho + g

@@ -89,7 +89,6 @@ __global__ void __launch_bounds__(kPlanThreads) verify_plan_kernel(VerifyArgs a)
   }
   if (threadIdx.x == blockDim.x - 1) *a.n_rows = base;
   if (threadIdx.x == 0) {
-    *a.n_res = 0;
     *a.work_next = 0;
   }
 }
@@ -286,10 +285,6 @@ __global__ void verify_accept_kernel(VerifyArgs a) {
   }
   if (n_acc < ell) {
     const int js = n_acc + 1;
-    if (lane == 0) {
-      const int slot = atomicAdd(a.n_res, 1);
-      a.res_list[slot] = r;
-    }
     // gather the factor row of position j* for the bias recomputation: W1[x_{j*-1}], or
     // the recurrent head's state s_{j*}
     size_t src;
