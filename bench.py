@@ -193,10 +193,10 @@ def tensor_core_path(w):
 
 
 def launches_per_round(w):
-    """Kernels of one round: confidence h-part, first-position prepare, the draft (a step
-    per position and one final merge on the tensor-core path; a step and a merge per
-    position on CUDA cores), the scheduler, and verify's plan / rows / accept / residual
-    step / residual combine."""
+    """Kernels of one round: confidence h-part, first-position prepare (CUDA-core path or no
+    hidden state), the draft (a step per position and one final merge on the tensor-core
+    path; a step and a merge per position on CUDA cores), the scheduler, and verify's plan /
+    rows / accept / correction step / correction combine."""
     g = w["gamma"]
     if w.get("head") == "rnn":
         # h projection, then a cell and a step per position, the merge (tensor cores: once;
@@ -204,7 +204,9 @@ def launches_per_round(w):
         draft = (1 if w["d"] > 0 else 0) + 2 * g + (1 if tensor_core_path(w) else g) + 1
         return (1 if w["d"] > 0 else 0) + draft + 1 + 5
     draft = g + 1 if tensor_core_path(w) else 2 * g
-    return (1 if w["d"] > 0 else 0) + 1 + draft + 1 + 5
+    # position 1's prepare launch: not needed on the tensor-core path with a hidden state
+    prepare = 0 if (tensor_core_path(w) and w["d"] > 0) else 1
+    return (1 if w["d"] > 0 else 0) + prepare + draft + 1 + 5
 
 
 def cpu_baseline(workload, w_host, sample_rounds=1):

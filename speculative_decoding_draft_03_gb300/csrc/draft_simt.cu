@@ -32,12 +32,19 @@ constexpr int kHdotWarpsPerRow = 4;
 constexpr int kHdotRowsPerCta = kHdotThreads / 32 / kHdotWarpsPerRow;
 constexpr int kHdotUnroll = 4;
 
+// With n_reset > 0 it also empties the tensor-core path's per-position bounds and winners
+// (hint, win: n_reset = gamma * R entries each), so that position 1 needs no prepare launch.
 __global__ void __launch_bounds__(kHdotThreads) conf_hdot_kernel(int rows, int d, int dtype_h,
                                                                  const void* __restrict__ h,
                                                                  const float* __restrict__ w_h,
-                                                                 float* __restrict__ s_h) {
+                                                                 float* __restrict__ s_h, int* hint,
+                                                                 unsigned long long* win, int n_reset) {
   griddep_allow_next();
   griddep_wait();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_reset; i += gridDim.x * blockDim.x) {
+    hint[i] = __float_as_int(-INFINITY) ^ 0x7FFFFFFF;  // order-preserving code of -inf
+    win[i] = 0ull;
+  }
   __shared__ float part[kHdotRowsPerCta][kHdotWarpsPerRow];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int local = warp / kHdotWarpsPerRow, sub = warp % kHdotWarpsPerRow;
@@ -325,11 +332,11 @@ __global__ void __launch_bounds__(256) draft_finalize_kernel(DraftArgs a, int np
 // ---------------------------------------------------------------------------------
 // Host-side launchers
 // ---------------------------------------------------------------------------------
-cudaError_t launch_conf_hdot(const DraftArgs& a, cudaStream_t s) {
+cudaError_t launch_conf_hdot(const DraftArgs& a, bool reset_bounds, cudaStream_t s) {
   const int rows = a.R * a.gamma;
   const int blocks = (rows + kHdotRowsPerCta - 1) / kHdotRowsPerCta;
   return launch_pdl(conf_hdot_kernel, dim3(blocks), dim3(kHdotThreads), 0, s, rows, a.d, a.dtype_h, a.h, a.conf_w,
-                    a.s_h);
+                    a.s_h, a.hint, a.win, reset_bounds ? rows : 0);
 }
 
 cudaError_t launch_draft_prepare(const DraftArgs& a, int k, cudaStream_t s) {

@@ -595,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          "r"(q.z), "r"(q.w)
                          : "memory");
         }
-        if (group == 0 && p.k >= 2 && rq < p.R) {
+        if (group == 0 && rq < p.R) {
           const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
           float acc = 0.f;
           if (has) {

@@ -281,14 +281,19 @@ dspark_status dspark_markov_draft(int R, int gamma, int V, int rank, int d, int 
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
+  const bool tc = dspark::tc_supported(V, rank, dtype_w) != 0;
+  // Tensor-core path: the step of position 1 gathers its own factor rows (from x0) and
+  // writes c_1; conf_hdot empties the bounds and winners.  Otherwise (CUDA-core path, or
+  // no hidden state) draft_prepare gathers position 1's factor rows, writes c_1 and
+  // empties them.
+  const bool prepare = !tc || d == 0;
   if (d > 0) {
-    if ((e = dspark::launch_conf_hdot(a, s)) != cudaSuccess) return cuda_fail(e, "conf_hdot");
+    if ((e = dspark::launch_conf_hdot(a, !prepare, s)) != cudaSuccess) return cuda_fail(e, "conf_hdot");
   } else {
     if ((e = cudaMemsetAsync(a.s_h, 0, sizeof(float) * (size_t)R * gamma, s)) != cudaSuccess)
       return cuda_fail(e, "s_h clear");
   }
-  if ((e = dspark::launch_draft_prepare(a, 1, s)) != cudaSuccess) return cuda_fail(e, "draft_prepare");
-  const bool tc = dspark::tc_supported(V, rank, dtype_w) != 0;
+  if (prepare && (e = dspark::launch_draft_prepare(a, 1, s)) != cudaSuccess) return cuda_fail(e, "draft_prepare");
   for (int k = 1; k <= gamma; ++k) {
     int npart;
     const bool prof = 2 * k <= g_prof_n;
@@ -606,7 +611,7 @@ dspark_status dspark_rnn_draft(int R, int gamma, int V, int ns, int ne, int d, i
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (d > 0) {
-    if ((e = dspark::launch_conf_hdot(a, s)) != cudaSuccess) return cuda_fail(e, "conf_hdot");
+    if ((e = dspark::launch_conf_hdot(a, false, s)) != cudaSuccess) return cuda_fail(e, "conf_hdot");
     if ((e = dspark::launch_rnn_hproj(a, s)) != cudaSuccess) return cuda_fail(e, "rnn_hproj");
   } else {
     if ((e = cudaMemsetAsync(a.s_h, 0, sizeof(float) * (size_t)R * gamma, s)) != cudaSuccess)

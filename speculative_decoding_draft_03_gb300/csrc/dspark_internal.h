@@ -168,7 +168,8 @@ int tc_num_partials(int R);
 int draft_num_partials(int R, int V, int rank, int dtype_w);
 int round_up_rows(int R);
 
-cudaError_t launch_conf_hdot(const DraftArgs& a, cudaStream_t s);
+// reset_bounds: also empty every position's published bound and winner (tensor-core path)
+cudaError_t launch_conf_hdot(const DraftArgs& a, bool reset_bounds, cudaStream_t s);
 cudaError_t launch_draft_prepare(const DraftArgs& a, int k, cudaStream_t s);
 cudaError_t launch_draft_step_simt(const DraftArgs& a, int k, cudaStream_t s);
 cudaError_t launch_draft_combine(const DraftArgs& a, int k, int npart, cudaStream_t s);
