@@ -5,9 +5,12 @@
 // and reduces each request's row to (max, sum exp, Gumbel-max key/id) partials, so the
 // vocabulary row is streamed exactly once per position (numb3r33 blog "DSpark:
 // confidence-scheduled speculative decoding", section "Markov sequential head";
-// DSpark 精读 §2: p_k = softmax(U_k + W1[x_{k-1}] W2), sampled left to right).  A
-// second epilogue mode recomputes the rejected position's row for the (p - q)+
-// residual draw of verification.
+// DSpark 精读 §2: p_k = softmax(U_k + W1[x_{k-1}] W2), sampled left to right).  Other
+// epilogue modes of the same pipeline: verification's correction draw (the rejected
+// position's row for the (p - q)+ residual, or the bonus draw from the target row), the
+// recurrent head's draft step (factor rows = the states), and the acceptance-overlap
+// diagnostic (sum min(q, p) per drafted position).  The file also holds the recurrent
+// head's hidden-state projection, a plain tcgen05 GEMM.
 //
 // GB300 mapping
 //   * The bias is an [R x rank] x [rank x V] contraction: tcgen05.mma kind::f16
@@ -262,7 +265,7 @@ struct TcParams {
   const int32_t* t_off;  // flattened target rows (nullptr: padded [R, gamma+1, V])
   int n_trows;
   int dtype_t;
-  const int* jstar;     // [R] rejected position (0 = none)
+  const int* jstar;     // [R] correction position (0 none; negative: a bonus draw)
   const float* lse_q;   // [R, gamma]
   const float* lse_t;   // [R]
   Partial* partials2;   // [ngroups, R] fallback draw
@@ -325,8 +328,8 @@ __device__ __forceinline__ void decode_run8(int dtype, const uint4 (&raw)[2], fl
 // RB: requests per block (32, 64 or 128); the 128 MMA rows hold 128/RB copies of it.
 // MODE: kModeDraft (one draft position for every request; the factor rows W1[x_{k-1}]
 // are gathered by the epilogue), kModeRnn (one draft position with the factor rows
-// given: the recurrent head's states), kModeResidual (the rejected position j* of each
-// request that has one) or kModeOverlap (every drafted position: sum_v min(q, p), the
+// given: the recurrent head's states), kModeResidual (each request's correction draw:
+// the residual at the rejected position j*, or the bonus draw) or kModeOverlap (every drafted position: sum_v min(q, p), the
 // expected acceptance).
 template <int RB, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)

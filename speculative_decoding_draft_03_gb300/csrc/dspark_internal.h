@@ -80,13 +80,13 @@ struct VerifyArgs {
   int* row_req;       // [R*(gamma+1)] request of compact row
   int* row_t;         // [R*(gamma+1)] target row index (0-based) of compact row
   int* row_base;      // [R] first compact row of request r
-  int* row_order;     // [R*(gamma+1)] processing order: the R bonus rows, then the others
+  int* row_order;     // [R*(gamma+1)] processing order: row ell_r of every request, then the others
   int* work_next;     // [1] next (row, chunk) item of verify_rows (a work queue)
   Partial* row_part;  // [R*(gamma+1), nchunk]
   int nchunk;         // vocabulary chunks per row
   int chunk;          // ids per chunk
   float* lse_t;       // [R] target log-normaliser of the residual row
-  int* jstar;         // [R] residual position (0 = none)
+  int* jstar;         // [R] correction position n_acc + 1: positive after a rejection, negative for a bonus draw
   void* W1g;          // [Rpad, rank] gathered factor rows of the residual positions
   const void* state;  // recurrent head: [R, gamma, rank] states, the factor rows (nullptr: W1[x_{j-1}])
   Partial* res_part;  // [npart, R] residual partials: key = ln rho + g
