@@ -73,30 +73,30 @@ __device__ __forceinline__ Philox4 rng_chunk(const RngRow& r, uint32_t chunk) {
 
 // The same generator specialised to one row: only the 4th counter word (the chunk)
 // varies, so the first round's products and half of the second round's are per-row
-// constants.  philox_row(...).block(chunk) == rng_chunk(row, chunk) bit for bit.
+// constants, and so are the round keys of rounds 3..10 (kept per row rather than
+// re-derived in every block).  philox_row(...).block(chunk) == rng_chunk(row, chunk) bit
+// for bit.
 struct PhiloxRow {
   uint32_t p;     // round 1 input word 2 without the chunk:  hi(M_A c0) ^ k1
   uint32_t g;     // round 2 output word 0 partial:          lo(M_B c2) ^ (k0 + W_A)
   uint32_t e, f;  // round 2 output words 2, 3 (constant)
   uint32_t k0, k1;
+  uint32_t ka[8], kb[8];
 
   __device__ __forceinline__ Philox4 block(uint32_t chunk) const {
     const uint32_t x2 = p ^ chunk;
     const unsigned long long pb = 0xCD9E8D57ull * (unsigned long long)x2;
     uint32_t c0 = (uint32_t)(pb >> 32) ^ g, c1 = (uint32_t)pb, c2 = e, c3 = f;
-    uint32_t a = k0 + 2u * 0x9E3779B9u, b = k1 + 2u * 0xBB67AE85u;
 #pragma unroll
     for (int i = 2; i < 10; ++i) {
       const unsigned long long qa = 0xD2511F53ull * (unsigned long long)c0;
       const unsigned long long qb = 0xCD9E8D57ull * (unsigned long long)c2;
-      const uint32_t n0 = (uint32_t)(qb >> 32) ^ c1 ^ a;
-      const uint32_t n2 = (uint32_t)(qa >> 32) ^ c3 ^ b;
+      const uint32_t n0 = (uint32_t)(qb >> 32) ^ c1 ^ ka[i - 2];
+      const uint32_t n2 = (uint32_t)(qa >> 32) ^ c3 ^ kb[i - 2];
       c0 = n0;
       c1 = (uint32_t)qb;
       c2 = n2;
       c3 = (uint32_t)qa;
-      a += 0x9E3779B9u;
-      b += 0xBB67AE85u;
     }
     return Philox4{c0, c1, c2, c3};
   }
@@ -119,6 +119,11 @@ __device__ __forceinline__ PhiloxRow philox_row(const RngRow& r) {
   o.f = (uint32_t)qa;
   o.k0 = r.k0;
   o.k1 = r.k1;
+#pragma unroll
+  for (int i = 2; i < 10; ++i) {
+    o.ka[i - 2] = r.k0 + (uint32_t)i * 0x9E3779B9u;
+    o.kb[i - 2] = r.k1 + (uint32_t)i * 0xBB67AE85u;
+  }
   return o;
 }
 
