@@ -693,14 +693,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < kCols; ++i) z[i] = (z[i] + bias[i]) * p.inv_temp;
         if constexpr (kDraftMath) {
-          float cmax = z[0];
-          int imax = 0;
-#pragma unroll
-          for (int i = 1; i < kCols; ++i)
-            if (z[i] > cmax) {
-              cmax = z[i];
-              imax = i;
-            }
+          // the run's largest logit (its position is only needed to key it, below)
+          const float cmax = fmaxf(fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3])), fmaxf(fmaxf(z[4], z[5]), fmaxf(z[6], z[7])));
           // online softmax statistics over the 8 ids; term_i = exp(z_i - m)
           const float mnew = fmaxf(st.m, cmax);
           float acc = (st.m == -INFINITY) ? 0.f : st.s * __expf(st.m - mnew);
@@ -731,6 +725,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             wd[4 * g4 + 3] = bits.w;
           }
           if (thr == -INFINITY) {
+            int imax = kCols - 1;
+#pragma unroll
+            for (int i = kCols - 2; i >= 0; --i)
+              if (z[i] == cmax) imax = i;
             uint32_t wm = wd[0];
 #pragma unroll
             for (int i = 1; i < kCols; ++i)
@@ -741,11 +739,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             st.zsel = cmax;
             thr = key;
           }
-          const float scale = __expf(mnew - thr) * kRejectSlack;
+          // 1 - u = n * 2^-25 with n = 2^25 - 2b - 1 exactly, so the test 1 - u >= term * scale
+          // is n >= term * scale * 2^25 (the power of two folded into scale)
+          const float scale = __expf(mnew - thr) * (kRejectSlack * 0x1.0p25f);
           uint32_t cand = 0;
 #pragma unroll
           for (int i = 0; i < kCols; ++i)
-            if (!gumbel_cannot_win(wd[i], term[i] * scale)) cand |= 1u << i;
+            if (!(__uint2float_rn((1u << 25) - 2u * (wd[i] >> 8) - 1u) >= term[i] * scale)) cand |= 1u << i;
           while (cand) {
             const int i = __ffs(cand) - 1;
             cand &= cand - 1;
