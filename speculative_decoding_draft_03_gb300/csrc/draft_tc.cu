@@ -197,6 +197,14 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
+// Draft modes carry their logits in base 2 (y = z log2(e)), so that each softmax term is
+// one ex2 instruction; keys and the selected logit are converted back to natural units.
+constexpr float kLog2ef = 1.4426950408889634f, kLn2f = 0.6931471805599453f;
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 
@@ -541,6 +549,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     Stats st = stats_empty();  // draft: softmax stats + Gumbel-max; residual: ln(p-q)+ + g
+    // draft modes: logits y = z log2(e) and st.m in base 2 until the merge below; st.key
+    // and st.zsel are natural throughout
+    const float zscale = kDraftMath ? p.inv_temp * kLog2ef : p.inv_temp;
     Stats fb = stats_empty();  // residual only: ln p + g (the rounding fallback)
     float ovl = 0.f;           // overlap only: this thread's sum of min(q, p)
     const PhiloxRow prow =
@@ -691,17 +702,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         float z[kCols];
         decode_run8(p.dtype_u, ucur[ps], z);
 #pragma unroll
-        for (int i = 0; i < kCols; ++i) z[i] = (z[i] + bias[i]) * p.inv_temp;
+        for (int i = 0; i < kCols; ++i) z[i] = (z[i] + bias[i]) * zscale;
         if constexpr (kDraftMath) {
-          // the run's largest logit (its position is only needed to key it, below)
+          // the run's largest (base-2) logit (its position is only needed to key it, below)
           const float cmax = fmaxf(fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3])), fmaxf(fmaxf(z[4], z[5]), fmaxf(z[6], z[7])));
-          // online softmax statistics over the 8 ids; term_i = exp(z_i - m)
+          // online softmax statistics over the 8 ids; term_i = 2^(y_i - m) = e^(z_i - m ln 2)
           const float mnew = fmaxf(st.m, cmax);
-          float acc = (st.m == -INFINITY) ? 0.f : st.s * __expf(st.m - mnew);
+          float acc = (st.m == -INFINITY) ? 0.f : st.s * ex2_approx(st.m - mnew);
           float term[kCols];
 #pragma unroll
           for (int i = 0; i < kCols; ++i) {
-            term[i] = __expf(z[i] - mnew);
+            term[i] = ex2_approx(z[i] - mnew);
             acc += term[i];
           }
           st.m = mnew;
@@ -714,7 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // their key.  Without any known key, the run's largest logit is keyed first so
           // that the others are tested against it.
           float thr = fmaxf(st.idx >= 0 ? st.key : -INFINITY, bound);
-          if (thr > -INFINITY && cmax + kGumbelMax < thr) continue;
+          if (thr > -INFINITY && fmaf(cmax, kLn2f, kGumbelMax) < thr) continue;
           uint32_t wd[kCols];
 #pragma unroll
           for (int g4 = 0; g4 < 2; ++g4) {
@@ -733,15 +744,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 1; i < kCols; ++i)
               if (i == imax) wm = wd[i];
-            const float key = cmax + gumbel_from_bits(wm);
+            const float cn = cmax * kLn2f;
+            const float key = cn + gumbel_from_bits(wm);
             st.key = key;
             st.idx = vb + imax;
-            st.zsel = cmax;
+            st.zsel = cn;
             thr = key;
           }
           // 1 - u = n * 2^-25 with n = 2^25 - 2b - 1 exactly, so the test 1 - u >= term * scale
-          // is n >= term * scale * 2^25 (the power of two folded into scale)
-          const float scale = __expf(mnew - thr) * (kRejectSlack * 0x1.0p25f);
+          // is n >= term * scale * 2^25 (the power of two folded into scale); the scale
+          // e^(m ln 2 - best) is 2^(m - best log2 e)
+          const float scale = ex2_approx(fmaf(-thr, kLog2ef, mnew)) * (kRejectSlack * 0x1.0p25f);
           uint32_t cand = 0;
 #pragma unroll
           for (int i = 0; i < kCols; ++i)
@@ -758,6 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 wi = wd[j];
               }
             if (vb + i == st.idx) continue;  // already keyed above
+            zi *= kLn2f;
             const float key = zi + gumbel_from_bits(wi);
             if (key > st.key || (key == st.key && vb + i < st.idx)) {
               st.key = key;
@@ -852,6 +866,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (valid) bound = key_from_ordered(hint_pref);
       }
     }
+    if constexpr (kDraftMath) st.m *= kLn2f;  // back to natural units
     // merge the threads that share a request: smem slots [ew][lane]
     Partial* red = reinterpret_cast<Partial*>(smem + SM::red);
     const int et = threadIdx.x - 32 * kFirstEpiWarp;  // 0..511
