@@ -197,7 +197,7 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
-// Draft modes carry their logits in base 2 (y = z log2(e)), so that each softmax term is
+// The epilogue carries its logits in base 2 (y = z log2(e)), so that each exponential is
 // one ex2 instruction; keys and the selected logit are converted back to natural units.
 constexpr float kLog2ef = 1.4426950408889634f, kLn2f = 0.6931471805599453f;
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -549,9 +549,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     Stats st = stats_empty();  // draft: softmax stats + Gumbel-max; residual: ln(p-q)+ + g
-    // draft modes: logits y = z log2(e) and st.m in base 2 until the merge below; st.key
-    // and st.zsel are natural throughout
-    const float zscale = kDraftMath ? p.inv_temp * kLog2ef : p.inv_temp;
+    // every mode scales its logits into base 2 (y = z log2(e)): the draft modes keep st.m
+    // in base 2 until the merge below, the correction and overlap modes take their
+    // normalisers in base 2 too; keys (st.key, fb.key) and st.zsel are natural throughout
+    const float zscale = p.inv_temp * kLog2ef;
+    const float lse_q2 = lse_q * kLog2ef, lse_t2 = lse_t * kLog2ef;
     Stats fb = stats_empty();  // residual only: ln p + g (the rounding fallback)
     float ovl = 0.f;           // overlap only: this thread's sum of min(q, p)
     const PhiloxRow prow =
@@ -780,17 +782,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         } else if constexpr (MODE == kModeOverlap) {
-          // overlap: min(q, p) with q = exp(z - lse_q), p = exp(t/T - lse_t)
+          // overlap: min(q, p) with q = exp(z - lse_q), p = exp(t/T - lse_t) (as powers of 2)
           uint4 traw[2];
           load_run8(p.target, p.dtype_t, trow, vb, p.V, true, traw);
           float tl[kCols];
           decode_run8(p.dtype_t, traw, tl);
 #pragma unroll
           for (int i = 0; i < kCols; ++i)
-            ovl += fminf(__expf(fmaf(tl[i], p.inv_temp, -lse_t)), __expf(z[i] - lse_q));
+            ovl += fminf(ex2_approx(fmaf(tl[i], zscale, -lse_t2)), ex2_approx(z[i] - lse_q2));
         } else {
           // residual: q = exp(z - lse_q), p = exp(t/T - lse_t); draw from (p - q)+ by
           // Gumbel-max over ln(p - q) where positive, and keep the ln p draw as fallback
+          // (lp holds log2 p; the fallback key is lp ln 2 + g)
           uint4 traw[2];
           load_run8(p.target, p.dtype_t, trow, vb, p.V, true, traw);
           float lp[kCols];
@@ -798,13 +801,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           float gmax = -INFINITY;
 #pragma unroll
           for (int i = 0; i < kCols; ++i) {
-            lp[i] = lp[i] * p.inv_temp - lse_t;
+            lp[i] = fmaf(lp[i], zscale, -lse_t2);
             gmax = fmaxf(gmax, lp[i]);
           }
+          const float gtop = fmaf(gmax, kLn2f, kGumbelMax);
           // ln(p - q) <= ln p: neither draw can improve once ln p + G_max is below both keys
           // (a bonus row keeps only the ln p record)
-          if (fb.idx >= 0 && gmax + kGumbelMax < fb.key &&
-              (bonus_row || (st.idx >= 0 && gmax + kGumbelMax < st.key)))
+          if (fb.idx >= 0 && gtop < fb.key && (bonus_row || (st.idx >= 0 && gtop < st.key)))
             continue;
 #pragma unroll
           for (int g4 = 0; g4 < 2; ++g4) {
@@ -816,15 +819,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int v = vb + 4 * g4 + e;
-              const float pv = __expf(lp[4 * g4 + e]);
-              const float rho = pv - __expf(z[4 * g4 + e] - lse_q);
+              const float pv = ex2_approx(lp[4 * g4 + e]);
+              const float rho = pv - ex2_approx(z[4 * g4 + e] - lse_q2);
               const float w = one_minus_uniform(wd[e]);
               const bool try1 = !bonus_row && rho > 0.f && !(w >= rho * s1);
               const bool try2 = !(w >= pv * s2);
               if (!try1 && !try2) continue;
               const float g = gumbel_from_bits(wd[e]);
               if (try2) {
-                const float k2 = lp[4 * g4 + e] + g;
+                const float k2 = fmaf(lp[4 * g4 + e], kLn2f, g);
                 if (fb.idx < 0 || k2 > fb.key) {
                   fb.key = k2;
                   fb.idx = v;
