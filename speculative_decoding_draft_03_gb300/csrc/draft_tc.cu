@@ -567,10 +567,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         (valid ? target_row_index(p.t_off, p.n_trows, p.gamma, req, pos - 1, p.status) : 0) * (size_t)p.V;
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
 
-    // Residual mode: U of the next tile is loaded into registers while the current one is
-    // processed (each request reads its own position).  Draft mode: U arrives through
-    // the TMA ring; this warp reads box my_box of each tile, from column box_col on.
+    // Residual and overlap modes: U of the next tile is loaded into registers while the
+    // current one is processed (each request reads its own position), and with 32-request
+    // blocks the target run too (larger blocks have no registers to spare for it).  Draft
+    // mode: U arrives through the TMA ring; this warp reads box my_box of each tile, from
+    // column box_col on.
     uint4 unext[kPass][2];
+    constexpr bool kTPref = !kDraftMath && RB == 32;
+    uint4 tnext[kPass][2];
+    auto load_t = [&](int t, uint4 (&dst)[kPass][2]) {
+      const int vt = (group + t * p.ngroups) * kN;
+#pragma unroll
+      for (int ps = 0; ps < kPass; ++ps)
+        load_run8(p.target, p.dtype_t, trow, vt + col0 + ps * kCols, p.V, valid && t < my_tiles, dst[ps]);
+    };
     auto load_u = [&](int t, uint4 (&dst)[kPass][2]) {
       const int vt = (group + t * p.ngroups) * kN;
 #pragma unroll
@@ -582,6 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int box_row = row0 + lane;
     const bool u_f32 = p.dtype_u == DSPARK_F32;
     if constexpr (!kDraftMath) load_u(0, unext);
+    if constexpr (kTPref) load_t(0, tnext);
     // the predecessor still reads the partial records this kernel overwrites at the end
     if constexpr (MODE == kModeDraft) {
       griddep_wait();
@@ -649,6 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // behind this tile's work
       const int hint_pref = (kDraftMath && valid) ? __ldcg(p.hint + r) : 0;
       uint4 ucur[kPass][2];
+      uint4 tcur[kPass][2];
       int uslot = 0;
       bool u_ready = true;
       if constexpr (!kDraftMath) {
@@ -658,6 +670,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           ucur[ps][1] = unext[ps][1];
         }
         load_u(t + 1, unext);
+        if constexpr (kTPref) {
+#pragma unroll
+          for (int ps = 0; ps < kPass; ++ps) {
+            tcur[ps][0] = tnext[ps][0];
+            tcur[ps][1] = tnext[ps][1];
+          }
+          load_t(t + 1, tnext);
+        }
       } else {
         const int i = t * uboxes_per_tile + my_box;
         uslot = i % n_uboxes;
@@ -784,7 +804,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if constexpr (MODE == kModeOverlap) {
           // overlap: min(q, p) with q = exp(z - lse_q), p = exp(t/T - lse_t) (as powers of 2)
           uint4 traw[2];
-          load_run8(p.target, p.dtype_t, trow, vb, p.V, true, traw);
+          if constexpr (kTPref) {
+            traw[0] = tcur[ps][0];
+            traw[1] = tcur[ps][1];
+          } else {
+            load_run8(p.target, p.dtype_t, trow, vb, p.V, true, traw);
+          }
           float tl[kCols];
           decode_run8(p.dtype_t, traw, tl);
 #pragma unroll
@@ -795,7 +820,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Gumbel-max over ln(p - q) where positive, and keep the ln p draw as fallback
           // (lp holds log2 p; the fallback key is lp ln 2 + g)
           uint4 traw[2];
-          load_run8(p.target, p.dtype_t, trow, vb, p.V, true, traw);
+          if constexpr (kTPref) {
+            traw[0] = tcur[ps][0];
+            traw[1] = tcur[ps][1];
+          } else {
+            load_run8(p.target, p.dtype_t, trow, vb, p.V, true, traw);
+          }
           float lp[kCols];
           decode_run8(p.dtype_t, traw, lp);
           float gmax = -INFINITY;
