@@ -773,14 +773,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             st.zsel = cn;
             thr = key;
           }
-          // 1 - u = n * 2^-25 with n = 2^25 - 2b - 1 exactly, so the test 1 - u >= term * scale
-          // is n >= term * scale * 2^25 (the power of two folded into scale); the scale
-          // e^(m ln 2 - best) is 2^(m - best log2 e)
-          const float scale = ex2_approx(fmaf(-thr, kLog2ef, mnew)) * (kRejectSlack * 0x1.0p25f);
+          // the test 1 - u >= term * scale in its conversion-free form (uniform_mantissa);
+          // the scale e^(m ln 2 - best) is 2^(m - best log2 e)
+          const float scale = ex2_approx(fmaf(-thr, kLog2ef, mnew)) * kRejectSlack;
           uint32_t cand = 0;
 #pragma unroll
           for (int i = 0; i < kCols; ++i)
-            if (!(__uint2float_rn((1u << 25) - 2u * (wd[i] >> 8) - 1u) >= term[i] * scale)) cand |= 1u << i;
+            if (!(fmaf(term[i], scale, uniform_mantissa(wd[i])) <= kRejectEdge)) cand |= 1u << i;
           while (cand) {
             const int i = __ffs(cand) - 1;
             cand &= cand - 1;

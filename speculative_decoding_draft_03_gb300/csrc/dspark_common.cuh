@@ -166,6 +166,14 @@ __device__ __forceinline__ bool gumbel_cannot_win(uint32_t bits, float t) { retu
 // fast exponential (a few ulp), the rounding of w, and leaves a wide margin (e^0.002).
 constexpr float kRejectSlack = 1.002f;
 
+// The same test without an integer-to-float conversion, for callers that test many
+// elements.  f = 1 + floor(b / 2) * 2^-23 (b = bits >> 8; the word's top 23 bits as a
+// mantissa) satisfies u - (f - 1) < 2^-23, so 1 - u > 2 - f - 2^-23.  f + t <= 2 - 2^-22
+// (evaluated as one FMA, whose rounding stays below 2^-24 in [1, 2)) therefore implies
+// 1 - u >= t: the element is rejected only when the exact test would reject it too.
+__device__ __forceinline__ float uniform_mantissa(uint32_t bits) { return __uint_as_float(0x3F800000u | (bits >> 9)); }
+constexpr float kRejectEdge = 2.f - 0x1.0p-22f;
+
 // ---------------------------------------------------------------------------------
 // Loads
 // ---------------------------------------------------------------------------------
