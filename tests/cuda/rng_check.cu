@@ -37,6 +37,14 @@ __global__ void gumbel_kernel(int n, const uint32_t* bits, const float* t, float
   reject[i] = gumbel_cannot_win(bits[i], t[i]) ? 1 : 0;
 }
 
+// The draft step's conversion-free rejection test for (bits, t * scale), as the draft
+// epilogue evaluates it.
+__global__ void reject_fast_kernel(int n, const uint32_t* bits, const float* t, float scale, int* reject) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  reject[i] = (fmaf(t[i], scale, uniform_mantissa(bits[i])) <= kRejectEdge) ? 1 : 0;
+}
+
 extern "C" int rng_check_philox(int n, const uint32_t* c0, const uint32_t* c1, const uint32_t* c2, const uint32_t* c3,
                                 uint32_t k0, uint32_t k1, uint32_t* out) {
   philox_kernel<<<(n + 255) / 256, 256>>>(n, c0, c1, c2, c3, k0, k1, out);
@@ -45,5 +53,10 @@ extern "C" int rng_check_philox(int n, const uint32_t* c0, const uint32_t* c1, c
 
 extern "C" int rng_check_gumbel(int n, const uint32_t* bits, const float* t, float* g, int* reject) {
   gumbel_kernel<<<(n + 255) / 256, 256>>>(n, bits, t, g, reject);
+  return (int)cudaDeviceSynchronize();
+}
+
+extern "C" int rng_check_reject_fast(int n, const uint32_t* bits, const float* t, float scale, int* reject) {
+  reject_fast_kernel<<<(n + 255) / 256, 256>>>(n, bits, t, scale, reject);
   return (int)cudaDeviceSynchronize();
 }

@@ -29,6 +29,7 @@ def lib():
     P = ctypes.c_void_p
     L.rng_check_philox.argtypes = [ctypes.c_int, P, P, P, P, ctypes.c_uint32, ctypes.c_uint32, P]
     L.rng_check_gumbel.argtypes = [ctypes.c_int, P, P, P, P]
+    L.rng_check_reject_fast.argtypes = [ctypes.c_int, P, P, ctypes.c_float, P]
     return L
 
 
@@ -88,3 +89,26 @@ def test_rejection_test_is_sound(lib):
     g64 = -np.log(-np.log1p(u - 1.0))
     assert (g64[rej] <= -np.log(t[rej].astype(np.float64)) + 1e-6).all()
     assert rej.mean() > 0.5  # and it does reject most draws
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.37, 3.0e4])
+def test_conversion_free_rejection_is_sound(lib, scale):
+    # the draft epilogue's form, fl(t * scale + f) <= 2 - 2^-22 with f from the word's top 23
+    # bits, must imply E = -ln u >= 1 - u >= t * scale, i.e. g <= -ln(t * scale)
+    rng = np.random.default_rng(2)
+    n = 1 << 20
+    bits = rng.integers(0, 2**32, n, dtype=np.uint64).astype(np.uint32)
+    bits[: n // 4] |= 0xFFF00000  # many draws near u -> 1
+    u = (2.0 * (bits >> 8).astype(np.float64) + 1.0) / 2.0**25
+    # thresholds at random, and within a few 1e-7 of 1 - u
+    tt = np.where(rng.random(n) < 0.5, np.exp(rng.uniform(-25, 1, n)), (1.0 - u) * (1 + rng.normal(0, 3e-7, n)))
+    t = (tt / scale).astype(np.float32)
+    tb = torch.from_numpy(bits.view(np.int32)).cuda()
+    rej = torch.zeros(n, dtype=torch.int32, device="cuda")
+    assert lib.rng_check_reject_fast(n, _p(tb), _p(torch.from_numpy(t).cuda()), scale, _p(rej)) == 0
+    rej = rej.cpu().numpy().astype(bool)
+    prod = t.astype(np.float64) * float(np.float32(scale))  # the kernel's operands are binary32
+    assert (1.0 - u[rej] >= prod[rej]).all()
+    # it rejects whatever lies clearly below the exact boundary
+    far = (1.0 - u) - prod > 2.0**-20
+    assert rej[far].all()
