@@ -59,9 +59,10 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--head", choices=["markov", "rnn"], default="markov",
                    help="draft head: the Markov head, or the recurrent head on the same workload")
-    p.add_argument("--diagnostic", choices=["overlap", "sts"], default=None,
-                   help="time the acceptance-overlap diagnostic on the workload's verified positions, or the "
-                        "sequential temperature fit on synthetic held-out rounds, instead of the round")
+    p.add_argument("--diagnostic", choices=["overlap", "verify_overlap", "sts"], default=None,
+                   help="time the acceptance-overlap diagnostic on the workload's verified positions (standalone, "
+                        "or fused into verification), or the sequential temperature fit on synthetic held-out "
+                        "rounds, instead of the round")
     return p.parse_args()
 
 
@@ -307,6 +308,77 @@ def run_overlap_diagnostic(args):
     return 0
 
 
+def _time_calls(call, steps, dev, clk=None):
+    """Mean device time (ms) of `call` over `steps` launches, L2 flushed before each."""
+    import torch
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, e in ev:
+        flush.zero_()
+        a.record(stream)
+        call()
+        e.record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(e) for a, e in ev) / steps
+
+
+def run_verify_overlap_diagnostic(args):
+    """Times dspark_verify_overlap (verification with the acceptance overlap of every
+    verified position fused in) against dspark_verify on one round of the workload (one
+    GPU).  Metric: overlap positions per second of the added time; roofline of the added
+    pass on its algorithmic bytes (the U rows of the evaluated positions and W2 once: the
+    target rows are read by the verification anyway)."""
+    import torch
+    from speculative_decoding_draft_03_gb300 import binding as b
+    from speculative_decoding_draft_03_gb300 import workloads as wl
+    dev = torch.device("cuda", 0)
+    w = wl.make(args.workload, device="cuda", seed=0)
+    rd = b.Round(w)
+    rnd = 1
+    d, s, _ = rd.run(rnd=rnd)
+    torch.cuda.synchronize()
+    R, gamma, V, rank = w["R"], w["gamma"], w["V"], w["rank"]
+    vargs = (w["target"], w["U"], w["W1"], w["W2"], rd.x0, d["x"], d["logq"], d["lse"], s["ell"], w["temperature"],
+             w["req_id"], w["seed"], rnd)
+    ws_v = b.workspace(b.verify_workspace_size(R, gamma, V, rank, w["W1"].dtype), dev)
+    ws_f = b.workspace(b.verify_overlap_workspace_size(R, gamma, V, rank, w["W1"].dtype), dev)
+    out_v = b.verify(*vargs, ws=ws_v)
+    out_f = b.verify_overlap(*vargs, ws=ws_f)
+    plain = lambda: b.verify(*vargs, out=out_v, ws=ws_v)
+    fused = lambda: b.verify_overlap(*vargs, out=out_f, ws=ws_f)
+    for _ in range(args.warmup):
+        plain()
+        fused()
+    torch.cuda.synchronize()
+    assert b.device_status(ws_v) == 0 and b.device_status(ws_f) == 0
+    assert torch.equal(out_v["tokens"], out_f["tokens"])
+    with ClockSampler(0) as clk:
+        ms_plain = _time_calls(plain, args.steps, dev)
+        ms_fused = _time_calls(fused, args.steps, dev)
+    added = max(ms_fused - ms_plain, 1e-6)
+    n_pos = int(s["ell"].sum().item())
+    es = lambda t: t.element_size()
+    alg = n_pos * V * es(w["U"]) + rank * V * es(w["W2"])
+    peaks, peak_kind = measured_peaks()
+    achieved = alg / (added / 1000.0) / 1e9
+    line = {"metric": "fused acceptance-overlap positions/s (added time)", "value": n_pos / (added / 1000.0),
+            "unit": "positions/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_fused,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded generator, random-init weights)",
+            "config": {"workload": WORKLOAD_DESC[args.workload], "positions": n_pos,
+                       "verify_ms": ms_plain, "verify_overlap_ms": ms_fused, "added_ms": added,
+                       "l2": "flushed between calls (256 MiB write outside the timed brackets)"},
+            "roofline": {"kernel": "overlap pass of dspark_verify_overlap (bias pass + combine)", "bound": "hbm",
+                         "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "peak_source": peak_kind, "traffic": None,
+                         "algorithmic_bytes_per_launch": alg},
+            # plan, rows, accept, correction, combine; the fused call adds the bias pass and its combine
+            "cpu_baseline": None, "e2e": None, "gpu_launches": (5 + 7) * args.steps, "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 # Sequential temperature scaling: one candidate evaluation is sigmoid(z / T) times the
 # prefix, binned: one exponential and two reciprocals on the special-function units
 # (16 results per SM and clock), so the ALU roofline is 152 * 16 * 2.07 GHz / 3.
@@ -367,6 +439,8 @@ def main():
         return run_reference(args)
     if args.diagnostic == "overlap":
         return run_overlap_diagnostic(args)
+    if args.diagnostic == "verify_overlap":
+        return run_verify_overlap_diagnostic(args)
     if args.diagnostic == "sts":
         return run_sts_diagnostic(args)
     import torch

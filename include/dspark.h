@@ -356,6 +356,31 @@ DSPARK_API dspark_status dspark_acceptance_overlap(
     float temperature, float* overlap_out, void* workspace, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------------
+ * Stage 3 with the acceptance overlap fused in.
+ *
+ * dspark_verify (same arguments, results and limits), and in the same pass the
+ * acceptance overlap of every verified position (numb3r33 blog "DSpark:
+ * confidence-scheduled speculative decoding", section "Total variation label"):
+ *   overlap_out [R,gamma] fp32, overlap_out[r,j-1] = sum_v min(q_j(v), p_j(v)) for
+ *   j = 1..ell[r], NaN for j > ell[r]; q_j and p_j as in dspark_acceptance_overlap.
+ * The target rows' log-normalisers come from the verification's own pass over them, so
+ * the target is read once; the overlap then takes one more bias contraction over the
+ * R*gamma positions.  The results equal dspark_acceptance_overlap(..., ell, ...) up to
+ * the order of fp32 sums.  Workspace: dspark_verify_overlap_workspace_size() (larger
+ * than dspark_verify's; 0 for unsupported sizes).  Without the tensor-core path (fp32
+ * weights, or rank / V outside its limits) R*gamma <= 262140.
+ * ---------------------------------------------------------------------------------- */
+DSPARK_API size_t dspark_verify_overlap_workspace_size(int R, int gamma, int V, int rank, int dtype_w);
+
+DSPARK_API dspark_status dspark_verify_overlap(
+    int R, int gamma, int V, int rank, int dtype_t, int dtype_u, int dtype_w,
+    const void* target, const void* U, const void* W1, const void* W2,
+    const int32_t* x0, const int32_t* x, const float* logq, const float* lse_q,
+    const int32_t* ell, float temperature, const int64_t* req_id, uint64_t seed, uint64_t round,
+    int32_t* n_acc_out, int32_t* tokens_out, int32_t* n_out, float* overlap_out,
+    void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------
  * Sequential temperature scaling (STS) of the confidence head on held-out rounds.
  *
  * Defines (numb3r33 blog "DSpark: confidence-scheduled speculative decoding", section

@@ -52,6 +52,11 @@ def _load_library():
     lib.dspark_verify_ragged.restype = i32
     lib.dspark_verify_static.argtypes = ([i32] * 7 + [P] * 4 + [P] * 5 + [f32, P, u64, u64] + [P] * 3 + [P])
     lib.dspark_verify_static.restype = i32
+    lib.dspark_verify_overlap_workspace_size.restype = sz
+    lib.dspark_verify_overlap_workspace_size.argtypes = [i32] * 5
+    lib.dspark_verify_overlap.argtypes = ([i32] * 7 + [P] * 4 + [P] * 5 + [f32, P, u64, u64] + [P] * 4
+                                          + [P, sz, P])
+    lib.dspark_verify_overlap.restype = i32
     lib.dspark_acceptance_overlap_workspace_size.restype = sz
     lib.dspark_acceptance_overlap_workspace_size.argtypes = [i32] * 5
     lib.dspark_acceptance_overlap.argtypes = [i32] * 7 + [P] * 4 + [P] * 4 + [f32, P, P, sz, P]
@@ -258,6 +263,42 @@ def verify_ragged(target_rows, row_offset, U, W1, W2, x0, x, logq, lse_q, ell, t
                                   int(rnd), _p(out["n_acc"]), _p(out["tokens"]), _p(out["n_out"]), _p(ws),
                                   ws.numel(), _stream(stream))
     _check(st, "dspark_verify_ragged")
+    return out
+
+
+def verify_overlap_workspace_size(R, gamma, V, rank, w_dtype) -> int:
+    return int(lib.dspark_verify_overlap_workspace_size(R, gamma, V, rank, _DT[w_dtype]))
+
+
+def verify_overlap(target, U, W1, W2, x0, x, logq, lse_q, ell, temperature, req_id, seed, rnd, out=None,
+                   ws=None, stream=None):
+    """Stage 3 with the acceptance overlap fused in (dspark_verify_overlap).  Returns dict
+    n_acc [R], tokens [R,gamma+1], n_out [R] and overlap [R,gamma] (NaN past ell[r])."""
+    R, g1, V = target.shape
+    gamma = g1 - 1
+    rank = W1.shape[1]
+    dev = target.device
+    for t, n in ((target, "target"), (U, "U"), (W1, "W1"), (W2, "W2")):
+        _cuda(t, n)
+    _cuda(x0, "x0", torch.int32)
+    _cuda(x, "x", torch.int32)
+    _cuda(logq, "logq", torch.float32)
+    _cuda(lse_q, "lse_q", torch.float32)
+    _cuda(ell, "ell", torch.int32)
+    _cuda(req_id, "req_id", torch.int64)
+    if out is None:
+        out = dict(n_acc=torch.empty(R, dtype=torch.int32, device=dev),
+                   tokens=torch.empty((R, gamma + 1), dtype=torch.int32, device=dev),
+                   n_out=torch.empty(R, dtype=torch.int32, device=dev),
+                   overlap=torch.empty((R, gamma), dtype=torch.float32, device=dev))
+    if ws is None:
+        ws = workspace(verify_overlap_workspace_size(R, gamma, V, rank, W1.dtype), dev)
+    st = lib.dspark_verify_overlap(R, gamma, V, rank, _dt(target, "target"), _dt(U, "U"), _dt(W1, "W1"),
+                                   _p(target), _p(U), _p(W1), _p(W2), _p(x0), _p(x), _p(logq), _p(lse_q), _p(ell),
+                                   float(temperature), _p(req_id), int(seed), int(rnd), _p(out["n_acc"]),
+                                   _p(out["tokens"]), _p(out["n_out"]), _p(out["overlap"]), _p(ws), ws.numel(),
+                                   _stream(stream))
+    _check(st, "dspark_verify_overlap")
     return out
 
 

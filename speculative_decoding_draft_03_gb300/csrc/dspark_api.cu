@@ -375,6 +375,30 @@ dspark_status dspark_schedule_threshold(int R, int gamma, const float* conf, dou
   return DSPARK_OK;
 }
 
+// dspark_verify_overlap: the verify workspace followed by the overlap pass's pieces
+struct VerifyOverlapLayout {
+  VerifyLayout v;
+  size_t W1g, lse, part, total;
+  int npart;
+};
+
+VerifyOverlapLayout verify_overlap_layout(int R, int gamma, int V, int rank, int dtype_w) {
+  using namespace dspark;
+  VerifyOverlapLayout L;
+  L.v = verify_layout(R, gamma, V, rank, dtype_w);
+  const size_t rows = (size_t)R * gamma;
+  L.npart = overlap_num_partials(R, gamma, V, rank, dtype_w);
+  size_t off = L.v.total;
+  L.W1g = off;
+  off += align256(elem_size(dtype_w) * (size_t)round_up_rows((int)rows) * rank);
+  L.lse = off;
+  off += align256(4 * rows);
+  L.part = off;
+  off += align256(4 * rows * (size_t)L.npart);
+  L.total = off;
+  return L;
+}
+
 size_t dspark_verify_workspace_size(int R, int gamma, int V, int rank, int dtype_w) {
   if (R < 1 || gamma < 1 || V < 1 || rank < 1) return 0;
   return verify_layout(R, gamma, V, rank, dtype_w).total;
@@ -388,12 +412,16 @@ static dspark_status verify_impl(int R, int gamma, int V, int rank, int dtype_t,
                                  const float* logq, const float* lse_q, const int32_t* ell, float temperature,
                                  const int64_t* req_id, uint64_t seed, uint64_t round, int32_t* n_acc_out,
                                  int32_t* tokens_out, int32_t* n_out, void* workspace, size_t ws_bytes,
-                                 void* stream) {
+                                 void* stream, float* overlap_out = nullptr) {
   if (R < 1 || gamma < 1 || V < 1 || rank < 1)
     return fail(DSPARK_INVALID_ARG, "sizes must be positive (R=%d gamma=%d V=%d rank=%d)", R, gamma, V, rank);
   if (gamma > kMaxGamma) return fail(DSPARK_UNSUPPORTED_SHAPE, "gamma=%d exceeds %d", gamma, kMaxGamma);
   if ((long long)V > (1ll << 30)) return fail(DSPARK_UNSUPPORTED_SHAPE, "V=%d too large", V);
   if ((long long)R * (gamma + 1) > (1ll << 24)) return fail(DSPARK_UNSUPPORTED_SHAPE, "R*(gamma+1) too large");
+  // the fused overlap's CUDA-core bias pass takes blocks of 4 positions along the grid's y
+  if (overlap_out != nullptr && !dspark::tc_supported(V, rank, dtype_w) && ((long long)R * gamma + 3) / 4 > 65535)
+    return fail(DSPARK_UNSUPPORTED_SHAPE, "R*gamma=%lld exceeds 262140 without the tensor-core path",
+                (long long)R * gamma);
   if (!valid_dtype(dtype_t) || !valid_dtype(dtype_u) || !valid_dtype(dtype_w))
     return fail(DSPARK_INVALID_ARG, "dtype codes must be DSPARK_F32 or DSPARK_BF16");
   if (!(temperature > 0.f) || !isfinite(temperature))
@@ -417,8 +445,10 @@ static dspark_status verify_impl(int R, int gamma, int V, int rank, int dtype_t,
   if (state == nullptr) CHECK_ALIGN16(W1);
   CHECK_ALIGN16(W2);
   if (!aligned256(workspace)) return fail(DSPARK_INVALID_ARG, "workspace must be 256-byte aligned");
-  const VerifyLayout L = verify_layout(R, gamma, V, rank, dtype_w);
-  if (ws_bytes < L.total) return fail(DSPARK_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, L.total);
+  const VerifyOverlapLayout LO = verify_overlap_layout(R, gamma, V, rank, dtype_w);
+  const VerifyLayout& L = LO.v;
+  const size_t need = overlap_out != nullptr ? LO.total : L.total;
+  if (ws_bytes < need) return fail(DSPARK_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, need);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   dspark::VerifyArgs a = {};
   a.R = R; a.gamma = gamma; a.V = V; a.rank = rank;
@@ -445,9 +475,29 @@ static dspark_status verify_impl(int R, int gamma, int V, int rank, int dtype_t,
   a.W1g = ws + L.W1g;
   a.res_part = reinterpret_cast<dspark::Partial*>(ws + L.res_part);
   a.res_part2 = reinterpret_cast<dspark::Partial*>(ws + L.res_part2);
+  if (overlap_out != nullptr) {
+    a.ovl_lse = reinterpret_cast<float*>(ws + LO.lse);
+    a.ovl_W1g = ws + LO.W1g;
+  }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = dspark::launch_verify(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "verify");
+  if (overlap_out != nullptr) {
+    // the acceptance overlap on the verify pass's row statistics and factor rows
+    dspark::OverlapArgs o = {};
+    o.R = R; o.gamma = gamma; o.V = V; o.rank = rank;
+    o.dtype_t = dtype_t; o.dtype_u = dtype_u; o.dtype_w = dtype_w;
+    o.target = target; o.U = U; o.W1 = W1; o.W2 = W2;
+    o.x0 = x0; o.x = x; o.lse_q = lse_q; o.ell = ell;
+    o.inv_temp = a.inv_temp;
+    o.out = overlap_out;
+    o.status = a.status;
+    o.W1g = a.ovl_W1g;
+    o.lse_t = a.ovl_lse;
+    o.part = reinterpret_cast<float*>(ws + LO.part);
+    o.npart = LO.npart;
+    if ((e = dspark::launch_overlap_pass(o, s)) != cudaSuccess) return cuda_fail(e, "verify_overlap");
+  }
   return DSPARK_OK;
 }
 
@@ -474,6 +524,24 @@ dspark_status dspark_verify_ragged(int R, int gamma, int V, int rank, int dtype_
   return verify_impl(R, gamma, V, rank, dtype_t, dtype_u, dtype_w, target, target_row_offset, n_target_rows, U, W1,
                      nullptr, W2, x0, x, logq, lse_q, ell, temperature, req_id, seed, round, n_acc_out, tokens_out,
                      n_out, workspace, ws_bytes, stream);
+}
+
+size_t dspark_verify_overlap_workspace_size(int R, int gamma, int V, int rank, int dtype_w) {
+  if (R < 1 || gamma < 1 || V < 1 || rank < 1) return 0;
+  if ((long long)R * (gamma + 1) > (1ll << 24)) return 0;
+  return verify_overlap_layout(R, gamma, V, rank, dtype_w).total;
+}
+
+dspark_status dspark_verify_overlap(int R, int gamma, int V, int rank, int dtype_t, int dtype_u, int dtype_w,
+                                    const void* target, const void* U, const void* W1, const void* W2,
+                                    const int32_t* x0, const int32_t* x, const float* logq, const float* lse_q,
+                                    const int32_t* ell, float temperature, const int64_t* req_id, uint64_t seed,
+                                    uint64_t round, int32_t* n_acc_out, int32_t* tokens_out, int32_t* n_out,
+                                    float* overlap_out, void* workspace, size_t ws_bytes, void* stream) {
+  CHECK_PTR(overlap_out);
+  return verify_impl(R, gamma, V, rank, dtype_t, dtype_u, dtype_w, target, nullptr, 0, U, W1, nullptr, W2, x0, x,
+                     logq, lse_q, ell, temperature, req_id, seed, round, n_acc_out, tokens_out, n_out, workspace,
+                     ws_bytes, stream, overlap_out);
 }
 
 size_t dspark_acceptance_overlap_workspace_size(int R, int gamma, int V, int rank, int dtype_w) {

@@ -91,6 +91,10 @@ struct VerifyArgs {
   const void* state;  // recurrent head: [R, gamma, rank] states, the factor rows (nullptr: W1[x_{j-1}])
   Partial* res_part;  // [npart, R] residual partials: key = ln rho + g
   Partial* res_part2; // [npart, R] fallback partials: key = ln p + g
+  // fused acceptance overlap (nullptr: off): verify_accept writes the target log-normaliser
+  // of every verified row and the factor row of every verified position
+  float* ovl_lse;     // [R*gamma] lse of target row j-1 for position j <= ell[r], NaN beyond
+  void* ovl_W1g;      // [round_up_rows(R*gamma), rank] W1[x_{j-1}], zero beyond ell[r]
 };
 
 // Acceptance-overlap diagnostic: c*[r, j-1] = sum_v min(q_j(v), p_j(v)) for the drafted
@@ -198,6 +202,8 @@ cudaError_t launch_residual_tc(const VerifyArgs& a, cudaStream_t s);
 int residual_num_partials(int R, int V, int rank, int dtype_w);
 
 cudaError_t launch_overlap(const OverlapArgs& a, cudaStream_t s);
+// the bias pass and the combine only, on lse_t and W1g already in place
+cudaError_t launch_overlap_pass(const OverlapArgs& a, cudaStream_t s);
 cudaError_t launch_overlap_tc(const OverlapArgs& a, cudaStream_t s);
 int overlap_num_partials(int R, int gamma, int V, int rank, int dtype_w);
 int overlap_num_chunks(int V);

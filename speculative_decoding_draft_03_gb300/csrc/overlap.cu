@@ -21,6 +21,8 @@
 //                     of min(q, p) per position
 //   overlap_combine   partial sums -> c*, in a fixed order (deterministic); NaN for the
 //                     positions that are not evaluated
+// Fused with verification (dspark_verify_overlap), the verify pass supplies the target
+// rows' log-normalisers and the factor rows, and only the bias pass and the combine run.
 #include "dspark_common.cuh"
 #include "dspark_internal.h"
 
@@ -299,6 +301,12 @@ cudaError_t launch_overlap(const OverlapArgs& a, cudaStream_t s) {
   if ((e = launch_pdl(overlap_lse_kernel, dim3((unsigned)(((size_t)rows * 32 + 255) / 256)), dim3(256), 0, s, a)) !=
       cudaSuccess)
     return e;
+  return launch_overlap_pass(a, s);
+}
+
+cudaError_t launch_overlap_pass(const OverlapArgs& a, cudaStream_t s) {
+  const int rows = a.R * a.gamma;
+  cudaError_t e;
   int npart;
   if (tc_supported(a.V, a.rank, a.dtype_w)) {
     if ((e = launch_overlap_tc(a, s)) != cudaSuccess) return e;

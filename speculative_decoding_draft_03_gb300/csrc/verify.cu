@@ -277,6 +277,31 @@ __global__ void verify_accept_kernel(VerifyArgs a) {
     a.n_acc_out[r] = n_acc;
     a.n_out[r] = n_acc + 1;
   }
+  // fused acceptance overlap: target row j's log-normaliser for position j + 1 (j < ell),
+  // and the factor row W1[x_{j-1}] of every verified position j (zero beyond ell)
+  if (a.ovl_lse != nullptr) {
+#pragma unroll
+    for (int s = 0; s < kRowSlots; ++s) {
+      const int j = lane + 32 * s;
+      if (j < a.gamma) a.ovl_lse[(size_t)r * a.gamma + j] = j < ell ? lse_own[s] : NAN;
+    }
+    for (int j = 1; j <= a.gamma; ++j) {
+      const bool on = j <= ell;
+      int xp = 0;
+      if (on)
+        xp = checked_token((j == 1) ? __ldg(a.x0 + r) : __ldg(a.x + (size_t)r * a.gamma + (j - 2)), a.V, a.status, 13);
+      const size_t src = (size_t)xp * a.rank, dst = ((size_t)r * a.gamma + (j - 1)) * a.rank;
+      if (a.dtype_w == DSPARK_BF16) {
+        const unsigned short* w1 = reinterpret_cast<const unsigned short*>(a.W1);
+        unsigned short* g = reinterpret_cast<unsigned short*>(a.ovl_W1g);
+        for (int i = lane; i < a.rank; i += 32) g[dst + i] = on ? __ldg(w1 + src + i) : (unsigned short)0;
+      } else {
+        const float* w1 = reinterpret_cast<const float*>(a.W1);
+        float* g = reinterpret_cast<float*>(a.ovl_W1g);
+        for (int i = lane; i < a.rank; i += 32) g[dst + i] = on ? __ldg(w1 + src + i) : 0.f;
+      }
+    }
+  }
   // the correction draw at position n_acc + 1 from target row n_acc: a residual draw after
   // a rejection (jstar = n_acc + 1), the bonus draw otherwise (jstar = -(n_acc + 1))
   if (lane == 0) {

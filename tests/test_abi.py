@@ -116,6 +116,33 @@ def test_verify_validation(b):
         assert "16-byte" in b.lib.dspark_last_error_message().decode()
 
 
+def test_verify_overlap_validation(b):
+    import torch
+    P = _fake(18)
+    L = b.lib.dspark_verify_overlap
+    need = b.verify_overlap_workspace_size(4, 4, 1024, 32, torch.float32)
+
+    def call(**kw):
+        a = dict(R=4, g=4, V=1024, rank=32, dt=0, T=1.0, ws=need)
+        a.update(kw)
+        p = list(P)
+        for k in kw.get("null", []):
+            p[k] = None
+        return L(a["R"], a["g"], a["V"], a["rank"], a["dt"], 0, 0, p[0], p[1], p[2], p[3], p[4], p[5], p[6],
+                 p[7], p[8], a["T"], p[9], 0, 0, p[10], p[11], p[12], p[13], p[14], a["ws"], None)
+
+    assert call(R=0) == 1
+    assert call(g=100) == 2
+    assert call(T=0.0) == 1
+    for k in range(15):  # every pointer, overlap_out and the workspace included
+        assert call(null=[k]) == 1, k
+    # the fused call needs the verify workspace plus the overlap pass's pieces
+    assert need > b.verify_workspace_size(4, 4, 1024, 32, torch.float32)
+    assert call(ws=b.verify_workspace_size(4, 4, 1024, 32, torch.float32)) == 3
+    assert call(ws=need - 1) == 3
+    assert b.verify_overlap_workspace_size(0, 4, 1024, 32, torch.float32) == 0
+
+
 def test_workspace_sizes_grow_with_shape(b):
     import torch
     s1 = b.draft_workspace_size(4, 4, 1024, 32, 64, torch.float32)

@@ -1,5 +1,6 @@
-"""dspark_acceptance_overlap against the fp64 oracle: c*_j = sum_v min(q_j, p_j) for the
-drafted positions of a round, given the GPU's own drafted tokens and draft normalisers.
+"""dspark_acceptance_overlap and dspark_verify_overlap against the fp64 oracle: c*_j =
+sum_v min(q_j, p_j) for the drafted positions of a round, given the GPU's own drafted tokens
+and draft normalisers (the fused call's verification also equals dspark_verify's).
 
 Shapes cover both bias paths (tensor cores for bf16 factors, CUDA cores for fp32),
 several vocabulary tiles with a ragged tail, more than one 128-row block of positions,
@@ -70,6 +71,34 @@ def test_overlap_matches_oracle(name, over, use_ell):
                                     w["temperature"])
     bf = any(w[k].dtype == torch.bfloat16 for k in ("U", "target", "W1", "W2"))
     _check(got.cpu().numpy(), ref, None if ell is None else _host(ell), 2e-3 if bf else 1e-5)
+
+
+@pytest.mark.parametrize("name,over", [
+    ("tiny", {}),                                         # CUDA-core paths, fp32
+    ("qwen3-8b", dict(R=5, gamma=4, V=2056, d=64)),       # tensor cores, ragged vocabulary tail
+    ("deepseek-v4", dict(R=40, gamma=5, V=1288, d=64)),   # bf16 logits, 2 row blocks of positions
+    ("stress", dict(R=24, gamma=6, V=4104, d=64)),
+])
+def test_verify_overlap_matches_verify_and_oracle(name, over):
+    # dspark_verify_overlap: verification identical to dspark_verify, and the overlap of
+    # every verified position equal to the oracle's (NaN past ell)
+    from speculative_decoding_draft_03_gb300 import binding as b
+    rnd = 6
+    w, rd, d, s = _round(name, rnd, **over)
+    ell = s["ell"].clone()
+    ell[0] = 0
+    ell[-1] = w["gamma"]
+    args = (w["target"], w["U"], w["W1"], w["W2"], rd.x0, d["x"], d["logq"], d["lse"], ell, w["temperature"],
+            w["req_id"], w["seed"], rnd)
+    v1 = b.verify(*args)
+    v2 = b.verify_overlap(*args)
+    torch.cuda.synchronize()
+    for k in ("n_acc", "tokens", "n_out"):
+        assert torch.equal(v1[k], v2[k]), k
+    ref = oracle.acceptance_overlap(_host(w["target"]), _host(w["U"]), _host(w["W1"]), _host(w["W2"]),
+                                    _host(rd.x0), _host(d["x"]), _host(ell), w["temperature"])
+    bf = any(w[k].dtype == torch.bfloat16 for k in ("U", "target", "W1", "W2"))
+    _check(v2["overlap"].cpu().numpy(), ref, _host(ell), 2e-3 if bf else 1e-5)
 
 
 def test_overlap_full_size_sampled_requests():
