@@ -327,8 +327,8 @@ def run_verify_overlap_diagnostic(args):
     """Times dspark_verify_overlap (verification with the acceptance overlap of every
     verified position fused in) against dspark_verify on one round of the workload (one
     GPU).  Metric: overlap positions per second of the added time; roofline of the added
-    pass on its algorithmic bytes (the U rows of the evaluated positions and W2 once: the
-    target rows are read by the verification anyway)."""
+    pass on its algorithmic bytes (the U and target rows of the evaluated positions and W2
+    once; p needs the target logits again, only their normalisers come from the verify pass)."""
     import torch
     from speculative_decoding_draft_03_gb300 import binding as b
     from speculative_decoding_draft_03_gb300 import workloads as wl
@@ -359,7 +359,7 @@ def run_verify_overlap_diagnostic(args):
     added = max(ms_fused - ms_plain, 1e-6)
     n_pos = int(s["ell"].sum().item())
     es = lambda t: t.element_size()
-    alg = n_pos * V * es(w["U"]) + rank * V * es(w["W2"])
+    alg = n_pos * V * (es(w["U"]) + es(w["target"])) + rank * V * es(w["W2"])
     peaks, peak_kind = measured_peaks()
     achieved = alg / (added / 1000.0) / 1e9
     line = {"metric": "fused acceptance-overlap positions/s (added time)", "value": n_pos / (added / 1000.0),

@@ -294,6 +294,15 @@ struct TcParams {
   // is at most ell[request] (every position without ell)
   const int32_t* ell;
   float* ovl_part;  // [ngroups, rows] partial sums of min(q, p)
+  // overlap mode on the verify plan's compact rows (nullptr: the flattened positions):
+  // row q is target row ovl_t[q] of request ovl_req[q] and evaluates position
+  // ovl_t[q] + 1 when ovl_t[q] < ell[request]; *ovl_nrows rows exist (known on the device
+  // only), so request blocks and vocabulary groups are derived from it in the kernel;
+  // lse_t is in row order
+  const int* ovl_req;
+  const int* ovl_t;
+  const int* ovl_nrows;
+  int grid;  // CTAs to launch (0: ngroups * rblocks)
 };
 
 constexpr int kModeDraft = 0;
@@ -352,8 +361,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kStages = SM::stages;
   // draft positions: U through the TMA ring, online softmax + Gumbel-max, winners published
   constexpr bool kDraftMath = MODE == kModeDraft || MODE == kModeRnn;
-  const int rb = blockIdx.x % p.rblocks;      // request block of this CTA
-  const int group = blockIdx.x / p.rblocks;   // vocabulary-tile group
+  int rblocks = p.rblocks, ngroups = p.ngroups;
+  if constexpr (MODE == kModeOverlap) {
+    if (p.ovl_nrows != nullptr) {
+      // compact rows: their number comes from the preceding verify pass; CTAs beyond the
+      // blocks in use leave before touching any barrier or tensor memory
+      griddep_wait();
+      const int n = *reinterpret_cast<const volatile int*>(p.ovl_nrows);
+      rblocks = (max(n, 0) + RB - 1) / RB;
+      if (rblocks == 0 || rblocks > p.rblocks) return;
+      ngroups = max(1, (int)gridDim.x / rblocks);
+      if ((int)blockIdx.x >= rblocks * ngroups) return;
+    }
+  }
+  const int rb = blockIdx.x % rblocks;        // request block of this CTA
+  const int group = blockIdx.x / rblocks;     // vocabulary-tile group
   const int katoms = p.rank / kKAtom;
 
   uint32_t bar_full = sbase + SM::bars;              // [kStages]
@@ -404,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   // tiles of this CTA: group, group + ngroups, ...
-  const int my_tiles = (p.ntiles > group) ? (p.ntiles - group + p.ngroups - 1) / p.ngroups : 0;
+  const int my_tiles = (p.ntiles > group) ? (p.ntiles - group + ngroups - 1) / ngroups : 0;
 
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------
@@ -434,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           a_issued = true;
         }
         const int t = it / katoms, ka = it % katoms;
-        const int v0 = (group + t * p.ngroups) * kN;
+        const int v0 = (group + t * ngroups) * kN;
         if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag, p.status, 100)) break;
         const uint32_t dst = sbase + SM::b + stage * kStageBytes;
         mbar_arrive_expect_tx(bar_full + 8 * stage, kStageBytes);
@@ -500,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ph = (uint32_t)(i / n_uboxes) & 1u;
         if (!mbar_wait(bar_uempty + 8 * slot, ph ^ 1, abort_flag, p.status, 400)) break;
         const int t = i / uboxes_per_tile, bx = i % uboxes_per_tile;
-        const int v0 = (group + t * p.ngroups) * kN + bx * p.ubox_cols;
+        const int v0 = (group + t * ngroups) * kN + bx * p.ubox_cols;
         mbar_arrive_expect_tx(bar_ufull + 8 * slot, (uint32_t)ubox_bytes);
         tma_load_3d(sbase + SM::u + slot * ubox_bytes, &map_u, bar_ufull + 8 * slot, v0, p.k - 1, rb * RB,
                     u_policy);
@@ -539,12 +561,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         lse_t = p.lse_t[r];
       }
     }
+    int ovl_flat = r;  // overlap: the position's flattened index (its U row and lse_q)
     if constexpr (MODE == kModeOverlap) {
-      req = r / p.gamma;
-      pos = r % p.gamma + 1;
-      if (valid && p.ell != nullptr) valid = pos <= min(max(__ldg(p.ell + req), 0), p.gamma);
+      if (p.ovl_nrows != nullptr) {
+        // compact rows: target row t of request req evaluates position t + 1 (t < ell)
+        valid = valid && r < *reinterpret_cast<const volatile int*>(p.ovl_nrows);
+        req = valid ? __ldg(p.ovl_req + r) : 0;
+        const int t = valid ? __ldg(p.ovl_t + r) : 0;
+        pos = t + 1;
+        valid = valid && t < min(max(__ldg(p.ell + req), 0), p.gamma);
+        ovl_flat = req * p.gamma + t;
+      } else {
+        req = r / p.gamma;
+        pos = r % p.gamma + 1;
+        if (valid && p.ell != nullptr) valid = pos <= min(max(__ldg(p.ell + req), 0), p.gamma);
+      }
       if (valid) {
-        lse_q = __ldg(p.lse_q + r);
+        lse_q = __ldg(p.lse_q + ovl_flat);
         lse_t = p.lse_t[r];
       }
     }
@@ -561,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                            kDraftMath ? kStreamDraft : kStreamCorrect, (uint32_t)pos));
     const bool u_valid = valid && !bonus_row;
     const size_t urow = MODE == kModeOverlap
-                            ? (size_t)(valid ? r : 0) * (size_t)p.V
+                            ? (size_t)(valid ? ovl_flat : 0) * (size_t)p.V
                             : ((size_t)(u_valid ? r : 0) * p.gamma + (u_valid ? pos - 1 : 0)) * (size_t)p.V;
     const size_t trow =
         (valid ? target_row_index(p.t_off, p.n_trows, p.gamma, req, pos - 1, p.status) : 0) * (size_t)p.V;
@@ -576,13 +609,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr bool kTPref = !kDraftMath && RB == 32;
     uint4 tnext[kPass][2];
     auto load_t = [&](int t, uint4 (&dst)[kPass][2]) {
-      const int vt = (group + t * p.ngroups) * kN;
+      const int vt = (group + t * ngroups) * kN;
 #pragma unroll
       for (int ps = 0; ps < kPass; ++ps)
         load_run8(p.target, p.dtype_t, trow, vt + col0 + ps * kCols, p.V, valid && t < my_tiles, dst[ps]);
     };
     auto load_u = [&](int t, uint4 (&dst)[kPass][2]) {
-      const int vt = (group + t * p.ngroups) * kN;
+      const int vt = (group + t * ngroups) * kN;
 #pragma unroll
       for (int ps = 0; ps < kPass; ++ps)
         load_run8(p.U, p.dtype_u, urow, vt + col0 + ps * kCols, p.V, u_valid && t < my_tiles, dst[ps]);
@@ -655,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < my_tiles; ++t) {
       const int buf = t & 1;
       const uint32_t use = (uint32_t)(t >> 1) & 1u;
-      const int vt = (group + t * p.ngroups) * kN;
+      const int vt = (group + t * ngroups) * kN;
       // the published bound is read a tile ahead of its use, so that its latency hides
       // behind this tile's work
       const int hint_pref = (kDraftMath && valid) ? __ldcg(p.hint + r) : 0;
@@ -1143,6 +1176,16 @@ int tc_num_partials(int R) {
   return groups > 0 ? groups : 1;
 }
 
+int tc_block_rows(int R) { return tc::block_rows(R); }
+
+int tc_grid_ctas(int R) {
+  // compact overlap rows: every SM (the kernel derives its blocks and groups from the row
+  // count), or one CTA per request block if there are more blocks than SMs
+  const int Rb = tc::block_rows(R);
+  const int rblocks = (R + Rb - 1) / Rb;
+  return rblocks > tc::num_sms() ? rblocks : tc::num_sms();
+}
+
 namespace tc {
 
 static TcParams base_params(int R, int gamma, int V, int rank, int dtype_u, float inv_temp, const void* U,
@@ -1185,7 +1228,8 @@ static cudaError_t launch(TcParams p, const void* W1g, const void* W2, cudaStrea
                          : (p.Rb == 64 ? draft_step_tc_kernel<64, MODE> : draft_step_tc_kernel<128, MODE>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(p.ngroups * p.rblocks), dim3(kThreads), (size_t)smem, s, map_a, map_b, map_u, p);
+  const int grid = p.grid > 0 ? p.grid : p.ngroups * p.rblocks;
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), (size_t)smem, s, map_a, map_b, map_u, p);
 }
 
 }  // namespace tc
@@ -1261,7 +1305,7 @@ cudaError_t launch_rnn_hproj_tc(const DraftArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_overlap_tc(const OverlapArgs& a, cudaStream_t s) {
-  const int rows = a.R * a.gamma;
+  const int rows = a.row_req != nullptr ? a.rows_max : a.R * a.gamma;
   tc::TcParams p = tc::base_params(rows, a.gamma, a.V, a.rank, a.dtype_u, a.inv_temp, a.U, nullptr, 0, 0, a.status);
   p.k = 1;
   p.target = a.target;
@@ -1270,6 +1314,12 @@ cudaError_t launch_overlap_tc(const OverlapArgs& a, cudaStream_t s) {
   p.lse_t = a.lse_t;
   p.ell = a.ell;
   p.ovl_part = a.part;
+  if (a.row_req != nullptr) {
+    p.ovl_req = a.row_req;
+    p.ovl_t = a.row_t;
+    p.ovl_nrows = a.n_rows;
+    p.grid = tc_grid_ctas(rows);
+  }
   return tc::launch<tc::kModeOverlap>(p, a.W1g, a.W2, s);
 }
 

@@ -375,19 +375,24 @@ dspark_status dspark_schedule_threshold(int R, int gamma, const float* conf, dou
   return DSPARK_OK;
 }
 
-// dspark_verify_overlap: the verify workspace followed by the overlap pass's pieces
+// dspark_verify_overlap: the verify workspace followed by the overlap pass's pieces.  The
+// tensor-core pass runs over the verify plan's compact rows (at most R*(gamma+1), one
+// partial per CTA of its grid); the CUDA-core pass over the R*gamma flattened positions.
 struct VerifyOverlapLayout {
   VerifyLayout v;
   size_t W1g, lse, part, total;
-  int npart;
+  int npart, rows;
+  bool compact;
 };
 
 VerifyOverlapLayout verify_overlap_layout(int R, int gamma, int V, int rank, int dtype_w) {
   using namespace dspark;
   VerifyOverlapLayout L;
   L.v = verify_layout(R, gamma, V, rank, dtype_w);
-  const size_t rows = (size_t)R * gamma;
-  L.npart = overlap_num_partials(R, gamma, V, rank, dtype_w);
+  L.compact = tc_supported(V, rank, dtype_w) != 0;
+  L.rows = L.compact ? R * (gamma + 1) : R * gamma;
+  const size_t rows = (size_t)L.rows;
+  L.npart = L.compact ? tc_grid_ctas(L.rows) : overlap_num_partials(R, gamma, V, rank, dtype_w);
   size_t off = L.v.total;
   L.W1g = off;
   off += align256(elem_size(dtype_w) * (size_t)round_up_rows((int)rows) * rank);
@@ -478,6 +483,7 @@ static dspark_status verify_impl(int R, int gamma, int V, int rank, int dtype_t,
   if (overlap_out != nullptr) {
     a.ovl_lse = reinterpret_cast<float*>(ws + LO.lse);
     a.ovl_W1g = ws + LO.W1g;
+    a.ovl_compact = LO.compact ? 1 : 0;
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = dspark::launch_verify(a, s);
@@ -496,6 +502,13 @@ static dspark_status verify_impl(int R, int gamma, int V, int rank, int dtype_t,
     o.lse_t = a.ovl_lse;
     o.part = reinterpret_cast<float*>(ws + LO.part);
     o.npart = LO.npart;
+    if (LO.compact) {
+      o.row_req = a.row_req;
+      o.row_t = a.row_t;
+      o.row_base = a.row_base;
+      o.n_rows = a.n_rows;
+      o.rows_max = LO.rows;
+    }
     if ((e = dspark::launch_overlap_pass(o, s)) != cudaSuccess) return cuda_fail(e, "verify_overlap");
   }
   return DSPARK_OK;

@@ -93,8 +93,10 @@ struct VerifyArgs {
   Partial* res_part2; // [npart, R] fallback partials: key = ln p + g
   // fused acceptance overlap (nullptr: off): verify_accept writes the target log-normaliser
   // of every verified row and the factor row of every verified position
-  float* ovl_lse;     // [R*gamma] lse of target row j-1 for position j <= ell[r], NaN beyond
-  void* ovl_W1g;      // [round_up_rows(R*gamma), rank] W1[x_{j-1}], zero beyond ell[r]
+  float* ovl_lse;     // lse of target row j-1 for position j <= ell[r]
+  void* ovl_W1g;      // W1[x_{j-1}] for position j <= ell[r]
+  int ovl_compact;    // 1: both in the compact row order (row row_base[r] + j - 1, tensor-core
+                      // pass); 0: at the flattened position r*gamma + j - 1 (NaN / zero beyond ell)
 };
 
 // Acceptance-overlap diagnostic: c*[r, j-1] = sum_v min(q_j(v), p_j(v)) for the drafted
@@ -121,6 +123,14 @@ struct OverlapArgs {
   int nchunk;
   float* part;          // [npart, R*gamma] partial sums of min(q, p)
   int npart;
+  // fused with verification on the tensor-core path: the bias pass runs over the verify
+  // plan's compact rows (request row_req[q], target row row_t[q], *n_rows of them, at most
+  // rows_max); W1g and lse_t are in that row order and part is [grid, rows_max]
+  const int* row_req;   // nullptr: the flattened R*gamma positions
+  const int* row_t;
+  const int* row_base;  // [R] first compact row of request r
+  const int* n_rows;
+  int rows_max;
 };
 
 // Sequential temperature scaling on held-out data (N samples, gamma positions, G grid
@@ -169,6 +179,8 @@ int record_error(int code, const char* msg);
 int simt_num_chunks(int V);
 int tc_supported(int V, int rank, int dtype_w);
 int tc_num_partials(int R);
+int tc_block_rows(int R);  // rows per request block of a tensor-core launch over R rows
+int tc_grid_ctas(int R);   // CTAs of the compact overlap pass over at most R rows
 int draft_num_partials(int R, int V, int rank, int dtype_w);
 int round_up_rows(int R);
 

@@ -286,6 +286,30 @@ __global__ void overlap_combine_kernel(OverlapArgs a, int npart) {
   if (lane == 0) a.out[i] = ok ? t : NAN;
 }
 
+// Compact rows (fused with verification): one warp per flattened position (r, j), the
+// partial sums of compact row row_base[r] + j - 1 over the vocabulary groups the bias pass
+// used.  The pass derived its request blocks and groups from the row count exactly as
+// here: blocks of rb_rows rows, grid / blocks groups.
+__global__ void overlap_combine_compact_kernel(OverlapArgs a, int rb_rows, int grid) {
+  griddep_allow_next();
+  griddep_wait();
+  const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (i >= a.R * a.gamma) return;
+  const int r = i / a.gamma, j = i % a.gamma + 1;
+  const bool ok = j <= overlap_len(a, r);
+  const int n = max(*a.n_rows, 0);
+  const int blocks = (n + rb_rows - 1) / rb_rows;
+  const int groups = blocks > 0 ? max(1, grid / blocks) : 0;
+  const size_t q = (size_t)a.row_base[r] + (j - 1);
+  float t = 0.f;
+  if (ok && q < (size_t)n)
+    for (int g = lane; g < groups; g += 32) t += a.part[(size_t)g * a.rows_max + q];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+  if (lane == 0) a.out[i] = ok ? t : NAN;
+}
+
 int overlap_num_partials(int R, int gamma, int V, int rank, int dtype_w) {
   const int simt = simt_num_chunks(V);
   if (!tc_supported(V, rank, dtype_w)) return simt;
@@ -307,6 +331,13 @@ cudaError_t launch_overlap(const OverlapArgs& a, cudaStream_t s) {
 cudaError_t launch_overlap_pass(const OverlapArgs& a, cudaStream_t s) {
   const int rows = a.R * a.gamma;
   cudaError_t e;
+  if (a.row_req != nullptr) {
+    // compact rows (tensor-core path only)
+    if (!tc_supported(a.V, a.rank, a.dtype_w) || tc_grid_ctas(a.rows_max) > a.npart) return cudaErrorInvalidValue;
+    if ((e = launch_overlap_tc(a, s)) != cudaSuccess) return e;
+    return launch_pdl(overlap_combine_compact_kernel, dim3((rows * 32 + 255) / 256), dim3(256), 0, s, a,
+                      tc_block_rows(a.rows_max), tc_grid_ctas(a.rows_max));
+  }
   int npart;
   if (tc_supported(a.V, a.rank, a.dtype_w)) {
     if ((e = launch_overlap_tc(a, s)) != cudaSuccess) return e;

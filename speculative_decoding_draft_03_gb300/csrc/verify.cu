@@ -278,19 +278,26 @@ __global__ void verify_accept_kernel(VerifyArgs a) {
     a.n_out[r] = n_acc + 1;
   }
   // fused acceptance overlap: target row j's log-normaliser for position j + 1 (j < ell),
-  // and the factor row W1[x_{j-1}] of every verified position j (zero beyond ell)
+  // and the factor row W1[x_{j-1}] of every verified position j; in the compact row order
+  // (row base + j - 1) for the tensor-core pass, else at the flattened position (NaN and
+  // zero rows beyond ell)
   if (a.ovl_lse != nullptr) {
+    const size_t obase = a.ovl_compact ? (size_t)base : (size_t)r * a.gamma;
 #pragma unroll
     for (int s = 0; s < kRowSlots; ++s) {
       const int j = lane + 32 * s;
-      if (j < a.gamma) a.ovl_lse[(size_t)r * a.gamma + j] = j < ell ? lse_own[s] : NAN;
+      if (j < ell)
+        a.ovl_lse[obase + j] = lse_own[s];
+      else if (!a.ovl_compact && j < a.gamma)
+        a.ovl_lse[obase + j] = NAN;
     }
-    for (int j = 1; j <= a.gamma; ++j) {
+    const int jmax = a.ovl_compact ? ell : a.gamma;
+    for (int j = 1; j <= jmax; ++j) {
       const bool on = j <= ell;
       int xp = 0;
       if (on)
         xp = checked_token((j == 1) ? __ldg(a.x0 + r) : __ldg(a.x + (size_t)r * a.gamma + (j - 2)), a.V, a.status, 13);
-      const size_t src = (size_t)xp * a.rank, dst = ((size_t)r * a.gamma + (j - 1)) * a.rank;
+      const size_t src = (size_t)xp * a.rank, dst = (obase + (j - 1)) * a.rank;
       if (a.dtype_w == DSPARK_BF16) {
         const unsigned short* w1 = reinterpret_cast<const unsigned short*>(a.W1);
         unsigned short* g = reinterpret_cast<unsigned short*>(a.ovl_W1g);
