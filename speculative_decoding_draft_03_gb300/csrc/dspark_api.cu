@@ -117,15 +117,18 @@ VerifyLayout verify_layout(int R, int gamma, int V, int rank, int dtype_w) {
 }
 
 struct OverlapLayout {
-  size_t W1g, lse_t, lse_part, part, total;
+  size_t W1g, lse_t, lse_part, part, row_req, row_t, row_base, n_rows, total;
   int npart, nchunk;
 };
 
+// Sized for either row order: the flattened positions, or the compact rows of the
+// evaluated positions (tensor-core path with lengths: one partial per CTA of its grid).
 OverlapLayout overlap_layout(int R, int gamma, int V, int rank, int dtype_w) {
   using namespace dspark;
   OverlapLayout L;
   const size_t rows = (size_t)R * gamma;
   L.npart = overlap_num_partials(R, gamma, V, rank, dtype_w);
+  if (tc_supported(V, rank, dtype_w) && tc_grid_ctas((int)rows) > L.npart) L.npart = tc_grid_ctas((int)rows);
   size_t off = 256;
   L.W1g = off;
   off += align256(elem_size(dtype_w) * (size_t)round_up_rows((int)rows) * rank);
@@ -136,6 +139,14 @@ OverlapLayout overlap_layout(int R, int gamma, int V, int rank, int dtype_w) {
   off += align256(8 * rows * (size_t)L.nchunk);
   L.part = off;
   off += align256(4 * rows * (size_t)L.npart);
+  L.row_req = off;
+  off += align256(4 * rows);
+  L.row_t = off;
+  off += align256(4 * rows);
+  L.row_base = off;
+  off += align256(4 * (size_t)R);
+  L.n_rows = off;
+  off += 256;
   L.total = off;
   return L;
 }
@@ -614,6 +625,14 @@ dspark_status dspark_acceptance_overlap(int R, int gamma, int V, int rank, int d
   a.nchunk = L.nchunk;
   a.part = reinterpret_cast<float*>(ws + L.part);
   a.npart = L.npart;
+  if (ell != nullptr && dspark::tc_supported(V, rank, dtype_w)) {
+    // only the evaluated positions go through the tensor-core pass
+    a.row_req = reinterpret_cast<int*>(ws + L.row_req);
+    a.row_t = reinterpret_cast<int*>(ws + L.row_t);
+    a.row_base = reinterpret_cast<int*>(ws + L.row_base);
+    a.n_rows = reinterpret_cast<int*>(ws + L.n_rows);
+    a.rows_max = R * gamma;
+  }
   cudaError_t e = dspark::launch_overlap(a, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "acceptance_overlap");
   return DSPARK_OK;

@@ -123,13 +123,14 @@ struct OverlapArgs {
   int nchunk;
   float* part;          // [npart, R*gamma] partial sums of min(q, p)
   int npart;
-  // fused with verification on the tensor-core path: the bias pass runs over the verify
-  // plan's compact rows (request row_req[q], target row row_t[q], *n_rows of them, at most
-  // rows_max); W1g and lse_t are in that row order and part is [grid, rows_max]
-  const int* row_req;   // nullptr: the flattened R*gamma positions
-  const int* row_t;
-  const int* row_base;  // [R] first compact row of request r
-  const int* n_rows;
+  // tensor-core path with lengths: the bias pass runs over compact rows (request
+  // row_req[q], target row row_t[q], *n_rows of them, at most rows_max): the verify plan's
+  // rows when fused with verification, else the evaluated positions only
+  // (overlap_plan_kernel); W1g and lse_t are in that row order and part is [grid, rows_max]
+  int* row_req;   // nullptr: the flattened R*gamma positions
+  int* row_t;
+  int* row_base;  // [R] first compact row of request r
+  int* n_rows;
   int rows_max;
 };
 

@@ -11,6 +11,8 @@
 // picture").  The confidence head is trained against this label; evaluating it on
 // verified rounds measures how well c_j is calibrated.
 //
+//   overlap_plan      (tensor-core path with lengths) compact rows of the evaluated
+//                     positions: an exclusive prefix over the lengths
 //   overlap_prepare   CTA (flattened position, 8192-id chunk): the chunk's softmax
 //                     statistics of target row j-1 / T, and the factor row W1[x_{j-1}]
 //                     (the A operand of the bias contraction)
@@ -67,8 +69,58 @@ __device__ __forceinline__ void online_add(float& m, float& s, float x) {
   }
 }
 
+// Compact rows (tensor-core path with lengths): the evaluated positions of request r are
+// rows row_base[r] .. row_base[r] + n_r - 1 (row_req = r, row_t = j - 1), n_rows in all.
+// One CTA: an exclusive prefix sum over the clamped lengths.
+constexpr int kOvlPlanThreads = 1024;
+__global__ void __launch_bounds__(kOvlPlanThreads) overlap_plan_kernel(OverlapArgs a) {
+  griddep_allow_next();
+  griddep_wait();
+  __shared__ int wsum[32];
+  const int per = (a.R + blockDim.x - 1) / blockDim.x;
+  const int lo = threadIdx.x * per, hi = min(lo + per, a.R);
+  int run = 0;
+  for (int r = lo; r < hi; ++r) run += overlap_len(a, r);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = (lane < (int)(blockDim.x >> 5)) ? wsum[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += t;
+    }
+    wsum[lane] = w;
+  }
+  __syncthreads();
+  int base = (incl - run) + (warp > 0 ? wsum[warp - 1] : 0);
+  for (int r = lo; r < hi; ++r) {
+    const int n = overlap_len(a, r);
+    a.row_base[r] = base;
+    for (int t = 0; t < n; ++t) {
+      a.row_req[base + t] = r;
+      a.row_t[base + t] = t;
+    }
+    base += n;
+  }
+  if (threadIdx.x == blockDim.x - 1) *a.n_rows = base;
+}
+
+// Row of position (r, j) in the prepared arrays: compact row, or the flattened position.
+__device__ __forceinline__ size_t overlap_row(const OverlapArgs& a, int r, int j) {
+  return a.row_req != nullptr ? (size_t)a.row_base[r] + (j - 1) : (size_t)r * a.gamma + (j - 1);
+}
+
 // CTA (position i, vocabulary chunk c): chunk c's (max, sum exp) of target row j-1 / T,
-// and for c = 0 the position's factor row (zero where the position is not evaluated).
+// and for c = 0 the position's factor row (flattened rows: zero where the position is not
+// evaluated; compact rows hold only evaluated positions).
 __global__ void __launch_bounds__(kOvlThreads) overlap_prepare_kernel(OverlapArgs a) {
   griddep_allow_next();
   griddep_wait();
@@ -79,13 +131,15 @@ __global__ void __launch_bounds__(kOvlThreads) overlap_prepare_kernel(OverlapArg
     if (l < 0 || l > a.gamma) report_bad_input(a.status, 31);
   }
   const bool valid = j <= overlap_len(a, r);
+  if (!valid && a.row_req != nullptr) return;  // compact: no row for this position
+  const size_t row = valid ? overlap_row(a, r, j) : (size_t)i;
   if (c == 0 && threadIdx.x < 32) {
     int xp = 0;
     if (valid) {
       const int raw = j == 1 ? __ldg(a.x0 + r) : __ldg(a.x + (size_t)r * a.gamma + (j - 2));
       xp = checked_token(raw, a.V, a.status, 30);
     }
-    const size_t src = (size_t)xp * a.rank, dst = (size_t)i * a.rank;
+    const size_t src = (size_t)xp * a.rank, dst = row * a.rank;
     if (a.dtype_w == DSPARK_F32) {
       const float* w1 = reinterpret_cast<const float*>(a.W1);
       float* g = reinterpret_cast<float*>(a.W1g);
@@ -97,7 +151,7 @@ __global__ void __launch_bounds__(kOvlThreads) overlap_prepare_kernel(OverlapArg
     }
   }
   if (!valid) {
-    if (threadIdx.x == 0) a.lse_part[(size_t)i * a.nchunk + c] = make_float2(-INFINITY, 0.f);
+    if (threadIdx.x == 0) a.lse_part[row * a.nchunk + c] = make_float2(-INFINITY, 0.f);
     return;  // uniform across the CTA
   }
   const size_t trow = ((size_t)r * (a.gamma + 1) + (j - 1)) * (size_t)a.V;
@@ -150,7 +204,7 @@ __global__ void __launch_bounds__(kOvlThreads) overlap_prepare_kernel(OverlapArg
       const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
       lse_merge(m, s, m2, s2);
     }
-    if (lane == 0) a.lse_part[(size_t)i * a.nchunk + c] = make_float2(m, s);
+    if (lane == 0) a.lse_part[row * a.nchunk + c] = make_float2(m, s);
   }
 }
 
@@ -162,13 +216,15 @@ __global__ void overlap_lse_kernel(OverlapArgs a) {
   const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (i >= a.R * a.gamma) return;
-  if ((i % a.gamma) + 1 > overlap_len(a, i / a.gamma)) {
-    if (lane == 0) a.lse_t[i] = NAN;
+  const int r = i / a.gamma, j = i % a.gamma + 1;
+  if (j > overlap_len(a, r)) {
+    if (lane == 0 && a.row_req == nullptr) a.lse_t[i] = NAN;
     return;
   }
+  const size_t row = overlap_row(a, r, j);
   float m = -INFINITY, s = 0.f;
   for (int c = lane; c < a.nchunk; c += 32) {
-    const float2 p = a.lse_part[(size_t)i * a.nchunk + c];
+    const float2 p = a.lse_part[row * a.nchunk + c];
     lse_merge(m, s, p.x, p.y);
   }
 #pragma unroll
@@ -176,7 +232,7 @@ __global__ void overlap_lse_kernel(OverlapArgs a) {
     const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
     lse_merge(m, s, m2, s2);
   }
-  if (lane == 0) a.lse_t[i] = m + logf(s);
+  if (lane == 0) a.lse_t[row] = m + logf(s);
 }
 
 // CUDA-core bias pass (fp32 weights or shapes the tensor-core path does not take).
@@ -319,8 +375,11 @@ int overlap_num_partials(int R, int gamma, int V, int rank, int dtype_w) {
 
 cudaError_t launch_overlap(const OverlapArgs& a, cudaStream_t s) {
   const int rows = a.R * a.gamma;
-  cudaError_t e = launch_pdl(overlap_prepare_kernel, dim3((unsigned)((size_t)rows * a.nchunk)), dim3(kOvlThreads), 0,
-                             s, a);
+  cudaError_t e;
+  if (a.row_req != nullptr &&
+      (e = launch_pdl(overlap_plan_kernel, dim3(1), dim3(kOvlPlanThreads), 0, s, a)) != cudaSuccess)
+    return e;
+  e = launch_pdl(overlap_prepare_kernel, dim3((unsigned)((size_t)rows * a.nchunk)), dim3(kOvlThreads), 0, s, a);
   if (e != cudaSuccess) return e;
   if ((e = launch_pdl(overlap_lse_kernel, dim3((unsigned)(((size_t)rows * 32 + 255) / 256)), dim3(256), 0, s, a)) !=
       cudaSuccess)
