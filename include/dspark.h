@@ -363,10 +363,10 @@ DSPARK_API dspark_status dspark_acceptance_overlap(
  * confidence-scheduled speculative decoding", section "Total variation label"):
  *   overlap_out [R,gamma] fp32, overlap_out[r,j-1] = sum_v min(q_j(v), p_j(v)) for
  *   j = 1..ell[r], NaN for j > ell[r]; q_j and p_j as in dspark_acceptance_overlap.
- * The target rows' log-normalisers come from the verification's own pass over them, so
- * the target is read once; the overlap then takes one more bias contraction over the
- * R*gamma positions.  The results equal dspark_acceptance_overlap(..., ell, ...) up to
- * the order of fp32 sums.  Workspace: dspark_verify_overlap_workspace_size() (larger
+ * The target rows' log-normalisers come from the verification's own pass over them; the
+ * overlap then takes one more bias contraction over the verified positions (which reads
+ * their U and target logits again).  The results equal dspark_acceptance_overlap(..., ell,
+ * ...) up to the order of fp32 sums.  Workspace: dspark_verify_overlap_workspace_size() (larger
  * than dspark_verify's; 0 for unsupported sizes).  Without the tensor-core path (fp32
  * weights, or rank / V outside its limits) R*gamma <= 262140.
  * ---------------------------------------------------------------------------------- */
