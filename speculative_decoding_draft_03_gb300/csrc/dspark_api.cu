@@ -128,7 +128,8 @@ OverlapLayout overlap_layout(int R, int gamma, int V, int rank, int dtype_w) {
   OverlapLayout L;
   const size_t rows = (size_t)R * gamma;
   L.npart = overlap_num_partials(R, gamma, V, rank, dtype_w);
-  if (tc_supported(V, rank, dtype_w) && tc_grid_ctas((int)rows) > L.npart) L.npart = tc_grid_ctas((int)rows);
+  if (tc_supported(V, rank, dtype_w) && tc_compact_ok((int)rows) && tc_grid_ctas((int)rows) > L.npart)
+    L.npart = tc_grid_ctas((int)rows);
   size_t off = 256;
   L.W1g = off;
   off += align256(elem_size(dtype_w) * (size_t)round_up_rows((int)rows) * rank);
@@ -400,7 +401,7 @@ VerifyOverlapLayout verify_overlap_layout(int R, int gamma, int V, int rank, int
   using namespace dspark;
   VerifyOverlapLayout L;
   L.v = verify_layout(R, gamma, V, rank, dtype_w);
-  L.compact = tc_supported(V, rank, dtype_w) != 0;
+  L.compact = tc_supported(V, rank, dtype_w) && tc_compact_ok(R * (gamma + 1));
   L.rows = L.compact ? R * (gamma + 1) : R * gamma;
   const size_t rows = (size_t)L.rows;
   L.npart = L.compact ? tc_grid_ctas(L.rows) : overlap_num_partials(R, gamma, V, rank, dtype_w);
@@ -625,7 +626,7 @@ dspark_status dspark_acceptance_overlap(int R, int gamma, int V, int rank, int d
   a.nchunk = L.nchunk;
   a.part = reinterpret_cast<float*>(ws + L.part);
   a.npart = L.npart;
-  if (ell != nullptr && dspark::tc_supported(V, rank, dtype_w)) {
+  if (ell != nullptr && dspark::tc_supported(V, rank, dtype_w) && dspark::tc_compact_ok(R * gamma)) {
     // only the evaluated positions go through the tensor-core pass
     a.row_req = reinterpret_cast<int*>(ws + L.row_req);
     a.row_t = reinterpret_cast<int*>(ws + L.row_t);

@@ -182,6 +182,9 @@ int tc_supported(int V, int rank, int dtype_w);
 int tc_num_partials(int R);
 int tc_block_rows(int R);  // rows per request block of a tensor-core launch over R rows
 int tc_grid_ctas(int R);   // CTAs of the compact overlap pass over at most R rows
+// the compact overlap pass is used only when its request blocks fit on the SMs (then it
+// launches one CTA per SM and its partials take SMs x R floats)
+int tc_compact_ok(int R);
 int draft_num_partials(int R, int V, int rank, int dtype_w);
 int round_up_rows(int R);
 

@@ -143,6 +143,18 @@ def test_verify_overlap_validation(b):
     assert b.verify_overlap_workspace_size(0, 4, 1024, 32, torch.float32) == 0
 
 
+def test_overlap_workspaces_stay_linear_in_rows(b):
+    # the compact tensor-core pass keeps one partial per SM per row only while its row
+    # blocks fit on the SMs; larger batches take the flattened path, whose partials do not
+    # grow with the grid (no quadratic growth in R * gamma)
+    import torch
+    bf = torch.bfloat16
+    for fn in (b.acceptance_overlap_workspace_size, b.verify_overlap_workspace_size):
+        small = fn(4096, 16, 151936, 256, bf)
+        big = fn(65536, 16, 151936, 256, bf)
+        assert 0 < small < big < 20 * small, (fn.__name__, small, big)
+
+
 def test_workspace_sizes_grow_with_shape(b):
     import torch
     s1 = b.draft_workspace_size(4, 4, 1024, 32, 64, torch.float32)
