@@ -1178,11 +1178,6 @@ int tc_num_partials(int R) {
 
 int tc_block_rows(int R) { return tc::block_rows(R); }
 
-int tc_compact_ok(int R) {
-  const int Rb = tc::block_rows(R);
-  return (R + Rb - 1) / Rb <= tc::num_sms();
-}
-
 int tc_grid_ctas(int R) {
   // compact overlap rows: every SM (the kernel derives its blocks and groups from the row
   // count), or one CTA per request block if there are more blocks than SMs

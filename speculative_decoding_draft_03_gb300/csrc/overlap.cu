@@ -366,6 +366,15 @@ __global__ void overlap_combine_compact_kernel(OverlapArgs a, int rb_rows, int g
   if (lane == 0) a.out[i] = ok ? t : NAN;
 }
 
+int tc_compact_ok(int R) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    sms = 148;
+  const int Rb = tc_block_rows(R);
+  return (R + Rb - 1) / Rb <= sms;
+}
+
 int overlap_num_partials(int R, int gamma, int V, int rank, int dtype_w) {
   const int simt = simt_num_chunks(V);
   if (!tc_supported(V, rank, dtype_w)) return simt;
