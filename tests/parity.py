@@ -5,8 +5,9 @@
   winner and the runner-up, |u - p/q| for an acceptance test, the relative Theta gap or
   the a-gap at the scheduler's cut, or a residual whose winner/runner-up has
   rho < 1e-3 max(p, q)).  A boundary case must also be consistent (the GPU picked the
-  oracle's runner-up).  Boundary cases are counted; after one, the request's later
-  positions are not compared (its path has legitimately diverged).
+  oracle's runner-up).  Boundary cases are counted.  compare_draft stops comparing the
+  request after one (its path has legitimately diverged); compare_draft_continuing lets
+  the oracle adopt the GPU's token and keeps comparing the later positions.
 * Probabilities and confidences: |gpu - ref| <= tol * max(|ref|, floor), tol = 1e-5
   where W1/W2 and the logits are fp32, 2e-3 where any of them is bf16; floor = 1 for
   log-domain values (logq, lse) and 1e-12 for confidences.
@@ -107,3 +108,86 @@ def compare_verify(gpu, ref, tally: Tally, rows=None):
                        f"(margin {ref['corr_margin'][r]:.3g}, rho {ref['corr_rho'][r]})"
             tally.boundary += 1
             tally.notes.append(("correction", r))
+
+
+def _row_f64(W, x):
+    """Row x of a host weight array (float32, or raw bf16 bits as uint16) in float64."""
+    row = np.asarray(W[int(x)])
+    if row.dtype == np.uint16:
+        return (row.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return row.astype(np.float64)
+
+
+def compare_draft_continuing(gpu, ref, host, tol, tally):
+    """Like compare_draft, but a boundary case does not end the comparison of its request:
+    the oracle adopts the GPU's token (the survey's comparison rule) and recomputes the
+    request's later positions from it, draw by draw (oracle.draft_row for the draw and
+    oracle.rnn_confidence with the factor row W1[x_{k-1}] as the state for c_k, which is
+    the Markov head's confidence), and those are compared too.
+
+    gpu: numpy arrays x, logq, lse, conf [n, gamma]; ref: oracle.markov_draft on the same n
+    requests; host: dict of the same requests' U [n,gamma,V], h [n,gamma,d], req_id [n]
+    and the shared W1, W2, conf_w, conf_b, conf_logit_scale, conf_temp, temperature, seed,
+    rnd.  Returns the number of positions compared exactly."""
+    import oracle
+    n, gamma = ref["x"].shape
+    compared = 0
+    for r in range(n):
+        adopted = False
+        for k in range(gamma):
+            if adopted:
+                xp = int(gpu["x"][r, k - 1])
+                arow = _row_f64(host["W1"], xp)
+                one = oracle.draft_row(host["U"][r, k], arow, host["W2"], host["temperature"], host["seed"],
+                                       int(host["req_id"][r]), host["rnd"], k + 1)
+                c = oracle.rnn_confidence(host["h"][r:r + 1, k:k + 1], arow.reshape(1, 1, -1), host["conf_w"],
+                                          host["conf_b"], host["conf_logit_scale"],
+                                          np.asarray(host["conf_temp"])[k:k + 1])[0, 0]
+                cur = dict(x=one["x"], logq=one["logq"], lse=one["lse"], conf=c, margin=one["margin"],
+                           runner_up=one["runner_up"])
+            else:
+                cur = {key: ref[key][r, k] for key in ("x", "logq", "lse", "conf", "margin", "runner_up")}
+            tally.draws += 1
+            gx = gpu["x"][r, k]
+            keys = (("logq", 1.0), ("lse", 1.0), ("conf", 1e-12))
+            if gx != cur["x"]:
+                ok = cur["margin"] < BOUNDARY and gx == cur["runner_up"]
+                assert ok, f"draft token mismatch r={r} k={k+1}: gpu {gx} oracle {cur['x']} " \
+                           f"(margin {cur['margin']:.3g}, runner-up {cur['runner_up']})"
+                tally.boundary += 1
+                tally.notes.append(("draft", r, k))
+                keys = (("lse", 1.0), ("conf", 1e-12))  # independent of the draw
+                adopted = True
+            else:
+                compared += 1
+            for key, fl in keys:
+                if close(gpu[key][r, k], cur[key], tol, fl):
+                    raise AssertionError(f"{key} r={r} k={k+1}: gpu {gpu[key][r, k]!r} oracle {cur[key]!r} tol {tol}")
+    return compared
+
+
+def check_round_stagewise(w, wn, d, s, v, rnd, x0, tally):
+    """Every request of one GPU round (numpy outputs d, s, v of the draft, scheduler and
+    verification) against the oracle, stage by stage: the draft with the oracle adopting
+    the GPU's token after a boundary case, the scheduler on the GPU's confidences, and
+    verification on the GPU's drafts and verify lengths.  w: the workload (device
+    tensors, for the dtypes); wn: its host copy; x0: the anchors the round used."""
+    import torch
+    import oracle
+    bf = any(w[k].dtype == torch.bfloat16 for k in ("U", "target", "W1", "W2"))
+    tol = 2e-3 if bf else 1e-5
+    ref_d = oracle.markov_draft(wn["U"], wn["W1"], wn["W2"], wn["h"], wn["conf_w"], wn["conf_b"],
+                                wn["conf_logit_scale"], wn["conf_temp"], wn["temperature"], x0, wn["req_id"],
+                                wn["seed"], rnd)
+    host = dict(wn, rnd=rnd)
+    compare_draft_continuing(d, ref_d, host, tol, tally)
+    ref_s = oracle.schedule(d["conf"], wn["sps"], wn["mode"], wn.get("conf_hist"), wn.get("fixed_len", 0))
+    same = compare_schedule(dict(ell=s["ell"], B=s["B"][0], tau=s["tau"][0]), ref_s, tally, tau_tol=1e-9)
+    ref_v = oracle.verify(wn["target"], wn["U"], wn["W1"], wn["W2"], x0, d["x"], d["logq"], d["lse"], s["ell"],
+                          wn["temperature"], wn["req_id"], wn["seed"], rnd)
+    compare_verify(v, ref_v, tally)
+    # every request's output is well formed
+    assert ((v["n_acc"] >= 0) & (v["n_acc"] <= s["ell"])).all()
+    assert (v["n_out"] == v["n_acc"] + 1).all()
+    assert int(s["B"][0]) == w["R"] + int(s["ell"].sum())
+    return same

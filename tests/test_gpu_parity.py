@@ -13,7 +13,7 @@ import torch
 
 import oracle
 from speculative_decoding_draft_03_gb300 import workloads as wl
-from tests.parity import Tally, compare_draft, compare_schedule, compare_verify
+from tests.parity import Tally, check_round_stagewise, compare_draft, compare_schedule, compare_verify
 
 pytestmark = pytest.mark.gpu
 
@@ -140,32 +140,24 @@ def test_round_matches_oracle(name):
 
 def test_stress_chained_rounds_match_oracle():
     """100 chained rounds of the stress workload (reduced vocabulary): x0 of round t+1
-    is the last token round t emitted, the RNG round index advances."""
+    is the last token round t emitted on the GPU, the RNG round index advances.  Every
+    round is compared stage by stage; after a boundary case the oracle adopts the GPU's
+    choice and the comparison goes on (no round or request is skipped)."""
     b = _b()
     wg, wn = _gpu_workload("stress", V=1032, rank=64, d=64)
     rd = b.Round(wg)
     x0_g = wg["x0"].clone()
-    x0_o = wn["x0"].copy()
     tally = Tally()
+    R = wn["R"]
     for t in range(100):
+        x0_h = x0_g.cpu().numpy()
         d, s, v = rd.run(rnd=t, x0=x0_g)
         torch.cuda.synchronize()
-        ref = oracle.run_round(wn, rnd=t, x0=x0_o)
-        before = tally.boundary
-        compare_draft(_np(d), ref["draft"], _tol(wg), tally)
-        if tally.boundary == before:
-            gs = _np(s)
-            if compare_schedule(dict(ell=gs["ell"], B=gs["B"][0], tau=gs["tau"][0]), ref["sched"], tally,
-                                _tol(wg)):
-                compare_verify(_np(v), ref["verify"], tally)
-        if tally.boundary != before:
-            break  # paths diverged legitimately at a boundary case; earlier rounds matched
         gv = _np(v)
-        last = gv["tokens"][np.arange(wn["R"]), gv["n_out"] - 1]
-        assert np.array_equal(last, ref["verify"]["tokens"][np.arange(wn["R"]), ref["verify"]["n_out"] - 1])
+        check_round_stagewise(wg, wn, _np(d), _np(s), gv, t, x0_h, tally)
+        last = gv["tokens"][np.arange(R), gv["n_out"] - 1]
         x0_g = torch.from_numpy(last.astype(np.int32)).cuda()
-        x0_o = ref["verify"]["tokens"][np.arange(wn["R"]), ref["verify"]["n_out"] - 1].astype(np.int32)
-    assert t >= 50 or tally.boundary > 0
+    assert tally.draws >= 100 * R * wn["gamma"]
     tally.check_rate()
 
 

@@ -1,12 +1,16 @@
 """dspark_verify_ragged: verification on a flattened target batch (each request's verify
-rows packed at its own offset, in any order, with unused rows in between) computes
-exactly what dspark_verify computes on the padded [R, gamma+1, V] target, whose results
-the parity tests compare with the oracle."""
+rows packed at its own offset, in any order, with unused rows in between; numb3r33 blog
+"Variable-length verification without wasting kernels") computes exactly what
+dspark_verify computes on the padded [R, gamma+1, V] target, and what the fp64 oracle
+computes on the padded target that the host rebuilds from the flattened rows and their
+offsets."""
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from speculative_decoding_draft_03_gb300 import workloads as wl
+from tests.parity import Tally, compare_verify
 
 pytestmark = pytest.mark.gpu
 
@@ -27,6 +31,22 @@ def _flatten(target, ell, rng):
     return torch.cat(rows, 0).contiguous(), torch.from_numpy(offsets).cuda()
 
 
+def _host(t):
+    t = t.detach().cpu().contiguous()
+    return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
+
+
+def _unflatten(flat, offsets, ell, gamma):
+    """[R, gamma+1, V] with request r's rows t = 0..ell[r] taken from flat[offsets[r] + t]
+    (the rows past ell[r] are never read; they stay zero)."""
+    R = len(offsets)
+    out = np.zeros((R, gamma + 1, flat.shape[1]), flat.dtype)
+    for r in range(R):
+        n = int(ell[r]) + 1
+        out[r, :n] = flat[offsets[r]:offsets[r] + n]
+    return out
+
+
 @pytest.mark.parametrize("name,over", [("tiny", {}), ("qwen3-8b", dict(V=20000, d=256)),
                                        ("deepseek-v4", dict(V=4104, d=256)), ("stress", dict(V=2056, d=64))])
 def test_ragged_matches_padded(name, over):
@@ -34,6 +54,7 @@ def test_ragged_matches_padded(name, over):
     w = wl.make(name, device="cuda", **over)
     rd = b.Round(w)
     rng = np.random.default_rng(7)
+    tally = Tally()
     for rnd in (2, 3):
         d, s, v = rd.run(rnd=rnd)
         torch.cuda.synchronize()
@@ -45,6 +66,13 @@ def test_ragged_matches_padded(name, over):
         torch.cuda.synchronize()
         for k in ("n_acc", "tokens", "n_out"):
             assert torch.equal(got[k], ref[k]), (name, rnd, k)
+        # the oracle on the padded target rebuilt on the host from the flattened rows
+        padded = _unflatten(_host(flat), off.cpu().numpy(), ell, w["gamma"])
+        ref_o = oracle.verify(padded, _host(w["U"]), _host(w["W1"]), _host(w["W2"]), _host(rd.x0), _host(d["x"]),
+                              _host(d["logq"]), _host(d["lse"]), ell, w["temperature"], _host(w["req_id"]),
+                              w["seed"], rnd)
+        compare_verify({k: t.cpu().numpy() for k, t in got.items()}, ref_o, tally)
+    tally.check_rate()
 
 
 def test_ragged_offset_out_of_range_is_reported():
