@@ -5,14 +5,17 @@ One step = one round over one batch: the Markov-head draft of gamma positions, t
 confidence scheduler, and exact verification (with the residual / bonus token), all
 through the C ABI of libdspark.so on device-resident inputs.  Prints one JSON line.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload qwen3-8b]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload stress]
   python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
 
-Timing: W untimed rounds, then K rounds, each bracketed by CUDA events on the launch
-stream; the L2 is flushed (a 256 MiB write) between rounds, outside the brackets.
-value = verified draft tokens (sum of accepted lengths) over all ranks / max over ranks
-of the summed round time.  Under torchrun each rank runs its own independent batch
-(weak scaling, no collective on the data path).
+The headline workload is the largest one, stress (R=512, gamma=15, V=151936); the other
+four workloads are timed the same way in the same run and reported under "workloads".
+
+Timing: W untimed rounds, then K rounds, each one CUDA graph bracketed by CUDA events on
+the launch stream; the L2 is flushed (a 256 MiB write) between rounds, outside the
+brackets.  value = verified draft tokens (sum of accepted lengths) over all ranks / max
+over ranks of the summed round time.  Under torchrun each rank runs its own independent
+batch (weak scaling, no collective on the data path).
 """
 from __future__ import annotations
 
@@ -37,9 +40,12 @@ WORKLOAD_DESC = {
     "deepseek-v4": "DeepSeek-V4-shaped: R=256 gamma=5 V=129280 rank=256 d=4096, U/target bf16, capacity-K",
     "stress": "stress: R=512 gamma=15 V=151936 rank=256 d=4096, fp32 logits, early-stop scheduler",
 }
-DRAFT_KERNEL_SOURCES = ["speculative_decoding_draft_03_gb300/csrc/draft_tc.cu",
-                        "speculative_decoding_draft_03_gb300/csrc/draft_simt.cu",
-                        "speculative_decoding_draft_03_gb300/csrc/dspark_common.cuh"]
+HEADLINE = "stress"
+# requests per reference-arm step (a bounded slice of the workload's batch; see run_reference)
+REFERENCE_SLICE = 32
+# ncu counters committed under profiles/ (per kernel and workload, with the hash of the
+# kernel sources they were taken on)
+COUNTERS = os.path.join(ROOT, "profiles", "counters.json")
 
 
 def workload_desc(args):
@@ -47,15 +53,16 @@ def workload_desc(args):
     return desc + "; recurrent draft head (ns = ne = rank)" if getattr(args, "head", "markov") == "rnn" else desc
 
 
-def parse():
+def parse(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=200)
-    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="dspark", choices=["dspark", "reference"])
-    p.add_argument("--workload", default="qwen3-8b", choices=list(WORKLOAD_DESC))
+    p.add_argument("--workload", default=HEADLINE, choices=list(WORKLOAD_DESC))
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-others", action="store_true", help="time only the named workload")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--head", choices=["markov", "rnn"], default="markov",
                    help="draft head: the Markov head, or the recurrent head on the same workload")
@@ -63,7 +70,7 @@ def parse():
                    help="time the acceptance-overlap diagnostic on the workload's verified positions (standalone, "
                         "or fused into verification), or the sequential temperature fit on synthetic held-out "
                         "rounds, instead of the round")
-    return p.parse_args()
+    return p.parse_args(argv)
 
 
 def dist_env():
@@ -82,30 +89,34 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def source_hash():
+def source_hash(sources):
     h = hashlib.sha256()
-    for rel in DRAFT_KERNEL_SOURCES:
+    for rel in sources:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def stored_traffic(workload):
-    """Per-launch DRAM bytes of the draft step kernel from the committed ncu summary,
-    only if it was taken on the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", f"draft_step_{workload}.md")
+def stored_counters(kernel, workload, path=COUNTERS):
+    """The committed ncu counters of `kernel` on `workload` (dict), only if they were taken
+    on the current kernel sources (else None)."""
     try:
-        txt = open(path).read()
-    except OSError:
+        with open(path) as f:
+            entry = json.load(f)[kernel][workload]
+    except (OSError, KeyError, ValueError):
         return None
-    vals = {}
-    for line in txt.splitlines():
-        if line.startswith("traffic_bytes_per_launch:") or line.startswith("source_sha:"):
-            k, v = line.split(":", 1)
-            vals[k.strip()] = v.strip()
-    if vals.get("source_sha") != source_hash() or "traffic_bytes_per_launch" not in vals:
+    try:
+        if entry.get("source_sha") != source_hash(entry["sources"]):
+            return None
+    except (OSError, KeyError):
         return None
-    return float(vals["traffic_bytes_per_launch"])
+    return entry
+
+
+def stored_traffic(kernel, workload, path=COUNTERS):
+    """Per-launch DRAM bytes (read + write) of `kernel` from the committed counters, or None."""
+    e = stored_counters(kernel, workload, path)
+    return None if e is None or e.get("traffic_bytes_per_launch") is None else float(e["traffic_bytes_per_launch"])
 
 
 class ClockSampler:
@@ -120,7 +131,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "200", "-i", str(self.index)], stdout=subprocess.PIPE,
+                                          "-lms", "100", "-i", str(self.index)], stdout=subprocess.PIPE,
                                          stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -175,14 +186,37 @@ def combine_ranks(round_ms, tokens, device):
     return float(t.item()), int(n.item())
 
 
+def _es(dtype):
+    import torch
+    return torch.tensor([], dtype=dtype).element_size()
+
+
 def draft_step_bytes(w):
     """Algorithmic bytes of one draft-step launch: the U row block of every request, the
     whole W2 factor, and the gathered W1 rows."""
-    import torch
-    es = lambda t: torch.tensor([], dtype=t.dtype).element_size()
     R, V, rank = w["R"], w["V"], w["rank"]
     W2 = w["Wo"] if w.get("head") == "rnn" else w["W2"]  # the factor rows have the weights' type
-    return R * V * es(w["U"]) + rank * V * es(W2) + R * rank * es(W2)
+    return R * V * _es(w["U"].dtype) + rank * V * _es(W2.dtype) + R * rank * _es(W2.dtype)
+
+
+def draft_step_flops(w):
+    """Flops of one draft step's bias contraction: 2 R rank V."""
+    return 2 * w["R"] * w["rank"] * w["V"]
+
+
+def verify_rows_bytes(w, ell):
+    """Algorithmic bytes of the target-row statistics pass: every verified row, sum_r (ell_r + 1) V s_T."""
+    return int(sum(int(l) + 1 for l in ell)) * w["V"] * _es(w["target"].dtype)
+
+
+def correction_bytes(w, ell, n_acc):
+    """Algorithmic bytes of the correction pass: the U and target rows of every rejected
+    position and W2 once: #rej V (s_U + s_T) + rank V s_W.  (The bonus rows are counted
+    with the row-statistics pass.)"""
+    W2 = w["Wo"] if w.get("head") == "rnn" else w["W2"]
+    n_rej = int(sum(1 for l, a in zip(ell, n_acc) if int(a) < int(l)))
+    V = w["V"]
+    return n_rej * V * (_es(w["U"].dtype) + _es(w["target"].dtype)) + w["rank"] * V * _es(W2.dtype)
 
 
 def tensor_core_path(w):
@@ -210,46 +244,275 @@ def launches_per_round(w):
     return (1 if w["d"] > 0 else 0) + prepare + draft + 1 + 5
 
 
-def cpu_baseline(workload, w_host, sample_rounds=1):
+def acceptance_stats(gamma, ells, n_accs):
+    """Per-round figures of the verified rounds: mean sum of verify lengths, mean sum of
+    accepted lengths, and the conditional acceptance rate at each depth j (accepted at j,
+    given that j was verified and every earlier draft accepted), over all rounds."""
     import numpy as np
+    ell = np.asarray(ells, np.int64)
+    acc = np.asarray(n_accs, np.int64)
+    reached = [(int(((ell >= j) & (acc >= j - 1)).sum()), int((acc >= j).sum())) for j in range(1, gamma + 1)]
+    return {"rounds": int(ell.shape[0]),
+            "sum_ell_per_round": float(ell.sum(axis=1).mean()),
+            "sum_n_acc_per_round": float(acc.sum(axis=1).mean()),
+            "verify_batch_B_per_round": float((ell + 1).sum(axis=1).mean()),
+            "conditional_acceptance_by_depth": [round(a / n, 4) if n else None for n, a in reached],
+            "verified_at_depth": [n for n, _ in reached]}
+
+
+def time_rounds(b, w, steps, warmup, stream, flush, world=1, clk_index=None):
+    """Times `steps` rounds of workload `w` (each one CUDA graph, its own round index),
+    after `warmup` eager rounds.  Every 4th timed graph also records CUDA events around the
+    first draft step and around verification's row-statistics and correction passes (the
+    events are recorded inside those graphs only, so the other rounds run undisturbed).
+    Returns the summed round time (ms), the verified tokens, the per-launch samples with
+    their algorithmic bytes, the per-round verify lengths and accepted lengths, and the
+    clock summary when `clk_index` is given."""
+    import torch
+    dev = w["U"].device
+    R, gamma = w["R"], w["gamma"]
+    rd = b.Round(w)
+    step_timer = b.StepTimer(1)
+    vtimer = b.VerifyTimer()
+    for t in range(warmup):
+        rd.run(rnd=t)
+    torch.cuda.synchronize()
+    assert rd.status() == 0, "device status word reports an error"
+
+    profiled = [t % 4 == 0 for t in range(steps)]
+    graphs = []
+    for t in range(steps):
+        if profiled[t]:
+            with vtimer:
+                graphs.append(rd.capture(rnd=warmup + t, timer=step_timer))
+        else:
+            graphs.append(rd.capture(rnd=warmup + t))
+    for g in graphs:
+        g.replay()
+    torch.cuda.synchronize()
+    assert rd.status() == 0, "device status word reports an error"
+    step_timer.samples.clear()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ells = torch.empty((steps, R), dtype=torch.int32, device=dev)
+    accs = torch.empty((steps, R), dtype=torch.int32, device=dev)
+    verify_samples = []  # (rows ms, rows bytes, correction ms, correction bytes)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    clk = ClockSampler(clk_index) if clk_index is not None else None
+    if clk is not None:
+        clk.__enter__()
+    wall0 = time.perf_counter()
+    for t in range(steps):
+        flush.zero_()
+        starts[t].record(stream)
+        graphs[t].replay()
+        ends[t].record(stream)
+        ells[t].copy_(rd.sched_out["ell"])
+        accs[t].copy_(rd.verify_out["n_acc"])
+        if profiled[t]:
+            torch.cuda.synchronize()  # the events are shared by the profiled graphs
+            step_timer.collect()
+            vtimer.collect()
+            ell, acc = ells[t].tolist(), accs[t].tolist()
+            verify_samples.append((vtimer.rows[-1], verify_rows_bytes(w, ell), vtimer.correction[-1],
+                                   correction_bytes(w, ell, acc)))
+    torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    if clk is not None:
+        clk.__exit__(None, None, None)
+    assert rd.status() == 0, "device status word reports an error"
+    round_ms = sum(a.elapsed_time(e) for a, e in zip(starts, ends))
+    ell_h, acc_h = ells.cpu().numpy(), accs.cpu().numpy()
+    return {"round_ms": round_ms, "tokens": int(acc_h.sum()), "wall_s": wall, "steps": steps,
+            "step_ms": list(step_timer.samples), "verify_samples": verify_samples,
+            "ell": ell_h, "n_acc": acc_h, "clocks": clk.summary() if clk is not None else None, "round": rd}
+
+
+def roofline_entries(w, res, peaks, peak_kind, workload):
+    """HBM roofline of the three vocabulary-streaming kernels of a round (the draft step at
+    position 1, verification's row-statistics pass, the correction pass): algorithmic
+    bytes per launch / mean CUDA-event duration of the launch, against the measured copy
+    bandwidth; plus the tensor-core throughput of the draft step's bias contraction."""
+    hbm = peaks["hbm_gbs"]
+    out = {}
+    step_ms = res["step_ms"]
+    if step_ms:
+        avg = sum(step_ms) / len(step_ms)
+        nbytes = draft_step_bytes(w)
+        ach = nbytes / (avg / 1e3) / 1e9
+        ctr = stored_counters("draft_step", workload)
+        out["draft_step"] = {
+            "kernel": "draft_step_tc at position 1 (fused bias contraction + softmax stats + Gumbel-max)",
+            "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "peak_source": peak_kind,
+            "traffic": None if ctr is None else ctr.get("traffic_bytes_per_launch"),
+            "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": avg, "launches_timed": len(step_ms)}
+        tflops = draft_step_flops(w) / (avg / 1e3) / 1e12
+        tpeak = peaks.get("bf16_tflops", 1900.0)
+        out["draft_step_tensor"] = {
+            "kernel": "bias contraction of the draft step (tcgen05.mma kind::f16, bf16 x bf16 -> fp32)",
+            "bound": "tensor", "achieved": tflops, "peak": tpeak, "unit": "TFLOP/s", "frac": tflops / tpeak,
+            "flops_per_launch": draft_step_flops(w),
+            "ncu_tensor_pipe_active_pct": None if ctr is None else ctr.get("tensor_pipe_active_pct")}
+    vs = res["verify_samples"]
+    if vs:
+        for name, ti, bi, label in (("verify_rows", 0, 1, "verify_rows (target-row log-normalisers of the verified rows)"),
+                                    ("correction", 2, 3, "correction pass (residual (p-q)+ or bonus draw per request)")):
+            ms = sum(s[ti] for s in vs) / len(vs)
+            nbytes = sum(s[bi] for s in vs) / len(vs)
+            ach = nbytes / (ms / 1e3) / 1e9
+            ctr = stored_counters(name, workload)
+            out[name] = {"kernel": label, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                         "frac": ach / hbm, "peak_source": peak_kind,
+                         "traffic": None if ctr is None else ctr.get("traffic_bytes_per_launch"),
+                         "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": ms, "launches_timed": len(vs)}
+    return out
+
+
+def slice_workload(wn, rows):
+    """The per-request slice of a host workload: requests are independent in the draft and
+    verify stages, and the slice runs the scheduler over its own requests (same SPS table)."""
+    import numpy as np
+    rows = np.asarray(rows)
+    out = dict(wn)
+    for k in ("U", "target", "h", "x0", "req_id"):
+        out[k] = np.ascontiguousarray(wn[k][rows])
+    if wn.get("conf_hist") is not None:
+        out["conf_hist"] = np.ascontiguousarray(wn["conf_hist"][rows])
+    out["R"] = len(rows)
+    return out
+
+
+def oracle_seconds_estimate(wn, cores):
+    """Rough wall time of one oracle round: R gamma V rank fp64 multiply-adds for the draft
+    (plus ~10% for verification) at ~1 GMAC/s per core."""
+    return 1.1 * wn["R"] * wn["gamma"] * wn["V"] * wn["rank"] / (1e9 * max(1, cores))
+
+
+def compare_round(gpu, ref):
+    """GPU round vs the oracle's round on the same inputs and round index: draws compared in
+    order per request up to the first difference.  A difference where the oracle's decision
+    margin is below 1e-5 (Gumbel key gap, |u - p/q|, the scheduler's Theta gap) is a
+    boundary case; any other difference is a mismatch.  Returns the counts."""
+    import numpy as np
+    d, s, v = ref["draft"], ref["sched"], ref["verify"]
+    gx, gell, gacc, gtok = gpu["x"], gpu["ell"], gpu["n_acc"], gpu["tokens"]
+    R, gamma = d["x"].shape
+    draws = boundary = mismatch = 0
+    same_draft = np.ones(R, bool)
+    for r in range(R):
+        for k in range(gamma):
+            draws += 1
+            if gx[r, k] != d["x"][r, k]:
+                if d["margin"][r, k] < 1e-5 and gx[r, k] == d["runner_up"][r, k]:
+                    boundary += 1
+                else:
+                    mismatch += 1
+                same_draft[r] = False
+                break
+    draws += 1
+    if not np.array_equal(gell, s["ell"]):
+        if min(s["gap"], s["tie"]) < 1e-5 or not same_draft.all():
+            boundary += 1
+        else:
+            mismatch += 1
+        same_sched = False
+    else:
+        same_sched = True
+    for r in range(R):
+        if not (same_draft[r] and same_sched):
+            continue
+        draws += int(v["n_acc"][r]) + 2
+        if gacc[r] != v["n_acc"][r]:
+            j = min(int(gacc[r]), int(v["n_acc"][r]))
+            if abs(v["acc_margin"][r, j]) < 1e-5:
+                boundary += 1
+            else:
+                mismatch += 1
+            continue
+        if not np.array_equal(gtok[r], v["tokens"][r]):
+            if v["corr_margin"][r] < 1e-5 or min(v["corr_rho"][r]) < 1e-3:
+                boundary += 1
+            else:
+                mismatch += 1
+    return {"draws": draws, "boundary_cases": boundary, "mismatches": mismatch}
+
+
+def cpu_baseline(args, w_host, rd, max_seconds=30.0):
+    """The fp64 oracle timed on the host cores on one round of the workload (rnd 0): the
+    whole batch when that is estimated to take at most `max_seconds`, else a slice of the
+    requests.  The GPU runs the same round afterwards and the two are compared draw by
+    draw (boundary cases and mismatches are counted)."""
+    import numpy as np
+    import torch
     import oracle
+    cores = oracle.max_threads()
+    R = w_host["R"]
+    n = R
+    while n > 8 and oracle_seconds_estimate(dict(w_host, R=n), cores) > max_seconds:
+        n //= 2
+    wn = w_host if n == R else slice_workload(w_host, np.arange(n))
     t0 = time.perf_counter()
-    acc = 0
-    for t in range(sample_rounds):
-        out = oracle.run_round(w_host, rnd=t)
-        acc += int(out["verify"]["n_acc"].sum())
+    out = oracle.run_round(wn, rnd=0)
     dt = time.perf_counter() - t0
-    return {"value": acc / dt, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": f"{sample_rounds} full round(s) of the {workload} workload ({w_host['R']} requests), "
-                      f"fp64 C oracle, OpenMP over requests; {dt:.2f} s wall",
-            "seconds": dt}
+    acc = int(out["verify"]["n_acc"].sum())
+    check = None
+    if n == R:
+        d, s, v = rd.run(rnd=0)
+        torch.cuda.synchronize()
+        gpu = {"x": d["x"].cpu().numpy(), "ell": s["ell"].cpu().numpy(), "n_acc": v["n_acc"].cpu().numpy(),
+               "tokens": v["tokens"].cpu().numpy()}
+        check = compare_round(gpu, out)
+    what = "the whole batch" if n == R else f"the first {n} of its {R} requests (own scheduler over them)"
+    return {"value": acc / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"one round (round index 0) of the {args.workload} workload, {what}; fp64 C oracle, "
+                      f"OpenMP over requests; {dt:.2f} s wall",
+            "seconds": dt, "requests": n}, check
 
 
 def run_reference(args):
+    """The reference arm: the fp64 oracle (the pages publish no implementation) on the host
+    cores.  Each step is one round of a bounded slice of the workload's batch
+    (REFERENCE_SLICE requests, a different slice every step, each with its own scheduler),
+    so that the whole run ends within a few minutes; value = accepted tokens / oracle time."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
+    import numpy as np
     from speculative_decoding_draft_03_gb300 import workloads as wl
     import oracle
     oracle.build()
     w = wl.make(args.workload, device="cpu")
     w = wl.to_numpy(wl.add_rnn_head(w) if args.head == "rnn" else w)
+    R = w["R"]
+    n = min(R, REFERENCE_SLICE)
     total_tok, total_t = 0, 0.0
     for t in range(args.warmup + args.steps):
+        lo = (t * n) % R
+        rows = (np.arange(n) + lo) % R
+        wn = w if n == R else slice_workload(w, rows)
         t0 = time.perf_counter()
-        out = oracle.run_round(w, rnd=t)
+        out = oracle.run_round(wn, rnd=t)
         dt = time.perf_counter() - t0
         if t >= args.warmup:
             total_tok += int(out["verify"]["n_acc"].sum())
             total_t += dt
     value = total_tok / total_t
+    sample = (f"each step one round of a {n}-request slice of the {args.workload} workload ({R} requests), "
+              f"slices rotating over the batch, scheduler over the slice")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total_t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded generator, random-init weights)",
-            "config": {"workload": workload_desc(args)},
+            "config": {"workload": workload_desc(args), "requests_per_step": n},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
-                             "sample": f"each step one full round of the {args.workload} workload"},
+                             "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -433,6 +696,29 @@ def run_sts_diagnostic(args):
     return 0
 
 
+def time_other_workloads(b, wl, names, args, stream, flush, peaks, peak_kind):
+    """The other workloads, each generated on the device and timed like the headline one
+    (fewer rounds): verified tokens/s, round time and the draft step's HBM fraction."""
+    import torch
+    out = {}
+    launches = 0
+    for name in names:
+        w = wl.make(name, device="cuda", seed=0)
+        steps = max(4, min(args.steps, 20))
+        res = time_rounds(b, w, steps, max(3, min(args.warmup, 5)), stream, flush)
+        roof = roofline_entries(w, res, peaks, peak_kind, name)
+        out[name] = {"config": WORKLOAD_DESC[name], "value": res["tokens"] / (res["round_ms"] / 1e3), "unit": UNIT,
+                     "ms_per_step": res["round_ms"] / steps, "steps": steps,
+                     "draft_step_frac": roof.get("draft_step", {}).get("frac"),
+                     "verify_rows_frac": roof.get("verify_rows", {}).get("frac"),
+                     "correction_frac": roof.get("correction", {}).get("frac"),
+                     "per_round": acceptance_stats(w["gamma"], res["ell"], res["n_acc"])}
+        launches += launches_per_round(w) * steps
+        del res, w
+        torch.cuda.empty_cache()
+    return out, launches
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -460,74 +746,29 @@ def main():
         w_cpu = wl.add_rnn_head(w_cpu)
     w = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in w_cpu.items()}
     w["req_id"] = rank_request_ids(w["req_id"], rank, w["R"])
-    rd = b.Round(w)
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    n_acc_sum = torch.zeros((), dtype=torch.int64, device=dev)
-    # events around the first draft position's step kernel only: each event sits between
-    # kernels that otherwise overlap through programmatic dependent launch
-    timer = b.StepTimer(1)
-
-    for t in range(args.warmup):
-        rd.run(rnd=t)
-    torch.cuda.synchronize()
-    assert rd.status() == 0, "device status word reports an error"
-
-    # Each timed round is one CUDA graph (its own round index, so its own random draws),
-    # captured and replayed once before timing.  Every 4th graph also records the events
-    # around the first draft step (after the L2 flush it reads U and W2 from HBM).
-    profiled = [t % 4 == 0 for t in range(args.steps)]
-    graphs = [rd.capture(rnd=args.warmup + t, timer=timer if profiled[t] else None) for t in range(args.steps)]
-    for g in graphs:
-        g.replay()
-    torch.cuda.synchronize()
-    assert rd.status() == 0, "device status word reports an error"
-
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        wall0 = time.perf_counter()
-        for t in range(args.steps):
-            flush.zero_()
-            starts[t].record(stream)
-            graphs[t].replay()
-            ends[t].record(stream)
-            if profiled[t]:
-                torch.cuda.synchronize()  # the step events are shared by the profiled graphs
-                timer.collect()
-            n_acc_sum += rd.verify_out["n_acc"].sum()
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-        wall = time.perf_counter() - wall0
-    round_ms = sum(a.elapsed_time(e) for a, e in zip(starts, ends))
-    tokens = int(n_acc_sum.item())
-    round_ms, tokens = combine_ranks(round_ms, tokens, dev)
-    value = tokens / (round_ms / 1000.0)
-    assert rd.status() == 0, "device status word reports an error"
-
-    # dominant kernel: the vocabulary-streaming draft step (one launch per draft position)
     peaks, peak_kind = measured_peaks()
-    step_ms = sorted(timer.samples)
-    avg_step_ms = sum(step_ms) / max(1, len(step_ms))
-    step_bytes = draft_step_bytes(w)
-    achieved = step_bytes / (avg_step_ms / 1000.0) / 1e9
-    roofline = {"kernel": "draft_step at position 1 (fused bias contraction + softmax stats + Gumbel-max)",
-                "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "peak_source": peak_kind,
-                "traffic": stored_traffic(args.workload), "algorithmic_bytes_per_launch": step_bytes,
-                "avg_launch_ms": avg_step_ms, "launches_timed": len(step_ms)}
+
+    res = time_rounds(b, w, args.steps, args.warmup, stream, flush, world=world, clk_index=local)
+    round_ms, tokens = combine_ranks(res["round_ms"], res["tokens"], dev)
+    value = tokens / (round_ms / 1000.0)
+    roof = roofline_entries(w, res, peaks, peak_kind, args.workload)
+    rd = res["round"]
 
     e2e = None
     if not args.no_e2e:
         e2e = measure_e2e(b, w, w_cpu, rd, args, stream)
 
-    cpu = None
+    cpu, check = None, None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(args.workload, wl.to_numpy(w_cpu))
+        cpu, check = cpu_baseline(args, wl.to_numpy(w_cpu), rd)
+    launches = launches_per_round(w) * args.steps
+    others = None
+    if rank == 0 and world == 1 and not args.no_others and args.head == "markov":
+        del w_cpu
+        names = [n for n in WORKLOAD_DESC if n != args.workload]
+        others, extra = time_other_workloads(b, wl, names, args, stream, flush, peaks, peak_kind)
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -541,9 +782,11 @@ def main():
                            "parallelism": f"{world} independent batch(es), one per GPU"},
                 "rounds_per_s": 1000.0 * args.steps / round_ms,
                 "verified_tokens_per_round": tokens / args.steps / world,
-                "wall_s": wall, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": launches_per_round(w) * args.steps,
-                "clocks": clk.summary()}
+                "per_round": acceptance_stats(w["gamma"], res["ell"], res["n_acc"]),
+                "parity_check": check,
+                "wall_s": res["wall_s"], "roofline": roof.get("draft_step"),
+                "rooflines": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": launches, "clocks": res["clocks"], "workloads": others}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -97,6 +97,14 @@ DSPARK_API dspark_status dspark_workspace_status(void* workspace, int reset, int
  * event-record nodes of the graph, so every replay records them. */
 DSPARK_API void dspark_set_profile_events(void* const* events, int n_events);
 
+/* Measurement hook (not part of the method), like dspark_set_profile_events for the
+ * verification calls (dspark_verify, dspark_verify_ragged, dspark_verify_static,
+ * dspark_verify_overlap): events[0] / events[1] are recorded just before / after the
+ * target-row statistics pass, events[2] / events[3] just before / after the correction
+ * pass (the residual and bonus draws).  n_events < 4 or NULL turns recording off.  The
+ * setting is per host thread. */
+DSPARK_API void dspark_set_verify_profile_events(void* const* events, int n_events);
+
 /* ------------------------------------------------------------------------------------
  * Stage 1: Markov-head draft loop with the confidence head.
  *
@@ -261,7 +269,8 @@ DSPARK_API dspark_status dspark_verify_ragged(
  *   - All calls share the array: calls that may overlap on the GPU (other streams, other
  *     host threads on the same device) race and must be ordered by the caller.
  *   - The status block that must start at zero is cleared on `stream` at every call, so
- *     device-side input reports of earlier calls are not kept.
+ *     device-side input reports of earlier calls are not kept; read the last call's
+ *     report with dspark_verify_static_status() before the next call.
  * ---------------------------------------------------------------------------------- */
 DSPARK_API dspark_status dspark_verify_static(
     int R, int gamma, int V, int rank, int dtype_t, int dtype_u, int dtype_w,
@@ -269,6 +278,14 @@ DSPARK_API dspark_status dspark_verify_static(
     const int32_t* x0, const int32_t* x, const float* logq, const float* lse_q,
     const int32_t* ell, float temperature, const int64_t* req_id, uint64_t seed, uint64_t round,
     int32_t* n_acc_out, int32_t* tokens_out, int32_t* n_out, void* stream);
+
+/* Device status word of dspark_verify_static's scratch on the current device (the paper
+ * has no counterpart either).  Copies it into *status after synchronising `stream`:
+ * 0 = OK, DSPARK_INVALID_ARG = the last call met a token id, verify length or target row
+ * out of range on the device (it clamped the value and carried on),
+ * DSPARK_TIMEOUT = a bounded device wait gave up.  reset != 0 clears the word afterwards.
+ * Allocates nothing.  Not for use while `stream` is being captured (it synchronises). */
+DSPARK_API dspark_status dspark_verify_static_status(int reset, int* status, void* stream);
 
 /* ------------------------------------------------------------------------------------
  * Stage 1 with the recurrent (RNN) draft head.

@@ -47,11 +47,15 @@ def _load_library():
     lib.dspark_verify.argtypes = ([i32] * 7 + [P] * 4 + [P] * 5 + [f32, P, u64, u64] + [P] * 3 + [P, sz, P])
     lib.dspark_set_profile_events.argtypes = [P, i32]
     lib.dspark_set_profile_events.restype = None
+    lib.dspark_set_verify_profile_events.argtypes = [P, i32]
+    lib.dspark_set_verify_profile_events.restype = None
     lib.dspark_verify_ragged.argtypes = ([i32] * 7 + [P, i32, P] + [P] * 3 + [P] * 5 + [f32, P, u64, u64] + [P] * 3
                                          + [P, sz, P])
     lib.dspark_verify_ragged.restype = i32
     lib.dspark_verify_static.argtypes = ([i32] * 7 + [P] * 4 + [P] * 5 + [f32, P, u64, u64] + [P] * 3 + [P])
     lib.dspark_verify_static.restype = i32
+    lib.dspark_verify_static_status.argtypes = [i32, P, P]
+    lib.dspark_verify_static_status.restype = i32
     lib.dspark_verify_overlap_workspace_size.restype = sz
     lib.dspark_verify_overlap_workspace_size.argtypes = [i32] * 5
     lib.dspark_verify_overlap.argtypes = ([i32] * 7 + [P] * 4 + [P] * 5 + [f32, P, u64, u64] + [P] * 4
@@ -459,6 +463,15 @@ def verify_static(target, U, W1, W2, x0, x, logq, lse_q, ell, temperature, req_i
     return out
 
 
+def verify_static_status(reset=False, stream=None) -> int:
+    """The device status word of dspark_verify_static's scratch on the current device: what
+    the last call's kernels reported (0 OK, 1 bad device data, 5 a bounded wait gave up)."""
+    val = ctypes.c_int(0)
+    _check(lib.dspark_verify_static_status(int(reset), ctypes.byref(val), _stream(stream)),
+           "dspark_verify_static_status")
+    return int(val.value)
+
+
 class StepTimer:
     """Times the draft stage's vocabulary-streaming step kernel (one launch per draft
     position) with CUDA events the library records around each launch."""
@@ -482,6 +495,31 @@ class StepTimer:
         """After the stream has synchronised: append this round's per-launch times (ms)."""
         for k in range(len(self.events) // 2):
             self.samples.append(self.events[2 * k].elapsed_time(self.events[2 * k + 1]))
+
+
+class VerifyTimer:
+    """Times verification's two vocabulary-streaming kernels, the target-row statistics
+    pass and the correction pass, with CUDA events the library records around them."""
+
+    def __init__(self):
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        for e in self.events:
+            e.record()
+        torch.cuda.synchronize()
+        self._arr = (ctypes.c_void_p * 4)(*[e.cuda_event for e in self.events])
+        self.rows, self.correction = [], []
+
+    def __enter__(self):
+        lib.dspark_set_verify_profile_events(self._arr, 4)
+        return self
+
+    def __exit__(self, *exc):
+        lib.dspark_set_verify_profile_events(None, 0)
+
+    def collect(self):
+        """After the stream has synchronised: append this round's two times (ms)."""
+        self.rows.append(self.events[0].elapsed_time(self.events[1]))
+        self.correction.append(self.events[2].elapsed_time(self.events[3]))
 
 
 def device_status(ws, reset=False, stream=None) -> int:

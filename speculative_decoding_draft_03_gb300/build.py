@@ -43,15 +43,18 @@ def _stale(target, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, force: bool = False, extra_flags=(), build_dir: str = BUILD) -> str:
+    """Compile every csrc/*.cu and link libdspark.so in `build_dir` (the package's _build by
+    default; tests build variants with extra -D flags into their own directories)."""
+    os.makedirs(build_dir, exist_ok=True)
+    lib = os.path.join(build_dir, "libdspark.so")
     nvcc = _nvcc()
     srcs = _sources()
     hdrs = _headers()
     objs = []
     jobs = []
     for s in srcs:
-        o = os.path.join(BUILD, os.path.basename(s).replace(".cu", ".o"))
+        o = os.path.join(build_dir, os.path.basename(s).replace(".cu", ".o"))
         objs.append(o)
         if force or _stale(o, [s] + hdrs):
             jobs.append([nvcc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", s, "-o", o])
@@ -66,11 +69,11 @@ def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(8, max(1, len(jobs)))) as ex:
         list(ex.map(run, jobs))
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or jobs or _stale(lib, objs):
+        tmp = lib + f".tmp{os.getpid()}"
         run([nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs])
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

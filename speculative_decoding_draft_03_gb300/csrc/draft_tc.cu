@@ -62,7 +62,15 @@ constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
 constexpr int kCols = 8;          // vocabulary ids per epilogue pass
 constexpr int kTmemCols = 2 * kN;
 constexpr int kMaxRank = 256;
+#ifdef DSPARK_TEST_WAIT_LIMIT
+// Test builds only (never the shipped library): a short wait limit, and a draft call
+// with round index kTestStallRound has its U producer issue nothing, so the epilogue's
+// first bounded wait gives up and the abort path runs.
+constexpr long long kWaitCycles = DSPARK_TEST_WAIT_LIMIT;
+constexpr uint64_t kTestStallRound = 0x5EEDull;
+#else
 constexpr long long kWaitCycles = 4000000000ll;  // ~2 s at 2 GHz
+#endif
 // Tiles after which a CTA publishes its best keys: one for 32-request blocks (eight
 // tiles per CTA, where each publication is a visible share of the step), two otherwise.
 template <int RB>
@@ -89,6 +97,7 @@ struct Smem {
   static_assert(kEpiWarps * 32 * 32 <= stages * kStageBytes, "merge scratch must fit in the W2 ring");
   static_assert(uboxes >= 4 && uboxes <= kMaxUBoxes, "U ring must hold one tile of fp32 boxes");
   static_assert(total + 1024 <= 232448, "shared memory plan exceeds 227 KB");
+  static_assert(8 * (2 * stages + 7 + 2 * kMaxUBoxes) + 16 <= 512, "barriers, TMEM slot and abort flag fit in 512 B");
 };
 
 // ------------------------------------------------------------------------------------
@@ -133,6 +142,15 @@ __device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_fla
       return false;
     }
   }
+}
+
+// Bounded wait on the abort path: returns once the phase completed or after kWaitCycles,
+// whatever the abort flag says (used to let copies and MMAs already in flight land
+// before the CTA exits).
+__device__ void mbar_drain(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > kWaitCycles) return;
 }
 
 // 2-D tensor load with an L2 eviction-priority policy.
@@ -386,7 +404,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t bar_a2 = bar_a + 8;                         // [1] A rows written (draft: epilogue)
   uint32_t bar_ufull = bar_a2 + 8;                     // [kMaxUBoxes]
   uint32_t bar_uempty = bar_ufull + 8 * kMaxUBoxes;    // [kMaxUBoxes]
-  constexpr int kBarBytes = 8 * (2 * kStages + 6 + 2 * kMaxUBoxes);
+  uint32_t bar_mma_drain = bar_uempty + 8 * kMaxUBoxes;  // [1] abort path: issued MMAs done
+  constexpr int kBarBytes = 8 * (2 * kStages + 7 + 2 * kMaxUBoxes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::bars + kBarBytes);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM::bars + kBarBytes + 8);
   // U boxes of a tile: 128/ubox_cols of them, each read by the 16/(128/ubox_cols) warps
@@ -410,6 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar_a, 1);
     mbar_init(bar_a2, 1);
+    mbar_init(bar_mma_drain, 1);
     for (int s = 0; s < kMaxUBoxes; ++s) {
       mbar_init(bar_ufull + 8 * s, 1);
       mbar_init(bar_uempty + 8 * s, warps_per_ubox);
@@ -447,27 +467,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       const int total = my_tiles * katoms;
       bool a_issued = false;
+      bool a_loaded = false;  // an A copy was issued (it must land before the CTA exits)
+      int issued = 0;
       int stage = 0;
       uint32_t phase = 0;
       if (MODE == kModeDraft) a_issued = true;  // draft: the epilogue writes A itself
       for (int it = 0; it < total && !*abort_flag; ++it) {
         if (it == kStages && !a_issued) {
           load_a();
-          a_issued = true;
+          a_issued = a_loaded = true;
         }
         const int t = it / katoms, ka = it % katoms;
         const int v0 = (group + t * ngroups) * kN;
         if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag, p.status, 100)) break;
+        if (*abort_flag) break;  // a role gave up while this stage was being released
         const uint32_t dst = sbase + SM::b + stage * kStageBytes;
         mbar_arrive_expect_tx(bar_full + 8 * stage, kStageBytes);
         tma_load_2d(dst, &map_b, bar_full + 8 * stage, v0, ka * kKAtom, w2_policy);
         tma_load_2d(dst + kStageBytes / 2, &map_b, bar_full + 8 * stage, v0 + 64, ka * kKAtom, w2_policy);
+        ++issued;
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1;
         }
       }
-      if (!a_issued) load_a();
+      if (!a_issued && !*abort_flag) {
+        load_a();
+        a_loaded = true;
+      }
+      if (*abort_flag) {
+        // abort path: the last kStages copies may still be in flight (earlier ones landed
+        // before their stage was refilled); let them land before the CTA exits
+        for (int i = max(0, issued - kStages); i < issued; ++i)
+          mbar_drain(bar_full + 8 * (i % kStages), (uint32_t)(i / kStages) & 1u);
+        if (a_loaded) mbar_drain(bar_a, 0);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------ MMA issuer --------------------------------
@@ -509,6 +543,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         mma_commit(bar_acc_full + 8 * buf);
       }
+      if (*abort_flag) {
+        // abort path: every MMA this thread issued completes before TMEM is released
+        mma_commit(bar_mma_drain);
+        mbar_drain(bar_mma_drain, 0);
+      }
     }
   } else if (warp == 2) {
     // ------------------------------ U producer (draft mode) -------------------
@@ -516,17 +555,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ring of n_uboxes slots, read once (evict-first in L2).
     if (kDraftMath && lane == 0) {
       const uint64_t u_policy = policy_evict_first();
-      const int total = my_tiles * uboxes_per_tile;
+      int total = my_tiles * uboxes_per_tile;
+#ifdef DSPARK_TEST_WAIT_LIMIT
+      if (p.round == kTestStallRound) total = 0;
+#endif
+      int issued = 0;
       for (int i = 0; i < total && !*abort_flag; ++i) {
         const int slot = i % n_uboxes;
         const uint32_t ph = (uint32_t)(i / n_uboxes) & 1u;
         if (!mbar_wait(bar_uempty + 8 * slot, ph ^ 1, abort_flag, p.status, 400)) break;
+        // an epilogue warp whose wait gave up still releases its slot, possibly with the
+        // slot's last copy in flight: never refill after an abort
+        if (*abort_flag) break;
         const int t = i / uboxes_per_tile, bx = i % uboxes_per_tile;
         const int v0 = (group + t * ngroups) * kN + bx * p.ubox_cols;
         mbar_arrive_expect_tx(bar_ufull + 8 * slot, (uint32_t)ubox_bytes);
         tma_load_3d(sbase + SM::u + slot * ubox_bytes, &map_u, bar_ufull + 8 * slot, v0, p.k - 1, rb * RB,
                     u_policy);
+        ++issued;
       }
+      if (*abort_flag)  // abort path: the last ring's worth of boxes may still be in flight
+        for (int i = max(0, issued - n_uboxes); i < issued; ++i)
+          mbar_drain(bar_ufull + 8 * (i % n_uboxes), (uint32_t)(i / n_uboxes) & 1u);
     }
   } else {
     // ------------------------------ epilogue ----------------------------------

@@ -16,6 +16,7 @@ namespace {
 thread_local char g_msg[512] = "";
 thread_local void* const* g_prof_events = nullptr;
 thread_local int g_prof_n = 0;
+thread_local void* const* g_vprof_events = nullptr;
 
 dspark_status fail(dspark_status code, const char* fmt, ...) {
   va_list ap;
@@ -203,17 +204,26 @@ const char* dspark_last_error_message(void) { return g_msg; }
 
 // A profiling event recorded while the stream is being captured must become an event
 // record node of the graph (not only a capture-ordering marker), so that replays time it.
-static cudaError_t record_profile_event(void* ev, cudaStream_t s) {
+extern "C++" {
+namespace dspark {
+cudaError_t record_profile_event(void* ev, cudaStream_t s) {
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   cudaError_t e = cudaStreamIsCapturing(s, &cs);
   if (e != cudaSuccess) return e;
   return cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags((cudaEvent_t)ev, s, cudaEventRecordExternal)
                                              : cudaEventRecord((cudaEvent_t)ev, s);
 }
+}  // namespace dspark
+}
+using dspark::record_profile_event;
 
 void dspark_set_profile_events(void* const* events, int n_events) {
   g_prof_events = (events != nullptr && n_events > 0) ? events : nullptr;
   g_prof_n = g_prof_events ? n_events : 0;
+}
+
+void dspark_set_verify_profile_events(void* const* events, int n_events) {
+  g_vprof_events = (events != nullptr && n_events >= 4) ? events : nullptr;
 }
 
 dspark_status dspark_workspace_status(void* workspace, int reset, int* status, void* stream) {
@@ -492,6 +502,7 @@ static dspark_status verify_impl(int R, int gamma, int V, int rank, int dtype_t,
   a.W1g = ws + L.W1g;
   a.res_part = reinterpret_cast<dspark::Partial*>(ws + L.res_part);
   a.res_part2 = reinterpret_cast<dspark::Partial*>(ws + L.res_part2);
+  a.prof = g_vprof_events;
   if (overlap_out != nullptr) {
     a.ovl_lse = reinterpret_cast<float*>(ws + LO.lse);
     a.ovl_W1g = ws + LO.W1g;

@@ -97,6 +97,9 @@ struct VerifyArgs {
   void* ovl_W1g;      // W1[x_{j-1}] for position j <= ell[r]
   int ovl_compact;    // 1: both in the compact row order (row row_base[r] + j - 1, tensor-core
                       // pass); 0: at the flattened position r*gamma + j - 1 (NaN / zero beyond ell)
+  // measurement hook (nullptr: off): cudaEvent_t handles recorded around the row-statistics
+  // pass ([0] before, [1] after) and the correction pass ([2] before, [3] after)
+  void* const* prof;
 };
 
 // Acceptance-overlap diagnostic: c*[r, j-1] = sum_v min(q_j(v), p_j(v)) for the drafted
@@ -176,6 +179,9 @@ __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size
 
 // Sets the thread's dspark_last_error_message() and returns `code`.
 int record_error(int code, const char* msg);
+
+// Records a caller's timing event on `s` (an external event node while `s` is captured).
+cudaError_t record_profile_event(void* ev, cudaStream_t s);
 
 int simt_num_chunks(int V);
 int tc_supported(int V, int rank, int dtype_w);

@@ -499,12 +499,15 @@ cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s) {
   const int max_items = a.R * (a.gamma + 1) * a.nchunk;
   const int grid = min(max_items, sms * 3);  // work queue: CTAs take items until none is left
   if (a.chunk != kRowThreads * kRowPer) return cudaErrorInvalidValue;
+  if (a.prof != nullptr && (e = record_profile_event(a.prof[0], s)) != cudaSuccess) return e;
   e = a.dtype_t == DSPARK_F32 ? launch_pdl(verify_rows_kernel<DSPARK_F32>, dim3(grid), dim3(kRowThreads), 0, s, a)
                               : launch_pdl(verify_rows_kernel<DSPARK_BF16>, dim3(grid), dim3(kRowThreads), 0, s, a);
   if (e != cudaSuccess) return e;
+  if (a.prof != nullptr && (e = record_profile_event(a.prof[1], s)) != cudaSuccess) return e;
   const int wblocks = (a.R * 32 + 255) / 256;
   if ((e = launch_pdl(verify_accept_kernel, dim3(wblocks), dim3(256), 0, s, a)) != cudaSuccess) return e;
   int npart;
+  if (a.prof != nullptr && (e = record_profile_event(a.prof[2], s)) != cudaSuccess) return e;
   if (tc_supported(a.V, a.rank, a.dtype_w)) {
     // the residual recomputes one bias row per rejected request on the tensor cores
     if ((e = launch_residual_tc(a, s)) != cudaSuccess) return e;
@@ -521,6 +524,7 @@ cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s) {
       return e;
     npart = (int)rgrid.x;
   }
+  if (a.prof != nullptr && (e = record_profile_event(a.prof[3], s)) != cudaSuccess) return e;
   return launch_pdl(residual_combine_kernel, dim3(wblocks), dim3(256), 0, s, a, npart);
 }
 

@@ -1,8 +1,9 @@
 """dspark_verify_static: verification for callers that cannot allocate device memory
 (a host framework whose memory pool must not be bypassed, or a serving loop that may
-not allocate after start-up).  It must give exactly the results of dspark_verify, on
-repeated calls that reuse the library's one static scratch array, and must reject a
-shape whose scratch would not fit.
+not allocate after start-up).  It must give exactly the results of dspark_verify, and
+those of the fp64 oracle, on repeated calls that reuse the library's one static scratch
+array; it must report bad device data through dspark_verify_static_status(); and it
+must reject a shape whose scratch would not fit.
 
 This file is named to be collected last: if it fails, a run that stops at the first
 failure has already run every other test."""
@@ -12,6 +13,7 @@ import torch
 
 import oracle
 from speculative_decoding_draft_03_gb300 import workloads as wl
+from tests.parity import Tally, compare_verify
 
 pytestmark = pytest.mark.gpu
 
@@ -25,23 +27,52 @@ def _case(name, **over):
                             wn["seed"], 0)
     rng = np.random.default_rng(1)
     ell = rng.integers(0, wn["gamma"] + 1, wn["R"]).astype(np.int32)
+    logq, lse = d["logq"].astype(np.float32), d["lse"].astype(np.float32)
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
-    inputs = (wg["target"], wg["U"], wg["W1"], wg["W2"], wg["x0"], t(d["x"]), t(d["logq"].astype(np.float32)),
-              t(d["lse"].astype(np.float32)), t(ell), wg["temperature"], wg["req_id"], wg["seed"])
-    return inputs
+    inputs = (wg["target"], wg["U"], wg["W1"], wg["W2"], wg["x0"], t(d["x"]), t(logq), t(lse), t(ell),
+              wg["temperature"], wg["req_id"], wg["seed"])
+    host = (wn["target"], wn["U"], wn["W1"], wn["W2"], wn["x0"], d["x"], logq, lse, ell, wn["temperature"],
+            wn["req_id"], wn["seed"])
+    return inputs, host
 
 
 @pytest.mark.parametrize("name,over", [("tiny", {}), ("qwen3-8b", dict(V=20000, d=256)),
                                        ("stress", dict(V=2056, d=64))])
 def test_static_scratch_matches_workspace_entry_point(name, over):
     from speculative_decoding_draft_03_gb300 import binding as b
-    inputs = _case(name, **over)
+    inputs, host = _case(name, **over)
+    tally = Tally()
     for rnd in (3, 4):  # two calls in a row: the second reuses the first call's scratch
         ref = b.verify(*inputs, rnd)
         got = b.verify_static(*inputs, rnd)
         torch.cuda.synchronize()
+        assert b.verify_static_status() == 0
         for k in ("n_acc", "tokens", "n_out"):
             assert torch.equal(ref[k], got[k]), (name, rnd, k)
+        # the same call checked against the fp64 oracle on the same inputs
+        ref_o = oracle.verify(*host, rnd)
+        compare_verify({k: v.cpu().numpy() for k, v in got.items()}, ref_o, tally)
+    tally.check_rate()
+
+
+def test_static_scratch_reports_bad_device_data():
+    """A verify length outside [0, gamma] on the device is clamped and reported in the
+    static scratch's status word; the next call clears the word."""
+    from speculative_decoding_draft_03_gb300 import binding as b
+    inputs, _ = _case("tiny")
+    bad = list(inputs)
+    ell = inputs[8].clone()
+    ell[1] = 99
+    bad[8] = ell
+    b.verify_static(*bad, 5)
+    torch.cuda.synchronize()
+    assert b.verify_static_status() == 1
+    assert b.verify_static_status(reset=True) == 1
+    assert b.verify_static_status() == 0
+    b.verify_static(*bad, 5)
+    b.verify_static(*inputs, 5)  # clears the word before its own kernels run
+    torch.cuda.synchronize()
+    assert b.verify_static_status() == 0
 
 
 def test_static_scratch_rejects_oversized_shapes():
