@@ -196,6 +196,8 @@ __global__ void __launch_bounds__(kSimtThreads) draft_step_simt_kernel(DraftArgs
     for (int rr = 0; rr < RB; ++rr)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[rr][e] = 0.f;
+    // unrolled so that several rank rows' W2 loads are in flight before their products
+#pragma unroll 8
     for (int i = 0; i < a.rank; ++i) {
       float w2[4];
 #pragma unroll
@@ -231,7 +233,7 @@ __global__ void __launch_bounds__(kSimtThreads) draft_step_simt_kernel(DraftArgs
         }
         // Gumbel-max: skip the draw when even the largest Gumbel cannot win
         if (z + kGumbelMax >= st[rr].key || st[rr].idx < 0) {
-          const float key = z + gumbel_from_bits(wd[e]);
+          const float key = z + gumbel_fast_from_bits(wd[e]);
           if (key > st[rr].key || st[rr].idx < 0) {
             st[rr].key = key;
             st[rr].idx = v;

@@ -223,6 +223,15 @@ __device__ __forceinline__ float ex2_approx(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// Packed fused multiply-add of two fp32 pairs (sm_100 f32x2), rounded as fmaf:
+// (a, b) <- (fmaf(x0, y0, a), fmaf(x1, y1, b))
+__device__ __forceinline__ void fma2(float& a, float& b, float x0, float x1, float y0, float y1) {
+  asm("{\n\t.reg .b64 x, y, c;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
+      "mov.b64 c, {%0, %1};\n\tfma.rn.f32x2 c, x, y, c;\n\tmov.b64 {%0, %1}, c;\n\t}"
+      : "+f"(a), "+f"(b)
+      : "f"(x0), "f"(x1), "f"(y0), "f"(y1));
+}
+
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 
@@ -307,6 +316,10 @@ struct TcParams {
   const float* conf_temp;              // [gamma]
   float* conf_out;                     // [R, gamma]
   float conf_b, conf_scale;
+  // residual mode: row q is compact slot q, request res_req[q] (*res_nrows slots, known on
+  // the device only, so request blocks and vocabulary groups are derived from it)
+  const int* res_req;
+  const int* res_nrows;
   // overlap mode: rows are the flattened [R*gamma] positions (R above counts rows);
   // row i is request i / gamma at position i % gamma + 1, evaluated when that position
   // is at most ell[request] (every position without ell)
@@ -360,6 +373,151 @@ __device__ __forceinline__ void decode_run8(int dtype, const uint4 (&raw)[2], fl
   }
 }
 
+// The 8 ids' random words of one run: Philox blocks (v0 / 4) and (v0 / 4 + 1).
+__device__ __forceinline__ void philox_run(const PhiloxRow& prow, int v0, uint32_t (&wd)[kCols]) {
+#pragma unroll
+  for (int g4 = 0; g4 < 2; ++g4) {
+    const Philox4 bits = prow.block((uint32_t)((v0 >> 2) + g4));
+    wd[4 * g4 + 0] = bits.x;
+    wd[4 * g4 + 1] = bits.y;
+    wd[4 * g4 + 2] = bits.z;
+    wd[4 * g4 + 3] = bits.w;
+  }
+}
+
+// Draft modes, one tile of one request row: the thread's KP runs of 8 ids (vocabulary ids
+// v0 + 8 ps + i; U in ucur, the bias in TMEM at taddr + 8 ps).  All logits of the tile
+// come first, so the online softmax is rescaled once per tile; then the Gumbel-max race
+// runs run by run against the best key known so far (own record or published bound).
+// (Generating the next run's Philox words while the current run is tested measured
+// slower: the extra live registers at 128-row blocks cost more than the overlap gained.)  An id is
+// rejected without logarithms when 1 - u >= exp(z - best) = term * exp(m - best) (the
+// conversion-free form v = term * scale + f > edge marks the ids that may beat it; the
+// run is done when even the largest v is not); survivors evaluate their key.  Without any
+// known key, the run's largest logit is keyed first so that the others are tested
+// against it.  Runs at or beyond V, and rows beyond R, contribute nothing.
+template <int KP>
+__device__ __forceinline__ void draft_tile(const TcParams& p, Stats& st, const PhiloxRow& prow,
+                                           const uint4 (&ucur)[KP][2], uint32_t taddr, bool acc_ready, bool valid,
+                                           int v0, float zscale, float bound, uint32_t bar_acc_empty, int lane) {
+  float y[KP][kCols];
+  float tmax = -INFINITY;
+#pragma unroll
+  for (int ps = 0; ps < KP; ++ps) {
+    if (acc_ready) {
+      float bias[kCols];
+      tmem_ld8(taddr + ps * kCols, bias);
+      if (ps == KP - 1) {
+        // all of this warp's columns are in registers: hand the accumulator back
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_acc_empty);
+      }
+      decode_run8(p.dtype_u, ucur[ps], y[ps]);
+      // y = (u + bias) * zscale, two ids per packed instruction (rounded as the scalar ops)
+#pragma unroll
+      for (int i = 0; i < kCols; i += 2) {
+        add2f(y[ps][i], y[ps][i + 1], bias[i], bias[i + 1]);
+        mul2f(y[ps][i], y[ps][i + 1], zscale, zscale);
+      }
+    }
+    if (!(acc_ready && valid && v0 + ps * kCols < p.V)) {
+#pragma unroll
+      for (int i = 0; i < kCols; ++i) y[ps][i] = -INFINITY;
+    }
+    tmax = max3f_(tmax, max3f_(max3f_(y[ps][0], y[ps][1], y[ps][2]), max3f_(y[ps][3], y[ps][4], y[ps][5]), y[ps][6]),
+                 y[ps][7]);
+  }
+  if (!(tmax > -INFINITY)) return;  // nothing of this row in the tile
+  // online softmax statistics, one rescale per tile; term_i = 2^(y_i - m) = e^(z_i - m ln 2)
+  const float mnew = fmaxf(st.m, tmax);
+  float acc = (st.m == -INFINITY) ? 0.f : st.s * ex2_approx(st.m - mnew);
+  st.m = mnew;
+  float thr = fmaxf(st.idx >= 0 ? st.key : -INFINITY, bound);
+  // no id of the tile can reach the best key even with the largest possible Gumbel: no
+  // random words are needed
+  const bool race = !(thr > -INFINITY && fmaf(tmax, kLn2f, kGumbelMax) < thr);
+#pragma unroll
+  for (int ps = 0; ps < KP; ++ps) {
+    const int vb = v0 + ps * kCols;
+    float term[kCols];
+#pragma unroll
+    for (int i = 0; i < kCols; i += 2) {
+      term[i] = y[ps][i];
+      term[i + 1] = y[ps][i + 1];
+      sub2f(term[i], term[i + 1], mnew, mnew);
+    }
+#pragma unroll
+    for (int i = 0; i < kCols; ++i) term[i] = ex2_approx(term[i]);
+    {
+      // pairwise sum of the 8 terms
+      float a0 = term[0], a1 = term[1], a4 = term[4], a5 = term[5];
+      add2f(a0, a1, term[2], term[3]);
+      add2f(a4, a5, term[6], term[7]);
+      add2f(a0, a1, a4, a5);
+      acc += a0 + a1;
+    }
+    // the run's largest logit (recomputed: cheaper than keeping every run's in registers)
+    const float cmax =
+        fmaxf(max3f_(max3f_(y[ps][0], y[ps][1], y[ps][2]), max3f_(y[ps][3], y[ps][4], y[ps][5]), y[ps][6]), y[ps][7]);
+    if (race && cmax > -INFINITY && !(thr > -INFINITY && fmaf(cmax, kLn2f, kGumbelMax) < thr)) {
+      uint32_t wd[kCols];
+      philox_run(prow, vb, wd);
+      if (thr == -INFINITY) {
+        int imax = kCols - 1;
+#pragma unroll
+        for (int i = kCols - 2; i >= 0; --i)
+          if (y[ps][i] == cmax) imax = i;
+        uint32_t wm = wd[0];
+#pragma unroll
+        for (int i = 1; i < kCols; ++i)
+          if (i == imax) wm = wd[i];
+        const float cn = cmax * kLn2f;
+        st.key = cn + gumbel_fast_from_bits(wm);
+        st.idx = vb + imax;
+        st.zsel = cn;
+        thr = st.key;
+      }
+      // the scale e^(m ln 2 - best) is 2^(m - best log2 e)
+      const float scale = ex2_approx(fmaf(-thr, kLog2ef, mnew)) * kRejectSlack;
+      float v[kCols];
+#pragma unroll
+      for (int i = 0; i < kCols; ++i) v[i] = uniform_mantissa(wd[i]);
+#pragma unroll
+      for (int i = 0; i < kCols; i += 2) fma2(v[i], v[i + 1], term[i], term[i + 1], scale, scale);
+      const float vmax = fmaxf(max3f_(max3f_(v[0], v[1], v[2]), max3f_(v[3], v[4], v[5]), v[6]), v[7]);
+      if (vmax > kRejectEdge) {
+        uint32_t cand = 0;
+#pragma unroll
+        for (int i = 0; i < kCols; ++i)
+          if (v[i] > kRejectEdge) cand |= 1u << i;
+        while (cand) {
+          const int i = __ffs(cand) - 1;
+          cand &= cand - 1;
+          float zi = 0.f;
+          uint32_t wi = 0u;
+#pragma unroll
+          for (int j = 0; j < kCols; ++j)  // static register selection (no local memory)
+            if (j == i) {
+              zi = y[ps][j];
+              wi = wd[j];
+            }
+          if (vb + i == st.idx) continue;  // already keyed above
+          zi *= kLn2f;
+          const float key = zi + gumbel_fast_from_bits(wi);
+          if (key > st.key || (key == st.key && vb + i < st.idx)) {
+            st.key = key;
+            st.idx = vb + i;
+            st.zsel = zi;
+            thr = fmaxf(thr, key);
+          }
+        }
+      }
+    }
+  }
+  st.s = acc;
+}
+
 // RB: requests per block (32, 64 or 128); the 128 MMA rows hold 128/RB copies of it.
 // MODE: kModeDraft (one draft position for every request; the factor rows W1[x_{k-1}]
 // are gathered by the epilogue), kModeRnn (one draft position with the factor rows
@@ -380,6 +538,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   // draft positions: U through the TMA ring, online softmax + Gumbel-max, winners published
   constexpr bool kDraftMath = MODE == kModeDraft || MODE == kModeRnn;
   int rblocks = p.rblocks, ngroups = p.ngroups;
+  if constexpr (MODE == kModeResidual) {
+    // the rejected requests' compact slots: their number comes from the preceding verify
+    // pass; CTAs beyond the blocks in use leave before touching any barrier or tensor memory
+    griddep_wait();
+    const int n = *reinterpret_cast<const volatile int*>(p.res_nrows);
+    rblocks = (max(n, 0) + RB - 1) / RB;
+    if (rblocks == 0 || rblocks > p.rblocks) return;
+    ngroups = max(1, (int)gridDim.x / rblocks);
+    if ((int)blockIdx.x >= rblocks * ngroups) return;
+  }
   if constexpr (MODE == kModeOverlap) {
     if (p.ovl_nrows != nullptr) {
       // compact rows: their number comes from the preceding verify pass; CTAs beyond the
@@ -592,23 +760,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // the residual's positions and normalisers come from the preceding kernel
     if constexpr (MODE != kModeDraft) griddep_wait();
-    // draft: position k of every request; residual: the rejected position j* (0 = none);
-    // overlap: row r is position r % gamma + 1 of request r / gamma
+    // draft: position k of every request; residual: row r is compact slot r, request
+    // res_req[r] at its rejected position j*; overlap: row r is position r % gamma + 1 of
+    // request r / gamma
     int pos = p.k;
     int req = r;
     float lse_q = 0.f, lse_t = 0.f;
-    // residual mode: a negative position marks a bonus draw (every verified draft
-    // survived): Gumbel-max of ln p alone, no draft law, and no U row (the position can
-    // lie one past the block)
-    bool bonus_row = false;
     if constexpr (MODE == kModeResidual) {
-      const int raw = valid ? p.jstar[r] : 0;
-      bonus_row = raw < 0;
-      pos = raw < 0 ? -raw : raw;
-      valid = valid && pos > 0;
+      valid = valid && r < *reinterpret_cast<const volatile int*>(p.res_nrows);
+      req = valid ? p.res_req[r] : 0;
+      pos = valid ? p.jstar[req] : 0;
+      valid = valid && pos > 0 && pos <= p.gamma;
       if (valid) {
-        lse_q = bonus_row ? 0.f : __ldg(p.lse_q + (size_t)r * p.gamma + (pos - 1));
-        lse_t = p.lse_t[r];
+        lse_q = __ldg(p.lse_q + (size_t)req * p.gamma + (pos - 1));
+        lse_t = p.lse_t[req];
       }
     }
     int ovl_flat = r;  // overlap: the position's flattened index (its U row and lse_q)
@@ -640,12 +805,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     Stats fb = stats_empty();  // residual only: ln p + g (the rounding fallback)
     float ovl = 0.f;           // overlap only: this thread's sum of min(q, p)
     const PhiloxRow prow =
-        philox_row(rng_row(p.seed, (MODE != kModeOverlap && valid) ? __ldg(p.req_id + r) : 0, p.round,
+        philox_row(rng_row(p.seed, (MODE != kModeOverlap && valid) ? __ldg(p.req_id + req) : 0, p.round,
                            kDraftMath ? kStreamDraft : kStreamCorrect, (uint32_t)pos));
-    const bool u_valid = valid && !bonus_row;
+    const bool u_valid = valid;
     const size_t urow = MODE == kModeOverlap
                             ? (size_t)(valid ? ovl_flat : 0) * (size_t)p.V
-                            : ((size_t)(u_valid ? r : 0) * p.gamma + (u_valid ? pos - 1 : 0)) * (size_t)p.V;
+                            : ((size_t)(u_valid ? req : 0) * p.gamma + (u_valid ? pos - 1 : 0)) * (size_t)p.V;
     const size_t trow =
         (valid ? target_row_index(p.t_off, p.n_trows, p.gamma, req, pos - 1, p.status) : 0) * (size_t)p.V;
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
@@ -670,11 +835,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ps = 0; ps < kPass; ++ps)
         load_run8(p.U, p.dtype_u, urow, vt + col0 + ps * kCols, p.V, u_valid && t < my_tiles, dst[ps]);
     };
+    // Residual mode with 64- and 128-request blocks: the U and target runs of this thread
+    // (run k = pass k % kPass of tile k / kPass) stream through a two-run register ring,
+    // each loaded two runs ahead of its use
+    constexpr bool kRing = MODE == kModeResidual && kPass % 2 == 0;
+    uint4 ring_u[2][2], ring_t[2][2];
+    auto load_run = [&](int k, uint4 (&du)[2], uint4 (&dt)[2]) {
+      const int tk = k / kPass, pk = k % kPass;
+      const int vk = (group + tk * ngroups) * kN + col0 + pk * kCols;
+      const bool ok = valid && tk < my_tiles;
+      load_run8(p.U, p.dtype_u, urow, vk, p.V, ok, du);
+      load_run8(p.target, p.dtype_t, trow, vk, p.V, ok, dt);
+    };
     const int my_box = col0 / p.ubox_cols;
     const int box_col = col0 % p.ubox_cols;
     const int box_row = row0 + lane;
     const bool u_f32 = p.dtype_u == DSPARK_F32;
-    if constexpr (!kDraftMath) load_u(0, unext);
+    if constexpr (kRing) {
+      load_run(0, ring_u[0], ring_t[0]);
+      load_run(1, ring_u[1], ring_t[1]);
+    } else if constexpr (!kDraftMath) {
+      load_u(0, unext);
+    }
     if constexpr (kTPref) load_t(0, tnext);
     // the predecessor still reads the partial records this kernel overwrites at the end
     if constexpr (MODE == kModeDraft) {
@@ -746,7 +928,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint4 tcur[kPass][2];
       int uslot = 0;
       bool u_ready = true;
-      if constexpr (!kDraftMath) {
+      if constexpr (kRing) {
+        // runs come from the ring, pass by pass
+      } else if constexpr (!kDraftMath) {
 #pragma unroll
         for (int ps = 0; ps < kPass; ++ps) {
           ucur[ps][0] = unext[ps][0];
@@ -790,9 +974,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every epilogue warp still meets the same named barriers.
       const bool acc_ready = mbar_wait(bar_acc_full + 8 * buf, use, abort_flag, p.status, 300) && u_ready;
       if (acc_ready) tc_fence_after();
+      if constexpr (kDraftMath) draft_tile(p, st, prow, ucur, tmem_base + lane_addr + buf * kN + col0, acc_ready, valid,
+                                           vt + col0, zscale, bound, bar_acc_empty + 8 * buf, lane);
 #pragma unroll
       for (int ps = 0; ps < kPass; ++ps) {
-        if (!acc_ready) break;
+        if (kDraftMath || !acc_ready) break;
         const int c = col0 + ps * kCols;
         float bias[kCols];
         tmem_ld8(tmem_base + lane_addr + buf * kN + c, bias);
@@ -803,87 +989,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(bar_acc_empty + 8 * buf);
         }
         const int vb = vt + c;
-        if (!valid || vb >= p.V) continue;
         float z[kCols];
-        decode_run8(p.dtype_u, ucur[ps], z);
+        float tl[kCols];  // ring: this run's target logits, decoded before the slot is refilled
+        if constexpr (kRing) {
+          decode_run8(p.dtype_u, ring_u[ps & 1], z);
+          decode_run8(p.dtype_t, ring_t[ps & 1], tl);
+          load_run(t * kPass + ps + 2, ring_u[ps & 1], ring_t[ps & 1]);
+        } else {
+          decode_run8(p.dtype_u, ucur[ps], z);
+        }
+        if (!valid || vb >= p.V) continue;
 #pragma unroll
         for (int i = 0; i < kCols; ++i) z[i] = (z[i] + bias[i]) * zscale;
-        if constexpr (kDraftMath) {
-          // the run's largest (base-2) logit (its position is only needed to key it, below)
-          const float cmax = fmaxf(fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3])), fmaxf(fmaxf(z[4], z[5]), fmaxf(z[6], z[7])));
-          // online softmax statistics over the 8 ids; term_i = 2^(y_i - m) = e^(z_i - m ln 2)
-          const float mnew = fmaxf(st.m, cmax);
-          float acc = (st.m == -INFINITY) ? 0.f : st.s * ex2_approx(st.m - mnew);
-          float term[kCols];
-#pragma unroll
-          for (int i = 0; i < kCols; ++i) {
-            term[i] = ex2_approx(z[i] - mnew);
-            acc += term[i];
-          }
-          st.m = mnew;
-          st.s = acc;
-          // Gumbel-max draw against the best key known so far (own record or published).
-          // A run whose largest logit cannot reach it even with the largest possible
-          // Gumbel needs no random bits.  Otherwise the 8 ids' words come from two
-          // independent Philox blocks; an element is rejected without logarithms when
-          // 1-u >= exp(z - best) = term * exp(m - best), and only survivors evaluate
-          // their key.  Without any known key, the run's largest logit is keyed first so
-          // that the others are tested against it.
-          float thr = fmaxf(st.idx >= 0 ? st.key : -INFINITY, bound);
-          if (thr > -INFINITY && fmaf(cmax, kLn2f, kGumbelMax) < thr) continue;
-          uint32_t wd[kCols];
-#pragma unroll
-          for (int g4 = 0; g4 < 2; ++g4) {
-            const Philox4 bits = prow.block((uint32_t)((vb >> 2) + g4));
-            wd[4 * g4 + 0] = bits.x;
-            wd[4 * g4 + 1] = bits.y;
-            wd[4 * g4 + 2] = bits.z;
-            wd[4 * g4 + 3] = bits.w;
-          }
-          if (thr == -INFINITY) {
-            int imax = kCols - 1;
-#pragma unroll
-            for (int i = kCols - 2; i >= 0; --i)
-              if (z[i] == cmax) imax = i;
-            uint32_t wm = wd[0];
-#pragma unroll
-            for (int i = 1; i < kCols; ++i)
-              if (i == imax) wm = wd[i];
-            const float cn = cmax * kLn2f;
-            const float key = cn + gumbel_from_bits(wm);
-            st.key = key;
-            st.idx = vb + imax;
-            st.zsel = cn;
-            thr = key;
-          }
-          // the test 1 - u >= term * scale in its conversion-free form (uniform_mantissa);
-          // the scale e^(m ln 2 - best) is 2^(m - best log2 e)
-          const float scale = ex2_approx(fmaf(-thr, kLog2ef, mnew)) * kRejectSlack;
-          uint32_t cand = 0;
-#pragma unroll
-          for (int i = 0; i < kCols; ++i)
-            if (!(fmaf(term[i], scale, uniform_mantissa(wd[i])) <= kRejectEdge)) cand |= 1u << i;
-          while (cand) {
-            const int i = __ffs(cand) - 1;
-            cand &= cand - 1;
-            float zi = 0.f;
-            uint32_t wi = 0u;
-#pragma unroll
-            for (int j = 0; j < kCols; ++j)  // static register selection (no local memory)
-              if (j == i) {
-                zi = z[j];
-                wi = wd[j];
-              }
-            if (vb + i == st.idx) continue;  // already keyed above
-            zi *= kLn2f;
-            const float key = zi + gumbel_from_bits(wi);
-            if (key > st.key || (key == st.key && vb + i < st.idx)) {
-              st.key = key;
-              st.idx = vb + i;
-              st.zsel = zi;
-            }
-          }
-        } else if constexpr (MODE == kModeOverlap) {
+        if constexpr (MODE == kModeOverlap) {
           // overlap: min(q, p) with q = exp(z - lse_q), p = exp(t/T - lse_t) (as powers of 2)
           uint4 traw[2];
           if constexpr (kTPref) {
@@ -901,15 +1019,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           // residual: q = exp(z - lse_q), p = exp(t/T - lse_t); draw from (p - q)+ by
           // Gumbel-max over ln(p - q) where positive, and keep the ln p draw as fallback
           // (lp holds log2 p; the fallback key is lp ln 2 + g)
-          uint4 traw[2];
-          if constexpr (kTPref) {
-            traw[0] = tcur[ps][0];
-            traw[1] = tcur[ps][1];
-          } else {
-            load_run8(p.target, p.dtype_t, trow, vb, p.V, true, traw);
-          }
           float lp[kCols];
-          decode_run8(p.dtype_t, traw, lp);
+          if constexpr (kRing) {
+#pragma unroll
+            for (int i = 0; i < kCols; ++i) lp[i] = tl[i];
+          } else {
+            uint4 traw[2];
+            if constexpr (kTPref) {
+              traw[0] = tcur[ps][0];
+              traw[1] = tcur[ps][1];
+            } else {
+              load_run8(p.target, p.dtype_t, trow, vb, p.V, true, traw);
+            }
+            decode_run8(p.dtype_t, traw, lp);
+          }
           float gmax = -INFINITY;
 #pragma unroll
           for (int i = 0; i < kCols; ++i) {
@@ -918,26 +1041,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const float gtop = fmaf(gmax, kLn2f, kGumbelMax);
           // ln(p - q) <= ln p: neither draw can improve once ln p + G_max is below both keys
-          // (a bonus row keeps only the ln p record)
-          if (fb.idx >= 0 && gtop < fb.key && (bonus_row || (st.idx >= 0 && gtop < st.key)))
-            continue;
+          if (fb.idx >= 0 && gtop < fb.key && st.idx >= 0 && gtop < st.key) continue;
+          // rejection scales: a key c + g beats best only if 1-u < e^{c - best}; the test
+          // 1 - u >= x scale in its conversion-free form (x = rho or p; without a record yet
+          // the scale is infinite and every id is keyed)
+          const float s1 = (st.idx >= 0) ? __expf(-st.key) * kRejectSlack : INFINITY;
+          const float s2 = (fb.idx >= 0) ? __expf(-fb.key) * kRejectSlack : INFINITY;
 #pragma unroll
           for (int g4 = 0; g4 < 2; ++g4) {
             const Philox4 bits = prow.block((uint32_t)((vb >> 2) + g4));
             const uint32_t wd[4] = {bits.x, bits.y, bits.z, bits.w};
-            // rejection scales: a key c + g beats best only if 1-u < e^{c - best}
-            const float s1 = (st.idx >= 0) ? __expf(-st.key) * kRejectSlack : INFINITY;
-            const float s2 = (fb.idx >= 0) ? __expf(-fb.key) * kRejectSlack : INFINITY;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int v = vb + 4 * g4 + e;
               const float pv = ex2_approx(lp[4 * g4 + e]);
               const float rho = pv - ex2_approx(z[4 * g4 + e] - lse_q2);
-              const float w = one_minus_uniform(wd[e]);
-              const bool try1 = !bonus_row && rho > 0.f && !(w >= rho * s1);
-              const bool try2 = !(w >= pv * s2);
+              const float f = uniform_mantissa(wd[e]);
+              const bool try1 = rho > 0.f && fmaf(rho, s1, f) > kRejectEdge;
+              const bool try2 = pv > 0.f && fmaf(pv, s2, f) > kRejectEdge;
               if (!try1 && !try2) continue;
-              const float g = gumbel_from_bits(wd[e]);
+              const float g = gumbel_fast_from_bits(wd[e]);
               if (try2) {
                 const float k2 = fmaf(lp[4 * g4 + e], kLn2f, g);
                 if (fb.idx < 0 || k2 > fb.key) {
@@ -1012,7 +1135,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (et >= r0 && et < r0 + 32) stats_merge(m, from_partial(red[w2 * 32 + (et - r0)]));
         }
         const int rr = rb * RB + et;
-        if (rr < p.R) (which ? p.partials2 : p.partials)[(size_t)group * p.R + rr] = to_partial(m);
+        if constexpr (MODE == kModeResidual) {
+          // [group, rblocks * RB] over the slots
+          if (rr < *reinterpret_cast<const volatile int*>(p.res_nrows))
+            (which ? p.partials2 : p.partials)[(size_t)group * rblocks * RB + rr] = to_partial(m);
+        } else if (rr < p.R) {
+          (which ? p.partials2 : p.partials)[(size_t)group * p.R + rr] = to_partial(m);
+        }
         // draft: this CTA's winner for the request, as one 64-bit maximum (key code in the
         // high half, sign-flipped so that the order is unsigned; ~id in the low half, so the
         // lowest id wins equal keys)
@@ -1386,6 +1515,9 @@ cudaError_t launch_residual_tc(const VerifyArgs& a, cudaStream_t s) {
   p.jstar = a.jstar;
   p.lse_q = a.lse_q;
   p.lse_t = a.lse_t;
+  p.res_req = a.rej_req;
+  p.res_nrows = a.n_rej;
+  p.grid = a.res_grid;
   return tc::launch<tc::kModeResidual>(p, a.W1g, a.W2, s);
 }
 

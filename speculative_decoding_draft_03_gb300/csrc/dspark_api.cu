@@ -79,9 +79,9 @@ RnnLayout rnn_layout(int R, int gamma, int V, int ns, int d, int dtype_w) {
 }
 
 struct VerifyLayout {
-  size_t counters, row_req, row_t, row_base, row_order, row_part, lse_t, jstar, W1g, res_part, res_part2,
+  size_t counters, row_req, row_t, row_base, row_order, row_part, lse_t, jstar, rej_req, W1g, res_part, res_part2,
       total;
-  int nchunk, npart;
+  int nchunk;
 };
 
 VerifyLayout verify_layout(int R, int gamma, int V, int rank, int dtype_w) {
@@ -89,7 +89,7 @@ VerifyLayout verify_layout(int R, int gamma, int V, int rank, int dtype_w) {
   VerifyLayout L;
   const size_t rows = (size_t)R * (gamma + 1);
   L.nchunk = (V + kVerifyChunk - 1) / kVerifyChunk;
-  L.npart = residual_num_partials(R, V, rank, dtype_w);
+  const size_t res_entries = residual_partial_entries(R, V, rank, dtype_w);
   size_t off = 256;
   L.counters = off;
   off += 256;
@@ -107,12 +107,14 @@ VerifyLayout verify_layout(int R, int gamma, int V, int rank, int dtype_w) {
   off += align256(4 * (size_t)R);
   L.jstar = off;
   off += align256(4 * (size_t)R);
+  L.rej_req = off;
+  off += align256(4 * (size_t)R);
   L.W1g = off;
   off += align256(elem_size(dtype_w) * (size_t)round_up_rows(R) * rank);
   L.res_part = off;
-  off += align256((size_t)32 * L.npart * R);
+  off += align256((size_t)32 * res_entries);
   L.res_part2 = off;
-  off += align256((size_t)32 * L.npart * R);
+  off += align256((size_t)32 * res_entries);
   L.total = off;
   return L;
 }
@@ -494,6 +496,10 @@ static dspark_status verify_impl(int R, int gamma, int V, int rank, int dtype_t,
   a.row_base = reinterpret_cast<int*>(ws + L.row_base);
   a.row_order = reinterpret_cast<int*>(ws + L.row_order);
   a.work_next = counters + 2;
+  a.n_rej = counters + 3;
+  a.rej_req = reinterpret_cast<int*>(ws + L.rej_req);
+  a.res_compact = dspark::tc_supported(V, rank, dtype_w);
+  a.res_grid = dspark::tc_grid_ctas(R);
   a.row_part = reinterpret_cast<dspark::Partial*>(ws + L.row_part);
   a.nchunk = L.nchunk;
   a.chunk = kVerifyChunk;

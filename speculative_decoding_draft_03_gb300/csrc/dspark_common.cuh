@@ -72,27 +72,31 @@ __device__ __forceinline__ Philox4 rng_chunk(const RngRow& r, uint32_t chunk) {
 }
 
 // The same generator specialised to one row: only the 4th counter word (the chunk)
-// varies, so the first round's products and half of the second round's are per-row
-// constants, and so are the round keys of rounds 3..10 (kept per row rather than
-// re-derived in every block).  philox_row(...).block(chunk) == rng_chunk(row, chunk) bit
-// for bit.
+// varies, so the first round's products, half of the second round's and half of the
+// third round's are per-row constants, and so are the round keys of rounds 4..10 (kept
+// per row rather than re-derived in every block).
+// philox_row(...).block(chunk) == rng_chunk(row, chunk) bit for bit.
 struct PhiloxRow {
-  uint32_t p;     // round 1 input word 2 without the chunk:  hi(M_A c0) ^ k1
-  uint32_t g;     // round 2 output word 0 partial:          lo(M_B c2) ^ (k0 + W_A)
-  uint32_t e, f;  // round 2 output words 2, 3 (constant)
-  uint32_t k0, k1;
-  uint32_t ka[8], kb[8];
+  uint32_t p;       // round 1 input word 2 without the chunk:  hi(M_A c0) ^ k1
+  uint32_t g;       // round 2 output word 0 partial:          lo(M_B c2) ^ (k0 + W_A)
+  uint32_t h3, l3;  // round 3: hi(M_B e) ^ (k0 + 2 W_A) and lo(M_B e), e = round 2 output word 2
+  uint32_t f3;      // round 3: f ^ (k1 + 2 W_B), f = round 2 output word 3
+  uint32_t ka[7], kb[7];  // round keys of rounds 4..10
 
   __device__ __forceinline__ Philox4 block(uint32_t chunk) const {
     const uint32_t x2 = p ^ chunk;
     const unsigned long long pb = 0xCD9E8D57ull * (unsigned long long)x2;
-    uint32_t c0 = (uint32_t)(pb >> 32) ^ g, c1 = (uint32_t)pb, c2 = e, c3 = f;
+    // round 2 output: (hi(pb) ^ g, lo(pb), e, f); round 3 on it, whose B product M_B e
+    // is a per-row constant
+    const uint32_t c0r2 = (uint32_t)(pb >> 32) ^ g;
+    const unsigned long long qa3 = 0xD2511F53ull * (unsigned long long)c0r2;
+    uint32_t c0 = (uint32_t)pb ^ h3, c1 = l3, c2 = (uint32_t)(qa3 >> 32) ^ f3, c3 = (uint32_t)qa3;
 #pragma unroll
-    for (int i = 2; i < 10; ++i) {
+    for (int i = 3; i < 10; ++i) {
       const unsigned long long qa = 0xD2511F53ull * (unsigned long long)c0;
       const unsigned long long qb = 0xCD9E8D57ull * (unsigned long long)c2;
-      const uint32_t n0 = (uint32_t)(qb >> 32) ^ c1 ^ ka[i - 2];
-      const uint32_t n2 = (uint32_t)(qa >> 32) ^ c3 ^ kb[i - 2];
+      const uint32_t n0 = (uint32_t)(qb >> 32) ^ c1 ^ ka[i - 3];
+      const uint32_t n2 = (uint32_t)(qa >> 32) ^ c3 ^ kb[i - 3];
       c0 = n0;
       c1 = (uint32_t)qb;
       c2 = n2;
@@ -112,17 +116,20 @@ __device__ __forceinline__ PhiloxRow philox_row(const RngRow& r) {
   // round 2 (key + W): its A-product uses y0 only, a per-row constant
   const uint32_t ka = r.k0 + 0x9E3779B9u, kb = r.k1 + 0xBB67AE85u;
   const unsigned long long qa = 0xD2511F53ull * (unsigned long long)y0;
+  const uint32_t e = (uint32_t)(qa >> 32) ^ y3 ^ kb;  // round 2 output word 2
+  const uint32_t f = (uint32_t)qa;                    // round 2 output word 3
+  // round 3 (key + 2W): its B-product uses e only
+  const unsigned long long qb3 = 0xCD9E8D57ull * (unsigned long long)e;
   PhiloxRow o;
   o.p = (uint32_t)(pa >> 32) ^ r.k1;
   o.g = y1 ^ ka;
-  o.e = (uint32_t)(qa >> 32) ^ y3 ^ kb;
-  o.f = (uint32_t)qa;
-  o.k0 = r.k0;
-  o.k1 = r.k1;
+  o.h3 = (uint32_t)(qb3 >> 32) ^ (r.k0 + 2u * 0x9E3779B9u);
+  o.l3 = (uint32_t)qb3;
+  o.f3 = f ^ (r.k1 + 2u * 0xBB67AE85u);
 #pragma unroll
-  for (int i = 2; i < 10; ++i) {
-    o.ka[i - 2] = r.k0 + (uint32_t)i * 0x9E3779B9u;
-    o.kb[i - 2] = r.k1 + (uint32_t)i * 0xBB67AE85u;
+  for (int i = 3; i < 10; ++i) {
+    o.ka[i - 3] = r.k0 + (uint32_t)i * 0x9E3779B9u;
+    o.kb[i - 3] = r.k1 + (uint32_t)i * 0xBB67AE85u;
   }
   return o;
 }
@@ -149,6 +156,88 @@ __device__ __forceinline__ float neg_log_uniform(uint32_t bits) {
 
 // Standard Gumbel g = -ln(-ln u) = -ln E.
 __device__ __forceinline__ float gumbel_from_bits(uint32_t bits) { return -logf(neg_log_uniform(bits)); }
+
+// Packed fp32 pairs (the f32x2 arithmetic of sm_100 and later): one instruction for two
+// independent adds / subtracts / multiplies, each rounded exactly like its scalar
+// counterpart; and the three-input maximum (a NaN operand is ignored, as by fmaxf).
+__device__ __forceinline__ void add2f(float& a, float& b, float c, float d) {
+  asm("{\n\t.reg .b64 x, y;\n\tmov.b64 x, {%0, %1};\n\tmov.b64 y, {%2, %3};\n\t"
+      "add.rn.f32x2 x, x, y;\n\tmov.b64 {%0, %1}, x;\n\t}"
+      : "+f"(a), "+f"(b)
+      : "f"(c), "f"(d));
+}
+__device__ __forceinline__ void sub2f(float& a, float& b, float c, float d) {
+  asm("{\n\t.reg .b64 x, y;\n\tmov.b64 x, {%0, %1};\n\tmov.b64 y, {%2, %3};\n\t"
+      "sub.rn.f32x2 x, x, y;\n\tmov.b64 {%0, %1}, x;\n\t}"
+      : "+f"(a), "+f"(b)
+      : "f"(c), "f"(d));
+}
+__device__ __forceinline__ void mul2f(float& a, float& b, float c, float d) {
+  asm("{\n\t.reg .b64 x, y;\n\tmov.b64 x, {%0, %1};\n\tmov.b64 y, {%2, %3};\n\t"
+      "mul.rn.f32x2 x, x, y;\n\tmov.b64 {%0, %1}, x;\n\t}"
+      : "+f"(a), "+f"(b)
+      : "f"(c), "f"(d));
+}
+__device__ __forceinline__ float max3f_(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+__device__ __forceinline__ float exp2f_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Standard Gumbel g = -ln(-ln u) from special-function approximations and a short series,
+// for the draws that survive the rejection test of a Gumbel-max race.  Its absolute error
+// stays far inside the 1e-5 boundary window (checked on the GPU against binary64 over every
+// 256th 24-bit uniform code and both tails):
+//   u < 1/2:  E = -ln u = -log2(u) ln 2, where |log2 u| >= 1 keeps the approximation's
+//             error relative;
+//   u >= 1/2: E = -ln(1 - w) = 2 atanh(s) with s = w / (2 - w) in (0, 1/3] (w = 1 - u, exact),
+//             the odd series of atanh through s^13 (truncation below 2e-8 relative), so E
+//             keeps full relative accuracy as u -> 1, where the winning draws live;
+//   g = -ln E with E = 2^e m, m in [1, 2): -(e ln 2 + log2(m) ln 2), e exact.
+__device__ __forceinline__ float gumbel_fast_from_bits(uint32_t bits) {
+  constexpr float kLn2 = 0.6931471805599453f;
+  const uint32_t b = bits >> 8;
+  float E;
+  if (b < (1u << 23)) {
+    const float u = __uint2float_rn(2u * b + 1u) * 0x1.0p-25f;
+    E = -lg2_approx(u) * kLn2;
+  } else {
+    const float w = __uint2float_rn((1u << 25) - 2u * b - 1u) * 0x1.0p-25f;
+    const float sv = w * rcp_approx(2.f - w);
+    const float t = sv * sv;
+    float q = fmaf(t, 1.f / 13.f, 1.f / 11.f);
+    q = fmaf(t, q, 1.f / 9.f);
+    q = fmaf(t, q, 1.f / 7.f);
+    q = fmaf(t, q, 1.f / 5.f);
+    q = fmaf(t, q, 1.f / 3.f);
+    q = fmaf(t, q, 1.f);
+    E = 2.f * sv * q;
+  }
+  // E is a positive normal number (at least 2^-25): split off its exponent exactly
+  const uint32_t eb = __float_as_uint(E);
+  const float m = __uint_as_float((eb & 0x007FFFFFu) | 0x3F800000u);
+  // the unbiased exponent as a float, without a conversion: 1.5 * 2^23 + e, minus 1.5 * 2^23
+  const float e = __int_as_float(0x4B400000 + (int)(eb >> 23) - 127) - 12582912.f;
+  return -fmaf(e, kLn2, lg2_approx(m) * kLn2);
+}
 
 // 1 - u in binary32 (exact for u >= 1/2, within one rounding below).  Since
 // E = -ln u = -ln(1 - w) >= w, an element with w >= t has E >= t.

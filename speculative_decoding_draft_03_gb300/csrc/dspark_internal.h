@@ -100,6 +100,13 @@ struct VerifyArgs {
   // measurement hook (nullptr: off): cudaEvent_t handles recorded around the row-statistics
   // pass ([0] before, [1] after) and the correction pass ([2] before, [3] after)
   void* const* prof;
+  // rejected requests in compact slots (tensor-core correction pass): verify_accept takes
+  // slot = atomicAdd(n_rej, 1) for each request that rejected a draft, writes its factor
+  // row at W1g row `slot` and rej_req[slot] = r; the correction pass runs over the slots
+  int* n_rej;         // [1]
+  int* rej_req;       // [R]
+  int res_compact;    // 1: compact slots (tensor cores); 0: W1g at the request index (CUDA cores)
+  int res_grid;       // CTAs of the compact correction pass (its partial count follows from *n_rej)
 };
 
 // Acceptance-overlap diagnostic: c*[r, j-1] = sum_v min(q_j(v), p_j(v)) for the drafted
@@ -187,6 +194,8 @@ int simt_num_chunks(int V);
 int tc_supported(int V, int rank, int dtype_w);
 int tc_num_partials(int R);
 int tc_block_rows(int R);  // rows per request block of a tensor-core launch over R rows
+// the same on the device: 32, 64 or 128 rows
+__host__ __device__ inline int tc_rows_per_block(int R) { return R <= 32 ? 32 : (R <= 64 ? 64 : 128); }
 int tc_grid_ctas(int R);   // CTAs of the compact overlap pass over at most R rows
 // the compact overlap pass is used only when its request blocks fit on the SMs (then it
 // launches one CTA per SM and its partials take SMs x R floats)
@@ -221,7 +230,7 @@ size_t schedule_smem_bytes(int R, int gamma);
 
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s);
 cudaError_t launch_residual_tc(const VerifyArgs& a, cudaStream_t s);
-int residual_num_partials(int R, int V, int rank, int dtype_w);
+size_t residual_partial_entries(int R, int V, int rank, int dtype_w);
 
 cudaError_t launch_overlap(const OverlapArgs& a, cudaStream_t s);
 // the bias pass and the combine only, on lse_t and W1g already in place

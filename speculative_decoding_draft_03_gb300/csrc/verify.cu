@@ -10,20 +10,20 @@
 // Kernels (one round, stream-ordered, no host synchronisation):
 //   verify_plan      ell -> compact list of the target rows that must be read:
 //                    rows 0..ell_r of request r (sum_r (ell_r + 1) rows)
-//   verify_rows      streams those rows once, coalesced and vectorised: per
-//                    (row, vocabulary chunk) item, taken from a work queue, the
-//                    (max, sum exp) of t/T
-//   verify_accept    per request: row log-normalisers, the acceptance scan, and the
-//                    position of the correction draw, n_acc + 1 (a residual draw after a
-//                    rejection, the bonus draw when every verified draft survived)
-//   residual_step    per request: the correction draw at n_acc + 1 from target row
-//                    n_acc.  After a rejection: recompute the draft logits of that
-//                    position (U + W1[x_{j*-1}] W2), q = exp(z - lse_q), p = exp(t/T -
-//                    lse_t), Gumbel-max of ln(p - q)+ (and of ln p, the rounding
-//                    fallback).  Bonus: the Gumbel-max of ln p alone, which has the
-//                    same winner as t/T + g.  Either way one pass over one target row
-//                    per request, so the bonus rows of requests that reject are never
-//                    sampled.
+//   verify_rows      streams those rows once, coalesced and vectorised, per (row,
+//                    vocabulary chunk) item taken from a work queue: for rows
+//                    0..ell_r - 1 the (max, sum exp) of t/T (their log-normalisers, which
+//                    the acceptance tests need); for row ell_r the bonus draw's
+//                    Gumbel-max of t/T + g (stream 2 at position ell_r + 1), which needs
+//                    no normaliser
+//   verify_accept    per request: row log-normalisers, the acceptance scan; every
+//                    verified draft accepted -> the bonus token (merged from row ell_r's
+//                    race); a rejection at j* = n_acc + 1 -> a compact slot for the
+//                    correction pass, with the factor row of position j*
+//   residual_step    per rejected request: recompute the draft logits of position j*
+//                    (U + W1[x_{j*-1}] W2), q = exp(z - lse_q), p = exp(t/T - lse_t) from
+//                    target row n_acc, Gumbel-max of ln(p - q)+ (and of ln p, the rounding
+//                    fallback), stream 2 at position j*
 //   residual_combine merges the correction partials into the emitted token.
 #include <climits>
 
@@ -80,8 +80,8 @@ __global__ void __launch_bounds__(kPlanThreads) verify_plan_kernel(VerifyArgs a)
       a.row_req[base + t] = r;
       a.row_t[base + t] = t;
     }
-    // processing order: row t = ell of every request first (the correction draw reads
-    // it again), then rows 0..ell-1
+    // processing order: row t = ell of every request first (the bonus draw's race, the
+    // longest items), then rows 0..ell-1
     a.row_order[r] = base + n - 1;
     for (int t = 0; t + 1 < n; ++t) a.row_order[a.R + (base - r) + t] = base + t;
     a.jstar[r] = 0;
@@ -90,6 +90,7 @@ __global__ void __launch_bounds__(kPlanThreads) verify_plan_kernel(VerifyArgs a)
   if (threadIdx.x == blockDim.x - 1) *a.n_rows = base;
   if (threadIdx.x == 0) {
     *a.work_next = 0;
+    *a.n_rej = 0;
   }
 }
 
@@ -109,6 +110,80 @@ __device__ __forceinline__ float block_max(float v, float* sm) {
   return r;
 }
 
+// The bonus draw's race over one chunk of target row t = ell of request r: the Gumbel-max
+// of t/T + g with g from stream 2 at position ell + 1 (the normaliser of that row is a
+// constant shift of every key, so it is not needed).  z holds the thread's kRowPer logits
+// (already divided by T; -inf past the row), thread ids v0 + (threadIdx.x + i kRowThreads)
+// EPV + e for vector i, element e; m is their maximum.  Each thread keys its largest logit
+// first; the warp's best such key (an actual element's key) bounds every lane's race, so
+// ids are rejected without logarithms when 1 - u >= exp(z - best) (the conversion-free
+// form of the draft step), and only survivors evaluate their key.  The chunk's winner is
+// written as a partial record (key, id) of the row.
+template <int EPV>
+__device__ __forceinline__ void bonus_race(const VerifyArgs& a, const float (&z)[kRowPer], float m, int r, int t,
+                                           int v0, int row, int c, Partial* sm_red) {
+  constexpr int NV = kRowPer / EPV;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const PhiloxRow prow = philox_row(rng_row(a.seed, __ldg(a.req_id + r), a.round, kStreamCorrect, (uint32_t)(t + 1)));
+  auto id_of = [&](int k) { return v0 + (threadIdx.x + (k / EPV) * kRowThreads) * EPV + (k % EPV); };
+  Stats own = stats_empty();
+  if (m > -INFINITY) {
+    int km = 0;
+#pragma unroll
+    for (int k = kRowPer - 1; k >= 0; --k)
+      if (z[k] == m) km = k;  // the lowest id among equal maxima
+    const int vm = id_of(km);
+    const Philox4 b = prow.block((uint32_t)(vm >> 2));
+    const uint32_t w = (vm & 3) == 0 ? b.x : ((vm & 3) == 1 ? b.y : ((vm & 3) == 2 ? b.z : b.w));
+    own.key = m + gumbel_fast_from_bits(w);
+    own.idx = vm;
+  }
+  float thr = own.key;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) thr = fmaxf(thr, __shfl_xor_sync(0xffffffffu, thr, o));
+  if (m > -INFINITY && thr > -INFINITY) {
+    constexpr float kLog2e = 1.4426950408889634f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+#pragma unroll
+      for (int g4 = 0; g4 < EPV / 4; ++g4) {
+        const int k0 = i * EPV + 4 * g4;
+        const float gm = fmaxf(fmaxf(z[k0], z[k0 + 1]), fmaxf(z[k0 + 2], z[k0 + 3]));
+        if (gm + kGumbelMax < thr) continue;  // no id of the group can reach the bound
+        const int vb = id_of(k0);
+        const Philox4 b = prow.block((uint32_t)(vb >> 2));
+        const uint32_t wd[4] = {b.x, b.y, b.z, b.w};
+        const float s = -thr * kLog2e;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          // 1 - u >= exp(z - best) rejects; v > edge marks the ids that may beat it
+          const float term = exp2f_approx(fmaf(z[k0 + e], kLog2e, s)) * kRejectSlack;
+          if (!(fmaf(term, 1.f, uniform_mantissa(wd[e])) > kRejectEdge)) continue;
+          if (vb + e == own.idx) continue;  // keyed above
+          const float key = z[k0 + e] + gumbel_fast_from_bits(wd[e]);
+          if (key_better(key, vb + e, own.key, own.idx)) {
+            own.key = key;
+            own.idx = vb + e;
+            thr = fmaxf(thr, key);
+          }
+        }
+      }
+    }
+  }
+  own = warp_reduce_stats(own);
+  if (lane == 0) sm_red[warp] = to_partial(own);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    Stats b = from_partial(sm_red[0]);
+#pragma unroll
+    for (int w2 = 1; w2 < kRowThreads / 32; ++w2) stats_merge(b, from_partial(sm_red[w2]));
+    b.m = -INFINITY;
+    b.s = 0.f;
+    a.row_part[(size_t)row * a.nchunk + c] = to_partial(b);
+  }
+  __syncthreads();
+}
+
 // Work items are (row position, chunk) pairs taken from a queue in row_order.  Per item
 // the CTA needs the chunk maximum M (block max; every thread then sums exp(z - M) against
 // the same M, so the partial sums add without rescaling).
@@ -120,6 +195,7 @@ __global__ void __launch_bounds__(kRowThreads, 3) verify_rows_kernel(VerifyArgs 
   constexpr int NV = kRowPer / EPV;              // vectors per thread per item
   constexpr int kWarps = kRowThreads / 32;
   __shared__ float sm_f[kWarps];
+  __shared__ Partial sm_red[kWarps];
   __shared__ int item_s;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int n_items = (*a.n_rows) * a.nchunk;
@@ -161,16 +237,38 @@ __global__ void __launch_bounds__(kRowThreads, 3) verify_rows_kernel(VerifyArgs 
         for (int e = 0; e < EPV; ++e) z[i * EPV + e] = (vb + e < v1) ? load_elem(a.target, DT, rbase + vb + e) : -INFINITY;
       }
     }
+    if (pos < a.R) {
+      // row ell of request r (the first R processing positions): the bonus draw's race
+      float m = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < kRowPer; ++k) {
+        z[k] *= a.inv_temp;
+        m = fmaxf(m, z[k]);
+      }
+      bonus_race<EPV>(a, z, m, r, t, v0, row, c, sm_red);
+      continue;
+    }
+    // statistics in base 2: y = t log2(e) / T, two ids per packed instruction; each term
+    // 2^(y - M) is one ex2, and the chunk maximum goes back to natural units once
+    constexpr float kLog2e = 1.4426950408889634f, kLn2 = 0.6931471805599453f;
+    const float ys = a.inv_temp * kLog2e;
     float m = -INFINITY;
 #pragma unroll
-    for (int k = 0; k < kRowPer; ++k) {
-      z[k] *= a.inv_temp;
-      m = fmaxf(m, z[k]);
+    for (int k = 0; k < kRowPer; k += 2) {
+      mul2f(z[k], z[k + 1], ys, ys);
+      m = max3f_(m, z[k], z[k + 1]);
     }
-    const float M = block_max(m, sm_f);
-    float ssum = 0.f;
+    const float M2 = block_max(m, sm_f);
+    const float M = M2 * kLn2;
+    float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-    for (int k = 0; k < kRowPer; ++k) ssum += __expf(z[k] - M);
+    for (int k = 0; k < kRowPer; k += 2) {
+      sub2f(z[k], z[k + 1], M2, M2);
+      z[k] = exp2f_approx(z[k]);
+      z[k + 1] = exp2f_approx(z[k + 1]);
+      add2f(s0, s1, z[k], z[k + 1]);
+    }
+    float ssum = s0 + s1;
     // sum of exp(z - M) (one common M: no rescaling): warp reductions, then the warps in
     // a fixed order
 #pragma unroll
@@ -211,7 +309,9 @@ __global__ void verify_accept_kernel(VerifyArgs a) {
   float lse_own[kRowSlots];
 #pragma unroll
   for (int s = 0; s < kRowSlots; ++s) lse_own[s] = 0.f;
-  // rows 0..ell, eight at a time; each lane merges chunks lane, lane+32, ... of each row
+  // rows 0..ell-1 (log-normalisers), eight at a time, and row ell (the bonus race), all
+  // merged the same way: each lane merges chunks lane, lane+32, ... of each row
+  int bonus_id = -1;
   for (int t0 = 0; t0 <= ell; t0 += 8) {
     Stats acc[8];
 #pragma unroll
@@ -229,6 +329,10 @@ __global__ void verify_accept_kernel(VerifyArgs a) {
     for (int q = 0; q < 8; ++q) {
       const int t = t0 + q;
       if (t > ell) break;  // uniform across the warp
+      if (t == ell) {
+        bonus_id = warp_reduce_stats(acc[q]).idx;
+        break;
+      }
       const Stats st = warp_reduce_stats(acc[q]);
 #pragma unroll
       for (int s = 0; s < kRowSlots; ++s)
@@ -309,14 +413,23 @@ __global__ void verify_accept_kernel(VerifyArgs a) {
       }
     }
   }
-  // the correction draw at position n_acc + 1 from target row n_acc: a residual draw after
-  // a rejection (jstar = n_acc + 1), the bonus draw otherwise (jstar = -(n_acc + 1))
+  // every verified draft accepted: the bonus token is row ell's race winner (position
+  // ell + 1, stream 2).  A rejection: the residual draw at position n_acc + 1 from target
+  // row n_acc, in the correction pass (jstar = n_acc + 1, a compact slot on the tensor-core
+  // path)
   if (lane == 0) {
-    a.jstar[r] = n_acc < ell ? n_acc + 1 : -(n_acc + 1);
+    a.jstar[r] = n_acc < ell ? n_acc + 1 : 0;
     a.lse_t[r] = lse_stop;
+    if (n_acc == ell) a.tokens_out[orow + ell] = bonus_id >= 0 ? bonus_id : 0;
   }
   if (n_acc < ell) {
     const int js = n_acc + 1;
+    int slot = r;
+    if (a.res_compact) {
+      if (lane == 0) slot = atomicAdd(a.n_rej, 1);
+      slot = __shfl_sync(0xffffffffu, slot, 0);
+      if (lane == 0) a.rej_req[slot] = r;
+    }
     // gather the factor row of position j* for the bias recomputation: W1[x_{j*-1}], or
     // the recurrent head's state s_{j*}
     size_t src;
@@ -328,7 +441,7 @@ __global__ void verify_accept_kernel(VerifyArgs a) {
                                       a.V, a.status, 12);
       src = (size_t)xprev * a.rank;
     }
-    const size_t dst = (size_t)r * a.rank;
+    const size_t dst = (size_t)slot * a.rank;
     if (a.dtype_w == DSPARK_BF16) {
       const unsigned short* w1 = reinterpret_cast<const unsigned short*>(rows);
       unsigned short* g = reinterpret_cast<unsigned short*>(a.W1g);
@@ -348,16 +461,13 @@ __global__ void __launch_bounds__(kSimtThreads) residual_step_simt_kernel(Verify
   griddep_wait();
   extern __shared__ float w1s[];  // [RB][rank]
   const int r0 = blockIdx.y * RB;
-  // correction position (0 = none) and whether it is a bonus draw (no draft law)
+  // correction position of each request (0 = none: every verified draft was accepted)
   int js[RB];
-  bool bon[RB];
   bool any = false;
 #pragma unroll
   for (int rr = 0; rr < RB; ++rr) {
     const int r = r0 + rr;
-    const int raw = (r < a.R) ? a.jstar[r] : 0;
-    js[rr] = raw < 0 ? -raw : raw;
-    bon[rr] = raw < 0;
+    js[rr] = (r < a.R) ? a.jstar[r] : 0;
     any |= js[rr] > 0;
   }
   if (!any) {
@@ -373,7 +483,7 @@ __global__ void __launch_bounds__(kSimtThreads) residual_step_simt_kernel(Verify
   for (int i = threadIdx.x; i < RB * a.rank; i += blockDim.x) {
     const int rr = i / a.rank, c = i % a.rank;
     const int r = r0 + rr;
-    w1s[i] = (r < a.R && js[rr] > 0 && !bon[rr]) ? load_elem(a.W1g, a.dtype_w, (size_t)r * a.rank + c) : 0.f;
+    w1s[i] = (r < a.R && js[rr] > 0) ? load_elem(a.W1g, a.dtype_w, (size_t)r * a.rank + c) : 0.f;
   }
   __syncthreads();
   Stats st[RB], fb[RB];
@@ -386,7 +496,7 @@ __global__ void __launch_bounds__(kSimtThreads) residual_step_simt_kernel(Verify
     const int r = min(r0 + rr, a.R - 1);
     const int j = max(js[rr], 1);
     rng[rr] = rng_row(a.seed, __ldg(a.req_id + r), a.round, kStreamCorrect, (uint32_t)j);
-    lq[rr] = bon[rr] ? 0.f : __ldg(a.lse_q + (size_t)r * a.gamma + (j - 1));
+    lq[rr] = __ldg(a.lse_q + (size_t)r * a.gamma + (j - 1));
     lt[rr] = a.lse_t[r];
   }
   const int groups_total = (a.V + 3) / 4;
@@ -399,6 +509,8 @@ __global__ void __launch_bounds__(kSimtThreads) residual_step_simt_kernel(Verify
     for (int rr = 0; rr < RB; ++rr)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[rr][e] = 0.f;
+    // unrolled so that several rank rows' W2 loads are in flight before their products
+#pragma unroll 8
     for (int i = 0; i < a.rank; ++i) {
       float w2[4];
 #pragma unroll
@@ -419,8 +531,7 @@ __global__ void __launch_bounds__(kSimtThreads) residual_step_simt_kernel(Verify
       if (r >= a.R || js[rr] == 0) continue;
       const Philox4 bits = rng_chunk(rng[rr], (uint32_t)g);
       const uint32_t wd[4] = {bits.x, bits.y, bits.z, bits.w};
-      // a bonus row has no draft law (and position n_acc + 1 may lie past the block)
-      const size_t urow = bon[rr] ? 0 : ((size_t)r * a.gamma + (js[rr] - 1)) * a.V;
+      const size_t urow = ((size_t)r * a.gamma + (js[rr] - 1)) * a.V;
       const size_t trow = target_row_index(a.t_off, a.n_trows, a.gamma, r, js[rr] - 1, a.status) * a.V;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -428,12 +539,9 @@ __global__ void __launch_bounds__(kSimtThreads) residual_step_simt_kernel(Verify
         if (v >= a.V) break;
         const float lp = load_elem(a.target, a.dtype_t, trow + v) * a.inv_temp - lt[rr];
         const float p = __expf(lp);
-        float rho = 0.f;
-        if (!bon[rr]) {
-          const float z = (load_elem(a.U, a.dtype_u, urow + v) + acc[rr][e]) * a.inv_temp;
-          rho = p - __expf(z - lq[rr]);
-        }
-        const float g_ = gumbel_from_bits(wd[e]);
+        const float z = (load_elem(a.U, a.dtype_u, urow + v) + acc[rr][e]) * a.inv_temp;
+        const float rho = p - __expf(z - lq[rr]);
+        const float g_ = gumbel_fast_from_bits(wd[e]);
         if (rho > 0.f) {
           const float key = __logf(rho) + g_;
           if (key > st[rr].key || st[rr].idx < 0) {
@@ -475,19 +583,32 @@ __global__ void residual_combine_kernel(VerifyArgs a, int npart) {
   const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (r >= a.R) return;
-  const int raw = a.jstar[r];
-  if (raw == 0) return;
-  const int js = raw < 0 ? -raw : raw;
+  // CUDA-core pass: warp r merges request r's chunk partials ([chunk, R]).  Compact
+  // tensor-core pass: warp q merges slot q's group partials ([group, rblocks * RB]), with the
+  // kernel's own split of its grid into groups
+  int req = r, slot = r;
+  size_t stride = (size_t)a.R;
+  if (a.res_compact) {
+    const int n = *reinterpret_cast<const volatile int*>(a.n_rej);
+    if (r >= n) return;
+    req = a.rej_req[r];
+    const int rb_rows = tc_rows_per_block(a.R);
+    const int rblocks = (n + rb_rows - 1) / rb_rows;
+    npart = max(1, a.res_grid / rblocks);
+    stride = (size_t)rblocks * rb_rows;
+  }
+  const int js = a.jstar[req];
+  if (js <= 0) return;  // no rejection: the bonus token is already written
   Stats st = stats_empty(), fb = stats_empty();
   for (int p = lane; p < npart; p += 32) {
-    stats_merge(st, from_partial(a.res_part[(size_t)p * a.R + r]));
-    stats_merge(fb, from_partial(a.res_part2[(size_t)p * a.R + r]));
+    stats_merge(st, from_partial(a.res_part[(size_t)p * stride + slot]));
+    stats_merge(fb, from_partial(a.res_part2[(size_t)p * stride + slot]));
   }
   st = warp_reduce_stats(st);
   fb = warp_reduce_stats(fb);
-  // a bonus row has only the ln p record; a residual row falls back to it only when no
-  // p - q was positive (rounding)
-  if (lane == 0) a.tokens_out[(size_t)r * (a.gamma + 1) + (js - 1)] = (raw > 0 && st.idx >= 0) ? st.idx : fb.idx;
+  // the residual draw falls back to the ln p record only when no p - q was positive
+  // (rounding)
+  if (lane == 0) a.tokens_out[(size_t)req * (a.gamma + 1) + (js - 1)] = st.idx >= 0 ? st.idx : fb.idx;
 }
 
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s) {
@@ -508,10 +629,11 @@ cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s) {
   if ((e = launch_pdl(verify_accept_kernel, dim3(wblocks), dim3(256), 0, s, a)) != cudaSuccess) return e;
   int npart;
   if (a.prof != nullptr && (e = record_profile_event(a.prof[2], s)) != cudaSuccess) return e;
-  if (tc_supported(a.V, a.rank, a.dtype_w)) {
-    // the residual recomputes one bias row per rejected request on the tensor cores
+  if (a.res_compact) {
+    // the residual recomputes one bias row per rejected request on the tensor cores, over
+    // the compact slots (the partial count is derived on the device from their number)
     if ((e = launch_residual_tc(a, s)) != cudaSuccess) return e;
-    npart = tc_num_partials(a.R);
+    npart = 0;
   } else {
     dim3 rgrid(simt_num_chunks(a.V), (a.R + kSimtRB - 1) / kSimtRB);
     const size_t smem = sizeof(float) * kSimtRB * a.rank;
@@ -528,11 +650,13 @@ cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s) {
   return launch_pdl(residual_combine_kernel, dim3(wblocks), dim3(256), 0, s, a, npart);
 }
 
-int residual_num_partials(int R, int V, int rank, int dtype_w) {
-  const int simt = simt_num_chunks(V);
-  if (!tc_supported(V, rank, dtype_w)) return simt;
-  const int tc = tc_num_partials(R);
-  return simt > tc ? simt : tc;
+// Partial records of the correction pass: the CUDA-core pass keeps one per (vocabulary
+// chunk, request); the compact tensor-core pass one per (vocabulary group, slot), at most
+// its grid times the rows of a block (every CTA covers one block of slots), which stays
+// linear in R.
+size_t residual_partial_entries(int R, int V, int rank, int dtype_w) {
+  if (!tc_supported(V, rank, dtype_w)) return (size_t)simt_num_chunks(V) * R;
+  return (size_t)tc_grid_ctas(R) * tc_rows_per_block(R);
 }
 
 }  // namespace dspark

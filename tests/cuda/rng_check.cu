@@ -37,6 +37,13 @@ __global__ void gumbel_kernel(int n, const uint32_t* bits, const float* t, float
   reject[i] = gumbel_cannot_win(bits[i], t[i]) ? 1 : 0;
 }
 
+// The fast Gumbel of the draft epilogue's survivors.
+__global__ void gumbel_fast_kernel(int n, const uint32_t* bits, float* g) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  g[i] = gumbel_fast_from_bits(bits[i]);
+}
+
 // The draft step's conversion-free rejection test for (bits, t * scale), as the draft
 // epilogue evaluates it.
 __global__ void reject_fast_kernel(int n, const uint32_t* bits, const float* t, float scale, int* reject) {
@@ -58,5 +65,10 @@ extern "C" int rng_check_gumbel(int n, const uint32_t* bits, const float* t, flo
 
 extern "C" int rng_check_reject_fast(int n, const uint32_t* bits, const float* t, float scale, int* reject) {
   reject_fast_kernel<<<(n + 255) / 256, 256>>>(n, bits, t, scale, reject);
+  return (int)cudaDeviceSynchronize();
+}
+
+extern "C" int rng_check_gumbel_fast(int n, const uint32_t* bits, float* g) {
+  gumbel_fast_kernel<<<(n + 255) / 256, 256>>>(n, bits, g);
   return (int)cudaDeviceSynchronize();
 }

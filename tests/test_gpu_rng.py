@@ -29,6 +29,7 @@ def lib():
     P = ctypes.c_void_p
     L.rng_check_philox.argtypes = [ctypes.c_int, P, P, P, P, ctypes.c_uint32, ctypes.c_uint32, P]
     L.rng_check_gumbel.argtypes = [ctypes.c_int, P, P, P, P]
+    L.rng_check_gumbel_fast.argtypes = [ctypes.c_int, P, P]
     L.rng_check_reject_fast.argtypes = [ctypes.c_int, P, P, ctypes.c_float, P]
     return L
 
@@ -69,6 +70,22 @@ def test_gumbel_single_precision_accuracy(lib):
     err = np.abs(g.cpu().numpy().astype(np.float64) - exact)
     # absolute accuracy of the key z + g: far inside the 1e-5 boundary window
     assert err.max() < 2e-6, err.max()
+
+
+def test_fast_gumbel_single_precision_accuracy(lib):
+    # the survivors' Gumbel of the draft epilogue: every 2^8-th 24-bit code, both tails,
+    # and the codes around the branch point u = 1/2
+    b24 = np.concatenate([np.arange(0, 1 << 24, 256), np.arange(0, 4096), np.arange((1 << 24) - 4096, 1 << 24),
+                          np.arange((1 << 23) - 2048, (1 << 23) + 2048)])
+    bits = (b24.astype(np.uint64) << 8).astype(np.uint32) | np.uint32(0xA5)  # low bits must not matter
+    n = len(bits)
+    tb = torch.from_numpy(bits.view(np.int32)).cuda()
+    g = torch.zeros(n, dtype=torch.float32, device="cuda")
+    assert lib.rng_check_gumbel_fast(n, _p(tb), _p(g)) == 0
+    u = (b24.astype(np.float64) + 0.5) / 2**24
+    exact = -np.log(-np.log1p(u - 1.0))
+    err = np.abs(g.cpu().numpy().astype(np.float64) - exact)
+    assert err.max() < 2e-6, (err.max(), b24[np.argmax(err)])
 
 
 def test_rejection_test_is_sound(lib):

@@ -77,7 +77,7 @@ def test_static_scratch_reports_bad_device_data():
 
 def test_static_scratch_rejects_oversized_shapes():
     from speculative_decoding_draft_03_gb300 import binding as b
-    R, gamma, V, rank = 2048, 3, 151936, 256  # needs tens of MiB of scratch
+    R, gamma, V, rank = 8192, 3, 151936, 256  # needs about 25 MiB of scratch
     need = b.verify_workspace_size(R, gamma, V, rank, torch.bfloat16)
     assert need > (8 << 20)
     dev = torch.device("cuda")
