@@ -199,6 +199,12 @@ def draft_step_bytes(w):
     return R * V * _es(w["U"].dtype) + rank * V * _es(W2.dtype) + R * rank * _es(W2.dtype)
 
 
+def draft_positions_per_launch(w):
+    """Draft positions one timed draft launch covers: all of them when the CUDA-core path
+    runs the whole draft loop in one launch (a vocabulary of one 4096-id chunk), else one."""
+    return w["gamma"] if (not tensor_core_path(w) and w["V"] <= 4096 and w.get("head") != "rnn") else 1
+
+
 def draft_step_flops(w):
     """Flops of one draft step's bias contraction: 2 R rank V."""
     return 2 * w["R"] * w["rank"] * w["V"]
@@ -237,11 +243,16 @@ def launches_per_round(w):
         # h projection, then a cell and a step per position, the merge (tensor cores: once;
         # CUDA cores: per position) and the confidences
         draft = (1 if w["d"] > 0 else 0) + 2 * g + (1 if tensor_core_path(w) else g) + 1
-        return (1 if w["d"] > 0 else 0) + draft + 1 + 5
+        return (1 if w["d"] > 0 else 0) + draft + 1 + 5 + (1 if tensor_core_path(w) else 0)
+    # verification: plan, rows, accept, correction, combine (and the rounding-fallback pass
+    # on the tensor-core path)
+    verify = 5 + (1 if tensor_core_path(w) else 0)
+    if draft_positions_per_launch(w) > 1:  # one launch for the whole CUDA-core draft loop
+        return (1 if w["d"] > 0 else 0) + 1 + 1 + verify
     draft = g + 1 if tensor_core_path(w) else 2 * g
     # position 1's prepare launch: not needed on the tensor-core path with a hidden state
     prepare = 0 if (tensor_core_path(w) and w["d"] > 0) else 1
-    return (1 if w["d"] > 0 else 0) + prepare + draft + 1 + 5
+    return (1 if w["d"] > 0 else 0) + prepare + draft + 1 + verify
 
 
 def acceptance_stats(gamma, ells, n_accs):
@@ -345,7 +356,7 @@ def roofline_entries(w, res, peaks, peak_kind, workload):
     step_ms = res["step_ms"]
     if step_ms:
         avg = sum(step_ms) / len(step_ms)
-        nbytes = draft_step_bytes(w)
+        nbytes = draft_step_bytes(w) * draft_positions_per_launch(w)
         ach = nbytes / (avg / 1e3) / 1e9
         ctr = stored_counters("draft_step", workload)
         out["draft_step"] = {
@@ -353,12 +364,12 @@ def roofline_entries(w, res, peaks, peak_kind, workload):
             "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "peak_source": peak_kind,
             "traffic": None if ctr is None else ctr.get("traffic_bytes_per_launch"),
             "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": avg, "launches_timed": len(step_ms)}
-        tflops = draft_step_flops(w) / (avg / 1e3) / 1e12
+        tflops = draft_step_flops(w) * draft_positions_per_launch(w) / (avg / 1e3) / 1e12
         tpeak = peaks.get("bf16_tflops", 1900.0)
         out["draft_step_tensor"] = {
             "kernel": "bias contraction of the draft step (tcgen05.mma kind::f16, bf16 x bf16 -> fp32)",
             "bound": "tensor", "achieved": tflops, "peak": tpeak, "unit": "TFLOP/s", "frac": tflops / tpeak,
-            "flops_per_launch": draft_step_flops(w),
+            "flops_per_launch": draft_step_flops(w) * draft_positions_per_launch(w),
             "ncu_tensor_pipe_active_pct": None if ctr is None else ctr.get("tensor_pipe_active_pct")}
     vs = res["verify_samples"]
     if vs:

@@ -91,8 +91,10 @@ DSPARK_API dspark_status dspark_workspace_status(void* workspace, int reset, int
 /* Measurement hook (not part of the method).  While set, dspark_markov_draft records
  * events[2(k-1)] just before and events[2(k-1)+1] just after the launch of draft
  * position k's vocabulary-streaming step kernel, on the call's stream, for
- * k = 1..min(gamma, n_events/2).  `events` holds cudaEvent_t handles owned by the
- * caller; NULL or n_events = 0 turns recording off.  The setting is per host thread.
+ * k = 1..min(gamma, n_events/2).  (On the CUDA-core path a vocabulary of at most 4096
+ * ids runs every position in one launch; events[0] and events[1] then bracket that
+ * launch.)  `events` holds cudaEvent_t handles owned by the caller; NULL or n_events = 0
+ * turns recording off.  The setting is per host thread.
  * While the stream is being captured into a CUDA graph, the events become external
  * event-record nodes of the graph, so every replay records them. */
 DSPARK_API void dspark_set_profile_events(void* const* events, int n_events);

@@ -10,6 +10,8 @@
 //                  (vocabulary chunk, request)
 //   draft_combine  merges the partials of a position into x_k, lse_k, logq_k and
 //                  prepares position k+1 (one CTA per request).
+//   draft_round_simt  the three above for every position in one launch, when the
+//                  vocabulary is a single chunk (small vocabularies).
 //
 // Method: numb3r33 blog "DSpark: confidence-scheduled speculative decoding", sections
 // "Markov sequential head" (p_k(v|x_{k-1}) = softmax(U_k(v) + W1[x_{k-1}] W2)) and
@@ -166,11 +168,13 @@ __global__ void __launch_bounds__(32) draft_prepare_kernel(DraftArgs a, int k) {
 // blockIdx.y: block of RB requests.  Each thread owns groups of 4 consecutive ids so
 // that one Philox block serves its 4 elements of a request row.
 // ---------------------------------------------------------------------------------
+// One draft position for request block r0 .. r0+RB-1 over vocabulary chunk `chunk`
+// (the caller has synchronised after writing the block's factor rows W1g).  Writes the
+// chunk's partial record per request, or, when the chunk is the whole vocabulary
+// (final), the position's x_k, lse_k and logq_k directly (the merge of one record).
 template <int RB>
-__global__ void __launch_bounds__(kSimtThreads) draft_step_simt_kernel(DraftArgs a, int k) {
-  griddep_wait();
-  extern __shared__ float w1s[];  // [RB][rank]
-  const int r0 = blockIdx.y * RB;
+__device__ __forceinline__ void simt_step_block(const DraftArgs& a, int k, int chunk, int r0, bool final,
+                                                float* w1s) {
   for (int i = threadIdx.x; i < RB * a.rank; i += blockDim.x) {
     const int rr = i / a.rank, c = i % a.rank;
     const int r = r0 + rr;
@@ -187,7 +191,7 @@ __global__ void __launch_bounds__(kSimtThreads) draft_step_simt_kernel(DraftArgs
     rng[rr] = rng_row(a.seed, __ldg(a.req_id + r), a.round, kStreamDraft, (uint32_t)k);
   }
   const int groups_total = (a.V + 3) / 4;
-  const int g0 = blockIdx.x * kSimtGroups * blockDim.x;
+  const int g0 = chunk * kSimtGroups * blockDim.x;
   for (int t = 0; t < kSimtGroups; ++t) {
     const int g = g0 + t * blockDim.x + threadIdx.x;
     if (g >= groups_total) break;
@@ -255,9 +259,52 @@ __global__ void __launch_bounds__(kSimtThreads) draft_step_simt_kernel(DraftArgs
     if (warp == 0) {
       Stats b = (lane < (int)(blockDim.x >> 5)) ? from_partial(red[lane]) : stats_empty();
       b = warp_reduce_stats(b);
-      if (lane == 0 && r < a.R) a.partials[(size_t)blockIdx.x * a.R + r] = to_partial(b);
+      if (lane == 0 && r < a.R) {
+        if (final) {
+          // the merge of this single record, as the combine kernel computes it
+          Stats m = stats_empty();
+          stats_merge(m, b);
+          const size_t row = (size_t)r * a.gamma + (k - 1);
+          const float lse = m.m + logf(m.s);
+          a.x_out[row] = m.idx;
+          a.lse_out[row] = lse;
+          a.logq_out[row] = m.zsel - lse;
+        } else {
+          a.partials[(size_t)chunk * a.R + r] = to_partial(b);
+        }
+      }
     }
     __syncthreads();
+  }
+}
+
+template <int RB>
+__global__ void __launch_bounds__(kSimtThreads) draft_step_simt_kernel(DraftArgs a, int k) {
+  griddep_wait();
+  extern __shared__ float w1s[];  // [RB][rank]
+  simt_step_block<RB>(a, k, blockIdx.x, blockIdx.y * RB, false, w1s);
+}
+
+// The whole draft loop of one request block when the vocabulary is one chunk: for
+// k = 1..gamma, warps 0..RB-1 gather their request's factor row W1[x_{k-1}] and c_k
+// (x_0 = the anchor, then the previous position's draw), then the block runs the position
+// and writes x_k, lse_k, logq_k itself.  The same arithmetic as the per-position kernels
+// (step, combine, prepare) in one launch.
+template <int RB>
+__global__ void __launch_bounds__(kSimtThreads) draft_round_simt_kernel(DraftArgs a) {
+  griddep_allow_next();
+  griddep_wait();
+  extern __shared__ float w1s[];  // [RB][rank]
+  const int r0 = blockIdx.x * RB;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int k = 1; k <= a.gamma; ++k) {
+    if (warp < RB && r0 + warp < a.R) {
+      const int r = r0 + warp;
+      const int raw = (k == 1) ? __ldg(a.x0 + r) : a.x_out[(size_t)r * a.gamma + (k - 2)];
+      prepare_position_warp(a, r, k, checked_token(raw, a.V, a.status, 1), lane);
+    }
+    __syncthreads();
+    simt_step_block<RB>(a, k, 0, r0, true, w1s);
   }
 }
 
@@ -360,6 +407,19 @@ cudaError_t launch_draft_step_simt(const DraftArgs& a, int k, cudaStream_t s) {
     if (e != cudaSuccess) return e;
   }
   return launch_pdl(draft_step_simt_kernel<kSimtRB>, grid, dim3(kSimtThreads), smem, s, a, k);
+}
+
+int simt_whole_round(int V) { return simt_num_chunks(V) == 1; }
+
+cudaError_t launch_draft_round_simt(const DraftArgs& a, cudaStream_t s) {
+  const size_t smem = sizeof(float) * kSimtRB * a.rank;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(draft_round_simt_kernel<kSimtRB>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_pdl(draft_round_simt_kernel<kSimtRB>, dim3((a.R + kSimtRB - 1) / kSimtRB), dim3(kSimtThreads), smem,
+                    s, a);
 }
 
 cudaError_t launch_draft_finalize(const DraftArgs& a, int npart, cudaStream_t s) {

@@ -97,7 +97,8 @@ struct Smem {
   static_assert(kEpiWarps * 32 * 32 <= stages * kStageBytes, "merge scratch must fit in the W2 ring");
   static_assert(uboxes >= 4 && uboxes <= kMaxUBoxes, "U ring must hold one tile of fp32 boxes");
   static_assert(total + 1024 <= 232448, "shared memory plan exceeds 227 KB");
-  static_assert(8 * (2 * stages + 7 + 2 * kMaxUBoxes) + 16 <= 512, "barriers, TMEM slot and abort flag fit in 512 B");
+  static_assert(8 * (2 * stages + 7 + 2 * kMaxUBoxes) + 16 <= 512,
+                "barriers, TMEM slot, abort flag and release counter fit in 512 B");
 };
 
 // ------------------------------------------------------------------------------------
@@ -293,7 +294,7 @@ struct TcParams {
   const int64_t* req_id;
   uint64_t seed, round;
   Partial* partials;  // [ngroups, R]
-  int* hint;          // [R] published best keys (draft mode)
+  int* hint;          // [R] published best keys (draft mode; residual mode: per slot)
   DeviceStatus* status;
   // residual mode
   const void* target;
@@ -394,7 +395,7 @@ __device__ __forceinline__ void philox_run(const PhiloxRow& prow, int v0, uint32
 // rejected without logarithms when 1 - u >= exp(z - best) = term * exp(m - best) (the
 // conversion-free form v = term * scale + f > edge marks the ids that may beat it; the
 // run is done when even the largest v is not); survivors evaluate their key.  Without any
-// known key, the run's largest logit is keyed first so that the others are tested
+// known key, the tile's largest logit is keyed first so that the others are tested
 // against it.  Runs at or beyond V, and rows beyond R, contribute nothing.
 template <int KP>
 __device__ __forceinline__ void draft_tile(const TcParams& p, Stats& st, const PhiloxRow& prow,
@@ -437,6 +438,23 @@ __device__ __forceinline__ void draft_tile(const TcParams& p, Stats& st, const P
   // no id of the tile can reach the best key even with the largest possible Gumbel: no
   // random words are needed
   const bool race = !(thr > -INFINITY && fmaf(tmax, kLn2f, kGumbelMax) < thr);
+  if (race && thr == -INFINITY) {
+    // no key known yet (this thread's first tile, no bound published): key the tile's
+    // largest logit first, the strongest threshold a single draw can give, so that the
+    // other ids are tested against it (the lowest id among equal maxima)
+    int kb = 0;
+#pragma unroll
+    for (int q = KP * kCols - 1; q >= 0; --q)
+      if (y[q / kCols][q % kCols] == tmax) kb = q;
+    const int vm = v0 + kb;
+    const Philox4 b4 = prow.block((uint32_t)(vm >> 2));
+    const uint32_t w = (vm & 3) == 0 ? b4.x : ((vm & 3) == 1 ? b4.y : ((vm & 3) == 2 ? b4.z : b4.w));
+    const float cn = tmax * kLn2f;
+    st.key = cn + gumbel_fast_from_bits(w);
+    st.idx = vm;
+    st.zsel = cn;
+    thr = st.key;
+  }
 #pragma unroll
   for (int ps = 0; ps < KP; ++ps) {
     const int vb = v0 + ps * kCols;
@@ -463,21 +481,6 @@ __device__ __forceinline__ void draft_tile(const TcParams& p, Stats& st, const P
     if (race && cmax > -INFINITY && !(thr > -INFINITY && fmaf(cmax, kLn2f, kGumbelMax) < thr)) {
       uint32_t wd[kCols];
       philox_run(prow, vb, wd);
-      if (thr == -INFINITY) {
-        int imax = kCols - 1;
-#pragma unroll
-        for (int i = kCols - 2; i >= 0; --i)
-          if (y[ps][i] == cmax) imax = i;
-        uint32_t wm = wd[0];
-#pragma unroll
-        for (int i = 1; i < kCols; ++i)
-          if (i == imax) wm = wd[i];
-        const float cn = cmax * kLn2f;
-        st.key = cn + gumbel_fast_from_bits(wm);
-        st.idx = vb + imax;
-        st.zsel = cn;
-        thr = st.key;
-      }
       // the scale e^(m ln 2 - best) is 2^(m - best log2 e)
       const float scale = ex2_approx(fmaf(-thr, kLog2ef, mnew)) * kRejectSlack;
       float v[kCols];
@@ -576,6 +579,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kBarBytes = 8 * (2 * kStages + 7 + 2 * kMaxUBoxes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::bars + kBarBytes);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM::bars + kBarBytes + 8);
+  // residual mode: tiles whose accumulator epilogue warp 0 has released (paces the L2 prefetcher)
+  volatile int* released = reinterpret_cast<volatile int*>(smem + SM::bars + kBarBytes + 12);
   // U boxes of a tile: 128/ubox_cols of them, each read by the 16/(128/ubox_cols) warps
   // whose columns fall inside it
   const int uboxes_per_tile = kN / p.ubox_cols;
@@ -603,6 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_uempty + 8 * s, warps_per_ubox);
     }
     *abort_flag = 0;
+    *released = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
@@ -717,6 +723,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_drain(bar_mma_drain, 0);
       }
     }
+  } else if (warp == 2 && MODE == kModeResidual) {
+    // ------------------------------ L2 prefetcher (residual mode) -------------
+    // The slots' U and target rows lie at scattered positions, so the epilogue loads them
+    // itself; this warp brings each tile's row segments into L2 kPrefTiles tiles ahead of
+    // the epilogue (paced by the accumulator releases), so those loads hit L2.
+    constexpr int kPrefTiles = 2;
+    const int n = *reinterpret_cast<const volatile int*>(p.res_nrows);
+    const int es_u = p.dtype_u == DSPARK_F32 ? 4 : 2, es_t = p.dtype_t == DSPARK_F32 ? 4 : 2;
+    const char* ubase[RB / 32];
+    const char* tbase[RB / 32];
+#pragma unroll
+    for (int i = 0; i < RB / 32; ++i) {
+      const int q = rb * RB + lane + 32 * i;
+      ubase[i] = tbase[i] = nullptr;
+      if (q < n) {
+        const int rq = p.res_req[q];
+        const int js = p.jstar[rq];
+        if (js > 0 && js <= p.gamma) {
+          ubase[i] = reinterpret_cast<const char*>(p.U) + ((size_t)rq * p.gamma + (js - 1)) * (size_t)p.V * es_u;
+          tbase[i] = reinterpret_cast<const char*>(p.target) +
+                     target_row_index(p.t_off, p.n_trows, p.gamma, rq, js - 1, p.status) * (size_t)p.V * es_t;
+        }
+      }
+    }
+    auto prefetch_tile = [&](int t) {
+      const int v0 = (group + t * ngroups) * kN;
+      const int ids = min(kN, p.V - v0);
+#pragma unroll
+      for (int i = 0; i < RB / 32; ++i) {
+        if (ubase[i] == nullptr) continue;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ubase[i] + (size_t)v0 * es_u), "r"(ids * es_u)
+                     : "memory");
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(tbase[i] + (size_t)v0 * es_t), "r"(ids * es_t)
+                     : "memory");
+      }
+    };
+    for (int t = 0; t < min(kPrefTiles, my_tiles); ++t) prefetch_tile(t);
+    const long long t0 = clock64();
+    for (int t = 0; t + kPrefTiles < my_tiles && !*abort_flag; ++t) {
+      // wait (bounded) until tile t has been released, then prefetch tile t + kPrefTiles
+      bool ok = true;
+      while (*released <= t) {
+        if (*abort_flag || clock64() - t0 > kWaitCycles) {
+          ok = false;
+          break;
+        }
+      }
+      if (!ok) break;
+      prefetch_tile(t + kPrefTiles);
+    }
   } else if (warp == 2) {
     // ------------------------------ U producer (draft mode) -------------------
     // U is an input of the round: its boxes stream ahead of the epilogue through a
@@ -802,7 +858,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // normalisers in base 2 too; keys (st.key, fb.key) and st.zsel are natural throughout
     const float zscale = p.inv_temp * kLog2ef;
     const float lse_q2 = lse_q * kLog2ef, lse_t2 = lse_t * kLog2ef;
-    Stats fb = stats_empty();  // residual only: ln p + g (the rounding fallback)
     float ovl = 0.f;           // overlap only: this thread's sum of min(q, p)
     const PhiloxRow prow =
         philox_row(rng_row(p.seed, (MODE != kModeOverlap && valid) ? __ldg(p.req_id + req) : 0, p.round,
@@ -921,9 +976,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int buf = t & 1;
       const uint32_t use = (uint32_t)(t >> 1) & 1u;
       const int vt = (group + t * ngroups) * kN;
-      // the published bound is read a tile ahead of its use, so that its latency hides
-      // behind this tile's work
-      const int hint_pref = (kDraftMath && valid) ? __ldcg(p.hint + r) : 0;
+      // the best key published for this request so far (an order-preserving int code)
+      const int hint_pref =
+          ((kDraftMath || MODE == kModeResidual) && valid) ? __ldcg(p.hint + r) : (int)(0xFF800000u ^ 0x7FFFFFFFu);
+      // residual mode: the race's bound for this tile (own record aside)
+      const float tile_bound = fmaxf(bound, key_from_ordered(hint_pref));
       uint4 ucur[kPass][2];
       uint4 tcur[kPass][2];
       int uslot = 0;
@@ -974,8 +1031,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every epilogue warp still meets the same named barriers.
       const bool acc_ready = mbar_wait(bar_acc_full + 8 * buf, use, abort_flag, p.status, 300) && u_ready;
       if (acc_ready) tc_fence_after();
+      // the bound published so far, read at the start of this tile (its latency hides
+      // behind the tile's logits; it is first needed by the race)
       if constexpr (kDraftMath) draft_tile(p, st, prow, ucur, tmem_base + lane_addr + buf * kN + col0, acc_ready, valid,
-                                           vt + col0, zscale, bound, bar_acc_empty + 8 * buf, lane);
+                                           vt + col0, zscale, fmaxf(bound, key_from_ordered(hint_pref)),
+                                           bar_acc_empty + 8 * buf, lane);
 #pragma unroll
       for (int ps = 0; ps < kPass; ++ps) {
         if (kDraftMath || !acc_ready) break;
@@ -987,6 +1047,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_acc_empty + 8 * buf);
+          if (MODE == kModeResidual && ew == 0 && lane == 0) *released = t + 1;
         }
         const int vb = vt + c;
         float z[kCols];
@@ -1017,8 +1078,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ovl += fminf(ex2_approx(fmaf(tl[i], zscale, -lse_t2)), ex2_approx(z[i] - lse_q2));
         } else {
           // residual: q = exp(z - lse_q), p = exp(t/T - lse_t); draw from (p - q)+ by
-          // Gumbel-max over ln(p - q) where positive, and keep the ln p draw as fallback
-          // (lp holds log2 p; the fallback key is lp ln 2 + g)
+          // Gumbel-max over ln(p - q) where positive.  (A row with no positive p - q, which
+          // only rounding can produce, is drawn from p by the fallback pass.)
           float lp[kCols];
           if constexpr (kRing) {
 #pragma unroll
@@ -1040,48 +1101,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             gmax = fmaxf(gmax, lp[i]);
           }
           const float gtop = fmaf(gmax, kLn2f, kGumbelMax);
-          // ln(p - q) <= ln p: neither draw can improve once ln p + G_max is below both keys
-          if (fb.idx >= 0 && gtop < fb.key && st.idx >= 0 && gtop < st.key) continue;
-          // rejection scales: a key c + g beats best only if 1-u < e^{c - best}; the test
-          // 1 - u >= x scale in its conversion-free form (x = rho or p; without a record yet
-          // the scale is infinite and every id is keyed)
-          const float s1 = (st.idx >= 0) ? __expf(-st.key) * kRejectSlack : INFINITY;
-          const float s2 = (fb.idx >= 0) ? __expf(-fb.key) * kRejectSlack : INFINITY;
+          // the best key known: own record, or the best any CTA has published for this slot
+          const float thr = fmaxf(st.idx >= 0 ? st.key : -INFINITY, tile_bound);
+          // ln(p - q) <= ln p: no draw of the run can improve once ln p + G_max is below it
+          if (thr > -INFINITY && gtop < thr) continue;
+          // rejection scale: a key ln rho + g beats best only if 1-u < rho e^{-best}; the test
+          // in its conversion-free form (without any key yet the scale is infinite and every
+          // id with rho > 0 is keyed)
+          const float s1 = (thr > -INFINITY) ? __expf(-thr) * kRejectSlack : INFINITY;
+          uint32_t wd[kCols];
+          float rho[kCols];
+          uint32_t cand = 0;
 #pragma unroll
           for (int g4 = 0; g4 < 2; ++g4) {
             const Philox4 bits = prow.block((uint32_t)((vb >> 2) + g4));
-            const uint32_t wd[4] = {bits.x, bits.y, bits.z, bits.w};
+            wd[4 * g4 + 0] = bits.x;
+            wd[4 * g4 + 1] = bits.y;
+            wd[4 * g4 + 2] = bits.z;
+            wd[4 * g4 + 3] = bits.w;
+          }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int v = vb + 4 * g4 + e;
-              const float pv = ex2_approx(lp[4 * g4 + e]);
-              const float rho = pv - ex2_approx(z[4 * g4 + e] - lse_q2);
-              const float f = uniform_mantissa(wd[e]);
-              const bool try1 = rho > 0.f && fmaf(rho, s1, f) > kRejectEdge;
-              const bool try2 = pv > 0.f && fmaf(pv, s2, f) > kRejectEdge;
-              if (!try1 && !try2) continue;
-              const float g = gumbel_fast_from_bits(wd[e]);
-              if (try2) {
-                const float k2 = fmaf(lp[4 * g4 + e], kLn2f, g);
-                if (fb.idx < 0 || k2 > fb.key) {
-                  fb.key = k2;
-                  fb.idx = v;
-                }
+          for (int i = 0; i < kCols; ++i) {
+            rho[i] = ex2_approx(lp[i]) - ex2_approx(z[i] - lse_q2);
+            if (rho[i] > 0.f && fmaf(rho[i], s1, uniform_mantissa(wd[i])) > kRejectEdge) cand |= 1u << i;
+          }
+          while (cand) {
+            const int i = __ffs(cand) - 1;
+            cand &= cand - 1;
+            float ri = 0.f;
+            uint32_t wi = 0u;
+#pragma unroll
+            for (int j = 0; j < kCols; ++j)  // static register selection (no local memory)
+              if (j == i) {
+                ri = rho[j];
+                wi = wd[j];
               }
-              if (try1) {
-                const float k1 = logf(rho) + g;
-                if (st.idx < 0 || k1 > st.key) {
-                  st.key = k1;
-                  st.idx = v;
-                }
-              }
+            const float k1 = ln_fast(ri) + gumbel_fast_from_bits(wi);
+            if (st.idx < 0 || k1 > st.key) {
+              st.key = k1;
+              st.idx = vb + i;
             }
           }
         }
       }
-      if constexpr (kDraftMath) {
-        // After the first tiles, publish the CTA's best key per request (one atomic per
-        // request per CTA), so that CTAs still streaming can skip more of their draws.
+      if constexpr (kDraftMath || MODE == kModeResidual) {
+        // After the first tiles, publish the CTA's best key per request (residual mode: per
+        // slot), one atomic per request per CTA, so that CTAs still streaming can reject more
+        // of their draws without evaluating them.
         if (t < publish_tiles<RB>()) {
           float* pub = reinterpret_cast<float*>(smem + SM::pub);
           pub[ew * 32 + lane] = (valid && st.idx >= 0) ? st.key : -INFINITY;
@@ -1124,8 +1190,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
 #pragma unroll
-    for (int which = 0; which < (kDraftMath ? 1 : (MODE == kModeResidual ? 2 : 0)); ++which) {
-      red[ew * 32 + lane] = to_partial(which ? fb : st);
+    for (int which = 0; which < ((kDraftMath || MODE == kModeResidual) ? 1 : 0); ++which) {
+      red[ew * 32 + lane] = to_partial(st);
       asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
       if (et < RB) {
         Stats m = stats_empty();
@@ -1138,9 +1204,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (MODE == kModeResidual) {
           // [group, rblocks * RB] over the slots
           if (rr < *reinterpret_cast<const volatile int*>(p.res_nrows))
-            (which ? p.partials2 : p.partials)[(size_t)group * rblocks * RB + rr] = to_partial(m);
+            p.partials[(size_t)group * rblocks * RB + rr] = to_partial(m);
         } else if (rr < p.R) {
-          (which ? p.partials2 : p.partials)[(size_t)group * p.R + rr] = to_partial(m);
+          p.partials[(size_t)group * p.R + rr] = to_partial(m);
         }
         // draft: this CTA's winner for the request, as one 64-bit maximum (key code in the
         // high half, sign-flipped so that the order is unsigned; ~id in the low half, so the
@@ -1517,6 +1583,7 @@ cudaError_t launch_residual_tc(const VerifyArgs& a, cudaStream_t s) {
   p.lse_t = a.lse_t;
   p.res_req = a.rej_req;
   p.res_nrows = a.n_rej;
+  p.hint = a.res_hint;
   p.grid = a.res_grid;
   return tc::launch<tc::kModeResidual>(p, a.W1g, a.W2, s);
 }

@@ -79,8 +79,8 @@ RnnLayout rnn_layout(int R, int gamma, int V, int ns, int d, int dtype_w) {
 }
 
 struct VerifyLayout {
-  size_t counters, row_req, row_t, row_base, row_order, row_part, lse_t, jstar, rej_req, W1g, res_part, res_part2,
-      total;
+  size_t counters, row_req, row_t, row_base, row_order, row_part, lse_t, jstar, rej_req, fb_req, res_hint, W1g,
+      res_part, res_part2, total;
   int nchunk;
 };
 
@@ -108,6 +108,10 @@ VerifyLayout verify_layout(int R, int gamma, int V, int rank, int dtype_w) {
   L.jstar = off;
   off += align256(4 * (size_t)R);
   L.rej_req = off;
+  off += align256(4 * (size_t)R);
+  L.fb_req = off;
+  off += align256(4 * (size_t)R);
+  L.res_hint = off;
   off += align256(4 * (size_t)R);
   L.W1g = off;
   off += align256(elem_size(dtype_w) * (size_t)round_up_rows(R) * rank);
@@ -317,6 +321,15 @@ dspark_status dspark_markov_draft(int R, int gamma, int V, int rank, int d, int 
     if ((e = cudaMemsetAsync(a.s_h, 0, sizeof(float) * (size_t)R * gamma, s)) != cudaSuccess)
       return cuda_fail(e, "s_h clear");
   }
+  if (!tc && dspark::simt_whole_round(V)) {
+    // one vocabulary chunk: the whole draft loop in one launch (the profiling events, if
+    // set, bracket that launch)
+    const bool prof = g_prof_n >= 2;
+    if (prof && (e = record_profile_event(g_prof_events[0], s)) != cudaSuccess) return cuda_fail(e, "profile event");
+    if ((e = dspark::launch_draft_round_simt(a, s)) != cudaSuccess) return cuda_fail(e, "draft_round_simt");
+    if (prof && (e = record_profile_event(g_prof_events[1], s)) != cudaSuccess) return cuda_fail(e, "profile event");
+    return DSPARK_OK;
+  }
   if (prepare && (e = dspark::launch_draft_prepare(a, 1, s)) != cudaSuccess) return cuda_fail(e, "draft_prepare");
   for (int k = 1; k <= gamma; ++k) {
     int npart;
@@ -498,6 +511,9 @@ static dspark_status verify_impl(int R, int gamma, int V, int rank, int dtype_t,
   a.work_next = counters + 2;
   a.n_rej = counters + 3;
   a.rej_req = reinterpret_cast<int*>(ws + L.rej_req);
+  a.n_fb = counters + 4;
+  a.fb_req = reinterpret_cast<int*>(ws + L.fb_req);
+  a.res_hint = reinterpret_cast<int*>(ws + L.res_hint);
   a.res_compact = dspark::tc_supported(V, rank, dtype_w);
   a.res_grid = dspark::tc_grid_ctas(R);
   a.row_part = reinterpret_cast<dspark::Partial*>(ws + L.row_part);

@@ -239,6 +239,17 @@ __device__ __forceinline__ float gumbel_fast_from_bits(uint32_t bits) {
   return -fmaf(e, kLn2, lg2_approx(m) * kLn2);
 }
 
+// Natural logarithm of a positive normal float from its exact exponent and the
+// special-function log2 of its mantissa in [1, 2) (absolute error a few 1e-7); values below
+// the normal range count as 2^-126 (they never decide a draw: their keys lie ~87 below).
+__device__ __forceinline__ float ln_fast(float x) {
+  constexpr float kLn2 = 0.6931471805599453f;
+  const uint32_t b = __float_as_uint(fmaxf(x, 0x1.0p-126f));
+  const float m = __uint_as_float((b & 0x007FFFFFu) | 0x3F800000u);
+  const float e = __int_as_float(0x4B400000 + (int)(b >> 23) - 127) - 12582912.f;
+  return fmaf(e, kLn2, lg2_approx(m) * kLn2);
+}
+
 // 1 - u in binary32 (exact for u >= 1/2, within one rounding below).  Since
 // E = -ln u = -ln(1 - w) >= w, an element with w >= t has E >= t.
 __device__ __forceinline__ float one_minus_uniform(uint32_t bits) {

@@ -105,8 +105,13 @@ struct VerifyArgs {
   // row at W1g row `slot` and rej_req[slot] = r; the correction pass runs over the slots
   int* n_rej;         // [1]
   int* rej_req;       // [R]
+  int* res_hint;      // [R] per slot: the best residual key published so far (order-preserving code)
   int res_compact;    // 1: compact slots (tensor cores); 0: W1g at the request index (CUDA cores)
   int res_grid;       // CTAs of the compact correction pass (its partial count follows from *n_rej)
+  // compact slots whose residual had no positive p - q (only rounding can cause it): drawn
+  // from p by the fallback pass
+  int* n_fb;          // [1]
+  int* fb_req;        // [R]
 };
 
 // Acceptance-overlap diagnostic: c*[r, j-1] = sum_v min(q_j(v), p_j(v)) for the drafted
@@ -208,6 +213,8 @@ cudaError_t launch_conf_hdot(const DraftArgs& a, bool reset_bounds, cudaStream_t
 cudaError_t launch_draft_prepare(const DraftArgs& a, int k, cudaStream_t s);
 cudaError_t launch_draft_step_simt(const DraftArgs& a, int k, cudaStream_t s);
 cudaError_t launch_draft_combine(const DraftArgs& a, int k, int npart, cudaStream_t s);
+int simt_whole_round(int V);  // the CUDA-core draft fits one vocabulary chunk: one launch per round
+cudaError_t launch_draft_round_simt(const DraftArgs& a, cudaStream_t s);
 cudaError_t launch_draft_step_tc(const DraftArgs& a, int k, cudaStream_t s);
 cudaError_t launch_rnn_step_tc(const DraftArgs& a, int k, cudaStream_t s);
 // Recurrent head: h Wh for every position (before the loop), the cell of position k

@@ -91,6 +91,7 @@ __global__ void __launch_bounds__(kPlanThreads) verify_plan_kernel(VerifyArgs a)
   if (threadIdx.x == 0) {
     *a.work_next = 0;
     *a.n_rej = 0;
+    *a.n_fb = 0;
   }
 }
 
@@ -428,7 +429,10 @@ __global__ void verify_accept_kernel(VerifyArgs a) {
     if (a.res_compact) {
       if (lane == 0) slot = atomicAdd(a.n_rej, 1);
       slot = __shfl_sync(0xffffffffu, slot, 0);
-      if (lane == 0) a.rej_req[slot] = r;
+      if (lane == 0) {
+        a.rej_req[slot] = r;
+        a.res_hint[slot] = __float_as_int(-INFINITY) ^ 0x7FFFFFFF;  // no key published yet
+      }
     }
     // gather the factor row of position j* for the bias recomputation: W1[x_{j*-1}], or
     // the recurrent head's state s_{j*}
@@ -602,13 +606,63 @@ __global__ void residual_combine_kernel(VerifyArgs a, int npart) {
   Stats st = stats_empty(), fb = stats_empty();
   for (int p = lane; p < npart; p += 32) {
     stats_merge(st, from_partial(a.res_part[(size_t)p * stride + slot]));
-    stats_merge(fb, from_partial(a.res_part2[(size_t)p * stride + slot]));
+    if (!a.res_compact) stats_merge(fb, from_partial(a.res_part2[(size_t)p * stride + slot]));
   }
   st = warp_reduce_stats(st);
   fb = warp_reduce_stats(fb);
-  // the residual draw falls back to the ln p record only when no p - q was positive
-  // (rounding)
-  if (lane == 0) a.tokens_out[(size_t)req * (a.gamma + 1) + (js - 1)] = st.idx >= 0 ? st.idx : fb.idx;
+  if (lane != 0) return;
+  if (st.idx >= 0) {
+    a.tokens_out[(size_t)req * (a.gamma + 1) + (js - 1)] = st.idx;
+  } else if (!a.res_compact) {
+    // no p - q was positive (rounding): the CUDA-core pass kept the ln p draw as well
+    a.tokens_out[(size_t)req * (a.gamma + 1) + (js - 1)] = fb.idx;
+  } else {
+    // the compact pass ran the (p - q)+ race only: the fallback pass draws from p
+    a.fb_req[atomicAdd(a.n_fb, 1)] = req;
+  }
+}
+
+// The rounding fallback of the compact correction pass: for each request whose residual
+// had no positive p - q (which exact arithmetic rules out), the draw from p instead, with the
+// residual's random numbers (stream 2 at position j*): the Gumbel-max of t/T + g over target
+// row j* - 1 (the row's normaliser shifts every key alike).  One CTA per such request; the
+// queue is normally empty and every CTA leaves at once.
+__global__ void __launch_bounds__(kRowThreads) residual_fallback_kernel(VerifyArgs a) {
+  griddep_allow_next();
+  griddep_wait();
+  __shared__ Partial red[kRowThreads / 32];
+  const int n = *reinterpret_cast<const volatile int*>(a.n_fb);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int q = blockIdx.x; q < n; q += gridDim.x) {
+    const int req = a.fb_req[q];
+    const int js = a.jstar[req];
+    const size_t rbase = target_row_index(a.t_off, a.n_trows, a.gamma, req, js - 1, a.status) * a.V;
+    const RngRow rr = rng_row(a.seed, __ldg(a.req_id + req), a.round, kStreamCorrect, (uint32_t)js);
+    Stats own = stats_empty();
+    for (int g = threadIdx.x; g < (a.V + 3) / 4; g += blockDim.x) {
+      const Philox4 b = rng_chunk(rr, (uint32_t)g);
+      const uint32_t wd[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int v = 4 * g + e;
+        if (v >= a.V) break;
+        const float key = load_elem(a.target, a.dtype_t, rbase + v) * a.inv_temp + gumbel_from_bits(wd[e]);
+        if (key_better(key, v, own.key, own.idx)) {
+          own.key = key;
+          own.idx = v;
+        }
+      }
+    }
+    own = warp_reduce_stats(own);
+    if (lane == 0) red[warp] = to_partial(own);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      Stats b = from_partial(red[0]);
+      for (int w = 1; w < kRowThreads / 32; ++w) stats_merge(b, from_partial(red[w]));
+      a.tokens_out[(size_t)req * (a.gamma + 1) + (js - 1)] = b.idx >= 0 ? b.idx : 0;
+    }
+    __syncthreads();
+  }
 }
 
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s) {
@@ -647,7 +701,9 @@ cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s) {
     npart = (int)rgrid.x;
   }
   if (a.prof != nullptr && (e = record_profile_event(a.prof[3], s)) != cudaSuccess) return e;
-  return launch_pdl(residual_combine_kernel, dim3(wblocks), dim3(256), 0, s, a, npart);
+  if ((e = launch_pdl(residual_combine_kernel, dim3(wblocks), dim3(256), 0, s, a, npart)) != cudaSuccess) return e;
+  if (!a.res_compact) return cudaSuccess;
+  return launch_pdl(residual_fallback_kernel, dim3(32), dim3(kRowThreads), 0, s, a);
 }
 
 // Partial records of the correction pass: the CUDA-core pass keeps one per (vocabulary

@@ -116,6 +116,32 @@ def test_verify_stage_matches_oracle(name):
     assert 0 in kinds and (1 in kinds or R < 8)
 
 
+@pytest.mark.parametrize("name,over", [("qwen3-8b", dict(V=4104, d=64)), ("tiny", {})])
+def test_residual_without_positive_mass_draws_from_p(name, over):
+    """The residual's rounding fallback: with the draft normalisers handed in far too small,
+    q exceeds p everywhere, so (p - q)+ is empty and every rejected request must be drawn
+    from p with the residual's own random numbers (the oracle does the same); logq is made
+    large so that the first draft is rejected."""
+    b = _b()
+    wg, wn = _gpu_workload(name, **over)
+    ref_d = _oracle_draft(wn, rnd=1)
+    R, gamma = wn["R"], wn["gamma"]
+    ell = np.full(R, gamma, np.int32)
+    x = ref_d["x"]
+    logq = np.full((R, gamma), 50.0, np.float32)          # ratio p/q ~ e^-50: reject at j = 1
+    lse = (ref_d["lse"] - 30.0).astype(np.float32)        # q = e^(z - lse) inflated by e^30
+    ref = oracle.verify(wn["target"], wn["U"], wn["W1"], wn["W2"], wn["x0"], x, logq, lse, ell,
+                        wn["temperature"], wn["req_id"], wn["seed"], 1)
+    assert (ref["n_acc"] == 0).all()
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    g = b.verify(wg["target"], wg["U"], wg["W1"], wg["W2"], wg["x0"], t(x), t(logq), t(lse), t(ell),
+                 wg["temperature"], wg["req_id"], wg["seed"], 1)
+    torch.cuda.synchronize()
+    tally = Tally()
+    compare_verify(_np(g), ref, tally)
+    tally.check_rate()
+
+
 @pytest.mark.parametrize("name", list(SMALL))
 def test_round_matches_oracle(name):
     """Whole round on the GPU (draft -> schedule -> verify chained on device) vs the
