@@ -475,10 +475,9 @@ __device__ __forceinline__ void draft_tile(const TcParams& p, Stats& st, const P
       add2f(a0, a1, a4, a5);
       acc += a0 + a1;
     }
-    // the run's largest logit (recomputed: cheaper than keeping every run's in registers)
-    const float cmax =
-        fmaxf(max3f_(max3f_(y[ps][0], y[ps][1], y[ps][2]), max3f_(y[ps][3], y[ps][4], y[ps][5]), y[ps][6]), y[ps][7]);
-    if (race && cmax > -INFINITY && !(thr > -INFINITY && fmaf(cmax, kLn2f, kGumbelMax) < thr)) {
+    // (no per-run skip test: the tile's test above covers the common case, and a run at or
+    // beyond V has only -inf logits, whose keys can never win)
+    if (race) {
       uint32_t wd[kCols];
       philox_run(prow, vb, wd);
       // the scale e^(m ln 2 - best) is 2^(m - best log2 e)
@@ -917,22 +916,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (MODE == kModeDraft) {
       griddep_wait();
       // A rows of this position: W1[x_{k-1}] for the request block, x_{k-1} from x0 or
-      // the previous position's winner.  Lane l moves 16-byte chunk l of the row (rank
-      // <= 256) into the 128-byte swizzled K-atom rows of every replica.  Group-0 CTAs
-      // also write c_k (k >= 2).
+      // the previous position's winner.  Warp ew takes rows ew, ew + 16, ...: lane i loads
+      // row i's token, then every lane loads its 16-byte chunk of every row at once (two
+      // dependent loads per warp, not two per row), and moves it into the 128-byte
+      // swizzled K-atom rows of every replica (lane l: chunk l, rank <= 256).  Group-0
+      // CTAs also write c_k.
       const int et0 = threadIdx.x - 32 * kFirstEpiWarp;
-      for (int rr = ew; rr < RB; rr += kEpiWarps) {
-        const int rq = rb * RB + rr;
-        int xp = 0;
+      constexpr int kRowsW = RB / kEpiWarps;  // 2, 4 or 8 rows per warp
+      int tok = 0;
+      if (lane < kRowsW) {
+        const int rq = rb * RB + ew + lane * kEpiWarps;
         if (rq < p.R) {
           const int raw = p.k == 1 ? __ldg(p.x0 + rq) : (int)~(uint32_t)(__ldcg(p.win_prev + rq) & 0xFFFFFFFFull);
-          xp = checked_token(raw, p.V, p.status, 3);
+          tok = checked_token(raw, p.V, p.status, 3);
         }
-        const bool has = lane * 8 < p.rank;
-        uint4 q = make_uint4(0u, 0u, 0u, 0u);
+      }
+      const bool has = lane * 8 < p.rank;
+      uint4 qa[kRowsW];
+#pragma unroll
+      for (int i = 0; i < kRowsW; ++i) {
+        const int xp = __shfl_sync(0xffffffffu, tok, i);
+        const int rq = rb * RB + ew + i * kEpiWarps;
+        qa[i] = make_uint4(0u, 0u, 0u, 0u);
         if (rq < p.R && has)
-          q = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned short*>(p.W1) + (size_t)xp * p.rank) +
-                    lane);
+          qa[i] = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned short*>(p.W1) +
+                                                        (size_t)xp * p.rank) + lane);
+      }
+      float we[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) we[e] = (group == 0 && has) ? __ldg(p.w_e + lane * 8 + e) : 0.f;
+#pragma unroll
+      for (int i = 0; i < kRowsW; ++i) {
+        const int rr = ew + i * kEpiWarps;
+        const int rq = rb * RB + rr;
+        const uint4 q = qa[i];
         if (has) {
           const int ka = lane >> 3, c = lane & 7;
           const uint32_t dst = sbase + SM::a + ka * (kM * 128) + rr * 128 + ((c ^ (rr & 7)) << 4);
@@ -945,12 +962,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (group == 0 && rq < p.R) {
           const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
           float acc = 0.f;
-          if (has) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              acc = fmaf(__ldg(p.w_e + lane * 8 + 2 * e), bf16_bits_to_float(wd[e] & 0xFFFFu), acc);
-              acc = fmaf(__ldg(p.w_e + lane * 8 + 2 * e + 1), bf16_bits_to_float(wd[e] >> 16), acc);
-            }
+          for (int e = 0; e < 4; ++e) {
+            acc = fmaf(we[2 * e], bf16_bits_to_float(wd[e] & 0xFFFFu), acc);
+            acc = fmaf(we[2 * e + 1], bf16_bits_to_float(wd[e] >> 16), acc);
           }
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
