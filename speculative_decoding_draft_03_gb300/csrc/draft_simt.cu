@@ -55,7 +55,8 @@ __global__ void __launch_bounds__(kHdotThreads) conf_hdot_kernel(int rows, int d
   float acc = 0.f;
   if (row < rows) {
     const size_t base = (size_t)row * d;
-    const bool vec = dtype_h == DSPARK_BF16 && (d % 8) == 0 && (reinterpret_cast<uintptr_t>(h) & 15u) == 0;
+    const bool vec = dtype_h == DSPARK_BF16 && (d % 8) == 0 && (reinterpret_cast<uintptr_t>(h) & 15u) == 0 &&
+                     (reinterpret_cast<uintptr_t>(w_h) & 15u) == 0;
     if (vec) {
       const int n8 = d / 8;
       const uint4* hp = reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned short*>(h) + base);
@@ -71,10 +72,14 @@ __global__ void __launch_bounds__(kHdotThreads) conf_hdot_kernel(int rows, int d
           const int c = c0 + u * kStride;
           if (c >= n8) break;
           const uint32_t wd[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+          // the 8 weights of the chunk in two 16-byte loads (L1/L2 hits: w_h is 4d bytes)
+          const float4 w0 = __ldg(reinterpret_cast<const float4*>(w_h) + 2 * c);
+          const float4 w1 = __ldg(reinterpret_cast<const float4*>(w_h) + 2 * c + 1);
+          const float we[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            acc = fmaf(__ldg(w_h + c * 8 + 2 * e), bf16_bits_to_float(wd[e] & 0xFFFFu), acc);
-            acc = fmaf(__ldg(w_h + c * 8 + 2 * e + 1), bf16_bits_to_float(wd[e] >> 16), acc);
+            acc = fmaf(we[2 * e], bf16_bits_to_float(wd[e] & 0xFFFFu), acc);
+            acc = fmaf(we[2 * e + 1], bf16_bits_to_float(wd[e] >> 16), acc);
           }
         }
       }

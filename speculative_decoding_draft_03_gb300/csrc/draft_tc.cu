@@ -130,12 +130,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same test, but a thread whose phase is still open is suspended until the phase
+// completes or kSuspendNs nanoseconds pass (the PTX suspend-time hint), instead of
+// returning at once: a waiting warp then takes no issue slots from the warps that
+// share its scheduler, which a tight polling loop does.
+constexpr uint32_t kSuspendNs = 1u << 18;  // 262 us, well inside every wait bound
+
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "n"(kSuspendNs)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait: gives up when another role aborted or after kWaitCycles.
 __device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, DeviceStatus* st, int where) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_suspend(bar, parity)) return true;
     if (*abort_flag) return false;
     if (clock64() - t0 > kWaitCycles) {
       *abort_flag = 1;
@@ -150,7 +168,7 @@ __device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_fla
 // before the CTA exits).
 __device__ void mbar_drain(uint32_t bar, uint32_t parity) {
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity))
+  while (!mbar_try_wait_suspend(bar, parity))
     if (clock64() - t0 > kWaitCycles) return;
 }
 
@@ -293,6 +311,7 @@ struct TcParams {
   const void* U;
   const int64_t* req_id;
   uint64_t seed, round;
+  PhiloxKeys keys;  // round keys of the seed (uniform over the launch)
   Partial* partials;  // [ngroups, R]
   int* hint;          // [R] published best keys (draft mode; residual mode: per slot)
   DeviceStatus* status;
@@ -375,10 +394,11 @@ __device__ __forceinline__ void decode_run8(int dtype, const uint4 (&raw)[2], fl
 }
 
 // The 8 ids' random words of one run: Philox blocks (v0 / 4) and (v0 / 4 + 1).
-__device__ __forceinline__ void philox_run(const PhiloxRow& prow, int v0, uint32_t (&wd)[kCols]) {
+__device__ __forceinline__ void philox_run(const PhiloxRowWords& prow, const PhiloxKeys& keys, int v0,
+                                           uint32_t (&wd)[kCols]) {
 #pragma unroll
   for (int g4 = 0; g4 < 2; ++g4) {
-    const Philox4 bits = prow.block((uint32_t)((v0 >> 2) + g4));
+    const Philox4 bits = prow.block((uint32_t)((v0 >> 2) + g4), keys);
     wd[4 * g4 + 0] = bits.x;
     wd[4 * g4 + 1] = bits.y;
     wd[4 * g4 + 2] = bits.z;
@@ -398,7 +418,7 @@ __device__ __forceinline__ void philox_run(const PhiloxRow& prow, int v0, uint32
 // known key, the tile's largest logit is keyed first so that the others are tested
 // against it.  Runs at or beyond V, and rows beyond R, contribute nothing.
 template <int KP>
-__device__ __forceinline__ void draft_tile(const TcParams& p, Stats& st, const PhiloxRow& prow,
+__device__ __forceinline__ void draft_tile(const TcParams& p, Stats& st, const PhiloxRowWords& prow,
                                            const uint4 (&ucur)[KP][2], uint32_t taddr, bool acc_ready, bool valid,
                                            int v0, float zscale, float bound, uint32_t bar_acc_empty, int lane) {
   float y[KP][kCols];
@@ -447,7 +467,7 @@ __device__ __forceinline__ void draft_tile(const TcParams& p, Stats& st, const P
     for (int q = KP * kCols - 1; q >= 0; --q)
       if (y[q / kCols][q % kCols] == tmax) kb = q;
     const int vm = v0 + kb;
-    const Philox4 b4 = prow.block((uint32_t)(vm >> 2));
+    const Philox4 b4 = prow.block((uint32_t)(vm >> 2), p.keys);
     const uint32_t w = (vm & 3) == 0 ? b4.x : ((vm & 3) == 1 ? b4.y : ((vm & 3) == 2 ? b4.z : b4.w));
     const float cn = tmax * kLn2f;
     st.key = cn + gumbel_fast_from_bits(w);
@@ -479,7 +499,7 @@ __device__ __forceinline__ void draft_tile(const TcParams& p, Stats& st, const P
     // beyond V has only -inf logits, whose keys can never win)
     if (race) {
       uint32_t wd[kCols];
-      philox_run(prow, vb, wd);
+      philox_run(prow, p.keys, vb, wd);
       // the scale e^(m ln 2 - best) is 2^(m - best log2 e)
       const float scale = ex2_approx(fmaf(-thr, kLog2ef, mnew)) * kRejectSlack;
       float v[kCols];
@@ -768,6 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
+        __nanosleep(128);  // a sleeping warp leaves the issue slots to the epilogue warps
       }
       if (!ok) break;
       prefetch_tile(t + kPrefTiles);
@@ -858,8 +879,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float zscale = p.inv_temp * kLog2ef;
     const float lse_q2 = lse_q * kLog2ef, lse_t2 = lse_t * kLog2ef;
     float ovl = 0.f;           // overlap only: this thread's sum of min(q, p)
-    const PhiloxRow prow =
-        philox_row(rng_row(p.seed, (MODE != kModeOverlap && valid) ? __ldg(p.req_id + req) : 0, p.round,
+    const PhiloxRowWords prow =
+        philox_row_words(rng_row(p.seed, (MODE != kModeOverlap && valid) ? __ldg(p.req_id + req) : 0, p.round,
                            kDraftMath ? kStreamDraft : kStreamCorrect, (uint32_t)pos));
     const bool u_valid = valid;
     const size_t urow = MODE == kModeOverlap
@@ -1129,7 +1150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t cand = 0;
 #pragma unroll
           for (int g4 = 0; g4 < 2; ++g4) {
-            const Philox4 bits = prow.block((uint32_t)((vb >> 2) + g4));
+            const Philox4 bits = prow.block((uint32_t)((vb >> 2) + g4), p.keys);
             wd[4 * g4 + 0] = bits.x;
             wd[4 * g4 + 1] = bits.y;
             wd[4 * g4 + 2] = bits.z;
@@ -1465,6 +1486,7 @@ static TcParams base_params(int R, int gamma, int V, int rank, int dtype_u, floa
   p.U = U;
   p.req_id = req_id;
   p.seed = seed;
+  p.keys = philox_keys(seed);
   p.round = round;
   p.status = status;
   return p;

@@ -134,6 +134,52 @@ __device__ __forceinline__ PhiloxRow philox_row(const RngRow& r) {
   return o;
 }
 
+// The round keys of rounds 4..10 depend on the seed alone, which every row of a launch
+// shares: a kernel that carries them in its parameters (constant memory, read as
+// instruction operands) holds only the five per-row words of PhiloxRowWords in
+// registers.  PhiloxRowWords::block(chunk, keys) == PhiloxRow::block(chunk) bit for bit.
+struct PhiloxKeys {
+  uint32_t ka[7], kb[7];
+};
+
+__host__ __device__ inline PhiloxKeys philox_keys(uint64_t seed) {
+  PhiloxKeys k;
+  for (int i = 3; i < 10; ++i) {
+    k.ka[i - 3] = (uint32_t)seed + (uint32_t)i * 0x9E3779B9u;
+    k.kb[i - 3] = (uint32_t)(seed >> 32) + (uint32_t)i * 0xBB67AE85u;
+  }
+  return k;
+}
+
+struct PhiloxRowWords {
+  uint32_t p, g, h3, l3, f3;  // as in PhiloxRow
+
+  __device__ __forceinline__ Philox4 block(uint32_t chunk, const PhiloxKeys& k) const {
+    const uint32_t x2 = p ^ chunk;
+    const unsigned long long pb = 0xCD9E8D57ull * (unsigned long long)x2;
+    const uint32_t c0r2 = (uint32_t)(pb >> 32) ^ g;
+    const unsigned long long qa3 = 0xD2511F53ull * (unsigned long long)c0r2;
+    uint32_t c0 = (uint32_t)pb ^ h3, c1 = l3, c2 = (uint32_t)(qa3 >> 32) ^ f3, c3 = (uint32_t)qa3;
+#pragma unroll
+    for (int i = 3; i < 10; ++i) {
+      const unsigned long long qa = 0xD2511F53ull * (unsigned long long)c0;
+      const unsigned long long qb = 0xCD9E8D57ull * (unsigned long long)c2;
+      const uint32_t n0 = (uint32_t)(qb >> 32) ^ c1 ^ k.ka[i - 3];
+      const uint32_t n2 = (uint32_t)(qa >> 32) ^ c3 ^ k.kb[i - 3];
+      c0 = n0;
+      c1 = (uint32_t)qb;
+      c2 = n2;
+      c3 = (uint32_t)qa;
+    }
+    return Philox4{c0, c1, c2, c3};
+  }
+};
+
+__device__ __forceinline__ PhiloxRowWords philox_row_words(const RngRow& r) {
+  const PhiloxRow f = philox_row(r);
+  return PhiloxRowWords{f.p, f.g, f.h3, f.l3, f.f3};
+}
+
 // u = ((bits >> 8) + 0.5) * 2^-24 = (2b+1) * 2^-25 with b = bits >> 8, strictly inside
 // (0,1).  binary64 holds it exactly; binary32 holds u exactly for b < 2^23 (u < 1/2)
 // and 1-u = (2^25-2b-1) * 2^-25 exactly for b >= 2^23.
