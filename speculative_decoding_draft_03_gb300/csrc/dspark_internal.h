@@ -71,6 +71,7 @@ struct VerifyArgs {
   float inv_temp;
   const int64_t* req_id;
   uint64_t seed, round;
+  PhiloxKeys keys;  // round keys of seed (filled by launch_verify for the row pass)
   int32_t* n_acc_out;
   int32_t* tokens_out;
   int32_t* n_out;

@@ -34,6 +34,7 @@ namespace dspark {
 
 constexpr int kPlanThreads = 1024;
 constexpr int kRowThreads = 256;
+constexpr int kRowCtasPerSm = 4;  // resident row-pass CTAs per SM (the grid is that many per SM)
 
 // verify length of request r, clamped to [0,gamma] (out-of-range values are reported)
 __device__ __forceinline__ int clamp_ell(const VerifyArgs& a, int r) {
@@ -125,7 +126,8 @@ __device__ __forceinline__ void bonus_race(const VerifyArgs& a, const float (&z)
                                            int v0, int row, int c, Partial* sm_red) {
   constexpr int NV = kRowPer / EPV;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const PhiloxRow prow = philox_row(rng_row(a.seed, __ldg(a.req_id + r), a.round, kStreamCorrect, (uint32_t)(t + 1)));
+  const PhiloxRowWords prow =
+      philox_row_words(rng_row(a.seed, __ldg(a.req_id + r), a.round, kStreamCorrect, (uint32_t)(t + 1)));
   auto id_of = [&](int k) { return v0 + (threadIdx.x + (k / EPV) * kRowThreads) * EPV + (k % EPV); };
   Stats own = stats_empty();
   if (m > -INFINITY) {
@@ -134,7 +136,7 @@ __device__ __forceinline__ void bonus_race(const VerifyArgs& a, const float (&z)
     for (int k = kRowPer - 1; k >= 0; --k)
       if (z[k] == m) km = k;  // the lowest id among equal maxima
     const int vm = id_of(km);
-    const Philox4 b = prow.block((uint32_t)(vm >> 2));
+    const Philox4 b = prow.block((uint32_t)(vm >> 2), a.keys);
     const uint32_t w = (vm & 3) == 0 ? b.x : ((vm & 3) == 1 ? b.y : ((vm & 3) == 2 ? b.z : b.w));
     own.key = m + gumbel_fast_from_bits(w);
     own.idx = vm;
@@ -152,7 +154,7 @@ __device__ __forceinline__ void bonus_race(const VerifyArgs& a, const float (&z)
         const float gm = fmaxf(fmaxf(z[k0], z[k0 + 1]), fmaxf(z[k0 + 2], z[k0 + 3]));
         if (gm + kGumbelMax < thr) continue;  // no id of the group can reach the bound
         const int vb = id_of(k0);
-        const Philox4 b = prow.block((uint32_t)(vb >> 2));
+        const Philox4 b = prow.block((uint32_t)(vb >> 2), a.keys);
         const uint32_t wd[4] = {b.x, b.y, b.z, b.w};
         const float s = -thr * kLog2e;
 #pragma unroll
@@ -187,9 +189,11 @@ __device__ __forceinline__ void bonus_race(const VerifyArgs& a, const float (&z)
 
 // Work items are (row position, chunk) pairs taken from a queue in row_order.  Per item
 // the CTA needs the chunk maximum M (block max; every thread then sums exp(z - M) against
-// the same M, so the partial sums add without rescaling).
+// the same M, so the partial sums add without rescaling).  The next item's index is taken
+// from the queue while the current one is processed, so the atomic's round trip is off
+// the critical path.
 template <int DT>
-__global__ void __launch_bounds__(kRowThreads, 3) verify_rows_kernel(VerifyArgs a) {
+__global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) verify_rows_kernel(VerifyArgs a) {
   griddep_allow_next();
   griddep_wait();
   constexpr int EPV = DT == DSPARK_F32 ? 4 : 8;  // ids per 16-byte vector
@@ -197,15 +201,17 @@ __global__ void __launch_bounds__(kRowThreads, 3) verify_rows_kernel(VerifyArgs 
   constexpr int kWarps = kRowThreads / 32;
   __shared__ float sm_f[kWarps];
   __shared__ Partial sm_red[kWarps];
-  __shared__ int item_s;
+  __shared__ int item_s[2];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int n_items = (*a.n_rows) * a.nchunk;
   const bool vec_ok = (a.V % EPV) == 0 && (reinterpret_cast<uintptr_t>(a.target) & 15u) == 0;
-  for (;;) {
-    if (threadIdx.x == 0) item_s = atomicAdd(a.work_next, 1);
-    __syncthreads();
-    const int item = item_s;
+  if (threadIdx.x == 0) item_s[0] = atomicAdd(a.work_next, 1);
+  __syncthreads();
+  // every item ends with a block barrier, after which item_s[cur] holds the next index
+  for (int cur = 0;; cur ^= 1) {
+    const int item = item_s[cur];
     if (item >= n_items) break;
+    if (threadIdx.x == 0) item_s[cur ^ 1] = atomicAdd(a.work_next, 1);
     const int pos = item / a.nchunk, c = item % a.nchunk;
     const int row = a.row_order[pos];
     const int r = a.row_req[row], t = a.row_t[row];
@@ -672,11 +678,13 @@ cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s) {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int max_items = a.R * (a.gamma + 1) * a.nchunk;
-  const int grid = min(max_items, sms * 3);  // work queue: CTAs take items until none is left
+  const int grid = min(max_items, sms * kRowCtasPerSm);  // work queue: CTAs take items until none is left
   if (a.chunk != kRowThreads * kRowPer) return cudaErrorInvalidValue;
   if (a.prof != nullptr && (e = record_profile_event(a.prof[0], s)) != cudaSuccess) return e;
-  e = a.dtype_t == DSPARK_F32 ? launch_pdl(verify_rows_kernel<DSPARK_F32>, dim3(grid), dim3(kRowThreads), 0, s, a)
-                              : launch_pdl(verify_rows_kernel<DSPARK_BF16>, dim3(grid), dim3(kRowThreads), 0, s, a);
+  VerifyArgs ra = a;
+  ra.keys = philox_keys(a.seed);
+  e = a.dtype_t == DSPARK_F32 ? launch_pdl(verify_rows_kernel<DSPARK_F32>, dim3(grid), dim3(kRowThreads), 0, s, ra)
+                              : launch_pdl(verify_rows_kernel<DSPARK_BF16>, dim3(grid), dim3(kRowThreads), 0, s, ra);
   if (e != cudaSuccess) return e;
   if (a.prof != nullptr && (e = record_profile_event(a.prof[1], s)) != cudaSuccess) return e;
   const int wblocks = (a.R * 32 + 255) / 256;
