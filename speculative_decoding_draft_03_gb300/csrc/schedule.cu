@@ -20,6 +20,7 @@
 namespace dspark {
 
 constexpr int kSchedThreads = 1024;  // one CTA; R*gamma <= 8192 candidates (host-checked)
+constexpr int kSchedLaunchThreads = 512;  // threads the confidence scheduler runs with
 
 size_t schedule_smem_bytes(int R, int gamma) {
   const size_t N = (size_t)R * gamma;
@@ -120,7 +121,7 @@ __device__ void merge_sort_chains(SchedSmem& sm, int N, int gamma) {
 
 // Inclusive prefix sums of the sorted a's, written over key[] in sorted order.  Each
 // thread gathers its run (at most 8 values) into registers before any is overwritten.
-constexpr int kScanPer = 8;  // 8192 candidates / 1024 threads
+constexpr int kScanPer = 16;  // 8192 candidates / 512 threads
 
 __device__ void scan_sorted(SchedSmem& sm, int N) {
   const int per = (N + blockDim.x - 1) / blockDim.x;
@@ -338,9 +339,11 @@ cudaError_t launch_schedule(int R, int gamma, const float* conf, const double* s
   const size_t smem = schedule_smem_bytes(R, gamma);
   cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  // up to 4096 candidates, 512 threads (at most 8 per thread, as the scan needs): fewer
-  // warps meet at every barrier (1% faster at 2048 candidates)
-  const int threads = (R * gamma <= 4096) ? 512 : kSchedThreads;
+  // 512 threads (at most 16 candidates each, as the scan needs): half as many merge-path
+  // searches per merge round as 1024 threads, against the same shared-memory traffic for
+  // the merges themselves (the rounds are bound by shared-memory bank conflicts); 68 ->
+  // 59 us at 7680 candidates
+  const int threads = kSchedLaunchThreads;
   return launch_pdl(schedule_kernel, dim3(1), dim3(threads), smem, s, R, gamma, conf, sps, mode, conf_hist,
                     fixed_len, ell_out, B_out, tau_out, status);
 }
