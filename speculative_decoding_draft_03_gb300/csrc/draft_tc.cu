@@ -1459,6 +1459,14 @@ int tc_num_partials(int R) {
 
 int tc_block_rows(int R) { return tc::block_rows(R); }
 
+int tc_residual_grid(int R) {
+  // the compact correction pass: every SM, or one CTA per slot block if there are more
+  // blocks than SMs (the kernel derives its blocks and groups from the device-side count)
+  const int Rb = tc_residual_rows_per_block(R);
+  const int rblocks = (R + Rb - 1) / Rb;
+  return rblocks > tc::num_sms() ? rblocks : tc::num_sms();
+}
+
 int tc_grid_ctas(int R) {
   // compact overlap rows: every SM (the kernel derives its blocks and groups from the row
   // count), or one CTA per request block if there are more blocks than SMs
@@ -1622,6 +1630,8 @@ cudaError_t launch_residual_tc(const VerifyArgs& a, cudaStream_t s) {
   p.res_nrows = a.n_rej;
   p.hint = a.res_hint;
   p.grid = a.res_grid;
+  p.Rb = tc_residual_rows_per_block(a.R);
+  p.rblocks = (a.R + p.Rb - 1) / p.Rb;
   return tc::launch<tc::kModeResidual>(p, a.W1g, a.W2, s);
 }
 

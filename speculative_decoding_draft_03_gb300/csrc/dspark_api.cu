@@ -515,7 +515,7 @@ static dspark_status verify_impl(int R, int gamma, int V, int rank, int dtype_t,
   a.fb_req = reinterpret_cast<int*>(ws + L.fb_req);
   a.res_hint = reinterpret_cast<int*>(ws + L.res_hint);
   a.res_compact = dspark::tc_supported(V, rank, dtype_w);
-  a.res_grid = dspark::tc_grid_ctas(R);
+  a.res_grid = dspark::tc_residual_grid(R);
   a.row_part = reinterpret_cast<dspark::Partial*>(ws + L.row_part);
   a.nchunk = L.nchunk;
   a.chunk = kVerifyChunk;

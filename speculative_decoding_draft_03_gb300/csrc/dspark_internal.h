@@ -202,7 +202,15 @@ int tc_num_partials(int R);
 int tc_block_rows(int R);  // rows per request block of a tensor-core launch over R rows
 // the same on the device: 32, 64 or 128 rows
 __host__ __device__ inline int tc_rows_per_block(int R) { return R <= 32 ? 32 : (R <= 64 ? 64 : 128); }
+// The compact correction pass takes at most 64 slots per block: every thread then holds
+// two 8-id runs per tile instead of four, so a block's tile time halves, and the pass's
+// CTAs split more evenly between the blocks that the device-side slot count needs (with
+// 128-slot blocks, 129 rejecting requests already doubled every CTA's tile count).
+__host__ __device__ inline int tc_residual_rows_per_block(int R) {
+  return tc_rows_per_block(R) < 64 ? tc_rows_per_block(R) : 64;
+}
 int tc_grid_ctas(int R);   // CTAs of the compact overlap pass over at most R rows
+int tc_residual_grid(int R);  // CTAs of the compact correction pass for R requests
 // the compact overlap pass is used only when its request blocks fit on the SMs (then it
 // launches one CTA per SM and its partials take SMs x R floats)
 int tc_compact_ok(int R);

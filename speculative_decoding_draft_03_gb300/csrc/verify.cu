@@ -602,7 +602,7 @@ __global__ void residual_combine_kernel(VerifyArgs a, int npart) {
     const int n = *reinterpret_cast<const volatile int*>(a.n_rej);
     if (r >= n) return;
     req = a.rej_req[r];
-    const int rb_rows = tc_rows_per_block(a.R);
+    const int rb_rows = tc_residual_rows_per_block(a.R);
     const int rblocks = (n + rb_rows - 1) / rb_rows;
     npart = max(1, a.res_grid / rblocks);
     stride = (size_t)rblocks * rb_rows;
@@ -720,7 +720,7 @@ cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s) {
 // linear in R.
 size_t residual_partial_entries(int R, int V, int rank, int dtype_w) {
   if (!tc_supported(V, rank, dtype_w)) return (size_t)simt_num_chunks(V) * R;
-  return (size_t)tc_grid_ctas(R) * tc_rows_per_block(R);
+  return (size_t)tc_residual_grid(R) * tc_residual_rows_per_block(R);
 }
 
 }  // namespace dspark
