@@ -98,7 +98,7 @@ struct Smem {
   static_assert(uboxes >= 4 && uboxes <= kMaxUBoxes, "U ring must hold one tile of fp32 boxes");
   static_assert(total + 1024 <= 232448, "shared memory plan exceeds 227 KB");
   static_assert(8 * (2 * stages + 7 + 2 * kMaxUBoxes) + 16 <= 512,
-                "barriers, TMEM slot, abort flag and release counter fit in 512 B");
+                "barriers, TMEM slot and abort flag fit in 512 B");
 };
 
 // ------------------------------------------------------------------------------------
@@ -598,8 +598,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kBarBytes = 8 * (2 * kStages + 7 + 2 * kMaxUBoxes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::bars + kBarBytes);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM::bars + kBarBytes + 8);
-  // residual mode: tiles whose accumulator epilogue warp 0 has released (paces the L2 prefetcher)
-  volatile int* released = reinterpret_cast<volatile int*>(smem + SM::bars + kBarBytes + 12);
   // U boxes of a tile: 128/ubox_cols of them, each read by the 16/(128/ubox_cols) warps
   // whose columns fall inside it
   const int uboxes_per_tile = kN / p.ubox_cols;
@@ -627,7 +625,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_uempty + 8 * s, warps_per_ubox);
     }
     *abort_flag = 0;
-    *released = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
@@ -741,57 +738,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar_mma_drain);
         mbar_drain(bar_mma_drain, 0);
       }
-    }
-  } else if (warp == 2 && MODE == kModeResidual) {
-    // ------------------------------ L2 prefetcher (residual mode) -------------
-    // The slots' U and target rows lie at scattered positions, so the epilogue loads them
-    // itself; this warp brings each tile's row segments into L2 kPrefTiles tiles ahead of
-    // the epilogue (paced by the accumulator releases), so those loads hit L2.
-    constexpr int kPrefTiles = 2;
-    const int n = *reinterpret_cast<const volatile int*>(p.res_nrows);
-    const int es_u = p.dtype_u == DSPARK_F32 ? 4 : 2, es_t = p.dtype_t == DSPARK_F32 ? 4 : 2;
-    const char* ubase[RB / 32];
-    const char* tbase[RB / 32];
-#pragma unroll
-    for (int i = 0; i < RB / 32; ++i) {
-      const int q = rb * RB + lane + 32 * i;
-      ubase[i] = tbase[i] = nullptr;
-      if (q < n) {
-        const int rq = p.res_req[q];
-        const int js = p.jstar[rq];
-        if (js > 0 && js <= p.gamma) {
-          ubase[i] = reinterpret_cast<const char*>(p.U) + ((size_t)rq * p.gamma + (js - 1)) * (size_t)p.V * es_u;
-          tbase[i] = reinterpret_cast<const char*>(p.target) +
-                     target_row_index(p.t_off, p.n_trows, p.gamma, rq, js - 1, p.status) * (size_t)p.V * es_t;
-        }
-      }
-    }
-    auto prefetch_tile = [&](int t) {
-      const int v0 = (group + t * ngroups) * kN;
-      const int ids = min(kN, p.V - v0);
-#pragma unroll
-      for (int i = 0; i < RB / 32; ++i) {
-        if (ubase[i] == nullptr) continue;
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ubase[i] + (size_t)v0 * es_u), "r"(ids * es_u)
-                     : "memory");
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(tbase[i] + (size_t)v0 * es_t), "r"(ids * es_t)
-                     : "memory");
-      }
-    };
-    for (int t = 0; t < min(kPrefTiles, my_tiles); ++t) prefetch_tile(t);
-    const long long t0 = clock64();
-    for (int t = 0; t + kPrefTiles < my_tiles && !*abort_flag; ++t) {
-      // wait (bounded) until tile t has been released, then prefetch tile t + kPrefTiles
-      bool ok = true;
-      while (*released <= t) {
-        if (*abort_flag || clock64() - t0 > kWaitCycles) {
-          ok = false;
-          break;
-        }
-        __nanosleep(128);  // a sleeping warp leaves the issue slots to the epilogue warps
-      }
-      if (!ok) break;
-      prefetch_tile(t + kPrefTiles);
     }
   } else if (warp == 2) {
     // ------------------------------ U producer (draft mode) -------------------
@@ -1083,7 +1029,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_acc_empty + 8 * buf);
-          if (MODE == kModeResidual && ew == 0 && lane == 0) *released = t + 1;
         }
         const int vb = vt + c;
         float z[kCols];
