@@ -120,7 +120,8 @@ def _row_f64(W, x):
 
 def compare_draft_continuing(gpu, ref, host, tol, tally):
     """Like compare_draft, but a boundary case does not end the comparison of its request:
-    the oracle adopts the GPU's token (the survey's comparison rule) and recomputes the
+    the oracle adopts the GPU's token (a draw within 1e-5 of a decision boundary may go
+    either way, so both tokens are correct) and recomputes the
     request's later positions from it, draw by draw (oracle.draft_row for the draw and
     oracle.rnn_confidence with the factor row W1[x_{k-1}] as the state for c_k, which is
     the Markov head's confidence), and those are compared too.
