@@ -119,26 +119,113 @@ def stored_traffic(kernel, workload, path=COUNTERS):
     return None if e is None or e.get("traffic_bytes_per_launch") is None else float(e["traffic_bytes_per_launch"])
 
 
+# NVML clock-event reason bits (nvml.h, nvmlClocksEventReason*) and the names the
+# nvidia-smi query fields use for them
+_NVML_REASONS = ((0x8 | 0x80, "hw_slowdown"), (0x40, "hw_thermal_slowdown"), (0x20, "sw_thermal_slowdown"),
+                 (0x4, "sw_power_cap"))
+
+
+def nvml_reason_names(bits):
+    """The throttle reasons of an NVML clock-event reason mask (HW power brake counts as HW
+    slowdown, as nvidia-smi reports it)."""
+    return [name for mask, name in _NVML_REASONS if bits & mask]
+
+
+def summarize_clock_samples(rows):
+    """rows: (sm_mhz, sm_max_mhz, [reason names]) per sample -> the bench line's clocks
+    object: median SM clock under load, the largest max clock seen, every reason seen."""
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+    sm = sorted(r[0] for r in rows)
+    return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(r[1] for r in rows),
+            "reasons": sorted({n for r in rows for n in r[2]}), "samples": len(rows)}
+
+
+class _NvmlClocks:
+    """Read-only clock queries through the driver's NVML library (ctypes; no settings are
+    touched): the SM clock, its maximum and the clock-event reasons of one device, found by
+    the CUDA device's PCI address."""
+
+    def __init__(self, cuda_index):
+        import ctypes
+        import torch
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.lib, self.ct = lib, ctypes
+        self.dev = ctypes.c_void_p()
+        props = torch.cuda.get_device_properties(cuda_index)
+        found = False
+        if all(hasattr(props, a) for a in ("pci_domain_id", "pci_bus_id", "pci_device_id")):
+            bus = "%08x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+            found = lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.dev)) == 0
+        if not found and lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(cuda_index), ctypes.byref(self.dev)) != 0:
+            raise OSError("no NVML handle for the device")
+        self.reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        if self.reasons is None:
+            self.reasons = lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint(0)
+        self.max_mhz = float(mx.value) if lib.nvmlDeviceGetMaxClockInfo(self.dev, 1, ctypes.byref(mx)) == 0 else None
+
+    def sample(self):
+        ct = self.ct
+        mhz, bits = ct.c_uint(0), ct.c_ulonglong(0)
+        if self.lib.nvmlDeviceGetClockInfo(self.dev, 1, ct.byref(mhz)) != 0:  # NVML_CLOCK_SM
+            return None
+        if self.reasons(self.dev, ct.byref(bits)) != 0:
+            return None
+        return (float(mhz.value), self.max_mhz if self.max_mhz is not None else float(mhz.value),
+                nvml_reason_names(bits.value))
+
+
 class ClockSampler:
+    """SM clocks and throttle reasons during a timed region: NVML polled every 2 ms from a
+    host thread (dozens of samples even in a 40 ms region), else `nvidia-smi -lms 100`."""
     FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
+    PERIOD_S = 0.002
 
     def __init__(self, index):
         self.index = index
         self.proc = None
+        self.thread = None
+        self.rows = []
+        self.source = None
+
+    def _poll(self, nv):
+        while not self.stop.is_set():
+            r = nv.sample()
+            if r is not None:
+                self.rows.append(r)
+            self.stop.wait(self.PERIOD_S)
 
     def __enter__(self):
+        import threading
+        try:
+            nv = _NvmlClocks(self.index)
+        except (OSError, AttributeError, RuntimeError):
+            nv = None
+        if nv is not None:
+            self.stop = threading.Event()
+            self.thread = threading.Thread(target=self._poll, args=(nv,), daemon=True)
+            self.thread.start()
+            self.source = "nvml"
+            return self
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                                           "-lms", "100", "-i", str(self.index)], stdout=subprocess.PIPE,
                                          stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi"
         except OSError:
             self.proc = None
         return self
 
     def __exit__(self, *exc):
         self.out = ""
+        if self.thread is not None:
+            self.stop.set()
+            self.thread.join(timeout=5)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -148,22 +235,22 @@ class ClockSampler:
                 self.out, _ = self.proc.communicate()
 
     def summary(self):
-        rows = []
-        for line in (self.out or "").splitlines():
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 7:
-                continue
-            try:
-                rows.append((float(parts[0]), float(parts[1]), parts[3:7]))
-            except ValueError:
-                continue
+        rows = list(self.rows)
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        sm = sorted(r[0] for r in rows)
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2]) if v.lower() == "active"})
-        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
-                "samples": len(rows)}
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for line in (self.out or "").splitlines():
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 7:
+                    continue
+                try:
+                    rows.append((float(parts[0]), float(parts[1]),
+                                 [names[i] for i, v in enumerate(parts[3:7]) if v.lower() == "active"]))
+                except ValueError:
+                    continue
+        out = summarize_clock_samples(rows)
+        if rows:
+            out["source"] = self.source
+        return out
 
 
 def rank_request_ids(req_id, rank, R):

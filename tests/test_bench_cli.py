@@ -95,3 +95,48 @@ def test_compare_round_counts_boundaries():
     gpu["tokens"][0, 1] = 8  # a correction token differing with a wide margin
     c = bench.compare_round(gpu, ref)
     assert c["mismatches"] == 1
+
+
+def test_clock_summary_and_nvml_reason_bits():
+    import bench
+    assert bench.nvml_reason_names(0) == []
+    assert bench.nvml_reason_names(0x4) == ["sw_power_cap"]
+    assert set(bench.nvml_reason_names(0x8 | 0x20 | 0x40)) == {"hw_slowdown", "sw_thermal_slowdown",
+                                                               "hw_thermal_slowdown"}
+    assert bench.nvml_reason_names(0x80) == ["hw_slowdown"]  # HW power brake
+    assert bench.nvml_reason_names(0x1 | 0x2) == []  # idle, application clocks: not throttling
+    s = bench.summarize_clock_samples([(2070.0, 2070.0, []), (1950.0, 2070.0, ["sw_power_cap"]),
+                                       (2070.0, 2070.0, [])])
+    assert s == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+    assert bench.summarize_clock_samples([])["reasons"] == ["unsampled"]
+
+
+def test_clock_sampler_polls_nvml_from_a_thread(monkeypatch):
+    """With an NVML device (a fake here: no driver on this machine) the sampler polls from a
+    host thread for the whole region; without one it falls back and reports 'unsampled'."""
+    import time
+    import bench
+
+    class FakeNvml:
+        def __init__(self, index):
+            self.n = 0
+
+        def sample(self):
+            self.n += 1
+            return (2070.0 if self.n % 3 else 1980.0, 2070.0, ["sw_power_cap"] if self.n == 2 else [])
+
+    monkeypatch.setattr(bench, "_NvmlClocks", FakeNvml)
+    with bench.ClockSampler(0) as c:
+        time.sleep(0.05)
+    s = c.summary()
+    assert s["source"] == "nvml" and s["samples"] >= 5
+    assert s["sm_mhz"] == 2070.0 and s["reasons"] == ["sw_power_cap"]
+
+    def no_nvml(index):
+        raise OSError("libnvidia-ml.so.1: cannot open shared object file")
+
+    monkeypatch.setattr(bench, "_NvmlClocks", no_nvml)
+    monkeypatch.setenv("PATH", "/nonexistent")  # no nvidia-smi either
+    with bench.ClockSampler(0) as c:
+        pass
+    assert c.summary()["reasons"] == ["unsampled"]
